@@ -1,0 +1,133 @@
+"""Concurrent attention in fp64, two independent ways (oracle; test infrastructure only).
+
+Both compute, for every problem p, worker w and query head h, softmax attention of the worker's
+query over every token of its view (Hogwild! Inference summary, gentlecold.top, sections 4-5
+and 9), with score scale 1/sqrt(D), GQA head h -> KV head floor(h / G), no other mask:
+
+* ``brute_force`` is the plain definition: lay the view's raw keys out at positions 0 .. n-1,
+  rotate each key at its view position, rotate the query at i_q, and run an ordinary softmax.
+  This is the "re-encode every token at its new position" formulation the summary calls too
+  costly for real use (section 4) -- exactly what makes it a good check.
+* ``method`` is the summary's section-5 identity: keys stay rotated at block-local positions,
+  and for each block of the view the query is rotated once by (i_q - the block's view offset);
+  per-block softmax partials (max, sum, weighted values) are then merged by log-sum-exp, the
+  "aggregate in the softmax weighting" / "partial result reduction" of sections 5 and 9.
+
+Returned ``lse`` is the natural-log log-sum-exp of the scaled scores (-inf for an empty view).
+"""
+from __future__ import annotations
+
+import math
+from typing import Tuple
+
+import numpy as np
+
+from .cache import HogwildCache
+from .rope import rope
+
+
+def _check_q(cache: HogwildCache, q: np.ndarray, num_q_heads: int) -> np.ndarray:
+    q = np.asarray(q, dtype=np.float64)
+    if q.shape != (cache.P, cache.W, num_q_heads, cache.D):
+        raise ValueError("q must be [P][W][H_q][D]")
+    if num_q_heads % cache.H_kv:
+        raise ValueError("H_q must be a multiple of H_kv")
+    return q
+
+
+def brute_force(cache: HogwildCache, layer: int, q: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Re-rotate every raw key at its full view position; plain softmax attention."""
+    P, W, Hq, D = np.asarray(q).shape
+    q = _check_q(cache, q, Hq)
+    G = Hq // cache.H_kv
+    scale = 1.0 / math.sqrt(D)
+    out = np.zeros((P, W, Hq, D))
+    lse = np.full((P, W, Hq), -np.inf)
+    for p in range(P):
+        for w in range(W):
+            entries, i_q = cache.view(p, w)
+            if not entries:
+                continue
+            kr = np.concatenate([cache.segments[s].raw_k(layer)[:n] for s, _, n in entries])
+            vr = np.concatenate([cache.segments[s].raw_v(layer)[:n] for s, _, n in entries])
+            pos = np.arange(kr.shape[0])
+            k = rope(kr, pos[:, None], cache.theta)              # [n][H_kv][D]
+            qr = rope(q[p, w], i_q, cache.theta)                  # [H_q][D]
+            for h in range(Hq):
+                s = (k[:, h // G, :] @ qr[h]) * scale
+                m = s.max()
+                e = np.exp(s - m)
+                out[p, w, h] = (e @ vr[:, h // G, :]) / e.sum()
+                lse[p, w, h] = m + math.log(e.sum())
+    return out, lse
+
+
+def segment_partial(stored_k: np.ndarray, v: np.ndarray, q_rot: np.ndarray, scale: float):
+    """Softmax partial of one block for a group of query rows sharing one KV head.
+
+    stored_k, v: [n][D]; q_rot: [rows][D].  Returns (m [rows], l [rows], o [rows][D]) with
+    m = max score, l = sum exp(score - m), o = sum exp(score - m) v (unnormalised).
+    """
+    s = (q_rot @ stored_k.T) * scale                 # [rows][n]
+    m = s.max(axis=1)
+    e = np.exp(s - m[:, None])
+    return m, e.sum(axis=1), e @ v
+
+
+def lse_merge(parts):
+    """Merge softmax partials [(m, l, o)] into (out, lse) by log-sum-exp."""
+    M = np.max(np.stack([m for m, _, _ in parts]), axis=0)
+    L = sum(l * np.exp(m - M) for m, l, _ in parts)
+    O = sum(o * np.exp(m - M)[:, None] for m, _, o in parts)
+    return O / L[:, None], M + np.log(L)
+
+
+def method(cache: HogwildCache, layer: int, q: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Keys at block-local positions, one query rotation per (worker, block), LSE merge."""
+    P, W, Hq, D = np.asarray(q).shape
+    q = _check_q(cache, q, Hq)
+    G = Hq // cache.H_kv
+    scale = 1.0 / math.sqrt(D)
+    out = np.zeros((P, W, Hq, D))
+    lse = np.full((P, W, Hq), -np.inf)
+    for p in range(P):
+        for w in range(W):
+            entries, i_q = cache.view(p, w)
+            if not entries:
+                continue
+            parts = {h: [] for h in range(cache.H_kv)}
+            for sid, off, n in entries:
+                seg = cache.segments[sid]
+                ks = seg.stored_k(layer)[:n]
+                vs = seg.raw_v(layer)[:n]
+                q_rot = rope(q[p, w], i_q - off, cache.theta)      # rotate by (i_q - offset)
+                for kh in range(cache.H_kv):
+                    parts[kh].append(segment_partial(ks[:, kh, :], vs[:, kh, :],
+                                                     q_rot[kh * G:(kh + 1) * G], scale))
+            for kh in range(cache.H_kv):
+                o, l = lse_merge(parts[kh])
+                out[p, w, kh * G:(kh + 1) * G] = o
+                lse[p, w, kh * G:(kh + 1) * G] = l
+    return out, lse
+
+
+def method_rows(cache: HogwildCache, layer: int, q: np.ndarray, rows) -> np.ndarray:
+    """``method`` for selected (p, w, h) rows only; returns out [len(rows)][D] (sampled checks)."""
+    P, W, Hq, D = np.asarray(q).shape
+    q = _check_q(cache, q, Hq)
+    G = Hq // cache.H_kv
+    scale = 1.0 / math.sqrt(D)
+    res = np.zeros((len(rows), D))
+    for r, (p, w, h) in enumerate(rows):
+        entries, i_q = cache.view(p, w)
+        if not entries:
+            continue
+        kh = h // G
+        parts = []
+        for sid, off, n in entries:
+            seg = cache.segments[sid]
+            q_rot = rope(q[p, w, h][None, :], i_q - off, cache.theta)
+            parts.append(segment_partial(seg.stored_k(layer)[:n, kh, :],
+                                         seg.raw_v(layer)[:n, kh, :], q_rot, scale))
+        res[r] = lse_merge(parts)[0][0]
+    return res

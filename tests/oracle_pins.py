@@ -1,0 +1,322 @@
+"""Pins that tie the fp64 oracle to something other than itself.
+
+Each ``check_*`` raises AssertionError when the oracle disagrees with: a closed form written
+out here, the pages' worked views (``tests/golden``), the textbook complex-number form of RoPE,
+torch's own scaled-dot-product attention, or the oracle's other (brute-force) formulation.
+``test_oracle_pins.py`` runs them as they are; ``test_oracle_mutations.py`` plants plausible
+mistakes in the oracle and checks that at least one of them fails.
+
+Modules are looked up at call time (``R.rope``, ``A.method`` ...) so that a planted mistake
+is seen.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+import oracle.attention as A
+import oracle.cache as C
+import oracle.rope as R
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ------------------------------------------------------------------------------- RoPE
+
+
+def rope_complex(x, pos, theta):
+    """Textbook RoPE as complex multiplication: z_i = x_i + i x_{i+D/2}, z_i *= e^{i pos f_i}."""
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    h = D // 2
+    f = np.array([theta ** (-(2.0 * i) / D) for i in range(h)])
+    z = (x[..., :h] + 1j * x[..., h:]) * np.exp(1j * np.asarray(pos, dtype=np.float64)[..., None] * f)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def check_rope_complex_form():
+    g = np.random.default_rng(11)
+    for D, theta in ((2, 1e4), (8, 1e4), (64, 1e4), (128, 1e6)):
+        x = g.standard_normal((7, D))
+        pos = g.integers(-(1 << 17), 1 << 17, size=7)
+        got = R.rope(x, pos, theta)
+        ref = rope_complex(x, pos, theta)
+        assert np.allclose(got, ref, rtol=0, atol=1e-9 * max(1.0, np.abs(ref).max())), (D, theta)
+
+
+def check_rope_d2_textbook():
+    # D = 2: one pair, f_0 = theta^0 = 1 rad per position: a plain 2-D rotation.
+    for p in (0, 1, 2, -3, 1000):
+        assert np.allclose(R.rope(np.array([1.0, 0.0]), p, 1e4), [math.cos(p), math.sin(p)], atol=1e-14)
+        assert np.allclose(R.rope(np.array([0.0, 1.0]), p, 1e4), [-math.sin(p), math.cos(p)], atol=1e-14)
+
+
+def check_inv_freq_values():
+    f = R.inv_freq(64, 1e4)
+    assert f[0] == 1.0
+    assert abs(f[1] - 10 ** (-0.125)) < 1e-15          # 1e4^(-2/64)
+    assert abs(f[31] - 10 ** (-4 * 62 / 64)) < 1e-18
+
+
+def check_rope_invariants():
+    """rho is orthogonal, composes additively, and q.k depends only on a - b."""
+    g = np.random.default_rng(12)
+    for D, theta in ((2, 1e4), (64, 1e4), (128, 1e6)):
+        q, k = g.standard_normal(D), g.standard_normal(D)
+        for _ in range(8):
+            a, b, d = (int(x) for x in g.integers(-(1 << 17), 1 << 17, size=3))
+            assert abs(np.linalg.norm(R.rope(q, a, theta)) - np.linalg.norm(q)) < 1e-12
+            assert np.allclose(R.rope(R.rope(q, a, theta), b, theta), R.rope(q, a + b, theta), atol=1e-9)
+            lhs = R.rope(q, a, theta) @ R.rope(k, b, theta)
+            mid = R.rope(q, a - b, theta) @ k
+            rhs = R.rope(q, a + d, theta) @ R.rope(k, b + d, theta)
+            assert abs(lhs - mid) < 1e-9 and abs(lhs - rhs) < 1e-9
+
+
+# ------------------------------------------------------------------------- cache views
+
+
+def _tiny_cache(W=2, S=4, pages=64, H_kv=1, D=2, order=None, contiguous=False, layers=1):
+    return C.HogwildCache(1, W, layers, H_kv, D, 1e4, S, pages, contiguous=contiguous,
+                          page_order=order)
+
+
+def _names_of_view(cache, p, w, names):
+    entries, _ = cache.view(p, w)
+    return [names[sid] for sid, _, _ in entries]
+
+
+def check_views_golden():
+    with open(os.path.join(GOLDEN, "views_w2.json")) as f:
+        g2 = json.load(f)
+    c = _tiny_cache(W=2)
+    c.append(0, [[3, 2, 1]], np.ones((6, 1, 2)), np.ones((6, 1, 2)))
+    names = {c.common[0][0]: "C", c.live[0][0]: "A", c.live[0][1]: "B"}
+    assert _names_of_view(c, 0, 0, names) == g2["views"]["A"]
+    assert _names_of_view(c, 0, 1, names) == g2["views"]["B"]
+    with open(os.path.join(GOLDEN, "views_ordering_w4.json")) as f:
+        g4 = json.load(f)
+    c = _tiny_cache(W=4)
+    c.append(0, [[2, 1, 1, 1, 1]], np.ones((6, 1, 2)), np.ones((6, 1, 2)))
+    names = {c.common[0][0]: "C"}
+    names.update({c.live[0][w]: f"W{w}" for w in range(4)})
+    for w in range(4):
+        assert _names_of_view(c, 0, w, names) == g4["views"][f"W{w}"]
+
+
+def check_view_offsets_and_query_position():
+    # Append happens before attention (inference flow): the own block includes this step's
+    # token and the query is the last position of the view; offsets are running sums.
+    c = _tiny_cache(W=2)
+    c.append(0, [[5, 3, 2]], np.ones((10, 1, 2)), np.ones((10, 1, 2)))
+    entries, i_q = c.view(0, 0)
+    assert [(off, n) for _, off, n in entries] == [(0, 5), (5, 2), (7, 3)] and i_q == 9
+    entries, i_q = c.view(0, 1)
+    assert [(off, n) for _, off, n in entries] == [(0, 5), (5, 3), (8, 2)] and i_q == 9
+
+
+def check_pages_hand_example():
+    """Deterministic FIFO page allocation, worked by hand (page size 4)."""
+    c = _tiny_cache(W=2, S=4, pages=8, order=[5, 2, 7, 0, 1, 3, 4, 6])
+    z = lambda n: np.zeros((n, 1, 2))
+    c.append(0, [[5, 3, 0]], z(8), z(8))        # common j=0..4 -> 5, 2 ; w0 j=0..2 -> 7
+    c.step_end([[0, 0]])
+    t = c.tables()
+    assert [s[4] for s in t["segments"]] == [[5, 2], [7], []]
+    c.append(0, [[0, 1, 1]], z(2), z(2))        # w0 j=3: none ; w1 j=0 -> 0
+    c.step_end([[1, 0]])                        # w0 commits: its block joins the common list
+    t = c.tables()
+    assert t["common"] == [[0, 1]] and t["live"] == [[3, 2]]
+    assert [s[2] for s in t["segments"]] == [5, 4, 1, 0]
+    c.append(0, [[2, 1, 1]], z(4), z(4))        # common tail = seg1 j=4,5 -> 1 ; seg3 j=0 -> 3
+    t = c.tables()
+    assert [s[4] for s in t["segments"]] == [[5, 2], [7, 1], [0], [3]]
+    assert t["free_count"] == 2
+    e0, q0 = c.view(0, 0)
+    e1, q1 = c.view(0, 1)
+    assert [(s, o, n) for s, o, n in e0] == [(0, 0, 5), (1, 5, 6), (2, 11, 2), (3, 13, 1)] and q0 == 13
+    assert [(s, o, n) for s, o, n in e1] == [(0, 0, 5), (1, 5, 6), (3, 11, 1), (2, 12, 2)] and q1 == 13
+    c.step_end([[0, 0]])
+    c.append(0, [[9, 0, 0]], z(9), z(9))        # seg1 j=6..14: pages at j=8 -> 4, j=12 -> 6
+    c.step_end([[0, 0]])
+    c.append(0, [[1, 0, 0]], z(1), z(1))        # j=15: no new page
+    c.step_end([[0, 0]])
+    before = c.tables()
+    assert before["free_count"] == 0 and before["segments"][1][4] == [7, 1, 4, 6]
+    try:
+        c.append(0, [[1, 0, 0]], z(1), z(1))    # j=16 needs a page and none is left
+        raise AssertionError("expected OutOfPages")
+    except C.OutOfPages:
+        pass
+    assert c.tables() == before                 # a refused append changes nothing
+
+
+def check_simultaneous_commits_in_ascending_id():
+    """Workers that finish in the same step join the common history in ascending id, each
+    keeping its pages; fresh blocks get new segment ids in the same order."""
+    c = _tiny_cache(W=3, S=4, pages=16)
+    z = lambda n: np.zeros((n, 1, 2))
+    c.append(0, [[2, 1, 2, 3]], z(8), z(8))
+    c.step_end([[1, 0, 1]])
+    t = c.tables()
+    assert t["common"] == [[0, 1, 3]] and t["live"] == [[4, 2, 5]]
+    e, i_q = c.view(0, 1)
+    assert [(s, o, n) for s, o, n in e] == [(0, 0, 2), (1, 2, 1), (3, 3, 3), (2, 6, 2)] and i_q == 7
+
+
+# ----------------------------------------------------------------- worked 2-worker example
+
+
+def _two_worker_d2(k_vec):
+    """C=[c0], A=[a0], B=[b0]; D=2, H=1; q=(1,0); every raw key = k_vec.
+    Values: v_C=(1,0), v_A=(0,0), v_B=(0,1), so out reads off the softmax weights."""
+    c = _tiny_cache(W=2, S=4)
+    k = np.array([k_vec, k_vec, k_vec], dtype=np.float64).reshape(3, 1, 2)
+    v = np.array([[1.0, 0.0], [0.0, 0.0], [0.0, 1.0]]).reshape(3, 1, 2)   # order C, A, B
+    c.append(0, [[1, 1, 1]], k, v)
+    q = np.array([1.0, 0.0]).reshape(1, 1, 1, 2).repeat(2, axis=1)
+    return c, q
+
+
+def check_two_worker_hand(fn_name="method"):
+    fn = getattr(A, fn_name)
+    r2 = 1.0 / math.sqrt(2.0)
+    for k_vec, raw in (((1.0, 0.0), (math.cos(2), math.cos(1), 1.0)),
+                       ((0.0, 1.0), (math.sin(2), math.sin(1), 0.0))):
+        c, q = _two_worker_d2(k_vec)
+        out, lse = fn(c, 0, q)
+        s = [x * r2 for x in raw]                  # scores at view positions 0, 1, 2 (i_q = 2)
+        e = [math.exp(x) for x in s]
+        w = [x / sum(e) for x in e]
+        # Alice (worker 0) sees C, B, A: out = w0 v_C + w1 v_B + w2 v_A = (w0, w1)
+        assert np.allclose(out[0, 0, 0], [w[0], w[1]], atol=1e-13), (k_vec, out[0, 0, 0], w)
+        # Bob (worker 1) sees C, A, B: out = w0 v_C + w1 v_A + w2 v_B = (w0, w2)
+        assert np.allclose(out[0, 1, 0], [w[0], w[2]], atol=1e-13), (k_vec, out[0, 1, 0], w)
+        assert abs(lse[0, 0, 0] - math.log(sum(e))) < 1e-13
+
+
+# --------------------------------------------------------------- random brute vs method
+
+
+def random_session(seed, D, W, H_kv=2, G=2, S=4, steps=4, P=2, commit_p=0.5, maxlen=40):
+    """Random cache history with appends to every block and random commits.
+
+    Yields (cache, q) after each step's append (before step_end)."""
+    g = np.random.default_rng(seed)
+    c = C.HogwildCache(P, W, 1, H_kv, D, 1e4 if D <= 64 else 1e6, S, 4096,
+                       page_order=g.permutation(4096))
+    Hq = H_kv * G
+    for step in range(steps):
+        if step == 0:
+            n = g.integers(0, maxlen + 1, size=(P, W + 1))
+        else:
+            n = g.integers(0, 4, size=(P, W + 1))
+        tot = int(n.sum())
+        c.append(0, n, g.standard_normal((tot, H_kv, D)), g.standard_normal((tot, H_kv, D)))
+        q = g.standard_normal((P, W, Hq, D))
+        yield c, q
+        c.step_end((g.random((P, W)) < commit_p).astype(np.uint8))
+
+
+def check_brute_vs_method(seeds=range(6)):
+    for seed in seeds:
+        for D in (2, 4, 64):
+            W = 1 + seed % 4
+            for c, q in random_session(seed, D, W):
+                ob, lb = A.brute_force(c, 0, q)
+                om, lm = A.method(c, 0, q)
+                assert np.allclose(ob, om, rtol=0, atol=1e-10), (seed, D, np.abs(ob - om).max())
+                fin = np.isfinite(lb)
+                assert (fin == np.isfinite(lm)).all()
+                assert np.allclose(lb[fin], lm[fin], rtol=0, atol=1e-10)
+
+
+# ------------------------------------------------------------------------- closed forms
+
+
+def check_zero_keys_give_mean_values():
+    g = np.random.default_rng(13)
+    for c, q in random_session(21, 64, 3, steps=2):
+        for seg in c.segments:
+            for lst in (seg._raw_k[0], seg._stored_k[0]):
+                for a in lst:
+                    a[:] = 0.0
+            seg._cat.clear()
+        for fn in (A.brute_force, A.method):
+            out, _ = fn(c, 0, q)
+            for p in range(c.P):
+                for w in range(c.W):
+                    entries, _ = c.view(p, w)
+                    if not entries:
+                        continue
+                    v = np.concatenate([c.segments[s].raw_v(0)[:n] for s, _, n in entries])
+                    for h in range(q.shape[2]):
+                        assert np.allclose(out[p, w, h], v[:, h // 2].mean(axis=0), atol=1e-12)
+    del g
+
+
+def check_single_token_returns_its_value():
+    c = _tiny_cache(W=1, S=4, H_kv=1, D=64)
+    g = np.random.default_rng(14)
+    v = g.standard_normal((1, 1, 64))
+    c.append(0, [[0, 1]], g.standard_normal((1, 1, 64)), v)
+    for fn in (A.brute_force, A.method):
+        out, lse = fn(c, 0, g.standard_normal((1, 1, 3, 64)))
+        assert np.allclose(out[0, 0], v[0, 0], atol=1e-14)
+
+
+def check_single_worker_is_textbook_decode():
+    """W = 1: the view is the common block then the own block, i.e. ordinary RoPE decode.
+    Compare with torch's scaled_dot_product_attention on keys rotated by the complex form."""
+    import torch
+    g = np.random.default_rng(15)
+    D, H_kv, G, theta = 64, 2, 3, 1e4
+    c = C.HogwildCache(1, 1, 1, H_kv, D, theta, 8, 256)
+    k0, v0 = g.standard_normal((23, H_kv, D)), g.standard_normal((23, H_kv, D))
+    c.append(0, [[17, 6]], k0, v0)
+    c.step_end([[0]])
+    k1, v1 = g.standard_normal((1, H_kv, D)), g.standard_normal((1, H_kv, D))
+    c.append(0, [[0, 1]], k1, v1)
+    q = g.standard_normal((1, 1, H_kv * G, D))
+    kk = np.concatenate([k0, k1])
+    vv = np.concatenate([v0, v1])
+    n = kk.shape[0]
+    krot = rope_complex(kk, np.arange(n)[:, None], theta)          # [n][H_kv][D]
+    qrot = rope_complex(q[0, 0], n - 1, theta)                      # [H_q][D]
+    kt = torch.from_numpy(np.repeat(krot.transpose(1, 0, 2), G, axis=0))   # [H_q][n][D]
+    vt = torch.from_numpy(np.repeat(vv.transpose(1, 0, 2), G, axis=0))
+    qt = torch.from_numpy(qrot[:, None, :])                         # [H_q][1][D]
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt).numpy()[:, 0, :]
+    for fn in (A.brute_force, A.method):
+        out, _ = fn(c, 0, q)
+        assert np.allclose(out[0, 0], ref, atol=1e-12), np.abs(out[0, 0] - ref).max()
+
+
+def check_relabel_two_workers():
+    """Swapping the two workers' data swaps their outputs (C+B+A <-> C+A+B)."""
+    g = np.random.default_rng(16)
+    D, H_kv = 64, 1
+    kc, vc = g.standard_normal((9, H_kv, D)), g.standard_normal((9, H_kv, D))
+    ka, va = g.standard_normal((4, H_kv, D)), g.standard_normal((4, H_kv, D))
+    kb, vb = g.standard_normal((6, H_kv, D)), g.standard_normal((6, H_kv, D))
+    qa, qb = g.standard_normal((2, D)), g.standard_normal((2, D))
+    c1 = C.HogwildCache(1, 2, 1, H_kv, D, 1e4, 8, 64)
+    c1.append(0, [[9, 4, 6]], np.concatenate([kc, ka, kb]), np.concatenate([vc, va, vb]))
+    c2 = C.HogwildCache(1, 2, 1, H_kv, D, 1e4, 8, 64)
+    c2.append(0, [[9, 6, 4]], np.concatenate([kc, kb, ka]), np.concatenate([vc, vb, va]))
+    o1, _ = A.method(c1, 0, np.stack([qa, qb])[None])
+    o2, _ = A.method(c2, 0, np.stack([qb, qa])[None])
+    assert np.allclose(o1[0, 0], o2[0, 1], atol=1e-13) and np.allclose(o1[0, 1], o2[0, 0], atol=1e-13)
+
+
+ALL_CHECKS = [
+    check_rope_complex_form, check_rope_d2_textbook, check_inv_freq_values, check_rope_invariants,
+    check_views_golden, check_view_offsets_and_query_position, check_pages_hand_example,
+    check_simultaneous_commits_in_ascending_id,
+    check_two_worker_hand, check_brute_vs_method, check_zero_keys_give_mean_values,
+    check_single_token_returns_its_value, check_single_worker_is_textbook_decode,
+    check_relabel_two_workers,
+]
