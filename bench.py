@@ -1,0 +1,353 @@
+"""Benchmark of the Hogwild! concurrent-attention decode step on GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input: append one new
+token per worker (K rotated to its block-local position, bf16 into its page), the concurrent
+attention of every worker over its own view (per-block query rotation, split over KV entries,
+log-sum-exp merge), and the step end.  Default workload: 1 problem, 8 workers, H_q 64, H_kv 8,
+D 128, a 32768-token common block plus 8 worker blocks of 128..2048 tokens in a paged cache
+(page 256, seeded random physical page order).
+
+Reported (one JSON line, rank 0):
+  value  effective HBM GB/s = algorithmic bytes / device time, inputs resident in HBM, L2
+         flushed before every timed step; the algorithmic bytes count every K/V element once
+         (not once per worker), plus q, out and the appended K/V.
+  e2e    the same metric through the public API with pinned host buffers: H2D copy of the
+         step's new K/V and queries, the step, D2H copy of the outputs, all inside the timer.
+  roofline  the attention kernel's algorithmic bytes / its CUDA-event duration vs measured HBM.
+  cpu_baseline  the fp64 oracle on the host cores on a bounded sample of the same workload.
+``--impl reference`` times that oracle alone on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "concurrent-attn effective HBM GB/s (% of peak) and worker-tokens/s per step"
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def workload_for(name):
+    import workload as wl
+    return wl.CONFIGS[name]()
+
+
+def step_bytes(w, step, out_bytes=2):
+    """Algorithmic bytes of decode ``step``: K/V of every view token read once, q read, out
+    written, the appended tokens' K/V read and written."""
+    T = w.view_tokens(step)                  # all problems, after this step's append
+    kv = T * w.num_kv_heads * w.head_dim * 2 * 2
+    q = w.num_problems * w.num_workers * w.num_q_heads * w.head_dim * 2
+    out = w.num_problems * w.num_workers * w.num_q_heads * w.head_dim * out_bytes
+    app = w.num_problems * w.num_workers * w.num_kv_heads * w.head_dim * 2 * 2 * 2
+    return w.num_layers * (kv + q + out + app), w.num_layers * (kv + q)
+
+
+# ---------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.proc = None
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- oracle leg
+
+
+def oracle_sample(w, seconds=12.0, max_steps=None):
+    """Time the fp64 oracle (as it stands) on decode steps of ``w``: append + method form.
+    Returns (seconds per step, steps timed, BLAS threads)."""
+    from oracle import attention as A
+    from oracle import run as orun
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    c = orun.prefill(w)
+    times = []
+    step = 0
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        orun.append_step(c, w, step)
+        for layer in range(c.L):
+            A.method(c, layer, orun.query(w, layer, step))
+        c.step_end(__import__("workload").finished_mask(w, step))
+        times.append(time.perf_counter() - t0)
+        step += 1
+        if time.perf_counter() - t_all > seconds or (max_steps and step >= max_steps):
+            break
+    return statistics.median(times), len(times), threads
+
+
+def cpu_baseline(w, seconds=12.0):
+    import workload as wl
+    sample_w = wl.scaled(w, steps=64)
+    per_step, n, threads = oracle_sample(sample_w, seconds)
+    b, _ = step_bytes(w, 0)
+    return {"value": b / per_step / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full decode steps of {w.name} (fp64 numpy method form: append, "
+                      f"per-block query rotation, LSE merge), median {per_step * 1e3:.1f} ms/step"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workload_for(args.config)
+    per_step, n, threads = oracle_sample(w, seconds=max(10.0, 3.0 * args.steps), max_steps=None)
+    b, _ = step_bytes(w, 0)
+    v = b / per_step / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name},
+            "worker_tokens_per_s": w.num_problems * w.num_workers / per_step,
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n} decode steps of {w.name}"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- GPU leg
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import workload as wl
+    from shared_kv_concurrent_gb300 import binding
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner, to_device_bf16
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    base = workload_for(args.config)
+    e2e_steps = args.e2e_steps
+    total_steps = args.warmup + args.steps + e2e_steps
+    w = wl.scaled(base, name=base.name, steps=total_steps + 1)
+    P, W, Hq, D, L = w.num_problems, w.num_workers, w.num_q_heads, w.head_dim, w.num_layers
+    runner = WorkloadRunner(w, device=dev)
+    ctx = runner.cache.ctx
+    # Inputs of every step generated up front and resident in HBM.
+    inputs = [runner.step_inputs(s) for s in range(args.warmup + args.steps)]
+    outs = [torch.empty(P, W, Hq, D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def one_step(s, inp):
+        runner.append(inp)
+        runner.attend(inp, outs)
+
+    for s in range(args.warmup):
+        flush.zero_()
+        one_step(s, inputs[s])
+        runner.end(s)
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    binding.hw_profile_enable(ctx, True)
+    binding.hw_profile_read(ctx)                      # reset counters
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(uuid)
+    time.sleep(0.3)
+    total_bytes = 0
+    attn_bytes = 0
+    for i in range(args.steps):
+        s = args.warmup + i
+        flush.zero_()
+        starts[i].record()
+        one_step(s, inputs[s])
+        ends[i].record()
+        runner.end(s)
+        b, ab = step_bytes(w, s)
+        total_bytes += b
+        attn_bytes += ab
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    prof = binding.hw_profile_read(ctx)
+    binding.hw_profile_enable(ctx, False)
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    t_total = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([t_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_total = float(t.item())
+
+    # End to end through the public API: inputs in pinned host memory.
+    e2e = None
+    if e2e_steps:
+        host_in = []
+        for i in range(e2e_steps):
+            s = args.warmup + args.steps + i
+            k, v, q = [], [], []
+            for layer in range(L):
+                kb, vb = wl.step_kv(w, layer, s)
+                k.append(torch.from_numpy(kb.view(np.int16)).pin_memory())
+                v.append(torch.from_numpy(vb.view(np.int16)).pin_memory())
+                q.append(torch.from_numpy(wl.step_q(w, layer, s).view(np.int16)).pin_memory())
+            host_in.append((k, v, q))
+        host_out = [torch.empty(P, W, Hq, D, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+        dk = [torch.empty(P * W, w.num_kv_heads, D, dtype=torch.int16, device=dev) for _ in range(L)]
+        dv = [torch.empty_like(x) for x in dk]
+        dq = [torch.empty(P, W, Hq, D, dtype=torch.int16, device=dev) for _ in range(L)]
+        e2e_times, e2e_bytes = [], 0
+        for i in range(e2e_steps):
+            s = args.warmup + args.steps + i
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            k, v, q = host_in[i]
+            for layer in range(L):
+                dk[layer].copy_(k[layer], non_blocking=True)
+                dv[layer].copy_(v[layer], non_blocking=True)
+                dq[layer].copy_(q[layer], non_blocking=True)
+            inp = ([x.view(torch.bfloat16) for x in dk], [x.view(torch.bfloat16) for x in dv],
+                   [x.view(torch.bfloat16) for x in dq])
+            one_step(s, inp)
+            for layer in range(L):
+                host_out[layer].copy_(outs[layer], non_blocking=True)
+            torch.cuda.synchronize()
+            e2e_times.append(time.perf_counter() - t0)
+            runner.end(s)
+            e2e_bytes += step_bytes(w, s)[0]
+        h2d = sum(x.numel() * 2 for x in dk + dv + dq)
+        d2h = sum(x.numel() * 2 for x in host_out)
+        e2e = {"value": e2e_bytes / sum(e2e_times) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": 1e3 * sum(e2e_times) / e2e_steps, "steps": e2e_steps}
+
+    st, info = runner.cache.check_device_errors()
+    if st != binding.HW_OK:
+        raise RuntimeError(f"device error word set: {info}")
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = measured_peaks()
+    value = world * total_bytes / t_total / 1e9
+    attn_ms = prof["attention_ms"] / max(1, prof["timed_attention"])
+    achieved = (attn_bytes / args.steps) / (attn_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "problems": P, "workers": W, "layers": L, "H_q": Hq,
+                   "H_kv": w.num_kv_heads, "head_dim": D, "page_size": w.page_size,
+                   "common_tokens": list(w.common_len), "view_tokens_first_step":
+                   w.view_tokens(args.warmup), "parallelism": f"replicas{world}",
+                   "l2": "flushed (memset of 2x L2) before every timed step",
+                   "step": "append 1 token/worker + concurrent attention + step end"},
+        "pct_of_peak": 100.0 * value / world / peak,
+        "worker_tokens_per_s": world * P * W * args.steps / t_total,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "concurrent attention (split-K partials)",
+                     "kernel_ms": attn_ms,
+                     "algorithmic_bytes_per_launch": attn_bytes / args.steps},
+        "gpu_launches": int(prof["launches"]),
+        "clocks": clk,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(base, seconds=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c4")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,210 @@
+/*
+ * hogwild.h -- C ABI of the GB300 concurrent-attention library (libhogwild.so).
+ *
+ * The method is Hogwild! Inference ("Parallel LLM Generation via Concurrent Attention";
+ * summary at gentlecold.top, cited below by section).  W workers decode in parallel and share
+ * one KV cache made of blocks: a common block (prompt and finished paragraphs) and one
+ * current block per worker (section 6; section 9 "the Hogwild! cache is split into blocks").
+ * Every block stores K/V of all layers at block-local positions 0 .. len-1 (section 9).  Worker
+ * w attends over the common history, then the other workers' current blocks, then its own
+ * block last (sections 4 and 6); instead of re-rotating stored keys, the query is rotated once
+ * per block by (query position - the block's offset in w's view) (section 5, the identity
+ * rho(q,i_q)[rho(A,i_A) (+) ...] = [rho(q,i_q - i_A) A (+) ...]).  A step appends each worker's
+ * new token, attends, and at the end of a paragraph moves the worker's block to the end of the
+ * common history (section 8, inference flow).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - P problems, W workers, L layers, H_q query heads, H_kv KV heads (G = H_q / H_kv; query head
+ *   h reads KV head h / G), head dimension D in {64, 128}, page size S (a multiple of 128).
+ * - All tensors are dense, row-major, and bf16 unless stated otherwise.
+ * - "device" pointers are CUDA device memory of the current device; "host" pointers are CPU
+ *   memory.  The caller owns every buffer: the library never allocates device memory (its
+ *   tables live inside the caller's workspace), it only creates host-side state, pinned
+ *   staging buffers, events and one TMA descriptor per layer.
+ * - ``stream`` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All work
+ *   is enqueued asynchronously on it.  A context is not thread-safe: use one host thread at a
+ *   time per context.
+ * - RoPE: half-split pairs (x_i, x_{i+D/2}) rotated by p * theta^(-2i/D).  The cos/sin table
+ *   is computed on the host in fp64 and stored as fp32.
+ * - Errors: arguments are validated on the host before anything is enqueued; on an error
+ *   nothing is enqueued and the state is unchanged.  Kernels never trap: an index that fails a
+ *   device-side range check is skipped and recorded in a device error word that
+ *   hw_check_device_errors() reads back.
+ */
+#ifndef HOGWILD_H_
+#define HOGWILD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum hw_status {
+  HW_OK = 0,
+  HW_ERR_INVALID_ARG = 1,     /* null pointer, bad size or shape, protocol misuse */
+  HW_ERR_OUT_OF_PAGES = 2,    /* the page pool cannot hold this append */
+  HW_ERR_CAPACITY = 3,        /* a table (segments, positions, workspace) would overflow */
+  HW_ERR_CUDA = 4,            /* a CUDA runtime call failed (see hw_last_cuda_error) */
+  HW_ERR_DEVICE_CHECK = 5,    /* a kernel's range check fired (hw_check_device_errors) */
+  HW_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device wait gave up (hw_check_device_errors) */
+  HW_ERR_UNSUPPORTED = 7      /* shape or device this build does not handle */
+} hw_status;
+
+enum { HW_OUT_BF16 = 0, HW_OUT_F32 = 1 };
+
+typedef struct hw_config {
+  int32_t num_problems;      /* P >= 1 independent Hogwild! problems */
+  int32_t num_workers;       /* W >= 1 workers per problem */
+  int32_t num_layers;        /* L >= 1; each layer has its own pages in the pools */
+  int32_t num_q_heads;       /* H_q, a multiple of H_kv */
+  int32_t num_kv_heads;      /* H_kv >= 1 */
+  int32_t head_dim;          /* D: 64 or 128 */
+  int32_t page_size;         /* S: tokens per page, a multiple of 128 */
+  int32_t contiguous;        /* 0: paged blocks; 1: each block is one page of S tokens */
+  int32_t num_pages;         /* pages per layer */
+  int32_t max_position;      /* exceeds every view length; rows of the RoPE table */
+  int32_t max_segments;      /* segment capacity over all problems (0: P * (1 + 4W)) */
+  int32_t max_append_tokens; /* largest sum of n_new in one append (0: num_pages * S) */
+  double rope_theta;         /* RoPE base */
+} hw_config;
+
+typedef struct hw_ctx hw_ctx;
+
+/* Human-readable name of a status code (static storage). */
+const char* hw_status_string(hw_status s);
+
+/* Last CUDA error code and message seen by a call that returned HW_ERR_CUDA (per process). */
+int32_t hw_last_cuda_error(const char** message);
+
+/*
+ * Bytes of ONE pool (the K pool or the V pool) for cfg: L * num_pages * H_kv * S * D bf16.
+ * Layout of a pool: [L][num_pages][H_kv][S][D]; a page holds S consecutive block-local
+ * positions of one block, for every KV head (section 9: blocks hold every layer's K/V).
+ */
+hw_status hw_pool_size(const hw_config* cfg, size_t* bytes);
+
+/* Bytes of device workspace hw_create() needs for cfg (tables, RoPE table, partials). */
+hw_status hw_workspace_size(const hw_config* cfg, size_t* bytes);
+
+/*
+ * Create a context over caller-owned device buffers.
+ *   k_pool, v_pool: device, hw_pool_size() bytes each, 256-byte aligned; zero-filled here.
+ *   workspace:      device, >= hw_workspace_size() bytes, 256-byte aligned.
+ *   page_order:     host int32[num_pages] (a permutation of 0..num_pages-1) giving the order
+ *                   in which physical pages are handed out, or NULL for 0, 1, 2, ...
+ * Each problem starts with an empty common block and W empty worker blocks (segment ids:
+ * per problem, the common block then workers 0..W-1).  Blocks until the set-up copies are
+ * done.  *out receives the handle; release it with hw_destroy().
+ */
+hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* workspace,
+                    size_t workspace_bytes, const int32_t* page_order, void* stream,
+                    hw_ctx** out);
+
+/* Release the host-side state (never the caller's device buffers).  NULL is a no-op. */
+void hw_destroy(hw_ctx* ctx);
+
+/*
+ * Append new tokens' K/V of one layer (section 8: each worker appends its token's K/V to its
+ * own block before attention; section 9: block-local positions).
+ *   n_new: host int32[P][W + 1]; n_new[p][0] tokens go to problem p's common block (the last
+ *          common segment), n_new[p][1 + w] to worker w's current block.
+ *   k_raw, v_raw: device bf16 [sum n_new][H_kv][D], UNROTATED keys and values, ordered
+ *          problem-major, then block 0 (common), 1..W, each in position order.
+ * Key token j of a block is stored as bf16(rho(k, j)) at (page_of(j), j mod S); values are
+ * copied.  The first append of a step allocates pages (FIFO from page_order; problems in
+ * order, then the common block, then workers in ascending id; a new page whenever j mod S == 0;
+ * in contiguous mode one page at j == 0).  Every layer must append once per step with the same
+ * n_new.  Attention in the step sees the appended tokens; lengths advance at hw_step_end().
+ * Errors: HW_ERR_INVALID_ARG (bad layer, counts differing from the step's first append, layer
+ * appended twice), HW_ERR_OUT_OF_PAGES, HW_ERR_CAPACITY (contiguous block full).
+ */
+hw_status hw_append_kv(hw_ctx* ctx, int32_t layer, const int32_t* n_new, const void* k_raw,
+                       const void* v_raw, void* stream);
+
+/*
+ * Concurrent attention of one layer (sections 5 and 9).
+ *   q:   device bf16 [P][W][H_q][D], UNROTATED queries (one token per worker).
+ *   out: device [P][W][H_q][D], bf16 (out_dtype HW_OUT_BF16) or fp32 (HW_OUT_F32).
+ *   lse: device fp32 [P][W][H_q] or NULL: natural-log log-sum-exp of the scaled scores.
+ * For worker w of problem p the view is [common segments in commit order] ++ [other workers'
+ * blocks, ascending id] ++ [own block]; empty blocks are skipped; i_q = view length - 1.  Each
+ * block at view offset o is attended with the query rotated by (i_q - o), scores scaled by
+ * 1/sqrt(D), and the per-block softmax partials merged by log-sum-exp.  An empty view gives
+ * out = 0 and lse = -inf.  Requires that, if the current step appended tokens, this layer
+ * has been appended (HW_ERR_INVALID_ARG otherwise).  Scratch: partial results live in the
+ * workspace; calls on one context must not overlap on the GPU (use one stream).
+ */
+hw_status hw_concurrent_attention(hw_ctx* ctx, int32_t layer, const void* q, void* out,
+                                  int32_t out_dtype, float* lse, void* stream);
+
+/*
+ * End the step (section 8): every block's length grows by the tokens appended in this step;
+ * then, for each problem and each worker in ascending id with finished[p][w] != 0 and a
+ * non-empty block, the worker's block is moved, unchanged, to the end of the common history
+ * and the worker starts a new empty block (new segment id).  No K/V byte moves and nothing is
+ * re-rotated: the new view offset is absorbed by the query rotation.
+ *   finished: host uint8[P][W] or NULL (no commits).
+ * Errors: HW_ERR_INVALID_ARG if the step appended some but not all layers; HW_ERR_CAPACITY
+ * if the segment table is full.  Enqueues nothing on the GPU.
+ */
+hw_status hw_step_end(hw_ctx* ctx, const uint8_t* finished, void* stream);
+
+/*
+ * Synchronise ``stream`` and read the device error word.  Returns HW_OK, or
+ * HW_ERR_DEVICE_CHECK / HW_ERR_DEVICE_TIMEOUT if a kernel recorded one (the word is then
+ * cleared).  info: host uint32[4] or NULL: {code, kernel id, detail a, detail b}.
+ */
+hw_status hw_check_device_errors(hw_ctx* ctx, void* stream, uint32_t* info);
+
+/* ---- measurement ------------------------------------------------------------------------ */
+
+typedef struct hw_profile {
+  int64_t launches;          /* kernels this context launched since the last read */
+  int64_t attention_launches;
+  int64_t append_launches;
+  double attention_ms;       /* summed CUDA-event time of the attention kernels (enabled only) */
+  double append_ms;          /* summed CUDA-event time of the append kernels (enabled only) */
+  int64_t timed_attention;   /* how many attention launches attention_ms covers */
+  int64_t timed_append;
+} hw_profile;
+
+/*
+ * Turn kernel timing on or off.  When on, every attention and append call records a pair of
+ * CUDA events on its stream directly around its main kernel (up to 4096 pairs per read).
+ * Launch counting is always on.
+ */
+hw_status hw_profile_enable(hw_ctx* ctx, int32_t enable);
+
+/* Synchronise the recorded events, sum their elapsed times, fill *out and reset. */
+hw_status hw_profile_read(hw_ctx* ctx, hw_profile* out);
+
+/* ---- read-back of the host tables (tests; bit-exact comparison with the oracle) ---------- */
+
+/* Number of segments created so far and pages still free. */
+hw_status hw_get_counts(const hw_ctx* ctx, int32_t* num_segments, int32_t* free_pages);
+
+/* One segment: problem, origin worker (-1 for the prompt), committed length, tokens pending
+ * in the current step, and its physical pages (pages_out: host int32[pages_cap]). */
+hw_status hw_get_segment(const hw_ctx* ctx, int32_t seg, int32_t* problem, int32_t* origin,
+                         int32_t* length, int32_t* pending, int32_t* num_pages,
+                         int32_t* pages_out, int32_t pages_cap);
+
+/* Problem p's common segment ids in commit order (host int32[cap]) and the W current-block
+ * segment ids (host int32[W]). */
+hw_status hw_get_blocks(const hw_ctx* ctx, int32_t problem, int32_t* common_ids, int32_t cap,
+                        int32_t* num_common, int32_t* live_ids);
+
+/* Worker w's view as the attention call will see it: segment ids, view offsets and visible
+ * lengths (host int32[cap] each), the entry count and i_q. */
+hw_status hw_get_view(const hw_ctx* ctx, int32_t problem, int32_t worker, int32_t* seg_ids,
+                      int32_t* view_offsets, int32_t* lengths, int32_t cap, int32_t* n,
+                      int32_t* i_q);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HOGWILD_H_ */

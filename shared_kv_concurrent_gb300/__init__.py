@@ -1,0 +1,106 @@
+"""GB300-native concurrent attention for Hogwild! Inference.
+
+The computation lives in ``libhogwild.so`` (C ABI: ``include/hogwild.h``; CUDA kernels for
+sm_103a under ``csrc/``).  ``binding`` is a thin ctypes layer with the same names as the C
+entry points; ``HogwildCache`` below only owns the device buffers (allocated with torch) and
+forwards every call to the library.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+
+from . import binding
+from .binding import (HW_OUT_BF16, HW_OUT_F32, HogwildError, hw_config)
+
+__all__ = ["HogwildCache", "HogwildError", "binding", "config_for"]
+
+
+def config_for(*, num_problems, num_workers, num_layers, num_q_heads, num_kv_heads, head_dim,
+               page_size, num_pages, max_position, rope_theta, contiguous=False,
+               max_segments=0, max_append_tokens=0) -> hw_config:
+    return hw_config(num_problems, num_workers, num_layers, num_q_heads, num_kv_heads, head_dim,
+                     page_size, int(bool(contiguous)), num_pages, max_position, max_segments,
+                     max_append_tokens, float(rope_theta))
+
+
+class HogwildCache:
+    """One library context plus the torch-owned pools and workspace it runs on."""
+
+    def __init__(self, cfg: hw_config, page_order=None, device="cuda"):
+        import torch
+        self.cfg = cfg
+        self.device = torch.device(device)
+        pool_bytes = binding.hw_pool_size(cfg)
+        ws_bytes = binding.hw_workspace_size(cfg)
+        self.k_pool = torch.empty(pool_bytes // 2, dtype=torch.bfloat16, device=self.device)
+        self.v_pool = torch.empty(pool_bytes // 2, dtype=torch.bfloat16, device=self.device)
+        self.workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device)
+        self.ctx = binding.hw_create(cfg, self.k_pool, self.v_pool, self.workspace, page_order)
+
+    @classmethod
+    def from_workload(cls, w, max_segments: int = 0, device="cuda") -> "HogwildCache":
+        cfg = config_for(num_problems=w.num_problems, num_workers=w.num_workers,
+                         num_layers=w.num_layers, num_q_heads=w.num_q_heads,
+                         num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                         page_size=w.page_size, num_pages=w.num_pages(),
+                         max_position=w.max_position(), rope_theta=w.rope_theta,
+                         contiguous=w.contiguous, max_segments=max_segments)
+        return cls(cfg, page_order=w.page_order(), device=device)
+
+    # -- the step protocol ---------------------------------------------------------------
+
+    def append_kv(self, layer: int, n_new, k_raw, v_raw, stream=None) -> None:
+        binding.hw_append_kv(self.ctx, layer, n_new, k_raw, v_raw, stream)
+
+    def concurrent_attention(self, layer: int, q, out=None, out_dtype: str = "bf16", lse=None,
+                             stream=None):
+        import torch
+        dt = HW_OUT_F32 if out_dtype == "f32" else HW_OUT_BF16
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32 if dt == HW_OUT_F32 else torch.bfloat16,
+                              device=q.device)
+        binding.hw_concurrent_attention(self.ctx, layer, q, out, dt, lse, stream)
+        return out
+
+    def step_end(self, finished=None, stream=None) -> None:
+        binding.hw_step_end(self.ctx, finished, stream)
+
+    def check_device_errors(self, stream=None):
+        return binding.hw_check_device_errors(self.ctx, stream)
+
+    # -- read-back ----------------------------------------------------------------------
+
+    def tables(self) -> dict:
+        nseg, free = binding.hw_get_counts(self.ctx)
+        segs = [tuple(binding.hw_get_segment(self.ctx, s)) for s in range(nseg)]
+        common, live = [], []
+        for p in range(self.cfg.num_problems):
+            c, l = binding.hw_get_blocks(self.ctx, p, self.cfg.num_workers)
+            common.append(c)
+            live.append(l)
+        return {"segments": [(a, b, c, d, list(e)) for a, b, c, d, e in segs],
+                "common": common, "live": live, "free_count": free}
+
+    def view(self, p: int, w: int):
+        return binding.hw_get_view(self.ctx, p, w)
+
+    def pools(self, layer: int):
+        """K and V pools of one layer as [num_pages][H_kv][S][D] bf16 tensors (views)."""
+        c = self.cfg
+        n = c.num_pages * c.num_kv_heads * c.page_size * c.head_dim
+        shape = (c.num_pages, c.num_kv_heads, c.page_size, c.head_dim)
+        return (self.k_pool[layer * n:(layer + 1) * n].view(shape),
+                self.v_pool[layer * n:(layer + 1) * n].view(shape))
+
+    def close(self) -> None:
+        if getattr(self, "ctx", None):
+            binding.hw_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,208 @@
+// K2 (FMA form) and K3 -- concurrent attention with per-(worker, block) query rotation, and
+// the log-sum-exp merge of the per-unit partial results.
+//
+// Method (Hogwild! Inference summary, gentlecold.top): keys are stored rotated at block-local
+// positions; for a block at offset o in worker w's view the query is rotated by (i_q - o)
+// (section 5), so one KV tile serves every worker and every query head of its GQA group, each
+// with its own rotated query.  Work is split over KV entries, not over blocks, and the partial
+// results are reduced afterwards (section 9, Flash-Decoding style kernel).
+//
+// This form uses FP32 FMA and is meant for small row counts (W * G below a 16-row tile); one
+// CTA per unit (a run of pieces of one (problem, KV head)), 8 warps, each warp owning rows
+// r = warp, warp + 8, ...; lane = token of a 32-token tile staged in shared memory.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "hw_device.cuh"
+
+namespace hw {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTile = 32;
+constexpr int kMaxRowsPerWarp = 16;   // rows <= 128
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
+  extern __shared__ float sm[];
+  constexpr int DJ = D / 32;
+  constexpr int KS = D + 1;                     // padded key row: conflict-free lane = token
+  const int rows = a.rows;
+  float* qs = sm;                               // [rows][D] rotated, pre-scaled queries
+  float* ks = qs + rows * D;                    // [kTile][D + 1]
+  float* vs = ks + kTile * KS;                  // [kTile][D]
+  const Unit u = a.units[blockIdx.x];
+  const Group g = a.groups[u.group];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  float m[kMaxRowsPerWarp], l[kMaxRowsPerWarp], o[kMaxRowsPerWarp][DJ];
+#pragma unroll
+  for (int k = 0; k < kMaxRowsPerWarp; ++k) {
+    m[k] = -CUDART_INF_F;
+    l[k] = 0.f;
+#pragma unroll
+    for (int j = 0; j < DJ; ++j) o[k][j] = 0.f;
+  }
+
+  int cur_slot = -1;
+  for (int pi = u.piece_begin; pi < u.piece_end; ++pi) {
+    const Piece pc = a.pieces[pi];
+    if (pc.page < 0 || pc.page >= a.num_pages || pc.slot0 < 0 || pc.ntok < 1 ||
+        pc.slot0 + pc.ntok > a.S || pc.seg_slot < 0 || pc.seg_slot >= a.num_seg_slots) {
+      if (threadIdx.x == 0) record_error(a.err, ERR_PLAN, KID_ATTN_FMA, blockIdx.x, pi);
+      continue;
+    }
+    const int* dl = a.delta + (size_t)pc.seg_slot * a.W;
+    if (pc.seg_slot != cur_slot) {
+      // New segment: rotate every row's query by (i_q - view offset) of this segment.
+      __syncthreads();
+      const int half = D / 2;
+      for (int idx = threadIdx.x; idx < rows * half; idx += kThreads) {
+        const int r = idx / half, i = idx % half;
+        const int w = r / a.G, hq = g.h * a.G + r % a.G;
+        const int delta = dl[w];
+        float y1 = 0.f, y2 = 0.f;
+        if (delta >= 0 && delta < a.max_position) {
+          const size_t qo = (((size_t)g.p * a.W + w) * a.H_q + hq) * D;
+          const float q1 = __bfloat162float(a.q[qo + i]);
+          const float q2 = __bfloat162float(a.q[qo + i + half]);
+          const float c = a.rope_cos[(size_t)delta * half + i];
+          const float s = a.rope_sin[(size_t)delta * half + i];
+          y1 = (q1 * c - q2 * s) * a.scale_log2;
+          y2 = (q2 * c + q1 * s) * a.scale_log2;
+        } else if (delta >= a.max_position && i == 0) {
+          record_error(a.err, ERR_POS_RANGE, KID_ATTN_FMA, blockIdx.x, delta);
+        }
+        qs[r * D + i] = y1;
+        qs[r * D + i + half] = y2;
+      }
+      cur_slot = pc.seg_slot;
+    }
+    const size_t base = (((size_t)pc.page * a.H_kv + g.h) * a.S + pc.slot0) * D;
+    for (int t0 = 0; t0 < pc.ntok; t0 += kTile) {
+      const int nt = min(kTile, pc.ntok - t0);
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < kTile * (D / 8); idx += kThreads) {
+        const int tok = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
+        uint4 kr = make_uint4(0, 0, 0, 0), vr = make_uint4(0, 0, 0, 0);
+        if (tok < nt) {
+          kr = *reinterpret_cast<const uint4*>(a.k_layer + base + (size_t)(t0 + tok) * D + c8);
+          vr = *reinterpret_cast<const uint4*>(a.v_layer + base + (size_t)(t0 + tok) * D + c8);
+        }
+        const __nv_bfloat162* kp = reinterpret_cast<const __nv_bfloat162*>(&kr);
+        const __nv_bfloat162* vp = reinterpret_cast<const __nv_bfloat162*>(&vr);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 kf = __bfloat1622float2(kp[j]);
+          const float2 vf = __bfloat1622float2(vp[j]);
+          ks[tok * KS + c8 + 2 * j] = kf.x;
+          ks[tok * KS + c8 + 2 * j + 1] = kf.y;
+          vs[tok * D + c8 + 2 * j] = vf.x;
+          vs[tok * D + c8 + 2 * j + 1] = vf.y;
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < kMaxRowsPerWarp; ++k) {
+        const int r = warp + k * kWarps;
+        if (r >= rows) continue;
+        if (dl[r / a.G] < 0) continue;              // this worker does not see the segment
+        const float* qr = qs + r * D;
+        const float* kr = ks + lane * KS;
+        float s = 0.f;
+#pragma unroll 16
+        for (int d = 0; d < D; ++d) s = fmaf(qr[d], kr[d], s);
+        if (lane >= nt) s = -CUDART_INF_F;
+        float tmax = s;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+        const float mn = fmaxf(m[k], tmax);
+        const float alpha = exp2f(m[k] - mn);
+        const float p = exp2f(s - mn);
+        float ps = p;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+        l[k] = l[k] * alpha + ps;
+#pragma unroll
+        for (int j = 0; j < DJ; ++j) o[k][j] *= alpha;
+        for (int t = 0; t < nt; ++t) {
+          const float pt = __shfl_sync(0xffffffffu, p, t);
+#pragma unroll
+          for (int j = 0; j < DJ; ++j) o[k][j] = fmaf(pt, vs[t * D + lane + 32 * j], o[k][j]);
+        }
+        m[k] = mn;
+      }
+    }
+  }
+  // Partial result of this unit: o (unnormalised), m, l in the log2 domain.
+#pragma unroll
+  for (int k = 0; k < kMaxRowsPerWarp; ++k) {
+    const int r = warp + k * kWarps;
+    if (r >= rows) continue;
+    float* part = a.partials + ((size_t)blockIdx.x * rows + r) * (D + 2);
+#pragma unroll
+    for (int j = 0; j < DJ; ++j) part[lane + 32 * j] = o[k][j];
+    if (lane == 0) {
+      part[D] = m[k];
+      part[D + 1] = l[k];
+    }
+  }
+}
+
+// K3: out = sum_u o_u 2^(m_u - M) / sum_u l_u 2^(m_u - M), M = max_u m_u; lse = (M + log2 L) ln 2.
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(const AttnArgs a) {
+  const Group g = a.groups[blockIdx.x];
+  constexpr int RPB = 256 / D;                  // rows handled side by side
+  const int d = threadIdx.x % D;
+  for (int r = threadIdx.x / D; r < a.rows; r += RPB) {
+    float M = -CUDART_INF_F;
+    for (int u = g.unit_begin; u < g.unit_end; ++u)
+      M = fmaxf(M, a.partials[((size_t)u * a.rows + r) * (D + 2) + D]);
+    float L = 0.f, O = 0.f;
+    if (M != -CUDART_INF_F) {
+      for (int u = g.unit_begin; u < g.unit_end; ++u) {
+        const float* part = a.partials + ((size_t)u * a.rows + r) * (D + 2);
+        const float sc = exp2f(part[D] - M);
+        L = fmaf(part[D + 1], sc, L);
+        O = fmaf(part[d], sc, O);
+      }
+    }
+    const float res = (L > 0.f) ? O / L : 0.f;
+    const int w = r / a.G, hq = g.h * a.G + r % a.G;
+    const size_t oi = ((size_t)g.p * a.W + w) * a.H_q + hq;
+    if (a.out_f32)
+      reinterpret_cast<float*>(a.out)[oi * D + d] = res;
+    else
+      reinterpret_cast<__nv_bfloat16*>(a.out)[oi * D + d] = __float2bfloat16_rn(res);
+    if (a.lse && d == 0) a.lse[oi] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+  }
+}
+
+template <int D>
+void launch_fma_d(const AttnArgs& a, cudaStream_t s) {
+  const size_t smem = ((size_t)a.rows * D + kTile * (D + 1) + kTile * D) * sizeof(float);
+  cudaFuncSetAttribute(attn_fma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  attn_fma_kernel<D><<<a.num_units, kThreads, smem, s>>>(a);
+}
+
+}  // namespace
+
+void launch_attention_fma(const AttnArgs& a, cudaStream_t s) {
+  if (a.num_units <= 0) return;
+  if (a.D == 64)
+    launch_fma_d<64>(a, s);
+  else
+    launch_fma_d<128>(a, s);
+}
+
+void launch_merge(const AttnArgs& a, cudaStream_t s) {
+  if (a.num_groups <= 0) return;
+  if (a.D == 64)
+    merge_kernel<64><<<a.num_groups, 256, 0, s>>>(a);
+  else
+    merge_kernel<128><<<a.num_groups, 256, 0, s>>>(a);
+}
+
+}  // namespace hw

@@ -1,0 +1,752 @@
+// Host side of libhogwild: argument checking, the cache's host tables (segments, page
+// allocator, commits), per-call plans and kernel launches.  See include/hogwild.h for the
+// contract of every entry point.
+//
+// The cache model is Hogwild! Inference's (summary at gentlecold.top): a common block plus one
+// current block per worker, K/V at block-local positions (section 9); views common ++ other
+// workers ascending ++ own (sections 4 and 6); append before attention and paragraph commits
+// at step end (section 8).  The host is the single owner of the tables: it knows how many
+// tokens every call appends, so no call ever reads state back from the GPU.
+#include "hogwild.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <deque>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "hw_internal.h"
+
+namespace {
+
+constexpr int kSlots = 8;              // pinned staging / device plan slots in flight
+constexpr size_t kAlign = 256;
+constexpr int kPieceMax = 256;         // tokens per piece (never crosses a page)
+constexpr int kProfPairs = 4096;       // timed launches kept per hw_profile_read
+
+thread_local int g_cuda_err = 0;
+std::mutex g_msg_mu;
+std::string g_cuda_msg;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+hw_status cuda_fail(cudaError_t e) {
+  g_cuda_err = (int)e;
+  std::lock_guard<std::mutex> lk(g_msg_mu);
+  g_cuda_msg = cudaGetErrorString(e);
+  return HW_ERR_CUDA;
+}
+
+#define HW_CUDA(call)                              \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_);   \
+  } while (0)
+
+struct Layout {
+  size_t err, cos, sin, slots, partials, tickets, total;
+  size_t slot_bytes;
+  int32_t max_segments, max_append, max_pieces, max_units, max_seg_slots, rows;
+};
+
+bool valid_config(const hw_config* c) {
+  if (!c) return false;
+  if (c->num_problems < 1 || c->num_workers < 1 || c->num_layers < 1) return false;
+  if (c->num_kv_heads < 1 || c->num_q_heads < c->num_kv_heads) return false;
+  if (c->num_q_heads % c->num_kv_heads) return false;
+  if (c->head_dim != 64 && c->head_dim != 128) return false;
+  if (c->page_size < 128 || c->page_size % 128) return false;
+  if (c->contiguous != 0 && c->contiguous != 1) return false;
+  if (c->num_pages < 1 || c->max_position < 1) return false;
+  if (c->max_segments < 0 || c->max_append_tokens < 0) return false;
+  if (!(c->rope_theta > 1.0) || !std::isfinite(c->rope_theta)) return false;
+  const int64_t rows = (int64_t)c->num_workers * (c->num_q_heads / c->num_kv_heads);
+  if (rows > 128) return false;
+  const int64_t pool_tokens = (int64_t)c->num_pages * c->page_size;
+  if (pool_tokens > (1ll << 30) || c->max_position > (1 << 26)) return false;
+  return true;
+}
+
+Layout make_layout(const hw_config* c) {
+  Layout L{};
+  const int64_t P = c->num_problems, W = c->num_workers, H = c->num_kv_heads;
+  L.rows = (int32_t)(W * (c->num_q_heads / c->num_kv_heads));
+  L.max_segments = c->max_segments ? c->max_segments : (int32_t)(P * (1 + 4 * W));
+  const int64_t pool_tokens = (int64_t)c->num_pages * c->page_size;
+  L.max_append = c->max_append_tokens ? c->max_append_tokens : (int32_t)pool_tokens;
+  // every visible token sits in a page: pieces <= H * (pool_tokens / 256 + one per segment)
+  L.max_pieces = (int32_t)(H * (pool_tokens / kPieceMax + L.max_segments + 1));
+  L.max_units = (int32_t)(P * H + 2048);
+  L.max_seg_slots = L.max_segments;
+  const size_t runs = (size_t)P * (W + 1) + (size_t)L.max_append / 128 + 2;
+  const size_t append_bytes = runs * sizeof(hw::AppendRun);
+  const size_t attn_bytes = align_up((size_t)L.max_pieces * sizeof(hw::Piece), 16) +
+                            align_up((size_t)L.max_units * sizeof(hw::Unit), 16) +
+                            align_up((size_t)P * H * sizeof(hw::Group), 16) +
+                            align_up((size_t)L.max_seg_slots * W * sizeof(int32_t), 16);
+  L.slot_bytes = align_up(std::max(append_bytes, attn_bytes), kAlign);
+  size_t off = 0;
+  L.err = off;
+  off += kAlign;
+  const size_t tab = align_up((size_t)c->max_position * (c->head_dim / 2) * sizeof(float), kAlign);
+  L.cos = off;
+  off += tab;
+  L.sin = off;
+  off += tab;
+  L.slots = off;
+  off += kSlots * L.slot_bytes;
+  L.partials = off;
+  off += align_up((size_t)L.max_units * L.rows * (c->head_dim + 2) * sizeof(float), kAlign);
+  L.tickets = off;
+  off += align_up((size_t)P * H * sizeof(uint32_t), kAlign);
+  L.total = off;
+  return L;
+}
+
+struct Seg {
+  int32_t problem, origin, length, pending;
+  std::vector<int32_t> pages;
+  int32_t visible() const { return length + pending; }
+};
+
+}  // namespace
+
+struct hw_ctx {
+  hw_config cfg{};
+  Layout lay{};
+  int32_t G = 0, rows = 0, num_sms = 0;
+  __nv_bfloat16* k_pool = nullptr;
+  __nv_bfloat16* v_pool = nullptr;
+  char* ws = nullptr;
+  size_t layer_elems = 0;
+  char* h_slots = nullptr;                 // pinned staging, kSlots * slot_bytes
+  cudaEvent_t slot_ev[kSlots] = {};
+  bool slot_used[kSlots] = {};
+  int next_slot = 0;
+  std::deque<int32_t> free_pages;
+  std::vector<Seg> segs;
+  std::vector<std::vector<int32_t>> common, live;
+  bool step_active = false;
+  std::vector<int32_t> step_n;
+  std::vector<uint8_t> appended;
+  // measurement
+  bool prof_on = false;
+  int64_t n_launch = 0, n_attn = 0, n_append = 0;
+  std::vector<cudaEvent_t> prof_ev;       // 2 * kProfPairs, created on first enable
+  std::vector<int8_t> prof_kind;          // 0 = attention, 1 = append, per recorded pair
+  int prof_next = 0;
+
+  // Record the opening event of a timed launch; returns the pair index or -1.
+  int prof_begin(cudaStream_t s, int8_t kind) {
+    if (!prof_on || prof_next >= kProfPairs) return -1;
+    const int i = prof_next++;
+    prof_kind[i] = kind;
+    cudaEventRecord(prof_ev[2 * i], s);
+    return i;
+  }
+  void prof_end(int i, cudaStream_t s) {
+    if (i >= 0) cudaEventRecord(prof_ev[2 * i + 1], s);
+  }
+
+  uint32_t* d_err() const { return reinterpret_cast<uint32_t*>(ws + lay.err); }
+  float* d_cos() const { return reinterpret_cast<float*>(ws + lay.cos); }
+  float* d_sin() const { return reinterpret_cast<float*>(ws + lay.sin); }
+  float* d_partials() const { return reinterpret_cast<float*>(ws + lay.partials); }
+  char* d_slot(int i) const { return ws + lay.slots + (size_t)i * lay.slot_bytes; }
+  char* h_slot(int i) const { return h_slots + (size_t)i * lay.slot_bytes; }
+
+  int32_t new_segment(int32_t p, int32_t origin) {
+    segs.push_back(Seg{p, origin, 0, 0, {}});
+    return (int32_t)segs.size() - 1;
+  }
+  Seg& block(int32_t p, int32_t b) {
+    return segs[b == 0 ? common[p].back() : live[p][b - 1]];
+  }
+  // Worker w's view: (segment, offset, visible length); returns i_q.
+  int32_t view(int32_t p, int32_t w, std::vector<int32_t>* ids, std::vector<int32_t>* offs,
+               std::vector<int32_t>* lens) const {
+    int32_t off = 0;
+    auto add = [&](int32_t sid) {
+      const int32_t n = segs[sid].visible();
+      if (n == 0) return;
+      ids->push_back(sid);
+      offs->push_back(off);
+      lens->push_back(n);
+      off += n;
+    };
+    for (int32_t sid : common[p]) add(sid);
+    for (int32_t u = 0; u < cfg.num_workers; ++u)
+      if (u != w) add(live[p][u]);
+    add(live[p][w]);
+    return off - 1;
+  }
+  // Pick the next staging slot; waits only if the slot's previous use is still in flight.
+  hw_status acquire_slot(int* slot) {
+    const int i = next_slot;
+    next_slot = (next_slot + 1) % kSlots;
+    if (slot_used[i]) HW_CUDA(cudaEventSynchronize(slot_ev[i]));
+    *slot = i;
+    return HW_OK;
+  }
+};
+
+extern "C" {
+
+const char* hw_status_string(hw_status s) {
+  switch (s) {
+    case HW_OK: return "HW_OK";
+    case HW_ERR_INVALID_ARG: return "HW_ERR_INVALID_ARG";
+    case HW_ERR_OUT_OF_PAGES: return "HW_ERR_OUT_OF_PAGES";
+    case HW_ERR_CAPACITY: return "HW_ERR_CAPACITY";
+    case HW_ERR_CUDA: return "HW_ERR_CUDA";
+    case HW_ERR_DEVICE_CHECK: return "HW_ERR_DEVICE_CHECK";
+    case HW_ERR_DEVICE_TIMEOUT: return "HW_ERR_DEVICE_TIMEOUT";
+    case HW_ERR_UNSUPPORTED: return "HW_ERR_UNSUPPORTED";
+  }
+  return "HW_ERR_UNKNOWN";
+}
+
+int32_t hw_last_cuda_error(const char** message) {
+  if (message) {
+    std::lock_guard<std::mutex> lk(g_msg_mu);
+    *message = g_cuda_msg.c_str();
+  }
+  return g_cuda_err;
+}
+
+hw_status hw_pool_size(const hw_config* cfg, size_t* bytes) {
+  if (!valid_config(cfg) || !bytes) return HW_ERR_INVALID_ARG;
+  *bytes = (size_t)cfg->num_layers * cfg->num_pages * cfg->num_kv_heads * cfg->page_size *
+           cfg->head_dim * sizeof(__nv_bfloat16);
+  return HW_OK;
+}
+
+hw_status hw_workspace_size(const hw_config* cfg, size_t* bytes) {
+  if (!valid_config(cfg) || !bytes) return HW_ERR_INVALID_ARG;
+  *bytes = make_layout(cfg).total;
+  return HW_OK;
+}
+
+void hw_destroy(hw_ctx* ctx) {
+  if (!ctx) return;
+  for (cudaEvent_t e : ctx->prof_ev)
+    if (e) cudaEventDestroy(e);
+  for (int i = 0; i < kSlots; ++i)
+    if (ctx->slot_ev[i]) {
+      cudaEventSynchronize(ctx->slot_ev[i]);
+      cudaEventDestroy(ctx->slot_ev[i]);
+    }
+  if (ctx->h_slots) cudaFreeHost(ctx->h_slots);
+  delete ctx;
+}
+
+hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* workspace,
+                    size_t workspace_bytes, const int32_t* page_order, void* stream,
+                    hw_ctx** out) {
+  if (!out) return HW_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!valid_config(cfg) || !k_pool || !v_pool || !workspace) return HW_ERR_INVALID_ARG;
+  if (((uintptr_t)k_pool | (uintptr_t)v_pool | (uintptr_t)workspace) % kAlign)
+    return HW_ERR_INVALID_ARG;
+  const Layout lay = make_layout(cfg);
+  if (workspace_bytes < lay.total) return HW_ERR_CAPACITY;
+  const int32_t P = cfg->num_problems, W = cfg->num_workers;
+  if ((int64_t)P * (1 + W) > lay.max_segments) return HW_ERR_CAPACITY;
+  std::vector<int32_t> order(cfg->num_pages);
+  if (page_order) {
+    std::vector<uint8_t> seen(cfg->num_pages, 0);
+    for (int32_t i = 0; i < cfg->num_pages; ++i) {
+      const int32_t pg = page_order[i];
+      if (pg < 0 || pg >= cfg->num_pages || seen[pg]) return HW_ERR_INVALID_ARG;
+      seen[pg] = 1;
+      order[i] = pg;
+    }
+  } else {
+    for (int32_t i = 0; i < cfg->num_pages; ++i) order[i] = i;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  hw_ctx* c = new (std::nothrow) hw_ctx();
+  if (!c) return HW_ERR_CAPACITY;
+  c->cfg = *cfg;
+  c->lay = lay;
+  c->G = cfg->num_q_heads / cfg->num_kv_heads;
+  c->rows = lay.rows;
+  c->k_pool = (__nv_bfloat16*)k_pool;
+  c->v_pool = (__nv_bfloat16*)v_pool;
+  c->ws = (char*)workspace;
+  c->layer_elems = (size_t)cfg->num_pages * cfg->num_kv_heads * cfg->page_size * cfg->head_dim;
+  c->free_pages.assign(order.begin(), order.end());
+  for (int32_t p = 0; p < P; ++p) {
+    c->common.push_back({c->new_segment(p, -1)});
+    std::vector<int32_t> lv;
+    for (int32_t w = 0; w < W; ++w) lv.push_back(c->new_segment(p, w));
+    c->live.push_back(lv);
+  }
+  auto fail = [&](hw_status st) {
+    hw_destroy(c);
+    return st;
+  };
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+  e = cudaHostAlloc((void**)&c->h_slots, kSlots * lay.slot_bytes, cudaHostAllocDefault);
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+  for (int i = 0; i < kSlots; ++i) {
+    e = cudaEventCreateWithFlags(&c->slot_ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return fail(cuda_fail(e));
+  }
+  // RoPE table: cos/sin of p * theta^(-2i/D) in fp64 on the host, stored as fp32.
+  const int32_t half = cfg->head_dim / 2;
+  std::vector<float> tc((size_t)cfg->max_position * half), ts(tc.size());
+  for (int32_t i = 0; i < half; ++i) {
+    const double f = std::pow(cfg->rope_theta, -2.0 * i / cfg->head_dim);
+    for (int32_t p = 0; p < cfg->max_position; ++p) {
+      const double a = (double)p * f;
+      tc[(size_t)p * half + i] = (float)std::cos(a);
+      ts[(size_t)p * half + i] = (float)std::sin(a);
+    }
+  }
+  size_t pool_bytes = 0;
+  hw_pool_size(cfg, &pool_bytes);
+  e = cudaMemsetAsync(k_pool, 0, pool_bytes, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(v_pool, 0, pool_bytes, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->ws + lay.err, 0, kAlign, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->ws + lay.tickets, 0, lay.total - lay.tickets, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(c->d_cos(), tc.data(), tc.size() * sizeof(float), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(c->d_sin(), ts.data(), ts.size() * sizeof(float), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+  *out = c;
+  return HW_OK;
+}
+
+hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const void* k_raw,
+                       const void* v_raw, void* stream) {
+  if (!c || !n_new || layer < 0 || layer >= c->cfg.num_layers) return HW_ERR_INVALID_ARG;
+  const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, S = c->cfg.page_size;
+  const int32_t B = W + 1;
+  int64_t total = 0;
+  for (int32_t i = 0; i < P * B; ++i) {
+    if (n_new[i] < 0) return HW_ERR_INVALID_ARG;
+    total += n_new[i];
+  }
+  if (total > 0 && (!k_raw || !v_raw)) return HW_ERR_INVALID_ARG;
+  if (total > c->lay.max_append) return HW_ERR_CAPACITY;
+  if (!c->step_active) {
+    // First append of the step: check, then allocate pages (all-or-nothing).
+    int64_t need = 0;
+    for (int32_t p = 0; p < P; ++p) {
+      // Every view of problem p spans all its tokens: RoPE angles reach the view length - 1.
+      int64_t view_len = 0;
+      for (int32_t sid : c->common[p]) view_len += c->segs[sid].length;
+      for (int32_t sid : c->live[p]) view_len += c->segs[sid].length;
+      for (int32_t b = 0; b < B; ++b) view_len += n_new[p * B + b];
+      if (view_len > c->cfg.max_position) return HW_ERR_CAPACITY;
+      for (int32_t b = 0; b < B; ++b) {
+        const int32_t n = n_new[p * B + b];
+        if (!n) continue;
+        const Seg& sg = c->block(p, b);
+        const int64_t j0 = sg.length;
+        if (c->cfg.contiguous) {
+          if (j0 + n > S) return HW_ERR_CAPACITY;
+          if (j0 == 0) need += 1;
+        } else {
+          const int64_t first = (j0 + S - 1) / S, last = (j0 + n - 1) / S;
+          need += std::max<int64_t>(0, last - first + 1);
+        }
+      }
+    }
+    if (need > (int64_t)c->free_pages.size()) return HW_ERR_OUT_OF_PAGES;
+    for (int32_t p = 0; p < P; ++p)
+      for (int32_t b = 0; b < B; ++b) {
+        const int32_t n = n_new[p * B + b];
+        if (!n) continue;
+        Seg& sg = c->block(p, b);
+        const int64_t j0 = sg.length;
+        int64_t cnt;
+        if (c->cfg.contiguous) {
+          cnt = (j0 == 0) ? 1 : 0;
+        } else {
+          const int64_t first = (j0 + S - 1) / S, last = (j0 + n - 1) / S;
+          cnt = std::max<int64_t>(0, last - first + 1);
+        }
+        for (int64_t k = 0; k < cnt; ++k) {
+          sg.pages.push_back(c->free_pages.front());
+          c->free_pages.pop_front();
+        }
+        sg.pending = n;
+      }
+    c->step_active = true;
+    c->step_n.assign(n_new, n_new + P * B);
+    c->appended.assign(c->cfg.num_layers, 0);
+  } else {
+    if (!std::equal(c->step_n.begin(), c->step_n.end(), n_new)) return HW_ERR_INVALID_ARG;
+    if (c->appended[layer]) return HW_ERR_INVALID_ARG;
+  }
+  if (total == 0) {
+    c->appended[layer] = 1;
+    return HW_OK;
+  }
+  int slot = 0;
+  hw_status st = c->acquire_slot(&slot);
+  if (st != HW_OK) return st;
+  hw::AppendRun* runs = reinterpret_cast<hw::AppendRun*>(c->h_slot(slot));
+  const size_t max_runs = c->lay.slot_bytes / sizeof(hw::AppendRun);
+  int32_t nr = 0, src = 0, max_run = 0;
+  for (int32_t p = 0; p < P; ++p)
+    for (int32_t b = 0; b < B; ++b) {
+      const int32_t n = n_new[p * B + b];
+      if (!n) continue;
+      const Seg& sg = c->block(p, b);
+      int32_t j = sg.length;
+      const int32_t end = sg.length + n;
+      while (j < end) {
+        const int32_t pg_idx = c->cfg.contiguous ? 0 : j / S;
+        const int32_t slot0 = c->cfg.contiguous ? j : j % S;
+        const int32_t len = std::min(end - j, S - slot0);
+        if ((size_t)nr >= max_runs) return HW_ERR_CAPACITY;
+        runs[nr++] = hw::AppendRun{src, len, sg.pages[pg_idx], slot0, j, 0};
+        max_run = std::max(max_run, len);
+        src += len;
+        j += len;
+      }
+    }
+  cudaStream_t s = (cudaStream_t)stream;
+  HW_CUDA(cudaMemcpyAsync(c->d_slot(slot), runs, nr * sizeof(hw::AppendRun),
+                          cudaMemcpyHostToDevice, s));
+  hw::AppendArgs a{};
+  a.runs = reinterpret_cast<const hw::AppendRun*>(c->d_slot(slot));
+  a.num_runs = nr;
+  a.max_run = max_run;
+  a.k_raw = (const __nv_bfloat16*)k_raw;
+  a.v_raw = (const __nv_bfloat16*)v_raw;
+  a.k_layer = c->k_pool + (size_t)layer * c->layer_elems;
+  a.v_layer = c->v_pool + (size_t)layer * c->layer_elems;
+  a.rope_cos = c->d_cos();
+  a.rope_sin = c->d_sin();
+  a.err = c->d_err();
+  a.H_kv = c->cfg.num_kv_heads;
+  a.D = c->cfg.head_dim;
+  a.S = S;
+  a.num_pages = c->cfg.num_pages;
+  a.max_position = c->cfg.max_position;
+  const int pi = c->prof_begin(s, 1);
+  hw::launch_append(a, s);
+  c->prof_end(pi, s);
+  HW_CUDA(cudaGetLastError());
+  c->n_launch += (nr + 65534) / 65535;
+  c->n_append += 1;
+  HW_CUDA(cudaEventRecord(c->slot_ev[slot], s));
+  c->slot_used[slot] = true;
+  c->appended[layer] = 1;
+  return HW_OK;
+}
+
+namespace {
+
+// Build the attention plan of the current state into host buffer `buf` (slot_bytes long).
+// Returns false if a table would overflow.  Offsets of each array are written to `off`.
+struct PlanOffsets {
+  size_t pieces, units, groups, delta, bytes;
+  int32_t num_pieces, num_units, num_groups, num_seg_slots;
+};
+
+bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po) {
+  const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
+  const int32_t S = c->cfg.page_size;
+  const Layout& L = c->lay;
+  std::vector<hw::Piece> pieces;
+  std::vector<int32_t> delta;
+  std::vector<int64_t> group_tokens(P * H, 0);
+  std::vector<int32_t> group_piece_begin(P * H + 1, 0);
+  struct SegRef { int32_t sid, slot; };
+  std::vector<hw::Piece> proto;   // per problem: the pieces of one KV head
+  for (int32_t p = 0; p < P; ++p) {
+    // Segments of the problem, in view order of the common part, then worker blocks.
+    std::vector<SegRef> refs;
+    auto add_ref = [&](int32_t sid) {
+      if (c->segs[sid].visible() > 0) refs.push_back({sid, 0});
+    };
+    for (int32_t sid : c->common[p]) add_ref(sid);
+    for (int32_t w = 0; w < W; ++w) add_ref(c->live[p][w]);
+    const int32_t slot_base = (int32_t)(delta.size() / (size_t)W);
+    if (slot_base + (int64_t)refs.size() > L.max_seg_slots) return false;
+    delta.resize(delta.size() + refs.size() * (size_t)W, -1);
+    for (size_t r = 0; r < refs.size(); ++r) refs[r].slot = slot_base + (int32_t)r;
+    for (int32_t w = 0; w < W; ++w) {
+      std::vector<int32_t> ids, offs, lens;
+      const int32_t i_q = c->view(p, w, &ids, &offs, &lens);
+      for (size_t e = 0; e < ids.size(); ++e)
+        for (const SegRef& r : refs)
+          if (r.sid == ids[e]) delta[(size_t)r.slot * W + w] = i_q - offs[e];
+    }
+    proto.clear();
+    int64_t tok = 0;
+    for (const SegRef& r : refs) {
+      const Seg& sg = c->segs[r.sid];
+      const int32_t n = sg.visible();
+      for (int32_t j = 0; j < n; j += std::min(kPieceMax, S)) {
+        const int32_t pg = c->cfg.contiguous ? sg.pages[0] : sg.pages[j / S];
+        const int32_t slot0 = c->cfg.contiguous ? j : j % S;
+        const int32_t cnt = std::min(std::min(kPieceMax, S - slot0), n - j);
+        proto.push_back(hw::Piece{r.slot, pg, slot0, cnt});
+        tok += cnt;
+      }
+    }
+    for (int32_t h = 0; h < H; ++h) {
+      group_piece_begin[p * H + h] = (int32_t)pieces.size();
+      pieces.insert(pieces.end(), proto.begin(), proto.end());
+      group_tokens[p * H + h] = tok;
+    }
+  }
+  group_piece_begin[P * H] = (int32_t)pieces.size();
+  if ((int64_t)pieces.size() > L.max_pieces) return false;
+  // Units: split every group into KV-entry-balanced runs of pieces (summary section 9: the
+  // kernel balances by KV entries, not by blocks, then reduces the partial results).
+  int64_t total_tok = 0;
+  for (int64_t t : group_tokens) total_tok += t;
+  const int64_t target_units = std::max<int64_t>((int64_t)P * H, 4ll * c->num_sms);
+  std::vector<hw::Unit> units;
+  std::vector<hw::Group> groups;
+  for (int32_t g = 0; g < P * H; ++g) {
+    const int32_t pb = group_piece_begin[g], pe = group_piece_begin[g + 1];
+    const int64_t T = group_tokens[g];
+    hw::Group gr{g / H, g % H, (int32_t)units.size(), 0};
+    int64_t n_units = total_tok ? (target_units * T + total_tok / 2) / total_tok : 1;
+    n_units = std::max<int64_t>(1, std::min<int64_t>(n_units, pe - pb));
+    if (pe == pb) {
+      units.push_back(hw::Unit{pb, pb, g, 0});
+    } else {
+      int64_t cum = 0;
+      int32_t cur = -1;
+      for (int32_t i = pb; i < pe; ++i) {
+        const int64_t mid2 = 2 * cum + pieces[i].ntok;        // twice the piece midpoint
+        const int32_t k = (int32_t)std::min<int64_t>(n_units - 1, (mid2 * n_units) / (2 * T));
+        if (k != cur) {
+          units.push_back(hw::Unit{i, i + 1, g, 0});
+          cur = k;
+        } else {
+          units.back().piece_end = i + 1;
+        }
+        cum += pieces[i].ntok;
+      }
+    }
+    gr.unit_end = (int32_t)units.size();
+    groups.push_back(gr);
+  }
+  if ((int64_t)units.size() > L.max_units) return false;
+  size_t off = 0;
+  po->pieces = off;
+  off = align_up(off + pieces.size() * sizeof(hw::Piece), 16);
+  po->units = off;
+  off = align_up(off + units.size() * sizeof(hw::Unit), 16);
+  po->groups = off;
+  off = align_up(off + groups.size() * sizeof(hw::Group), 16);
+  po->delta = off;
+  off = align_up(off + delta.size() * sizeof(int32_t), 16);
+  po->bytes = off;
+  if (off > L.slot_bytes) return false;
+  std::memcpy(buf + po->pieces, pieces.data(), pieces.size() * sizeof(hw::Piece));
+  std::memcpy(buf + po->units, units.data(), units.size() * sizeof(hw::Unit));
+  std::memcpy(buf + po->groups, groups.data(), groups.size() * sizeof(hw::Group));
+  std::memcpy(buf + po->delta, delta.data(), delta.size() * sizeof(int32_t));
+  po->num_pieces = (int32_t)pieces.size();
+  po->num_units = (int32_t)units.size();
+  po->num_groups = (int32_t)groups.size();
+  po->num_seg_slots = (int32_t)(delta.size() / (size_t)W);
+  return true;
+}
+
+}  // namespace
+
+hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void* out,
+                                  int32_t out_dtype, float* lse, void* stream) {
+  if (!c || !q || !out || layer < 0 || layer >= c->cfg.num_layers) return HW_ERR_INVALID_ARG;
+  if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
+  if (c->step_active && !c->appended[layer]) return HW_ERR_INVALID_ARG;
+  int slot = 0;
+  hw_status st = c->acquire_slot(&slot);
+  if (st != HW_OK) return st;
+  PlanOffsets po{};
+  if (!build_attention_plan(c, c->h_slot(slot), &po)) return HW_ERR_CAPACITY;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* dbase = c->d_slot(slot);
+  HW_CUDA(cudaMemcpyAsync(dbase, c->h_slot(slot), po.bytes, cudaMemcpyHostToDevice, s));
+  hw::AttnArgs a{};
+  a.pieces = reinterpret_cast<const hw::Piece*>(dbase + po.pieces);
+  a.units = reinterpret_cast<const hw::Unit*>(dbase + po.units);
+  a.groups = reinterpret_cast<const hw::Group*>(dbase + po.groups);
+  a.delta = reinterpret_cast<const int32_t*>(dbase + po.delta);
+  a.num_units = po.num_units;
+  a.num_groups = po.num_groups;
+  a.num_seg_slots = po.num_seg_slots;
+  a.k_layer = c->k_pool + (size_t)layer * c->layer_elems;
+  a.v_layer = c->v_pool + (size_t)layer * c->layer_elems;
+  a.q = (const __nv_bfloat16*)q;
+  a.out = out;
+  a.out_f32 = out_dtype == HW_OUT_F32;
+  a.lse = lse;
+  a.partials = c->d_partials();
+  a.rope_cos = c->d_cos();
+  a.rope_sin = c->d_sin();
+  a.err = c->d_err();
+  a.P = c->cfg.num_problems;
+  a.W = c->cfg.num_workers;
+  a.H_q = c->cfg.num_q_heads;
+  a.H_kv = c->cfg.num_kv_heads;
+  a.G = c->G;
+  a.D = c->cfg.head_dim;
+  a.S = c->cfg.page_size;
+  a.num_pages = c->cfg.num_pages;
+  a.max_position = c->cfg.max_position;
+  a.rows = c->rows;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+  const int pi = c->prof_begin(s, 0);
+  hw::launch_attention_fma(a, s);
+  c->prof_end(pi, s);
+  HW_CUDA(cudaGetLastError());
+  hw::launch_merge(a, s);
+  HW_CUDA(cudaGetLastError());
+  c->n_launch += 2;
+  c->n_attn += 1;
+  HW_CUDA(cudaEventRecord(c->slot_ev[slot], s));
+  c->slot_used[slot] = true;
+  return HW_OK;
+}
+
+hw_status hw_step_end(hw_ctx* c, const uint8_t* finished, void* stream) {
+  (void)stream;
+  if (!c) return HW_ERR_INVALID_ARG;
+  const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers;
+  if (c->step_active)
+    for (uint8_t a : c->appended)
+      if (!a) return HW_ERR_INVALID_ARG;
+  int64_t commits = 0;
+  if (finished)
+    for (int32_t p = 0; p < P; ++p)
+      for (int32_t w = 0; w < W; ++w)
+        if (finished[p * W + w] && c->segs[c->live[p][w]].visible() > 0) ++commits;
+  if ((int64_t)c->segs.size() + commits > c->lay.max_segments) return HW_ERR_CAPACITY;
+  for (Seg& sg : c->segs) {
+    sg.length += sg.pending;
+    sg.pending = 0;
+  }
+  c->step_active = false;
+  c->appended.clear();
+  c->step_n.clear();
+  if (finished)
+    for (int32_t p = 0; p < P; ++p)
+      for (int32_t w = 0; w < W; ++w)
+        if (finished[p * W + w] && c->segs[c->live[p][w]].length > 0) {
+          c->common[p].push_back(c->live[p][w]);
+          c->live[p][w] = c->new_segment(p, w);
+        }
+  return HW_OK;
+}
+
+hw_status hw_check_device_errors(hw_ctx* c, void* stream, uint32_t* info) {
+  if (!c) return HW_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t w[4] = {0, 0, 0, 0};
+  HW_CUDA(cudaStreamSynchronize(s));
+  HW_CUDA(cudaMemcpy(w, c->d_err(), sizeof(w), cudaMemcpyDeviceToHost));
+  if (info) std::memcpy(info, w, sizeof(w));
+  if (!w[0]) return HW_OK;
+  HW_CUDA(cudaMemset(c->d_err(), 0, sizeof(w)));
+  return (w[0] & hw::ERR_TIMEOUT) ? HW_ERR_DEVICE_TIMEOUT : HW_ERR_DEVICE_CHECK;
+}
+
+hw_status hw_profile_enable(hw_ctx* c, int32_t enable) {
+  if (!c) return HW_ERR_INVALID_ARG;
+  if (enable && c->prof_ev.empty()) {
+    c->prof_ev.assign(2 * kProfPairs, nullptr);
+    c->prof_kind.assign(kProfPairs, 0);
+    for (auto& e : c->prof_ev) HW_CUDA(cudaEventCreate(&e));
+  }
+  c->prof_on = enable != 0;
+  return HW_OK;
+}
+
+hw_status hw_profile_read(hw_ctx* c, hw_profile* out) {
+  if (!c || !out) return HW_ERR_INVALID_ARG;
+  hw_profile r{};
+  r.launches = c->n_launch;
+  r.attention_launches = c->n_attn;
+  r.append_launches = c->n_append;
+  for (int i = 0; i < c->prof_next; ++i) {
+    HW_CUDA(cudaEventSynchronize(c->prof_ev[2 * i + 1]));
+    float ms = 0.f;
+    HW_CUDA(cudaEventElapsedTime(&ms, c->prof_ev[2 * i], c->prof_ev[2 * i + 1]));
+    if (c->prof_kind[i] == 0) {
+      r.attention_ms += ms;
+      r.timed_attention += 1;
+    } else {
+      r.append_ms += ms;
+      r.timed_append += 1;
+    }
+  }
+  c->prof_next = 0;
+  c->n_launch = c->n_attn = c->n_append = 0;
+  *out = r;
+  return HW_OK;
+}
+
+hw_status hw_get_counts(const hw_ctx* c, int32_t* num_segments, int32_t* free_pages) {
+  if (!c || !num_segments || !free_pages) return HW_ERR_INVALID_ARG;
+  *num_segments = (int32_t)c->segs.size();
+  *free_pages = (int32_t)c->free_pages.size();
+  return HW_OK;
+}
+
+hw_status hw_get_segment(const hw_ctx* c, int32_t seg, int32_t* problem, int32_t* origin,
+                         int32_t* length, int32_t* pending, int32_t* num_pages,
+                         int32_t* pages_out, int32_t pages_cap) {
+  if (!c || seg < 0 || seg >= (int32_t)c->segs.size()) return HW_ERR_INVALID_ARG;
+  if (!problem || !origin || !length || !pending || !num_pages) return HW_ERR_INVALID_ARG;
+  const Seg& sg = c->segs[seg];
+  *problem = sg.problem;
+  *origin = sg.origin;
+  *length = sg.length;
+  *pending = sg.pending;
+  *num_pages = (int32_t)sg.pages.size();
+  if ((int32_t)sg.pages.size() > pages_cap || (!pages_out && !sg.pages.empty()))
+    return HW_ERR_CAPACITY;
+  std::copy(sg.pages.begin(), sg.pages.end(), pages_out);
+  return HW_OK;
+}
+
+hw_status hw_get_blocks(const hw_ctx* c, int32_t problem, int32_t* common_ids, int32_t cap,
+                        int32_t* num_common, int32_t* live_ids) {
+  if (!c || problem < 0 || problem >= c->cfg.num_problems || !num_common || !live_ids)
+    return HW_ERR_INVALID_ARG;
+  const auto& cm = c->common[problem];
+  *num_common = (int32_t)cm.size();
+  std::copy(c->live[problem].begin(), c->live[problem].end(), live_ids);
+  if ((int32_t)cm.size() > cap || !common_ids) return HW_ERR_CAPACITY;
+  std::copy(cm.begin(), cm.end(), common_ids);
+  return HW_OK;
+}
+
+hw_status hw_get_view(const hw_ctx* c, int32_t problem, int32_t worker, int32_t* seg_ids,
+                      int32_t* view_offsets, int32_t* lengths, int32_t cap, int32_t* n,
+                      int32_t* i_q) {
+  if (!c || problem < 0 || problem >= c->cfg.num_problems || worker < 0 ||
+      worker >= c->cfg.num_workers || !n || !i_q)
+    return HW_ERR_INVALID_ARG;
+  std::vector<int32_t> ids, offs, lens;
+  *i_q = c->view(problem, worker, &ids, &offs, &lens);
+  *n = (int32_t)ids.size();
+  if ((int32_t)ids.size() > cap || !seg_ids || !view_offsets || !lengths) return HW_ERR_CAPACITY;
+  std::copy(ids.begin(), ids.end(), seg_ids);
+  std::copy(offs.begin(), offs.end(), view_offsets);
+  std::copy(lens.begin(), lens.end(), lengths);
+  return HW_OK;
+}
+
+}  // extern "C"

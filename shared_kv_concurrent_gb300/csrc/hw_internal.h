@@ -1,0 +1,97 @@
+// Internal declarations of libhogwild: the per-call plans the host uploads, the kernel
+// argument blocks, and the launchers.  Host planning lives in hw_api.cpp, kernels in the .cu
+// files.  Nothing here is part of the public ABI (include/hogwild.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace hw {
+
+// Device error word layout (uint32[4] at the start of the workspace):
+//   [0] OR of error bits, [1] id of the first kernel that failed, [2], [3] its details.
+enum : uint32_t {
+  ERR_PAGE_RANGE = 1u << 0,    // a physical page index outside [0, num_pages)
+  ERR_SLOT_RANGE = 1u << 1,    // a slot range outside the page
+  ERR_POS_RANGE = 1u << 2,     // a RoPE position outside [0, max_position)
+  ERR_TIMEOUT = 1u << 3,       // a bounded wait gave up
+  ERR_PLAN = 1u << 4,          // an inconsistent plan entry
+};
+enum : uint32_t { KID_APPEND = 1, KID_ATTN_FMA = 2, KID_MERGE = 3, KID_ATTN_TC = 4 };
+
+// One run of appended tokens: ntok consecutive tokens of one block that land in one page.
+struct AppendRun {
+  int32_t src_tok;   // first token in k_raw / v_raw
+  int32_t ntok;
+  int32_t page;      // physical page
+  int32_t slot0;     // slot of the first token in the page
+  int32_t pos0;      // block-local position of the first token (RoPE angle)
+  int32_t pad;
+};
+
+// A piece: <= 256 consecutive tokens of one segment, inside one page, for one KV head.
+struct Piece {
+  int32_t seg_slot;  // row of the delta table (problem, segment) -> per-worker rotation
+  int32_t page;
+  int32_t slot0;
+  int32_t ntok;
+};
+
+// A unit: consecutive pieces of one (problem, KV head) group, one CTA, one partial result.
+struct Unit {
+  int32_t piece_begin;
+  int32_t piece_end;
+  int32_t group;
+  int32_t pad;
+};
+
+// A group: one (problem, KV head); its units are [unit_begin, unit_end).
+struct Group {
+  int32_t p;
+  int32_t h;
+  int32_t unit_begin;
+  int32_t unit_end;
+};
+
+struct AppendArgs {
+  const AppendRun* runs;
+  int32_t num_runs;
+  int32_t max_run;
+  const __nv_bfloat16* k_raw;
+  const __nv_bfloat16* v_raw;
+  __nv_bfloat16* k_layer;     // pool base of this layer: [num_pages][H_kv][S][D]
+  __nv_bfloat16* v_layer;
+  const float* rope_cos;      // [max_position][D/2]
+  const float* rope_sin;
+  uint32_t* err;
+  int32_t H_kv, D, S, num_pages, max_position;
+};
+
+struct AttnArgs {
+  const Piece* pieces;
+  const Unit* units;
+  const Group* groups;
+  const int32_t* delta;       // [seg_slots][W]: i_q(w) - view offset, or -1 (not visible)
+  int32_t num_units, num_groups, num_seg_slots;
+  const __nv_bfloat16* k_layer;
+  const __nv_bfloat16* v_layer;
+  const __nv_bfloat16* q;     // [P][W][H_q][D]
+  void* out;                  // [P][W][H_q][D] bf16 or fp32
+  int32_t out_f32;
+  float* lse;                 // [P][W][H_q] or null
+  float* partials;            // [units][rows][D + 2]: o[D], m, l (log2 domain)
+  const float* rope_cos;
+  const float* rope_sin;
+  uint32_t* err;
+  int32_t P, W, H_q, H_kv, G, D, S, num_pages, max_position, rows;
+  float scale_log2;           // log2(e) / sqrt(D)
+};
+
+void launch_append(const AppendArgs& a, cudaStream_t s);
+void launch_attention_fma(const AttnArgs& a, cudaStream_t s);
+void launch_merge(const AttnArgs& a, cudaStream_t s);
+
+}  // namespace hw

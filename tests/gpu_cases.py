@@ -1,0 +1,115 @@
+"""Shared driver of the GPU parity tests: run a workload through the library and the oracle
+side by side and compare every output, table and stored slot."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+import workload as wl
+from oracle import attention as A
+from oracle import run as orun
+
+# Output tolerance: max-abs 1e-2 on bf16 inputs with fp32 accumulation.  The budget: keys are
+# stored as bf16 (relative error 2^-9) which perturbs a logit q.k/sqrt(D) of N(0,1) data by
+# about 0.004; the bf16 output adds < 0.004 for |o| < 2.
+TOL = 1e-2
+
+
+def dev_tables_equal(runner, cache):
+    got = runner.cache.tables()
+    exp = cache.tables()
+    assert got["common"] == exp["common"], (got["common"], exp["common"])
+    assert got["live"] == exp["live"]
+    assert got["free_count"] == exp["free_count"]
+    assert [tuple(s[:4]) for s in got["segments"]] == [tuple(s[:4]) for s in exp["segments"]]
+    assert [list(s[4]) for s in got["segments"]] == [list(s[4]) for s in exp["segments"]]
+    for p in range(cache.P):
+        for w in range(cache.W):
+            e, iq = cache.view(p, w)
+            ge, giq = runner.cache.view(p, w)
+            assert giq == iq and [tuple(x) for x in ge] == [tuple(x) for x in e]
+
+
+def check_pools(runner, cache, layer, max_tokens_per_seg=None):
+    """Stored keys within 1 bf16 ulp of the fp64 rotation; values bit-exact; at the oracle's
+    (page, slot) of every token -- so page addressing is checked bit-exactly too."""
+    import torch
+    kp, vp = runner.cache.pools(layer)
+    kb = kp.view(torch.int16).cpu().numpy().view(np.uint16)
+    vb = vp.view(torch.int16).cpu().numpy().view(np.uint16)
+    for sid, seg in enumerate(cache.segments):
+        n = seg.visible
+        if n == 0:
+            continue
+        js = np.arange(n)
+        if max_tokens_per_seg and n > max_tokens_per_seg:
+            js = np.unique(np.concatenate([js[:8], js[-8:], np.random.default_rng(sid).choice(
+                n, max_tokens_per_seg, replace=False)]))
+        sk = seg.stored_k(layer)[js]
+        rv = seg.raw_v(layer)[js]
+        slots = [cache.slot_of(sid, int(j)) for j in js]
+        pg = np.array([s[0] for s in slots])
+        sl = np.array([s[1] for s in slots])
+        gk = wl.bf16_bits_to_f32(kb[pg, :, sl, :]).astype(np.float64)   # [n][H_kv][D]
+        gv = vb[pg, :, sl, :]
+        ev = wl.f32_to_bf16_bits(rv.astype(np.float32))
+        # Stored key = bf16(x1 c - x2 s) computed in fp32: rounding to bf16 costs at most half
+        # an ulp (unit roundoff 2^-8 relative) and the fp32 products, the fp32 cos/sin table and
+        # the cancellation at most a few 2^-24 of the pair's magnitude, which dominates when the
+        # rotated value nearly cancels.
+        rk = seg.raw_k(layer)[js]
+        half = rk.shape[-1] // 2
+        pair = np.abs(rk[..., :half]) + np.abs(rk[..., half:])
+        pair = np.concatenate([pair, pair], axis=-1)
+        bound = 2.0 ** -8 * np.abs(sk) + 2.0 ** -21 * pair
+        excess = np.abs(gk - sk) - bound
+        assert excess.max() <= 0, (sid, float(np.abs(gk - sk).max()), float(excess.max()))
+        assert np.array_equal(gv, ev), sid
+
+
+def run_case(w: wl.Workload, steps: int, out_dtype="f32", bernoulli=None, pools=True,
+             pool_sample=None, tol=TOL):
+    import torch
+    from shared_kv_concurrent_gb300 import binding
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner
+    r = WorkloadRunner(w)
+    c = orun.prefill(w)
+    dev_tables_equal(r, c)
+    worst = 0.0
+    P, W, Hq, D = w.num_problems, w.num_workers, w.num_q_heads, w.head_dim
+    dt = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    for step in range(steps):
+        inputs = r.step_inputs(step)
+        r.append(inputs)
+        orun.append_step(c, w, step)
+        outs = [torch.full((P, W, Hq, D), float("nan"), dtype=dt, device="cuda")
+                for _ in range(w.num_layers)]
+        lses = [torch.full((P, W, Hq), float("nan"), dtype=torch.float32, device="cuda")
+                for _ in range(w.num_layers)]
+        r.attend(inputs, outs, lses, out_dtype)
+        torch.cuda.synchronize()
+        for layer in range(w.num_layers):
+            ref, ref_lse = A.method(c, layer, orun.query(w, layer, step))
+            got = outs[layer].float().cpu().numpy()
+            err = np.abs(got - ref).max()
+            worst = max(worst, float(err))
+            assert err <= tol, (step, layer, err)
+            gl = lses[layer].cpu().numpy()
+            fin = np.isfinite(ref_lse)
+            assert np.array_equal(np.isfinite(gl), fin)
+            assert np.abs(gl[fin] - ref_lse[fin]).max() <= tol
+            if pools:
+                check_pools(r, c, layer, pool_sample)
+        fin = wl.finished_mask(w, step, bernoulli)
+        r.end(step, fin)
+        c.step_end(fin)
+        dev_tables_equal(r, c)
+    st, info = r.cache.check_device_errors()
+    assert st == binding.HW_OK, info
+    r.cache.close()
+    return worst
+
+
+def small(base: wl.Workload, **kw) -> wl.Workload:
+    return dataclasses.replace(base, **kw)

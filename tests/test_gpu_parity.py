@@ -1,0 +1,168 @@
+"""CUDA path against the fp64 oracle, element by element, through the C ABI (needs a GPU).
+
+Sizes span several tiles and pieces with ragged tails; the full 32K-common, 8-worker workload
+runs once in the launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+
+import workload as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from shared_kv_concurrent_gb300.build import build
+    build()
+
+
+def case(name):
+    import gpu_cases as G
+    return G
+
+
+def test_tiny_paged_with_commits():
+    import gpu_cases as G
+    G.run_case(wl.tiny(), steps=4, bernoulli=0.5)
+
+
+def test_tiny_contiguous():
+    import gpu_cases as G
+    G.run_case(wl.tiny(contiguous=True), steps=3)
+
+
+def test_tiny_bf16_output():
+    import gpu_cases as G
+    G.run_case(wl.tiny(), steps=2, out_dtype="bf16", pools=False)
+
+
+def test_w2_contiguous_scaled():
+    import gpu_cases as G
+    w = G.small(wl.c2(), common_len=(1000,), worker_len=((130, 70),), page_size=1280, steps=3)
+    G.run_case(w, steps=3)
+
+
+def test_w8_paged_permuted_ragged():
+    import gpu_cases as G
+    w = G.small(wl.c4(), common_len=(3001,), worker_len=((0, 1, 127, 128, 129, 255, 257, 600),),
+                steps=3)
+    G.run_case(w, steps=3, bernoulli=0.3)
+
+
+def test_batch_of_problems_with_commits():
+    import gpu_cases as G
+    w = G.small(wl.c5(), num_problems=3, common_len=(700, 2500, 1300),
+                worker_len=((0, 300, 17, 256), (5, 0, 0, 129), (511, 1, 64, 200)), steps=4,
+                commit_steps=(1,))
+    G.run_case(w, steps=4)
+
+
+def test_multi_layer():
+    import gpu_cases as G
+    w = G.small(wl.c3(), num_layers=3, common_len=(2000,), worker_len=((0, 700, 33, 1024),),
+                steps=2)
+    G.run_case(w, steps=2)
+
+
+def test_head_dim_64_no_gqa():
+    import gpu_cases as G
+    w = G.small(wl.tiny(), num_q_heads=4, num_kv_heads=4, num_workers=3, common_len=(300,),
+                worker_len=((10, 0, 140),), steps=2)
+    G.run_case(w, steps=2, bernoulli=0.5)
+
+
+def test_max_rows_128():
+    import gpu_cases as G
+    w = G.small(wl.c4(), num_workers=16, common_len=(600,),
+                worker_len=(tuple(range(0, 160, 10)),), random_page_order=False, steps=2)
+    G.run_case(w, steps=2, pools=False)
+
+
+def test_full_size_w8_common32768():
+    """The benchmark workload itself: 32768 common tokens, 8 worker blocks of 128..2048."""
+    import gpu_cases as G
+    w = G.small(wl.c4(), steps=1)
+    G.run_case(w, steps=1, pool_sample=64)
+
+
+def test_empty_view_gives_zero_and_minus_inf():
+    import torch
+    from shared_kv_concurrent_gb300 import HogwildCache
+    w = G_small_empty()
+    c = HogwildCache.from_workload(w)
+    q = torch.randn(1, 2, 8, 64, device="cuda").to(torch.bfloat16)
+    lse = torch.zeros(1, 2, 8, device="cuda")
+    out = c.concurrent_attention(0, q, out_dtype="f32", lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(torch.isinf(lse)) and torch.all(lse < 0)
+    c.close()
+
+
+def G_small_empty():
+    import dataclasses
+    return dataclasses.replace(wl.tiny(), common_len=(0,), worker_len=((0, 0),))
+
+
+def test_protocol_errors_leave_state_unchanged():
+    import torch
+    from shared_kv_concurrent_gb300 import HogwildCache, HogwildError, binding
+    w = wl.tiny()
+    c = HogwildCache.from_workload(w)
+    k = torch.zeros(2, 2, 64, dtype=torch.bfloat16, device="cuda")
+    n = np.array([[0, 1, 1]], np.int32)
+    c.append_kv(0, n, k, k)
+    with pytest.raises(HogwildError) as e:
+        c.append_kv(0, n, k, k)                      # same layer twice in one step
+    assert e.value.status == binding.HW_ERR_INVALID_ARG
+    c.step_end(None)
+    before = c.tables()
+    big = np.array([[10 ** 6, 0, 0]], np.int32)
+    kb = torch.zeros(1, 2, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(HogwildError) as e:
+        c.append_kv(0, big, kb, kb)
+    assert e.value.status in (binding.HW_ERR_OUT_OF_PAGES, binding.HW_ERR_CAPACITY)
+    assert c.tables() == before
+    st, info = c.check_device_errors()
+    assert st == binding.HW_OK, info
+    c.close()
+
+
+def test_out_of_pages_reported():
+    import dataclasses
+    import torch
+    from shared_kv_concurrent_gb300 import HogwildCache, HogwildError, binding, config_for
+    cfg = config_for(num_problems=1, num_workers=2, num_layers=1, num_q_heads=8, num_kv_heads=2,
+                     head_dim=64, page_size=128, num_pages=3, max_position=4096, rope_theta=1e4)
+    c = HogwildCache(cfg)
+    k = torch.zeros(300, 2, 64, dtype=torch.bfloat16, device="cuda")
+    c.append_kv(0, np.array([[300, 0, 0]], np.int32), k, k)       # 3 pages
+    c.step_end(None)
+    before = c.tables()
+    with pytest.raises(HogwildError) as e:
+        c.append_kv(0, np.array([[0, 1, 0]], np.int32), k[:1], k[:1])
+    assert e.value.status == binding.HW_ERR_OUT_OF_PAGES
+    assert c.tables() == before
+    c.close()
+    del dataclasses
+
+
+def test_deterministic_bitwise():
+    import torch
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner
+    import gpu_cases as G
+    w = G.small(wl.c4(), common_len=(2000,), worker_len=((5, 300, 0, 77, 128, 256, 1, 999),),
+                steps=1)
+    r = WorkloadRunner(w)
+    inp = r.step_inputs(0)
+    r.append(inp)
+    o1 = [torch.empty(1, 8, 64, 128, dtype=torch.float32, device="cuda")]
+    o2 = [torch.empty_like(o1[0])]
+    r.attend(inp, o1, None, "f32")
+    r.attend(inp, o2, None, "f32")
+    torch.cuda.synchronize()
+    assert torch.equal(o1[0].view(torch.int32), o2[0].view(torch.int32))
+    r.cache.close()
