@@ -141,6 +141,26 @@ hw_status hw_concurrent_attention(hw_ctx* ctx, int32_t layer, const void* q, voi
                                   int32_t out_dtype, float* lse, void* stream);
 
 /*
+ * hw_concurrent_attention for callers that cannot allocate device memory when they call it
+ * (no counterpart in the paper; a deployment need).  Same arguments, same result as
+ * hw_concurrent_attention; the context's pools, tables and RoPE table are used as usual, but
+ * the call's plan and its split-K partial results live in a fixed 16 MiB array in device global
+ * memory that the library defines, instead of in the workspace.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library routine is called.
+ *   - Limit: the plan plus one partial result per (problem, KV head) group, i.e.
+ *     P * H_kv * rows * (D + 2) * 4 bytes with rows = W * H_q / H_kv, must fit in 16 MiB, else
+ *     HW_ERR_CAPACITY and nothing is enqueued.  The KV split adapts to the space left.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call, from every context, shares the one array, which keeps the last call's
+ *     contents; nothing in it needs to start at zero (each call writes its plan and every
+ *     partial before reading them).  Calls whose GPU work overlaps -- on different streams,
+ *     or from different contexts -- race on the array: order them on one stream.
+ */
+hw_status hw_concurrent_attention_noalloc(hw_ctx* ctx, int32_t layer, const void* q, void* out,
+                                          int32_t out_dtype, float* lse, void* stream);
+
+/*
  * End the step (section 8): every block's length grows by the tokens appended in this step;
  * then, for each problem and each worker in ascending id with finished[p][w] != 0 and a
  * non-empty block, the worker's block is moved, unchanged, to the end of the common history

@@ -457,7 +457,8 @@ struct PlanOffsets {
   int32_t num_pieces, num_units, num_groups, num_seg_slots;
 };
 
-bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po) {
+// unit_cap > 0 bounds the number of units (one partial result each); 0 = the default split.
+bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0) {
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
   const int32_t S = c->cfg.page_size;
   const Layout& L = c->lay;
@@ -511,14 +512,19 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po) {
   // kernel balances by KV entries, not by blocks, then reduces the partial results).
   int64_t total_tok = 0;
   for (int64_t t : group_tokens) total_tok += t;
-  const int64_t target_units = std::max<int64_t>((int64_t)P * H, 4ll * c->num_sms);
+  int64_t target_units = std::max<int64_t>((int64_t)P * H, 4ll * c->num_sms);
+  if (unit_cap > 0) {
+    if (unit_cap < (int64_t)P * H) return false;
+    // per-group counts are floored and then raised to >= 1: keep room for that raise
+    target_units = std::max<int64_t>(0, std::min<int64_t>(target_units, unit_cap - (int64_t)P * H));
+  }
   std::vector<hw::Unit> units;
   std::vector<hw::Group> groups;
   for (int32_t g = 0; g < P * H; ++g) {
     const int32_t pb = group_piece_begin[g], pe = group_piece_begin[g + 1];
     const int64_t T = group_tokens[g];
     hw::Group gr{g / H, g % H, (int32_t)units.size(), 0};
-    int64_t n_units = total_tok ? (target_units * T + total_tok / 2) / total_tok : 1;
+    int64_t n_units = total_tok ? (target_units * T + (unit_cap > 0 ? 0 : total_tok / 2)) / total_tok : 1;
     n_units = std::max<int64_t>(1, std::min<int64_t>(n_units, pe - pb));
     if (pe == pb) {
       units.push_back(hw::Unit{pb, pb, g, 0});
@@ -541,6 +547,7 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po) {
     groups.push_back(gr);
   }
   if ((int64_t)units.size() > L.max_units) return false;
+  if (unit_cap > 0 && (int64_t)units.size() > unit_cap) return false;
   size_t off = 0;
   po->pieces = off;
   off = align_up(off + pieces.size() * sizeof(hw::Piece), 16);
@@ -619,6 +626,73 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   c->slot_used[slot] = true;
   return HW_OK;
 }
+
+}  // extern "C"
+
+// Same computation as hw_concurrent_attention, with the call's plan and the split-K partials
+// placed in caller-given device scratch instead of the workspace (used by the allocation-free
+// entry point).  The number of units is capped so that both fit.
+hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, void* out,
+                                     int32_t out_dtype, float* lse, void* stream, char* scratch,
+                                     size_t scratch_bytes) {
+  if (!c || !q || !out || !scratch || layer < 0 || layer >= c->cfg.num_layers)
+    return HW_ERR_INVALID_ARG;
+  if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
+  if (c->step_active && !c->appended[layer]) return HW_ERR_INVALID_ARG;
+  const size_t per_unit = (size_t)c->rows * (c->cfg.head_dim + 2) * sizeof(float);
+  const size_t plan_region = align_up(std::min(c->lay.slot_bytes, scratch_bytes / 4), kAlign);
+  if (plan_region >= scratch_bytes) return HW_ERR_CAPACITY;
+  const int64_t unit_cap = (int64_t)((scratch_bytes - plan_region) / per_unit);
+  if (unit_cap < (int64_t)c->cfg.num_problems * c->cfg.num_kv_heads) return HW_ERR_CAPACITY;
+  int slot = 0;
+  hw_status st = c->acquire_slot(&slot);
+  if (st != HW_OK) return st;
+  PlanOffsets po{};
+  if (!build_attention_plan(c, c->h_slot(slot), &po, unit_cap) || po.bytes > plan_region)
+    return HW_ERR_CAPACITY;
+  cudaStream_t s = (cudaStream_t)stream;
+  HW_CUDA(cudaMemcpyAsync(scratch, c->h_slot(slot), po.bytes, cudaMemcpyHostToDevice, s));
+  hw::AttnArgs a{};
+  a.pieces = reinterpret_cast<const hw::Piece*>(scratch + po.pieces);
+  a.units = reinterpret_cast<const hw::Unit*>(scratch + po.units);
+  a.groups = reinterpret_cast<const hw::Group*>(scratch + po.groups);
+  a.delta = reinterpret_cast<const int32_t*>(scratch + po.delta);
+  a.num_units = po.num_units;
+  a.num_groups = po.num_groups;
+  a.num_seg_slots = po.num_seg_slots;
+  a.k_layer = c->k_pool + (size_t)layer * c->layer_elems;
+  a.v_layer = c->v_pool + (size_t)layer * c->layer_elems;
+  a.q = (const __nv_bfloat16*)q;
+  a.out = out;
+  a.out_f32 = out_dtype == HW_OUT_F32;
+  a.lse = lse;
+  a.partials = reinterpret_cast<float*>(scratch + plan_region);
+  a.rope_cos = c->d_cos();
+  a.rope_sin = c->d_sin();
+  a.err = c->d_err();
+  a.P = c->cfg.num_problems;
+  a.W = c->cfg.num_workers;
+  a.H_q = c->cfg.num_q_heads;
+  a.H_kv = c->cfg.num_kv_heads;
+  a.G = c->G;
+  a.D = c->cfg.head_dim;
+  a.S = c->cfg.page_size;
+  a.num_pages = c->cfg.num_pages;
+  a.max_position = c->cfg.max_position;
+  a.rows = c->rows;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+  hw::launch_attention_fma(a, s);
+  HW_CUDA(cudaGetLastError());
+  hw::launch_merge(a, s);
+  HW_CUDA(cudaGetLastError());
+  HW_CUDA(cudaEventRecord(c->slot_ev[slot], s));
+  c->slot_used[slot] = true;
+  c->n_launch += 2;
+  c->n_attn += 1;
+  return HW_OK;
+}
+
+extern "C" {
 
 hw_status hw_step_end(hw_ctx* c, const uint8_t* finished, void* stream) {
   (void)stream;

@@ -9,6 +9,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "hogwild.h"
+
 namespace hw {
 
 // Device error word layout (uint32[4] at the start of the workspace):
@@ -93,5 +95,10 @@ struct AttnArgs {
 void launch_append(const AppendArgs& a, cudaStream_t s);
 void launch_attention_fma(const AttnArgs& a, cudaStream_t s);
 void launch_merge(const AttnArgs& a, cudaStream_t s);
+
+// hw_concurrent_attention with the plan and the partial results in `scratch` (device).
+hw_status attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, void* out,
+                                 int32_t out_dtype, float* lse, void* stream, char* scratch,
+                                 size_t scratch_bytes);
 
 }  // namespace hw
