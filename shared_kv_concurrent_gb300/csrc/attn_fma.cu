@@ -156,7 +156,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const AttnArgs a) {
   const Group g = a.groups[blockIdx.x];
   constexpr int RPB = 256 / D;                  // rows handled side by side
   const int d = threadIdx.x % D;
-  for (int r = threadIdx.x / D; r < a.rows; r += RPB) {
+  // blockIdx.y picks RPB consecutive rows of the group.
+  for (int r = blockIdx.y * RPB + threadIdx.x / D; r < min(a.rows, (int)(blockIdx.y + 1) * RPB);
+       r += RPB) {
     float M = -CUDART_INF_F;
     for (int u = g.unit_begin; u < g.unit_end; ++u)
       M = fmaxf(M, a.partials[((size_t)u * a.rows + r) * (D + 2) + D]);
@@ -200,9 +202,9 @@ void launch_attention_fma(const AttnArgs& a, cudaStream_t s) {
 void launch_merge(const AttnArgs& a, cudaStream_t s) {
   if (a.num_groups <= 0) return;
   if (a.D == 64)
-    merge_kernel<64><<<a.num_groups, 256, 0, s>>>(a);
+    merge_kernel<64><<<dim3(a.num_groups, (a.rows + 3) / 4), 256, 0, s>>>(a);
   else
-    merge_kernel<128><<<a.num_groups, 256, 0, s>>>(a);
+    merge_kernel<128><<<dim3(a.num_groups, (a.rows + 1) / 2), 256, 0, s>>>(a);
 }
 
 }  // namespace hw

@@ -126,6 +126,8 @@ struct hw_ctx {
   cudaEvent_t slot_ev[kSlots] = {};
   bool slot_used[kSlots] = {};
   int next_slot = 0;
+  hw::TcMaps maps{};
+  bool use_tc = false;                     // tensor-core attention (W*G >= 16 rows)
   std::deque<int32_t> free_pages;
   std::vector<Seg> segs;
   std::vector<std::vector<int32_t>> common, live;
@@ -293,6 +295,12 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return fail(cuda_fail(e));
+  // Tensor cores take the contraction once a dense 16-row tile of query rows exists; the TMA
+  // row coordinate of the pools must fit in int32.
+  const int64_t pool_rows = (int64_t)cfg->num_layers * cfg->num_pages * cfg->num_kv_heads *
+                            cfg->page_size;
+  c->use_tc = c->rows >= 16 && pool_rows < (1ll << 31);
+  if (c->use_tc && !hw::make_tc_maps(*cfg, k_pool, v_pool, &c->maps)) return fail(HW_ERR_UNSUPPORTED);
   e = cudaHostAlloc((void**)&c->h_slots, kSlots * lay.slot_bytes, cudaHostAllocDefault);
   if (e != cudaSuccess) return fail(cuda_fail(e));
   for (int i = 0; i < kSlots; ++i) {
@@ -458,7 +466,8 @@ struct PlanOffsets {
 };
 
 // unit_cap > 0 bounds the number of units (one partial result each); 0 = the default split.
-bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0) {
+bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0,
+                          int64_t target_override = 0) {
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
   const int32_t S = c->cfg.page_size;
   const Layout& L = c->lay;
@@ -512,7 +521,8 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t u
   // kernel balances by KV entries, not by blocks, then reduces the partial results).
   int64_t total_tok = 0;
   for (int64_t t : group_tokens) total_tok += t;
-  int64_t target_units = std::max<int64_t>((int64_t)P * H, 4ll * c->num_sms);
+  int64_t target_units = std::max<int64_t>((int64_t)P * H,
+                                           target_override > 0 ? target_override : 4ll * c->num_sms);
   if (unit_cap > 0) {
     if (unit_cap < (int64_t)P * H) return false;
     // per-group counts are floored and then raised to >= 1: keep room for that raise
@@ -581,7 +591,10 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   hw_status st = c->acquire_slot(&slot);
   if (st != HW_OK) return st;
   PlanOffsets po{};
-  if (!build_attention_plan(c, c->h_slot(slot), &po)) return HW_ERR_CAPACITY;
+  // Tensor-core kernel: one CTA per SM holds all of its shared memory and TMEM, so one unit
+  // per SM, balanced by KV entries.
+  if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0))
+    return HW_ERR_CAPACITY;
   cudaStream_t s = (cudaStream_t)stream;
   char* dbase = c->d_slot(slot);
   HW_CUDA(cudaMemcpyAsync(dbase, c->h_slot(slot), po.bytes, cudaMemcpyHostToDevice, s));
@@ -615,7 +628,10 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   a.rows = c->rows;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
   const int pi = c->prof_begin(s, 0);
-  hw::launch_attention_fma(a, s);
+  if (c->use_tc)
+    hw::launch_attention_tc(a, c->maps, layer, s);
+  else
+    hw::launch_attention_fma(a, s);
   c->prof_end(pi, s);
   HW_CUDA(cudaGetLastError());
   hw::launch_merge(a, s);

@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -92,9 +93,18 @@ struct AttnArgs {
   float scale_log2;           // log2(e) / sqrt(D)
 };
 
+// TMA descriptors of the two pools, each viewed as a 2-D tensor [L*pages*H_kv*S rows][D] bf16
+// with {64 elements, 128 rows} boxes and 128-byte swizzle.
+struct TcMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+};
+
 void launch_append(const AppendArgs& a, cudaStream_t s);
 void launch_attention_fma(const AttnArgs& a, cudaStream_t s);
+void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s);
 void launch_merge(const AttnArgs& a, cudaStream_t s);
+bool make_tc_maps(const hw_config& cfg, void* k_pool, void* v_pool, TcMaps* out);
 
 // hw_concurrent_attention with the plan and the partial results in `scratch` (device).
 hw_status attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, void* out,

@@ -75,6 +75,13 @@ def test_head_dim_64_no_gqa():
     G.run_case(w, steps=2, bernoulli=0.5)
 
 
+def test_head_dim_64_tensor_cores():
+    import gpu_cases as G
+    w = G.small(wl.tiny(), num_workers=4, num_q_heads=16, num_kv_heads=2, common_len=(700,),
+                worker_len=((0, 129, 64, 300),), steps=3)
+    G.run_case(w, steps=3, bernoulli=0.5)
+
+
 def test_max_rows_128():
     import gpu_cases as G
     w = G.small(wl.c4(), num_workers=16, common_len=(600,),
