@@ -50,19 +50,22 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
+def build(verbose: bool = False, force: bool = False, extra_flags=(), lib_path: str = LIB,
+          build_dir: str = BUILD_DIR) -> str:
+    """Compile and link; ``extra_flags``/``lib_path``/``build_dir`` serve debug builds (for
+    example ``-DHW_TRACE`` into a separate library)."""
     cuda = _cuda_home()
     nvcc = os.path.join(cuda, "bin", "nvcc")
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sources()
     hdrs = _headers()
     objs = []
     jobs = []
     for src in srcs:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + hdrs):
-            cmd = [nvcc] + ARCH + COMMON + ["-c", src, "-o", obj]
+            cmd = [nvcc] + ARCH + COMMON + list(extra_flags) + ["-c", src, "-o", obj]
             if src.endswith(".cu"):
                 cmd += ["-Xptxas", "-v"] if verbose else []
             jobs.append(cmd)
@@ -78,15 +81,15 @@ def build(verbose: bool = False, force: bool = False) -> str:
                     sys.stderr.write(r.stdout + r.stderr)
                 if r.returncode:
                     raise RuntimeError("nvcc failed: " + " ".join(cmd))
-    if force or jobs or _stale(LIB, objs):
-        cmd = [nvcc] + ARCH + ["-shared", "-o", LIB + ".tmp"] + objs + [
+    if force or jobs or _stale(lib_path, objs):
+        cmd = [nvcc] + ARCH + ["-shared", "-o", lib_path + ".tmp"] + objs + [
             "-cudart", "shared", "-Xlinker", "-rpath," + os.path.join(cuda, "lib64")]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link failed: " + " ".join(cmd))
-        os.replace(LIB + ".tmp", LIB)
-    return LIB
+        os.replace(lib_path + ".tmp", lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

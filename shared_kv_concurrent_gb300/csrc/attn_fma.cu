@@ -151,21 +151,25 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
 }
 
 // K3: out = sum_u o_u 2^(m_u - M) / sum_u l_u 2^(m_u - M), M = max_u m_u; lse = (M + log2 L) ln 2.
+// One CTA per (group, row), one thread per output column; the loops over units are unrolled so
+// that their loads are in flight together.
 template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(D) merge_kernel(const AttnArgs a) {
   const Group g = a.groups[blockIdx.x];
-  constexpr int RPB = 256 / D;                  // rows handled side by side
-  const int d = threadIdx.x % D;
-  // blockIdx.y picks RPB consecutive rows of the group.
-  for (int r = blockIdx.y * RPB + threadIdx.x / D; r < min(a.rows, (int)(blockIdx.y + 1) * RPB);
-       r += RPB) {
+  const int d = threadIdx.x;
+  const int r = blockIdx.y;
+  {
+    const size_t stride = (size_t)a.rows * (D + 2);
+    const float* base = a.partials + ((size_t)g.unit_begin * a.rows + r) * (D + 2);
+    const int nu = g.unit_end - g.unit_begin;
     float M = -CUDART_INF_F;
-    for (int u = g.unit_begin; u < g.unit_end; ++u)
-      M = fmaxf(M, a.partials[((size_t)u * a.rows + r) * (D + 2) + D]);
+#pragma unroll 8
+    for (int k = 0; k < nu; ++k) M = fmaxf(M, base[k * stride + D]);
     float L = 0.f, O = 0.f;
     if (M != -CUDART_INF_F) {
-      for (int u = g.unit_begin; u < g.unit_end; ++u) {
-        const float* part = a.partials + ((size_t)u * a.rows + r) * (D + 2);
+#pragma unroll 8
+      for (int k = 0; k < nu; ++k) {
+        const float* part = base + k * stride;
         const float sc = exp2f(part[D] - M);
         L = fmaf(part[D + 1], sc, L);
         O = fmaf(part[d], sc, O);
@@ -202,9 +206,9 @@ void launch_attention_fma(const AttnArgs& a, cudaStream_t s) {
 void launch_merge(const AttnArgs& a, cudaStream_t s) {
   if (a.num_groups <= 0) return;
   if (a.D == 64)
-    merge_kernel<64><<<dim3(a.num_groups, (a.rows + 3) / 4), 256, 0, s>>>(a);
+    merge_kernel<64><<<dim3(a.num_groups, a.rows), 64, 0, s>>>(a);
   else
-    merge_kernel<128><<<dim3(a.num_groups, (a.rows + 1) / 2), 256, 0, s>>>(a);
+    merge_kernel<128><<<dim3(a.num_groups, a.rows), 128, 0, s>>>(a);
 }
 
 }  // namespace hw

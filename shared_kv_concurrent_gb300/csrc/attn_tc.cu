@@ -6,19 +6,31 @@
 // group, each through its own rotated query.  The work is split over KV entries and the
 // partial results reduced afterwards (section 9).
 //
-// One CTA = one unit: a run of pieces (<= 256 tokens of one segment inside one page) of one
-// (problem, KV head).  Per 128-token tile:
-//   S  = Q~ K^T      tcgen05.mma, M = 128 query rows (W*G real rows, the rest zero),
-//                    N = 128 tokens, K = D; A = rotated queries (smem), B = K tile (smem, TMA)
-//   P  = 2^(S - m)   softmax threads, one query row per thread (row = TMEM lane), max and sum
-//                    thread-local; the running max only moves when it grows by > 2^8, and then
-//                    the thread rescales its own row of O in TMEM; P goes back to TMEM as bf16
-//   O += P V         tcgen05.mma with A = P from TMEM, B = V tile (smem, MN-major), D = TMEM
-// Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2-3 query rotation per segment,
+// Two kernels:
+//   rotate_kernel  one CTA per (segment slot, KV head): rotates the group's queries for that
+//                  segment, pre-scales them by log2(e)/sqrt(D) and writes the 128-row bf16 A
+//                  tile in exactly the swizzled layout the MMA reads from shared memory.
+//   attn_tc_kernel one CTA = one unit: a run of pieces (<= 256 tokens of one segment inside one
+//                  page) of one (problem, KV head).  Per 128-token tile:
+//     S  = Q~ K^T     tcgen05.mma, M = 128 TMEM lanes, N = 128 tokens, K = D; A = rotated
+//                     queries (smem, bulk-copied), B = K tile (smem, TMA, 128-byte swizzle)
+//     P  = 2^(S - m)  softmax threads, one TMEM lane each.  Every real query row is repeated T
+//                     times in A, once per softmax warp group, and warp group j takes tokens
+//                     [j*128/T, (j+1)*128/T) of every tile: each lane keeps its own running max
+//                     (moved only when it grows by more than 2^8, then the lane rescales its
+//                     own O row in TMEM), sum and O row over its tokens.  P goes to dedicated
+//                     TMEM columns as bf16, zero outside the warp's token range.
+//     O += P V        tcgen05.mma with A = P from TMEM, B = V tile (smem, MN-major), D = TMEM;
+//                     the epilogue merges the T partial rows of each query row by log-sum-exp
+// T = 4, 2, 1 for up to 32, 64, 128 real rows, so that every SM sub-partition runs softmax.
+// Warp roles: 0 TMA producer (query tiles, K and V tiles), 1 MMA issuer and TMEM owner,
 // 4-7 softmax / correction / epilogue.  Every K/V element is loaded from HBM once per unit and
 // used by all W*G rows; S is double-buffered so the softmax of tile i overlaps MMA2(i-1) and
-// MMA1(i+1).  All waits are bounded: a wait that runs out raises a CTA abort flag, records
-// ERR_TIMEOUT in the error word, drains the copies and MMAs already issued and frees TMEM.
+// MMA1(i+1).  All waits are bounded: one that runs out raises a CTA abort flag, records
+// ERR_TIMEOUT in the error word, and the CTA drains the copies and MMAs it issued and frees
+// its TMEM.  Launch chaining: rotate_kernel lets the attention kernel start early
+// (programmatic dependent launch); the attention kernel waits for it only before loading the
+// first query tile, and lets the merge kernel start during its epilogue.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -33,10 +45,13 @@ namespace {
 using namespace tc;
 
 constexpr int kTile = 128;                  // tokens per tile = N of the first MMA
-constexpr int kRowsM = 128;                 // M of both MMAs (query rows, zero padded)
+constexpr int kRowsM = 128;                 // M of both MMAs (TMEM lanes)
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+// TMEM columns: two S buffers, O, and two P buffers of their own.  P must not alias S: the
+// MMA that writes S(i+2) is issued right after the one that reads P(i), and the tensor core
+// may overlap the two.
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
@@ -45,7 +60,7 @@ struct Cfg {
   static constexpr int kHalves = D / 64;                       // 128-byte swizzle atoms per row
   static constexpr uint32_t kHalfBytes = kTile * 128;          // one {64, 128} TMA box
   static constexpr uint32_t kTileBytes = kHalves * kHalfBytes; // K or V tile
-  static constexpr uint32_t kQBytes = kRowsM * D * 2;
+  static constexpr uint32_t kQBytes = kRowsM * D * 2;          // rotated query tile
   static constexpr int kSlots = D == 128 ? 5 : 8;
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kRingOff = 2 * kQBytes;
@@ -55,6 +70,31 @@ struct Cfg {
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
 };
+
+// Timeline tracing, compiled in only with -DHW_TRACE (a separate debug build of the library):
+// %globaltimer stamps per CTA -- 0 start, 1 set-up done, 2 first query tile issued,
+// 3 producer done, 4 MMA issuer done, 5 epilogue start, 6 epilogue end, 7 end; then per tile
+// i < 60: 8+4i K(i) issued, 9+4i MMA1(i) issued, 10+4i S(i) seen by softmax, 11+4i P(i) written.
+#ifdef HW_TRACE
+constexpr int kTraceCtas = 160, kTraceEvents = 256;
+__device__ unsigned long long g_trace[kTraceCtas][kTraceEvents];
+#define HW_TRACE_EV(idx)                                                   \
+  do {                                                                     \
+    const int ev_ = (idx);                                                 \
+    if (blockIdx.x < kTraceCtas && ev_ < kTraceEvents)                     \
+      g_trace[blockIdx.x][ev_] = globaltimer_ns();                         \
+  } while (0)
+#else
+#define HW_TRACE_EV(idx) \
+  do {                   \
+  } while (0)
+#endif
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 struct TileInfo {
   int32_t seg_slot, page, slot0, nvalid;
@@ -112,10 +152,100 @@ struct TileWalker {
   }
 };
 
-template <int D>
+// ---------------------------------------------------------------------------- rotation
+
+// Tile (slot, h): 128 M-rows x D bf16 in the MMA's shared-memory layout (two 64-column atoms
+// for D = 128, 128-byte swizzle: the 16-byte chunk c of M-row m sits at chunk c ^ (m % 8)).
+// M-row m (TMEM lane m, softmax warp q = m / 32) holds query row r = 32 * (q % (4 / T)) +
+// m % 32 of the group: each query row is repeated T times, once per column chunk (see the
+// softmax below).  Rows are rotated by (i_q - view offset) of their worker for this segment
+// and pre-scaled by log2(e)/sqrt(D); rows past W*G, and rows whose worker does not see the
+// segment, are zero.  Two threads per M-row, each owning half of the 8-pair chunks; all loads
+// are issued before any is used.
+template <int D, int T>
+__global__ void __launch_bounds__(256) rotate_kernel(const AttnArgs a) {
+  pdl_launch_dependents();
+  constexpr int half = D / 2;
+  constexpr int CH = half / 8;                 // 8-pair chunks per M-row
+  constexpr int CPT = CH / 2;                  // chunks per thread
+  constexpr int WPC = 4 / T;                   // softmax warps per column chunk
+  constexpr uint32_t kHalfBytes = kTile * 128;
+  const int slot = blockIdx.x / a.H_kv, h = blockIdx.x % a.H_kv;
+  if (slot >= a.num_seg_slots) return;
+  const int p = a.slot_problem[slot];
+  const int m = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * CPT;
+  const int r = 32 * ((m >> 5) % WPC) + (m & 31);
+  int delta = -1;
+  size_t qo = 0;
+  if (r < a.rows && p >= 0 && p < a.P) {
+    const int w = r / a.G, hq = h * a.G + r % a.G;
+    delta = a.delta[(size_t)slot * a.W + w];
+    qo = (((size_t)p * a.W + w) * a.H_q + hq) * D;
+    if (delta >= a.max_position) {
+      record_error(a.err, ERR_POS_RANGE, KID_ATTN_TC, blockIdx.x, delta);
+      delta = -1;
+    }
+  }
+  uint4 q1[CPT], q2[CPT];
+  float4 cs[CPT][2], sn[CPT][2];
+  if (delta >= 0) {
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+      const int c = c0 + k;
+      q1[k] = *reinterpret_cast<const uint4*>(a.q + qo + 8 * c);
+      q2[k] = *reinterpret_cast<const uint4*>(a.q + qo + half + 8 * c);
+      const float4* cp = reinterpret_cast<const float4*>(a.rope_cos + (size_t)delta * half + 8 * c);
+      const float4* sp = reinterpret_cast<const float4*>(a.rope_sin + (size_t)delta * half + 8 * c);
+      cs[k][0] = cp[0];
+      cs[k][1] = cp[1];
+      sn[k][0] = sp[0];
+      sn[k][1] = sp[1];
+    }
+  }
+  uint8_t* tile = a.qtiles + ((size_t)slot * a.H_kv + h) * (size_t)(kRowsM * D * 2);
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) {
+    const int c = c0 + k;
+    uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
+    if (delta >= 0) {
+      const __nv_bfloat162* x1p = reinterpret_cast<const __nv_bfloat162*>(&q1[k]);
+      const __nv_bfloat162* x2p = reinterpret_cast<const __nv_bfloat162*>(&q2[k]);
+      const float cv[8] = {cs[k][0].x, cs[k][0].y, cs[k][0].z, cs[k][0].w,
+                           cs[k][1].x, cs[k][1].y, cs[k][1].z, cs[k][1].w};
+      const float sv[8] = {sn[k][0].x, sn[k][0].y, sn[k][0].z, sn[k][0].w,
+                           sn[k][1].x, sn[k][1].y, sn[k][1].z, sn[k][1].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x1 = __bfloat1622float2(x1p[e]);
+        const float2 x2 = __bfloat1622float2(x2p[e]);
+        const float ca = cv[2 * e], cb = cv[2 * e + 1];
+        const float sa = sv[2 * e], sb = sv[2 * e + 1];
+        const __nv_bfloat162 y1 = __floats2bfloat162_rn((x1.x * ca - x2.x * sa) * a.scale_log2,
+                                                        (x1.y * cb - x2.y * sb) * a.scale_log2);
+        const __nv_bfloat162 y2 = __floats2bfloat162_rn((x2.x * ca + x1.x * sa) * a.scale_log2,
+                                                        (x2.y * cb + x1.y * sb) * a.scale_log2);
+        lo[e] = *reinterpret_cast<const uint32_t*>(&y1);
+        hi[e] = *reinterpret_cast<const uint32_t*>(&y2);
+      }
+    }
+    const int d_lo = 8 * c, d_hi = half + 8 * c;
+    uint8_t* p_lo = tile + (d_lo >> 6) * kHalfBytes + m * 128 + ((((d_lo & 63) >> 3) ^ (m & 7)) << 4);
+    uint8_t* p_hi = tile + (d_hi >> 6) * kHalfBytes + m * 128 + ((((d_hi & 63) >> 3) ^ (m & 7)) << 4);
+    *reinterpret_cast<uint4*>(p_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(p_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  }
+}
+
+// ---------------------------------------------------------------------------- attention
+
+template <int D, int T>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ TcMaps maps, const int32_t layer) {
   using C = Cfg<D>;
+  static_assert(T == 1 || T == 2 || T == 4, "T copies of each query row, one per column chunk");
+  constexpr int WPC = 4 / T;                  // softmax warps per column chunk
+  constexpr int CPT = kTile / T;              // token columns per lane
+  constexpr int PCPT = CPT / 2;               // packed bf16 P columns per lane
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -138,7 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Unit u = a.units[blockIdx.x];
   const Group g = a.groups[u.group];
   const int R = a.rows;
-  const int active_softmax_warps = (R + 31) / 32;
+  int active_softmax_warps = 0;               // softmax warps that own at least one real row
+  for (int q = 0; q < 4; ++q) active_softmax_warps += (32 * (q % WPC) < R) ? 1 : 0;
+  if (threadIdx.x == 0) HW_TRACE_EV(0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kSlots; ++s) {
@@ -146,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_qfull(b), 64);
+      mbar_init(bar_qfull(b), 1);
       mbar_init(bar_qempty(b), 1);
       mbar_init(bar_sfull(b), 1);
       mbar_init(bar_pfull(b), 32 * active_softmax_warps);
@@ -168,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) HW_TRACE_EV(1);
 
   const int64_t page_base = (int64_t)layer * a.num_pages;   // first page of this layer's pool
 
@@ -178,27 +311,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileWalker tw;
       tw.init(a, u);
       TileInfo t;
-      bool ns;
-      uint32_t j = 0;
+      bool new_seg;
+      uint32_t j = 0, seg = 0;
       bool ok = true;
-      while (ok && tw.next(&t, &ns)) {
+      while (ok && tw.next(&t, &new_seg)) {
+        // K and V of the tile first: the pools were written by kernels that completed before
+        // this one started.
         const int32_t y = (int32_t)(((page_base + t.page) * a.H_kv + g.h) * a.S + t.slot0);
         for (int part = 0; part < 2 && ok; ++part, ++j) {
           const int s = j % C::kSlots;
           if (j >= (uint32_t)C::kSlots)
             ok = mbar_wait(bar_empty(s), ((j / C::kSlots) - 1) & 1, abort, kWaitLimitNs);
           if (!ok) break;
+          if (part == 0) HW_TRACE_EV(8 + 4 * (j >> 1));
           mbar_arrive_expect_tx(bar_full(s), C::kTileBytes);
           const CUtensorMap* m = part == 0 ? &maps.k : &maps.v;
+#pragma unroll
           for (int h = 0; h < C::kHalves; ++h)
             tma_load_2d(ring + s * C::kTileBytes + h * C::kHalfBytes, m, 64 * h, y, bar_full(s),
                         policy);
         }
+        if (ok && new_seg) {
+          // Rotated query tile of this segment, written by the rotation kernel that precedes
+          // this launch: wait for it (once) before the first read.
+          const int qb = seg & 1;
+          if (seg == 0) pdl_wait();
+          if (seg >= 2)
+            ok = mbar_wait(bar_qempty(qb), ((seg >> 1) - 1) & 1, abort, kWaitLimitNs);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar_qfull(qb), C::kQBytes);
+          bulk_load(q_base + qb * C::kQBytes,
+                    a.qtiles + ((size_t)t.seg_slot * a.H_kv + g.h) * C::kQBytes, C::kQBytes,
+                    bar_qfull(qb));
+          if (seg == 0) HW_TRACE_EV(2);
+          ++seg;
+        }
       }
-      // Drain: every load issued must have landed before the CTA can exit.
+      HW_TRACE_EV(3);
+      // Drain: every copy issued must have landed before the CTA can exit.
       for (uint32_t s = 0; s < (uint32_t)C::kSlots && s < j; ++s) {
         const uint32_t last = s + ((j - 1 - s) / C::kSlots) * C::kSlots;
         mbar_wait(bar_full(s), (last / C::kSlots) & 1, abort, kWaitLimitNs);
+      }
+      for (uint32_t b = 0; b < 2 && b < seg; ++b) {
+        const uint32_t last = b + ((seg - 1 - b) / 2) * 2;
+        mbar_wait(bar_qfull(b), (last >> 1) & 1, abort, kWaitLimitNs);
       }
       if (!ok && (*abort)) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 0);
     }
@@ -223,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar_full(s), (jv / C::kSlots) & 1, abort, kWaitLimitNs)) return false;
         tc_fence_after();
         const uint32_t vb = ring + s * C::kTileBytes;
-        const uint32_t p_tmem = tmem + (b ? kColS1 : kColS0);
+        const uint32_t p_tmem = tmem + (b ? kColP1 : kColP0);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint64_t bdesc = smem_desc(vb + kk * 2048, C::kHalfBytes, 1024, kSwizzle128);
@@ -256,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + (b ? kColS1 : kColS0), adesc, bdesc, idesc1, kk > 0 ? 1u : 0u);
         }
         issued_any = true;
+        HW_TRACE_EV(9 + 4 * i);
         mma_commit(bar_empty(s));
         mma_commit(bar_sfull(b));
         if (tw.last_of_segment()) mma_commit(bar_qempty(qbuf));
@@ -263,83 +421,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++i;
       }
       if (ok && i > 0) ok = issue_mma2(i - 1);
+      HW_TRACE_EV(4);
       if (issued_any) {
         mma_commit(bar_fin);
         mbar_wait(bar_fin, 0, abort, kWaitLimitNs);
       }
       if (!ok && (*abort)) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 1);
     }
-  } else if (warp < 4) {
-    // ---------------------------------------------------------------- query rotation
-    const int tq = threadIdx.x - 64;          // 0..63, rows tq and tq + 64
-    TileWalker tw;
-    tw.init(a, u);
-    TileInfo t;
-    bool new_seg;
-    uint32_t seg = 0;
-    const int half = D / 2;
-    while (tw.next(&t, &new_seg)) {
-      if (!new_seg) continue;
-      const int qb = seg & 1;
-      if (seg >= 2 && !mbar_wait(bar_qempty(qb), ((seg >> 1) - 1) & 1, abort, kWaitLimitNs)) break;
-      uint8_t* qs = smem + C::kQOff + qb * C::kQBytes;
-      const int32_t* dl = a.delta + (size_t)t.seg_slot * a.W;
-      for (int rr = 0; rr < 2; ++rr) {
-        const int r = tq + 64 * rr;
-        int delta = -1;
-        size_t qo = 0;
-        if (r < R) {
-          const int w = r / a.G, hq = g.h * a.G + r % a.G;
-          delta = dl[w];
-          qo = (((size_t)g.p * a.W + w) * a.H_q + hq) * D;
-          if (delta >= a.max_position) {
-            record_error(a.err, ERR_POS_RANGE, KID_ATTN_TC, blockIdx.x, delta);
-            delta = -1;
-          }
-        }
-        // 8-element chunks: chunk c of the first half pairs with chunk c of the second half.
-#pragma unroll 1
-        for (int c = 0; c < half / 8; ++c) {
-          uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
-          if (delta >= 0) {
-            const uint4 q1v = *reinterpret_cast<const uint4*>(a.q + qo + 8 * c);
-            const uint4 q2v = *reinterpret_cast<const uint4*>(a.q + qo + half + 8 * c);
-            const __nv_bfloat162* q1 = reinterpret_cast<const __nv_bfloat162*>(&q1v);
-            const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&q2v);
-            const float* cs = a.rope_cos + (size_t)delta * half + 8 * c;
-            const float* sn = a.rope_sin + (size_t)delta * half + 8 * c;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 x1 = __bfloat1622float2(q1[e]);
-              const float2 x2 = __bfloat1622float2(q2[e]);
-              const float c0 = cs[2 * e], c1 = cs[2 * e + 1];
-              const float s0 = sn[2 * e], s1 = sn[2 * e + 1];
-              const __nv_bfloat162 y1 = __floats2bfloat162_rn((x1.x * c0 - x2.x * s0) * a.scale_log2,
-                                                              (x1.y * c1 - x2.y * s1) * a.scale_log2);
-              const __nv_bfloat162 y2 = __floats2bfloat162_rn((x2.x * c0 + x1.x * s0) * a.scale_log2,
-                                                              (x2.y * c1 + x1.y * s1) * a.scale_log2);
-              lo[e] = *reinterpret_cast<const uint32_t*>(&y1);
-              hi[e] = *reinterpret_cast<const uint32_t*>(&y2);
-            }
-          }
-          // element d of row r: atom d / 64, 16-byte chunk ((d % 64) / 8) ^ (r % 8)
-          const int d_lo = 8 * c, d_hi = half + 8 * c;
-          uint8_t* p_lo = qs + (d_lo >> 6) * C::kHalfBytes + r * 128 + ((((d_lo & 63) >> 3) ^ (r & 7)) << 4);
-          uint8_t* p_hi = qs + (d_hi >> 6) * C::kHalfBytes + r * 128 + ((((d_hi & 63) >> 3) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(p_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          *reinterpret_cast<uint4*>(p_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar_qfull(qb));
-      ++seg;
-    }
-  } else {
+  } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax / epilogue
+    // Softmax warp q takes the token columns [cq * 128/T, (cq + 1) * 128/T) of every tile,
+    // cq = q / (4/T), for query rows 32 * (q % (4/T)) + lane.  The column range is the same for
+    // the whole warp, so S and P move with warp-uniform TMEM addresses, and every lane keeps
+    // its own running max, sum and O row over its columns; the epilogue merges the T lanes of
+    // a row by log-sum-exp.
     const int wq = warp - 4;                  // TMEM lane quarter of this warp
-    const int r = 32 * wq + lane;
-    if (wq < active_softmax_warps) {
+    const int cq = wq / WPC;                  // column chunk of this warp
+    const int r = 32 * (wq % WPC) + lane;     // query row of this lane
+    if (32 * (wq % WPC) < R) {
       const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
+      {
+        // This warp only ever writes its own P columns: zero both P buffers once.
+        uint32_t z[kTile / 2];
+#pragma unroll
+        for (int e = 0; e < kTile / 2; ++e) z[e] = 0u;
+        tmem_st64_sync(tmem + lane_off + kColP0, z);
+        tmem_st64_sync(tmem + lane_off + kColP1, z);
+      }
       float m_run = -CUDART_INF_F, l_sum = 0.f;
       TileWalker tw;
       tw.init(a, u);
@@ -349,99 +457,141 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       bool row_visible = false;
       while (tw.next(&t, &new_seg)) {
-        if (new_seg) {
-          row_visible = r < R && a.delta[(size_t)t.seg_slot * a.W + r / a.G] >= 0;
-        }
+        if (new_seg) row_visible = r < R && a.delta[(size_t)t.seg_slot * a.W + r / a.G] >= 0;
         const int b = i & 1;
-        if (!mbar_wait(bar_sfull(b), (i >> 1) & 1, abort, kWaitLimitNs)) {
+        // (warp-uniform outcome: the TMEM accesses below need every lane)
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(b), (i >> 1) & 1, abort, kWaitLimitNs))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t s_tmem = tmem + lane_off + (b ? kColS1 : kColS0);
-        float s[kTile];
+        if (threadIdx.x == 128) HW_TRACE_EV(10 + 4 * i);
+        float s[CPT];
+        {
+          uint32_t v[CPT];
+          tmem_ld_sync<CPT>(tmem + lane_off + (b ? kColS1 : kColS0) + cq * CPT, v);
 #pragma unroll
-        for (int c = 0; c < kTile / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(s_tmem + 32 * c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(v[e]);
+          for (int k = 0; k < CPT; ++k) s[k] = __uint_as_float(v[k]);
         }
+        const int limit = row_visible ? max(0, min(CPT, t.nvalid - cq * CPT)) : 0;
         float mx = -CUDART_INF_F;
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) {
-          if (c >= t.nvalid || !row_visible) s[c] = -CUDART_INF_F;
-          mx = fmaxf(mx, s[c]);
+        for (int k = 0; k < CPT; ++k) {
+          if (k >= limit) s[k] = -CUDART_INF_F;
+          mx = fmaxf(mx, s[k]);
         }
         const bool need = mx > m_run + kRescaleThreshold || (m_run == -CUDART_INF_F && mx > m_run);
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? fmaxf(m_run, mx) : m_run;
-          const float alpha = (m_run == -CUDART_INF_F) ? 0.f : exp2f(m_run - m_new);
-          l_sum *= need ? alpha : 1.f;
+          const float alpha = (m_run == -CUDART_INF_F) ? 0.f : fast_exp2(m_run - m_new);
+          const float sc = need ? alpha : 1.f;
+          l_sum *= sc;
           if (i > 0) {
-            // O holds MMA2 results up to tile i-1: wait for the last of them, rescale this row.
-            if (!mbar_wait(bar_odone, (i - 1) & 1, abort, kWaitLimitNs)) {
+            // O holds MMA2 results up to tile i-1: wait for the last of them, rescale the row.
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_odone, (i - 1) & 1, abort, kWaitLimitNs))) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const float sc = need ? alpha : 1.f;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
               uint32_t v[32];
-              tmem_ld32(tmem + lane_off + kColO + 32 * c, v);
-              tmem_wait_ld();
+              tmem_ld32_sync(tmem + lane_off + kColO + 32 * c, v);
 #pragma unroll
               for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * sc);
-              tmem_st32(tmem + lane_off + kColO + 32 * c, v);
+              tmem_st32_sync(tmem + lane_off + kColO + 32 * c, v);
             }
-            tmem_wait_st();
           }
           m_run = m_new;
         }
         const float m_use = (m_run == -CUDART_INF_F) ? 0.f : m_run;
+        uint32_t own[PCPT];
 #pragma unroll
-        for (int c = 0; c < kTile / 64; ++c) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float p0 = exp2f(s[64 * c + 2 * e] - m_use);
-            const float p1 = exp2f(s[64 * c + 2 * e + 1] - m_use);
-            l_sum += p0 + p1;
-            const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-            pk[e] = *reinterpret_cast<const uint32_t*>(&pp);
-          }
-          tmem_st32(s_tmem + 32 * c, pk);
+        for (int e = 0; e < PCPT; ++e) {
+          const float p0 = fast_exp2(s[2 * e] - m_use);
+          const float p1 = fast_exp2(s[2 * e + 1] - m_use);
+          l_sum += p0 + p1;
+          const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+          own[e] = *reinterpret_cast<const uint32_t*>(&pp);
         }
-        tmem_wait_st();
+        tmem_st_sync<PCPT>(tmem + lane_off + (b ? kColP1 : kColP0) + cq * PCPT, own);
         tc_fence_before();
         mbar_arrive(bar_pfull(b));
+        if (threadIdx.x == 128) HW_TRACE_EV(11 + 4 * i);
         ++i;
       }
-      // Epilogue: unnormalised o, running max and sum of this row (log2 domain).
-      float* part = a.partials + ((size_t)blockIdx.x * R + r) * (D + 2);
+      if (threadIdx.x == 128) {
+        HW_TRACE_EV(5);
+        pdl_launch_dependents();
+      }
+      // Epilogue.  Each lane's (O row, max, sum) over its columns goes to shared memory (the
+      // K/V ring is idle once the last MMA has completed) as stage[chunk][row][D + 2]; then the
+      // T chunks of every row are merged by log-sum-exp and the unit's partials -- unnormalised
+      // o, max and sum in the log2 domain, [rows][D + 2] fp32 -- are stored with coalesced
+      // writes.
+      // Wait for every MMA through the single-use `fin` barrier, not o_done: here o_done may be
+      // two phases behind (the last two P.V products can both be in flight), and a parity
+      // wait cannot tell that apart from "done".
       bool have = ok && i > 0;
       if (have) {
-        have = mbar_wait(bar_odone, (i - 1) & 1, abort, kWaitLimitNs);
+        have = mbar_wait(bar_fin, 0, abort, kWaitLimitNs);
         tc_fence_after();
       }
+      have = __all_sync(0xffffffffu, have);
+      if (threadIdx.x == 128) HW_TRACE_EV(250);
+      float* stage = reinterpret_cast<float*>(smem + C::kRingOff);
+      const bool writer = r < R;
+      float* srow = stage + ((size_t)cq * R + r) * (D + 2);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
-        if (have) {
-          tmem_ld32(tmem + lane_off + kColO + 32 * c, v);
-          tmem_wait_ld();
-        }
-        if (r < R) {
+        if (have) tmem_ld32_sync(tmem + lane_off + kColO + 32 * c, v);
+        if (writer) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) part[32 * c + e] = have ? __uint_as_float(v[e]) : 0.f;
+          for (int e = 0; e < 32; ++e) srow[32 * c + e] = have ? __uint_as_float(v[e]) : 0.f;
         }
       }
-      if (r < R) {
-        part[D] = have ? m_run : -CUDART_INF_F;
-        part[D + 1] = have ? l_sum : 0.f;
+      if (writer) {
+        srow[D] = have ? m_run : -CUDART_INF_F;
+        srow[D + 1] = have ? l_sum : 0.f;
       }
+      const int nthr = 32 * active_softmax_warps;
+      asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
+      if (threadIdx.x == 128) HW_TRACE_EV(251);
+      // Per row: M = max over the T chunks, and each chunk's weight 2^(m_j - M).
+      float* rowM = stage + (size_t)T * R * (D + 2);
+      float* rowW = rowM + R;                                  // [T][R]
+      for (int rr = threadIdx.x - 128; rr < R; rr += nthr) {
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int j = 0; j < T; ++j) M = fmaxf(M, stage[((size_t)j * R + rr) * (D + 2) + D]);
+        rowM[rr] = M;
+#pragma unroll
+        for (int j = 0; j < T; ++j)
+          rowW[j * R + rr] =
+              (M == -CUDART_INF_F) ? 0.f : fast_exp2(stage[((size_t)j * R + rr) * (D + 2) + D] - M);
+      }
+      asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
+      if (threadIdx.x == 128) HW_TRACE_EV(252);
+      // One warp per row, lanes across the D + 2 values: coalesced stores.
+      float* part = a.partials + (size_t)blockIdx.x * R * (D + 2);
+      for (int rr = wq; rr < R; rr += active_softmax_warps) {
+        float wj[T];
+#pragma unroll
+        for (int j = 0; j < T; ++j) wj[j] = rowW[j * R + rr];
+        for (int d = lane; d < D + 2; d += 32) {
+          float val;
+          if (d == D) {
+            val = rowM[rr];
+          } else {
+            val = 0.f;
+#pragma unroll
+            for (int j = 0; j < T; ++j) val = fmaf(stage[((size_t)j * R + rr) * (D + 2) + d], wj[j], val);
+          }
+          part[(size_t)rr * (D + 2) + d] = val;
+        }
+      }
+      if (threadIdx.x == 128) HW_TRACE_EV(6);
       if (!ok && (*abort) && lane == 0) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 2);
     }
   }
@@ -451,17 +601,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (threadIdx.x == 0) HW_TRACE_EV(7);
 }
 
 }  // namespace
 
-template <int D>
-static void launch_tc_d(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
+#ifdef HW_TRACE
+// Debug builds only: copy out / clear the timeline stamps (uint64 [160][256], ns).
+extern "C" int hw_trace_read(void* dst, size_t bytes) {
+  const size_t n = bytes < sizeof(g_trace) ? bytes : sizeof(g_trace);
+  return (int)cudaMemcpyFromSymbol(dst, g_trace, n);
+}
+extern "C" int hw_trace_clear(void) {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_trace);
+  if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(g_trace));
+  return (int)e;
+}
+#endif
+
+template <int D, int T>
+static void launch_tc_dt(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
   using C = Cfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
-  cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  rotate_kernel<D, T><<<a.num_seg_slots * a.H_kv, 256, 0, s>>>(a);
+  cudaFuncSetAttribute(attn_tc_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)C::kSmemBytes);
-  attn_tc_kernel<D><<<a.num_units, kThreads, C::kSmemBytes, s>>>(a, maps, layer);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_units);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, T>, a, maps, (int32_t)layer);
+}
+
+template <int D>
+static void launch_tc_d(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
+  if (a.rows <= 32)
+    launch_tc_dt<D, 4>(a, maps, layer, s);
+  else if (a.rows <= 64)
+    launch_tc_dt<D, 2>(a, maps, layer, s);
+  else
+    launch_tc_dt<D, 1>(a, maps, layer, s);
 }
 
 void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {

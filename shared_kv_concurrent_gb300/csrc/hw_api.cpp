@@ -47,7 +47,7 @@ hw_status cuda_fail(cudaError_t e) {
   } while (0)
 
 struct Layout {
-  size_t err, cos, sin, slots, partials, tickets, total;
+  size_t err, cos, sin, slots, partials, tickets, qtiles, total;
   size_t slot_bytes;
   int32_t max_segments, max_append, max_pieces, max_units, max_seg_slots, rows;
 };
@@ -86,7 +86,8 @@ Layout make_layout(const hw_config* c) {
   const size_t attn_bytes = align_up((size_t)L.max_pieces * sizeof(hw::Piece), 16) +
                             align_up((size_t)L.max_units * sizeof(hw::Unit), 16) +
                             align_up((size_t)P * H * sizeof(hw::Group), 16) +
-                            align_up((size_t)L.max_seg_slots * W * sizeof(int32_t), 16);
+                            align_up((size_t)L.max_seg_slots * W * sizeof(int32_t), 16) +
+                            align_up((size_t)L.max_seg_slots * sizeof(int32_t), 16);
   L.slot_bytes = align_up(std::max(append_bytes, attn_bytes), kAlign);
   size_t off = 0;
   L.err = off;
@@ -102,6 +103,10 @@ Layout make_layout(const hw_config* c) {
   off += align_up((size_t)L.max_units * L.rows * (c->head_dim + 2) * sizeof(float), kAlign);
   L.tickets = off;
   off += align_up((size_t)P * H * sizeof(uint32_t), kAlign);
+  // Rotated query tiles of the tensor-core path: one 128-row x D bf16 tile per (segment slot,
+  // KV head), laid out exactly as the kernel's shared-memory operand.
+  L.qtiles = off;
+  off += (size_t)L.max_seg_slots * H * 128 * c->head_dim * 2;
   L.total = off;
   return L;
 }
@@ -461,7 +466,7 @@ namespace {
 // Build the attention plan of the current state into host buffer `buf` (slot_bytes long).
 // Returns false if a table would overflow.  Offsets of each array are written to `off`.
 struct PlanOffsets {
-  size_t pieces, units, groups, delta, bytes;
+  size_t pieces, units, groups, delta, slot_problem, bytes;
   int32_t num_pieces, num_units, num_groups, num_seg_slots;
 };
 
@@ -473,6 +478,7 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t u
   const Layout& L = c->lay;
   std::vector<hw::Piece> pieces;
   std::vector<int32_t> delta;
+  std::vector<int32_t> slot_problem;
   std::vector<int64_t> group_tokens(P * H, 0);
   std::vector<int32_t> group_piece_begin(P * H + 1, 0);
   struct SegRef { int32_t sid, slot; };
@@ -488,6 +494,7 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t u
     const int32_t slot_base = (int32_t)(delta.size() / (size_t)W);
     if (slot_base + (int64_t)refs.size() > L.max_seg_slots) return false;
     delta.resize(delta.size() + refs.size() * (size_t)W, -1);
+    slot_problem.resize(slot_problem.size() + refs.size(), p);
     for (size_t r = 0; r < refs.size(); ++r) refs[r].slot = slot_base + (int32_t)r;
     for (int32_t w = 0; w < W; ++w) {
       std::vector<int32_t> ids, offs, lens;
@@ -506,7 +513,8 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t u
         const int32_t slot0 = c->cfg.contiguous ? j : j % S;
         const int32_t cnt = std::min(std::min(kPieceMax, S - slot0), n - j);
         proto.push_back(hw::Piece{r.slot, pg, slot0, cnt});
-        tok += cnt;
+        // Balance by 128-token tiles: a partial tile costs the kernels a full one.
+        tok += (cnt + 127) / 128 * 128;
       }
     }
     for (int32_t h = 0; h < H; ++h) {
@@ -542,7 +550,8 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t u
       int64_t cum = 0;
       int32_t cur = -1;
       for (int32_t i = pb; i < pe; ++i) {
-        const int64_t mid2 = 2 * cum + pieces[i].ntok;        // twice the piece midpoint
+        const int64_t wt = (pieces[i].ntok + 127) / 128 * 128;  // tile-rounded weight
+        const int64_t mid2 = 2 * cum + wt;                      // twice the piece midpoint
         const int32_t k = (int32_t)std::min<int64_t>(n_units - 1, (mid2 * n_units) / (2 * T));
         if (k != cur) {
           units.push_back(hw::Unit{i, i + 1, g, 0});
@@ -550,7 +559,7 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t u
         } else {
           units.back().piece_end = i + 1;
         }
-        cum += pieces[i].ntok;
+        cum += wt;
       }
     }
     gr.unit_end = (int32_t)units.size();
@@ -567,12 +576,15 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t u
   off = align_up(off + groups.size() * sizeof(hw::Group), 16);
   po->delta = off;
   off = align_up(off + delta.size() * sizeof(int32_t), 16);
+  po->slot_problem = off;
+  off = align_up(off + slot_problem.size() * sizeof(int32_t), 16);
   po->bytes = off;
   if (off > L.slot_bytes) return false;
   std::memcpy(buf + po->pieces, pieces.data(), pieces.size() * sizeof(hw::Piece));
   std::memcpy(buf + po->units, units.data(), units.size() * sizeof(hw::Unit));
   std::memcpy(buf + po->groups, groups.data(), groups.size() * sizeof(hw::Group));
   std::memcpy(buf + po->delta, delta.data(), delta.size() * sizeof(int32_t));
+  std::memcpy(buf + po->slot_problem, slot_problem.data(), slot_problem.size() * sizeof(int32_t));
   po->num_pieces = (int32_t)pieces.size();
   po->num_units = (int32_t)units.size();
   po->num_groups = (int32_t)groups.size();
@@ -603,6 +615,8 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   a.units = reinterpret_cast<const hw::Unit*>(dbase + po.units);
   a.groups = reinterpret_cast<const hw::Group*>(dbase + po.groups);
   a.delta = reinterpret_cast<const int32_t*>(dbase + po.delta);
+  a.slot_problem = reinterpret_cast<const int32_t*>(dbase + po.slot_problem);
+  a.qtiles = reinterpret_cast<uint8_t*>(c->ws + c->lay.qtiles);
   a.num_units = po.num_units;
   a.num_groups = po.num_groups;
   a.num_seg_slots = po.num_seg_slots;
@@ -673,6 +687,7 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
   a.units = reinterpret_cast<const hw::Unit*>(scratch + po.units);
   a.groups = reinterpret_cast<const hw::Group*>(scratch + po.groups);
   a.delta = reinterpret_cast<const int32_t*>(scratch + po.delta);
+  a.slot_problem = reinterpret_cast<const int32_t*>(scratch + po.slot_problem);
   a.num_units = po.num_units;
   a.num_groups = po.num_groups;
   a.num_seg_slots = po.num_seg_slots;

@@ -78,6 +78,8 @@ struct AttnArgs {
   const Unit* units;
   const Group* groups;
   const int32_t* delta;       // [seg_slots][W]: i_q(w) - view offset, or -1 (not visible)
+  const int32_t* slot_problem;  // [seg_slots]: problem of each delta row
+  uint8_t* qtiles;            // [seg_slots][H_kv] rotated query tiles (tensor-core path)
   int32_t num_units, num_groups, num_seg_slots;
   const __nv_bfloat16* k_layer;
   const __nv_bfloat16* v_layer;
