@@ -16,6 +16,9 @@ constexpr int kTokPerCta = 16;
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
+  // The next kernels of the step (query rotation, attention) may start their own prologue now;
+  // they wait for this grid before reading what it writes.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const AppendRun run = a.runs[blockIdx.y];
   const int t0 = blockIdx.x * kTokPerCta;
   if (t0 >= run.ntok) return;

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
   for (int k = 0; k < kMaxRowsPerWarp; ++k) {
     const int r = warp + k * kWarps;
     if (r >= rows) continue;
-    float* part = a.partials + ((size_t)blockIdx.x * rows + r) * (D + 2);
+    float* part = a.partials + ((size_t)blockIdx.x * rows + r) * part_stride(D);
 #pragma unroll
     for (int j = 0; j < DJ; ++j) part[lane + 32 * j] = o[k][j];
     if (lane == 0) {
@@ -155,12 +155,14 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
 // that their loads are in flight together.
 template <int D>
 __global__ void __launch_bounds__(D) merge_kernel(const AttnArgs a) {
+  // May be launched as a programmatic dependent of the attention kernel: wait for its writes.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const Group g = a.groups[blockIdx.x];
   const int d = threadIdx.x;
   const int r = blockIdx.y;
   {
-    const size_t stride = (size_t)a.rows * (D + 2);
-    const float* base = a.partials + ((size_t)g.unit_begin * a.rows + r) * (D + 2);
+    const size_t stride = (size_t)a.rows * part_stride(D);
+    const float* base = a.partials + ((size_t)g.unit_begin * a.rows + r) * part_stride(D);
     const int nu = g.unit_end - g.unit_begin;
     float M = -CUDART_INF_F;
 #pragma unroll 8
@@ -203,12 +205,21 @@ void launch_attention_fma(const AttnArgs& a, cudaStream_t s) {
     launch_fma_d<128>(a, s);
 }
 
-void launch_merge(const AttnArgs& a, cudaStream_t s) {
+void launch_merge(const AttnArgs& a, cudaStream_t s, bool pdl) {
   if (a.num_groups <= 0) return;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_groups, a.rows);
+  cfg.blockDim = dim3(a.D);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
   if (a.D == 64)
-    merge_kernel<64><<<dim3(a.num_groups, a.rows), 64, 0, s>>>(a);
+    cudaLaunchKernelEx(&cfg, merge_kernel<64>, a);
   else
-    merge_kernel<128><<<dim3(a.num_groups, a.rows), 128, 0, s>>>(a);
+    cudaLaunchKernelEx(&cfg, merge_kernel<128>, a);
 }
 
 }  // namespace hw

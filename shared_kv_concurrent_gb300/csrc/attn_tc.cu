@@ -97,7 +97,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 struct TileInfo {
-  int32_t seg_slot, page, slot0, nvalid;
+  int32_t seg_slot, page, slot0, nvalid, fresh;
 };
 
 // Walk the tiles of a unit in order; every role runs the same walk.
@@ -135,6 +135,7 @@ struct TileWalker {
     t->page = pc.page;
     t->slot0 = pc.slot0 + k * kTile;
     t->nvalid = min(kTile, pc.ntok - k * kTile);
+    t->fresh = pc.fresh;
     *new_seg = pc.seg_slot != last_slot;
     last_slot = pc.seg_slot;
     ++k;
@@ -234,6 +235,10 @@ __global__ void __launch_bounds__(256) rotate_kernel(const AttnArgs a) {
     *reinterpret_cast<uint4*>(p_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     *reinterpret_cast<uint4*>(p_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
   }
+  // Launched as a programmatic dependent of the append kernel, whose writes it does not read:
+  // finishing only after that kernel has finished lets the attention kernel's single wait
+  // cover both.
+  pdl_wait();
 }
 
 // ---------------------------------------------------------------------------- attention
@@ -314,14 +319,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool new_seg;
       uint32_t j = 0, seg = 0;
       bool ok = true;
+      // The rotated query tiles come from the rotation kernel just before this launch, and the
+      // tiles holding this step's new tokens from the append kernel before that: neither is
+      // read before griddepcontrol.wait.  Tiles of older tokens are streamed before it, so the
+      // ring fills while the previous kernels finish; the first query tile is loaded at the
+      // latest when the ring is full, a fresh tile or a second segment comes up, or the walk ends.
+      int32_t q0_slot = -1;
+      bool waited = false;
+      uint32_t qloads = 0;         // query tiles issued (load k goes to buffer k & 1)
+      auto load_q = [&](int qb, int32_t slot) {
+        ++qloads;
+        mbar_arrive_expect_tx(bar_qfull(qb), C::kQBytes);
+        bulk_load(q_base + qb * C::kQBytes, a.qtiles + ((size_t)slot * a.H_kv + g.h) * C::kQBytes,
+                  C::kQBytes, bar_qfull(qb));
+      };
+      auto release_q0 = [&]() {
+        if (!waited) {
+          pdl_wait();
+          waited = true;
+          if (q0_slot >= 0) load_q(0, q0_slot);
+          HW_TRACE_EV(2);
+        }
+      };
       while (ok && tw.next(&t, &new_seg)) {
-        // K and V of the tile first: the pools were written by kernels that completed before
-        // this one started.
+        if (new_seg) {
+          if (seg == 0) {
+            q0_slot = t.seg_slot;
+          } else {
+            release_q0();
+            const int qb = seg & 1;
+            if (seg >= 2)
+              ok = mbar_wait(bar_qempty(qb), ((seg >> 1) - 1) & 1, abort, kWaitLimitNs);
+            if (!ok) break;
+            load_q(qb, t.seg_slot);
+          }
+          ++seg;
+        }
+        if (t.fresh) release_q0();
         const int32_t y = (int32_t)(((page_base + t.page) * a.H_kv + g.h) * a.S + t.slot0);
         for (int part = 0; part < 2 && ok; ++part, ++j) {
           const int s = j % C::kSlots;
-          if (j >= (uint32_t)C::kSlots)
+          if (j >= (uint32_t)C::kSlots) {
+            release_q0();          // the MMA issuer cannot free a slot without the query tile
             ok = mbar_wait(bar_empty(s), ((j / C::kSlots) - 1) & 1, abort, kWaitLimitNs);
+          }
           if (!ok) break;
           if (part == 0) HW_TRACE_EV(8 + 4 * (j >> 1));
           mbar_arrive_expect_tx(bar_full(s), C::kTileBytes);
@@ -331,30 +372,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(ring + s * C::kTileBytes + h * C::kHalfBytes, m, 64 * h, y, bar_full(s),
                         policy);
         }
-        if (ok && new_seg) {
-          // Rotated query tile of this segment, written by the rotation kernel that precedes
-          // this launch: wait for it (once) before the first read.
-          const int qb = seg & 1;
-          if (seg == 0) pdl_wait();
-          if (seg >= 2)
-            ok = mbar_wait(bar_qempty(qb), ((seg >> 1) - 1) & 1, abort, kWaitLimitNs);
-          if (!ok) break;
-          mbar_arrive_expect_tx(bar_qfull(qb), C::kQBytes);
-          bulk_load(q_base + qb * C::kQBytes,
-                    a.qtiles + ((size_t)t.seg_slot * a.H_kv + g.h) * C::kQBytes, C::kQBytes,
-                    bar_qfull(qb));
-          if (seg == 0) HW_TRACE_EV(2);
-          ++seg;
-        }
       }
+      if (ok) release_q0();
       HW_TRACE_EV(3);
       // Drain: every copy issued must have landed before the CTA can exit.
       for (uint32_t s = 0; s < (uint32_t)C::kSlots && s < j; ++s) {
         const uint32_t last = s + ((j - 1 - s) / C::kSlots) * C::kSlots;
         mbar_wait(bar_full(s), (last / C::kSlots) & 1, abort, kWaitLimitNs);
       }
-      for (uint32_t b = 0; b < 2 && b < seg; ++b) {
-        const uint32_t last = b + ((seg - 1 - b) / 2) * 2;
+      for (uint32_t b = 0; b < 2 && b < qloads; ++b) {
+        const uint32_t last = b + ((qloads - 1 - b) / 2) * 2;
         mbar_wait(bar_qfull(b), (last >> 1) & 1, abort, kWaitLimitNs);
       }
       if (!ok && (*abort)) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 0);
@@ -525,13 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_launch_dependents();
       }
       // Epilogue.  Each lane's (O row, max, sum) over its columns goes to shared memory (the
-      // K/V ring is idle once the last MMA has completed) as stage[chunk][row][D + 2]; then the
-      // T chunks of every row are merged by log-sum-exp and the unit's partials -- unnormalised
-      // o, max and sum in the log2 domain, [rows][D + 2] fp32 -- are stored with coalesced
-      // writes.
+      // K/V ring is idle once the last MMA has completed) as stage[chunk][row][PS]; then the T
+      // chunks of every row are merged by log-sum-exp and the unit's partials -- unnormalised
+      // o, max and sum in the log2 domain, [rows][PS] fp32 -- are stored with 16-byte writes.
       // Wait for every MMA through the single-use `fin` barrier, not o_done: here o_done may be
       // two phases behind (the last two P.V products can both be in flight), and a parity
       // wait cannot tell that apart from "done".
+      constexpr int PS = part_stride(D);
       bool have = ok && i > 0;
       if (have) {
         have = mbar_wait(bar_fin, 0, abort, kWaitLimitNs);
@@ -541,55 +568,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (threadIdx.x == 128) HW_TRACE_EV(250);
       float* stage = reinterpret_cast<float*>(smem + C::kRingOff);
       const bool writer = r < R;
-      float* srow = stage + ((size_t)cq * R + r) * (D + 2);
+      float4* srow = reinterpret_cast<float4*>(stage + ((size_t)cq * R + r) * PS);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         if (have) tmem_ld32_sync(tmem + lane_off + kColO + 32 * c, v);
         if (writer) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) srow[32 * c + e] = have ? __uint_as_float(v[e]) : 0.f;
+          for (int e = 0; e < 8; ++e)
+            srow[8 * c + e] = have ? make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                                 __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      if (writer) {
-        srow[D] = have ? m_run : -CUDART_INF_F;
-        srow[D + 1] = have ? l_sum : 0.f;
-      }
+      if (writer)
+        srow[D / 4] = make_float4(have ? m_run : -CUDART_INF_F, have ? l_sum : 0.f, 0.f, 0.f);
       const int nthr = 32 * active_softmax_warps;
       asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
       if (threadIdx.x == 128) HW_TRACE_EV(251);
       // Per row: M = max over the T chunks, and each chunk's weight 2^(m_j - M).
-      float* rowM = stage + (size_t)T * R * (D + 2);
+      float* rowM = stage + (size_t)T * R * PS;
       float* rowW = rowM + R;                                  // [T][R]
       for (int rr = threadIdx.x - 128; rr < R; rr += nthr) {
         float M = -CUDART_INF_F;
 #pragma unroll
-        for (int j = 0; j < T; ++j) M = fmaxf(M, stage[((size_t)j * R + rr) * (D + 2) + D]);
+        for (int j = 0; j < T; ++j) M = fmaxf(M, stage[((size_t)j * R + rr) * PS + D]);
         rowM[rr] = M;
 #pragma unroll
         for (int j = 0; j < T; ++j)
-          rowW[j * R + rr] =
-              (M == -CUDART_INF_F) ? 0.f : fast_exp2(stage[((size_t)j * R + rr) * (D + 2) + D] - M);
+          rowW[j * R + rr] = (M == -CUDART_INF_F) ? 0.f : fast_exp2(stage[((size_t)j * R + rr) * PS + D] - M);
       }
       asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
       if (threadIdx.x == 128) HW_TRACE_EV(252);
-      // One warp per row, lanes across the D + 2 values: coalesced stores.
-      float* part = a.partials + (size_t)blockIdx.x * R * (D + 2);
-      for (int rr = wq; rr < R; rr += active_softmax_warps) {
-        float wj[T];
+      // The unit's [R][PS] block as float4s: o columns are weighted sums over the chunks; the
+      // (m, l, pad, pad) float4 of a row holds M and the weighted sum of the chunks' l.
+      constexpr int Q4 = PS / 4;                               // float4s per row
+      float4* part = reinterpret_cast<float4*>(a.partials + (size_t)blockIdx.x * R * PS);
+      const float4* st4 = reinterpret_cast<const float4*>(stage);
+      for (int idx = threadIdx.x - 128; idx < R * Q4; idx += nthr) {
+        const int rr = idx / Q4, c4 = idx - rr * Q4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < T; ++j) wj[j] = rowW[j * R + rr];
-        for (int d = lane; d < D + 2; d += 32) {
-          float val;
-          if (d == D) {
-            val = rowM[rr];
+        for (int j = 0; j < T; ++j) {
+          const float wj = rowW[j * R + rr];
+          const float4 x = st4[((size_t)j * R + rr) * Q4 + c4];
+          if (c4 < D / 4) {
+            acc.x = fmaf(x.x, wj, acc.x);
+            acc.y = fmaf(x.y, wj, acc.y);
+            acc.z = fmaf(x.z, wj, acc.z);
+            acc.w = fmaf(x.w, wj, acc.w);
           } else {
-            val = 0.f;
-#pragma unroll
-            for (int j = 0; j < T; ++j) val = fmaf(stage[((size_t)j * R + rr) * (D + 2) + d], wj[j], val);
+            acc.y = fmaf(x.y, wj, acc.y);                      // l
           }
-          part[(size_t)rr * (D + 2) + d] = val;
         }
+        if (c4 == D / 4) acc.x = rowM[rr];
+        part[idx] = acc;
       }
       if (threadIdx.x == 128) HW_TRACE_EV(6);
       if (!ok && (*abort) && lane == 0) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 2);
@@ -621,10 +654,20 @@ extern "C" int hw_trace_clear(void) {
 #endif
 
 template <int D, int T>
-static void launch_tc_dt(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
+static void launch_tc_dt(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s,
+                         cudaEvent_t e0, cudaEvent_t e1) {
   using C = Cfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
-  rotate_kernel<D, T><<<a.num_seg_slots * a.H_kv, 256, 0, s>>>(a);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t rc = {};
+  rc.gridDim = dim3(a.num_seg_slots * a.H_kv);
+  rc.blockDim = dim3(256);
+  rc.stream = s;
+  rc.attrs = attr;
+  rc.numAttrs = 1;
+  cudaLaunchKernelEx(&rc, rotate_kernel<D, T>, a);
   cudaFuncSetAttribute(attn_tc_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)C::kSmemBytes);
   cudaLaunchConfig_t cfg = {};
@@ -632,30 +675,31 @@ static void launch_tc_dt(const AttnArgs& a, const TcMaps& maps, int layer, cudaS
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = e0 ? 0 : 1;        // a timing event in between ends the programmatic chain
+  if (e0) cudaEventRecord(e0, s);
   cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, T>, a, maps, (int32_t)layer);
+  if (e1) cudaEventRecord(e1, s);
 }
 
 template <int D>
-static void launch_tc_d(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
+static void launch_tc_d(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s,
+                        cudaEvent_t e0, cudaEvent_t e1) {
   if (a.rows <= 32)
-    launch_tc_dt<D, 4>(a, maps, layer, s);
+    launch_tc_dt<D, 4>(a, maps, layer, s, e0, e1);
   else if (a.rows <= 64)
-    launch_tc_dt<D, 2>(a, maps, layer, s);
+    launch_tc_dt<D, 2>(a, maps, layer, s, e0, e1);
   else
-    launch_tc_dt<D, 1>(a, maps, layer, s);
+    launch_tc_dt<D, 1>(a, maps, layer, s, e0, e1);
 }
 
-void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
+void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s,
+                         cudaEvent_t ev_before, cudaEvent_t ev_after) {
   if (a.num_units <= 0) return;
   if (a.D == 64)
-    launch_tc_d<64>(a, maps, layer, s);
+    launch_tc_d<64>(a, maps, layer, s, ev_before, ev_after);
   else
-    launch_tc_d<128>(a, maps, layer, s);
+    launch_tc_d<128>(a, maps, layer, s, ev_before, ev_after);
 }
 
 // ---- tensor maps (host) ------------------------------------------------------------------

@@ -88,7 +88,8 @@ Layout make_layout(const hw_config* c) {
                             align_up((size_t)P * H * sizeof(hw::Group), 16) +
                             align_up((size_t)L.max_seg_slots * W * sizeof(int32_t), 16) +
                             align_up((size_t)L.max_seg_slots * sizeof(int32_t), 16);
-  L.slot_bytes = align_up(std::max(append_bytes, attn_bytes), kAlign);
+  // A slot holds a step's append runs followed by its attention plan (uploaded together).
+  L.slot_bytes = align_up(append_bytes, kAlign) + align_up(attn_bytes, kAlign);
   size_t off = 0;
   L.err = off;
   off += kAlign;
@@ -100,7 +101,7 @@ Layout make_layout(const hw_config* c) {
   L.slots = off;
   off += kSlots * L.slot_bytes;
   L.partials = off;
-  off += align_up((size_t)L.max_units * L.rows * (c->head_dim + 2) * sizeof(float), kAlign);
+  off += align_up((size_t)L.max_units * L.rows * hw::part_stride(c->head_dim) * sizeof(float), kAlign);
   L.tickets = off;
   off += align_up((size_t)P * H * sizeof(uint32_t), kAlign);
   // Rotated query tiles of the tensor-core path: one 128-row x D bf16 tile per (segment slot,
@@ -110,6 +111,12 @@ Layout make_layout(const hw_config* c) {
   L.total = off;
   return L;
 }
+
+// Offsets of the arrays of an attention plan inside its buffer, and their sizes.
+struct PlanOffsets {
+  size_t pieces, units, groups, delta, slot_problem, bytes;
+  int32_t num_pieces, num_units, num_groups, num_seg_slots;
+};
 
 struct Seg {
   int32_t problem, origin, length, pending;
@@ -139,6 +146,14 @@ struct hw_ctx {
   bool step_active = false;
   std::vector<int32_t> step_n;
   std::vector<uint8_t> appended;
+  // The step's append runs and attention plan, uploaded together by its first append and
+  // reused by every layer while the tables stay unchanged (epoch counts table changes).
+  uint64_t epoch = 0, step_epoch = ~0ull;
+  int step_slot = -1;
+  int32_t step_runs = 0, step_max_run = 0;
+  size_t step_plan_off = 0;
+  bool step_plan_ok = false;
+  PlanOffsets step_po{};
   // measurement
   bool prof_on = false;
   int64_t n_launch = 0, n_attn = 0, n_append = 0;
@@ -146,12 +161,17 @@ struct hw_ctx {
   std::vector<int8_t> prof_kind;          // 0 = attention, 1 = append, per recorded pair
   int prof_next = 0;
 
-  // Record the opening event of a timed launch; returns the pair index or -1.
-  int prof_begin(cudaStream_t s, int8_t kind) {
+  // Reserve an event pair for a timed launch (the caller records it); -1 when not timing.
+  int prof_reserve(int8_t kind) {
     if (!prof_on || prof_next >= kProfPairs) return -1;
     const int i = prof_next++;
     prof_kind[i] = kind;
-    cudaEventRecord(prof_ev[2 * i], s);
+    return i;
+  }
+  // Record the opening event of a timed launch; returns the pair index or -1.
+  int prof_begin(cudaStream_t s, int8_t kind) {
+    const int i = prof_reserve(kind);
+    if (i >= 0) cudaEventRecord(prof_ev[2 * i], s);
     return i;
   }
   void prof_end(int i, cudaStream_t s) {
@@ -339,6 +359,15 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
   return HW_OK;
 }
 
+}  // extern "C"
+
+namespace {
+bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap,
+                          int64_t target_override);
+}  // namespace
+
+extern "C" {
+
 hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const void* k_raw,
                        const void* v_raw, void* stream) {
   if (!c || !n_new || layer < 0 || layer >= c->cfg.num_layers) return HW_ERR_INVALID_ARG;
@@ -396,6 +425,7 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
         sg.pending = n;
       }
     c->step_active = true;
+    ++c->epoch;                            // tables changed: any uploaded plan is stale
     c->step_n.assign(n_new, n_new + P * B);
     c->appended.assign(c->cfg.num_layers, 0);
   } else {
@@ -406,37 +436,56 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
     c->appended[layer] = 1;
     return HW_OK;
   }
-  int slot = 0;
-  hw_status st = c->acquire_slot(&slot);
-  if (st != HW_OK) return st;
-  hw::AppendRun* runs = reinterpret_cast<hw::AppendRun*>(c->h_slot(slot));
-  const size_t max_runs = c->lay.slot_bytes / sizeof(hw::AppendRun);
-  int32_t nr = 0, src = 0, max_run = 0;
-  for (int32_t p = 0; p < P; ++p)
-    for (int32_t b = 0; b < B; ++b) {
-      const int32_t n = n_new[p * B + b];
-      if (!n) continue;
-      const Seg& sg = c->block(p, b);
-      int32_t j = sg.length;
-      const int32_t end = sg.length + n;
-      while (j < end) {
-        const int32_t pg_idx = c->cfg.contiguous ? 0 : j / S;
-        const int32_t slot0 = c->cfg.contiguous ? j : j % S;
-        const int32_t len = std::min(end - j, S - slot0);
-        if ((size_t)nr >= max_runs) return HW_ERR_CAPACITY;
-        runs[nr++] = hw::AppendRun{src, len, sg.pages[pg_idx], slot0, j, 0};
-        max_run = std::max(max_run, len);
-        src += len;
-        j += len;
-      }
-    }
   cudaStream_t s = (cudaStream_t)stream;
-  HW_CUDA(cudaMemcpyAsync(c->d_slot(slot), runs, nr * sizeof(hw::AppendRun),
-                          cudaMemcpyHostToDevice, s));
+  if (c->step_slot < 0 || c->step_epoch != c->epoch) {
+    // First append since the tables changed: the runs (identical for every layer of the step)
+    // and the attention plan of the post-append state go up in one copy.
+    int slot = 0;
+    hw_status st = c->acquire_slot(&slot);
+    if (st != HW_OK) return st;
+    hw::AppendRun* runs = reinterpret_cast<hw::AppendRun*>(c->h_slot(slot));
+    const size_t max_runs = (c->lay.slot_bytes / 2) / sizeof(hw::AppendRun);
+    int32_t nr = 0, src = 0, max_run = 0;
+    for (int32_t p = 0; p < P; ++p)
+      for (int32_t b = 0; b < B; ++b) {
+        const int32_t n = n_new[p * B + b];
+        if (!n) continue;
+        const Seg& sg = c->block(p, b);
+        int32_t j = sg.length;
+        const int32_t end = sg.length + n;
+        while (j < end) {
+          const int32_t pg_idx = c->cfg.contiguous ? 0 : j / S;
+          const int32_t slot0 = c->cfg.contiguous ? j : j % S;
+          const int32_t len = std::min(end - j, S - slot0);
+          if ((size_t)nr >= max_runs) return HW_ERR_CAPACITY;
+          runs[nr++] = hw::AppendRun{src, len, sg.pages[pg_idx], slot0, j, 0};
+          max_run = std::max(max_run, len);
+          src += len;
+          j += len;
+        }
+      }
+    const size_t plan_off = align_up((size_t)nr * sizeof(hw::AppendRun), kAlign);
+    PlanOffsets po{};
+    const bool plan_ok =
+        plan_off < c->lay.slot_bytes &&
+        build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->use_tc ? c->num_sms : 0) &&
+        plan_off + po.bytes <= c->lay.slot_bytes;
+    HW_CUDA(cudaMemcpyAsync(c->d_slot(slot), c->h_slot(slot),
+                            plan_off + (plan_ok ? po.bytes : 0), cudaMemcpyHostToDevice, s));
+    c->step_slot = slot;
+    c->step_runs = nr;
+    c->step_max_run = max_run;
+    c->step_plan_off = plan_off;
+    c->step_plan_ok = plan_ok;
+    c->step_po = po;
+    c->step_epoch = c->epoch;
+  }
+  const int slot = c->step_slot;
+  const int32_t nr = c->step_runs;
   hw::AppendArgs a{};
   a.runs = reinterpret_cast<const hw::AppendRun*>(c->d_slot(slot));
   a.num_runs = nr;
-  a.max_run = max_run;
+  a.max_run = c->step_max_run;
   a.k_raw = (const __nv_bfloat16*)k_raw;
   a.v_raw = (const __nv_bfloat16*)v_raw;
   a.k_layer = c->k_pool + (size_t)layer * c->layer_elems;
@@ -461,14 +510,12 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
   return HW_OK;
 }
 
+}  // extern "C"
+
 namespace {
 
 // Build the attention plan of the current state into host buffer `buf` (slot_bytes long).
 // Returns false if a table would overflow.  Offsets of each array are written to `off`.
-struct PlanOffsets {
-  size_t pieces, units, groups, delta, slot_problem, bytes;
-  int32_t num_pieces, num_units, num_groups, num_seg_slots;
-};
 
 // unit_cap > 0 bounds the number of units (one partial result each); 0 = the default split.
 bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0,
@@ -512,7 +559,9 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t u
         const int32_t pg = c->cfg.contiguous ? sg.pages[0] : sg.pages[j / S];
         const int32_t slot0 = c->cfg.contiguous ? j : j % S;
         const int32_t cnt = std::min(std::min(kPieceMax, S - slot0), n - j);
-        proto.push_back(hw::Piece{r.slot, pg, slot0, cnt});
+        // fresh: holds tokens appended in this step (the kernels read it only after the append)
+        const int32_t fresh = (sg.pending > 0 && j + cnt > sg.length) ? 1 : 0;
+        proto.push_back(hw::Piece{r.slot, pg, slot0, cnt, fresh});
         // Balance by 128-token tiles: a partial tile costs the kernels a full one.
         tok += (cnt + 127) / 128 * 128;
       }
@@ -594,22 +643,32 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t u
 
 }  // namespace
 
+extern "C" {
+
 hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void* out,
                                   int32_t out_dtype, float* lse, void* stream) {
   if (!c || !q || !out || layer < 0 || layer >= c->cfg.num_layers) return HW_ERR_INVALID_ARG;
   if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
   if (c->step_active && !c->appended[layer]) return HW_ERR_INVALID_ARG;
-  int slot = 0;
-  hw_status st = c->acquire_slot(&slot);
-  if (st != HW_OK) return st;
-  PlanOffsets po{};
-  // Tensor-core kernel: one CTA per SM holds all of its shared memory and TMEM, so one unit
-  // per SM, balanced by KV entries.
-  if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0))
-    return HW_ERR_CAPACITY;
   cudaStream_t s = (cudaStream_t)stream;
-  char* dbase = c->d_slot(slot);
-  HW_CUDA(cudaMemcpyAsync(dbase, c->h_slot(slot), po.bytes, cudaMemcpyHostToDevice, s));
+  int slot = 0;
+  PlanOffsets po{};
+  char* dbase = nullptr;
+  if (c->step_slot >= 0 && c->step_epoch == c->epoch && c->step_plan_ok) {
+    // The plan of this step went up with its first append.
+    slot = c->step_slot;
+    po = c->step_po;
+    dbase = c->d_slot(slot) + c->step_plan_off;
+  } else {
+    hw_status st = c->acquire_slot(&slot);
+    if (st != HW_OK) return st;
+    // Tensor-core kernel: one CTA per SM holds all of its shared memory and TMEM, so one unit
+    // per SM, balanced by KV entries.
+    if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0))
+      return HW_ERR_CAPACITY;
+    dbase = c->d_slot(slot);
+    HW_CUDA(cudaMemcpyAsync(dbase, c->h_slot(slot), po.bytes, cudaMemcpyHostToDevice, s));
+  }
   hw::AttnArgs a{};
   a.pieces = reinterpret_cast<const hw::Piece*>(dbase + po.pieces);
   a.units = reinterpret_cast<const hw::Unit*>(dbase + po.units);
@@ -641,16 +700,22 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   a.max_position = c->cfg.max_position;
   a.rows = c->rows;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
-  const int pi = c->prof_begin(s, 0);
-  if (c->use_tc)
-    hw::launch_attention_tc(a, c->maps, layer, s);
-  else
+  // Timing events (when enabled) go directly around the attention kernel only.
+  const int pi = c->prof_reserve(0);
+  cudaEvent_t e0 = pi >= 0 ? c->prof_ev[2 * pi] : nullptr;
+  cudaEvent_t e1 = pi >= 0 ? c->prof_ev[2 * pi + 1] : nullptr;
+  if (c->use_tc) {
+    // query rotation, then the attention kernel and the merge as programmatic dependents
+    hw::launch_attention_tc(a, c->maps, layer, s, e0, e1);
+  } else {
+    if (e0) cudaEventRecord(e0, s);
     hw::launch_attention_fma(a, s);
-  c->prof_end(pi, s);
+    if (e1) cudaEventRecord(e1, s);
+  }
   HW_CUDA(cudaGetLastError());
-  hw::launch_merge(a, s);
+  hw::launch_merge(a, s, c->use_tc);
   HW_CUDA(cudaGetLastError());
-  c->n_launch += 2;
+  c->n_launch += c->use_tc ? 3 : 2;
   c->n_attn += 1;
   HW_CUDA(cudaEventRecord(c->slot_ev[slot], s));
   c->slot_used[slot] = true;
@@ -669,7 +734,7 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
     return HW_ERR_INVALID_ARG;
   if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
   if (c->step_active && !c->appended[layer]) return HW_ERR_INVALID_ARG;
-  const size_t per_unit = (size_t)c->rows * (c->cfg.head_dim + 2) * sizeof(float);
+  const size_t per_unit = (size_t)c->rows * hw::part_stride(c->cfg.head_dim) * sizeof(float);
   const size_t plan_region = align_up(std::min(c->lay.slot_bytes, scratch_bytes / 4), kAlign);
   if (plan_region >= scratch_bytes) return HW_ERR_CAPACITY;
   const int64_t unit_cap = (int64_t)((scratch_bytes - plan_region) / per_unit);
@@ -743,6 +808,8 @@ hw_status hw_step_end(hw_ctx* c, const uint8_t* finished, void* stream) {
     sg.pending = 0;
   }
   c->step_active = false;
+  ++c->epoch;
+  c->step_slot = -1;
   c->appended.clear();
   c->step_n.clear();
   if (finished)

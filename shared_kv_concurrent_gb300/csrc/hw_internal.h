@@ -41,7 +41,11 @@ struct Piece {
   int32_t page;
   int32_t slot0;
   int32_t ntok;
+  int32_t fresh;     // 1 if the piece holds tokens appended in the current step
 };
+
+// Row stride (floats) of a partial result: o[D], m, l, 2 pad -- 16-byte aligned rows.
+__host__ __device__ constexpr int part_stride(int D) { return D + 4; }
 
 // A unit: consecutive pieces of one (problem, KV head) group, one CTA, one partial result.
 struct Unit {
@@ -87,7 +91,7 @@ struct AttnArgs {
   void* out;                  // [P][W][H_q][D] bf16 or fp32
   int32_t out_f32;
   float* lse;                 // [P][W][H_q] or null
-  float* partials;            // [units][rows][D + 2]: o[D], m, l (log2 domain)
+  float* partials;            // [units][rows][part_stride(D)]: o[D], m, l (log2 domain), pad
   const float* rope_cos;
   const float* rope_sin;
   uint32_t* err;
@@ -104,8 +108,12 @@ struct TcMaps {
 
 void launch_append(const AppendArgs& a, cudaStream_t s);
 void launch_attention_fma(const AttnArgs& a, cudaStream_t s);
-void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s);
-void launch_merge(const AttnArgs& a, cudaStream_t s);
+// Launches the query rotation and the attention kernel; ev_before / ev_after (optional) are
+// recorded directly around the attention kernel.
+void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s,
+                         cudaEvent_t ev_before = nullptr, cudaEvent_t ev_after = nullptr);
+// pdl: launch as a programmatic dependent of the preceding kernel (it waits for its writes).
+void launch_merge(const AttnArgs& a, cudaStream_t s, bool pdl = false);
 bool make_tc_maps(const hw_config& cfg, void* k_pool, void* v_pool, TcMaps* out);
 
 // hw_concurrent_attention with the plan and the partial results in `scratch` (device).
