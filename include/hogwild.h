@@ -126,16 +126,18 @@ hw_status hw_append_kv(hw_ctx* ctx, int32_t layer, const int32_t* n_new, const v
 
 /*
  * Concurrent attention of one layer (sections 5 and 9).
- *   q:   device bf16 [P][W][H_q][D], UNROTATED queries (one token per worker).
- *   out: device [P][W][H_q][D], bf16 (out_dtype HW_OUT_BF16) or fp32 (HW_OUT_F32).
+ *   q:   device bf16 [P][W][H_q][D], UNROTATED queries (one token per worker), 16-byte aligned.
+ *   out: device [P][W][H_q][D], bf16 (out_dtype HW_OUT_BF16) or fp32 (HW_OUT_F32), 16-byte
+ *        aligned.
  *   lse: device fp32 [P][W][H_q] or NULL: natural-log log-sum-exp of the scaled scores.
  * For worker w of problem p the view is [common segments in commit order] ++ [other workers'
  * blocks, ascending id] ++ [own block]; empty blocks are skipped; i_q = view length - 1.  Each
  * block at view offset o is attended with the query rotated by (i_q - o), scores scaled by
  * 1/sqrt(D), and the per-block softmax partials merged by log-sum-exp.  An empty view gives
  * out = 0 and lse = -inf.  Requires that, if the current step appended tokens, this layer
- * has been appended (HW_ERR_INVALID_ARG otherwise).  Scratch: partial results live in the
- * workspace; calls on one context must not overlap on the GPU (use one stream).
+ * has been appended, and q and out aligned (HW_ERR_INVALID_ARG otherwise).  Scratch: partial
+ * results live in the workspace; calls on one context must not overlap on the GPU (use one
+ * stream).
  */
 hw_status hw_concurrent_attention(hw_ctx* ctx, int32_t layer, const void* q, void* out,
                                   int32_t out_dtype, float* lse, void* stream);
@@ -148,7 +150,7 @@ hw_status hw_concurrent_attention(hw_ctx* ctx, int32_t layer, const void* q, voi
  * memory that the library defines, instead of in the workspace.  Nothing is allocated: no
  * cudaMalloc, cudaFree or allocating library routine is called.
  *   - Limit: the plan plus one partial result per (problem, KV head) group, i.e.
- *     P * H_kv * rows * (D + 2) * 4 bytes with rows = W * H_q / H_kv, must fit in 16 MiB, else
+ *     P * H_kv * rows * (D + 4) * 4 bytes with rows = W * H_q / H_kv, must fit in 16 MiB, else
  *     HW_ERR_CAPACITY and nothing is enqueued.  The KV split adapts to the space left.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
  *     with that device current); make that first call before any stream capture.

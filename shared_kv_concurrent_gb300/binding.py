@@ -86,10 +86,10 @@ def load() -> ctypes.CDLL:
         "hw_create": (ctypes.c_int, [ctypes.POINTER(hw_config), _P, _P, _P, ctypes.c_size_t, _PI32, _P,
                                      ctypes.POINTER(_P)]),
         "hw_destroy": (None, [_P]),
-        "hw_append_kv": (ctypes.c_int, [_P, _I32, _PI32, _P, _P, _P]),
+        "hw_append_kv": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P]),
         "hw_concurrent_attention": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P]),
         "hw_concurrent_attention_noalloc": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P]),
-        "hw_step_end": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint8), _P]),
+        "hw_step_end": (ctypes.c_int, [_P, _P, _P]),
         "hw_check_device_errors": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
         "hw_profile_enable": (ctypes.c_int, [_P, _I32]),
         "hw_profile_read": (ctypes.c_int, [_P, ctypes.POINTER(hw_profile)]),
@@ -124,6 +124,8 @@ def _check(st: int, where: str):
 
 
 def _i32(a) -> np.ndarray:
+    if isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous:
+        return a
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
 
@@ -178,14 +180,18 @@ def hw_destroy(ctx: int) -> None:
 
 def hw_append_kv(ctx: int, layer: int, n_new, k_raw, v_raw, stream=None) -> None:
     n = _i32(n_new)
-    _check(load().hw_append_kv(ctx, layer, _ptr(n, ctypes.c_int32), _dptr(k_raw), _dptr(v_raw),
-                               _stream(stream)), "hw_append_kv")
+    st = (_lib or load()).hw_append_kv(ctx, layer, n.ctypes.data, _dptr(k_raw), _dptr(v_raw),
+                                       _stream(stream))
+    if st:
+        _check(st, "hw_append_kv")
 
 
 def hw_concurrent_attention(ctx: int, layer: int, q, out, out_dtype: int, lse=None,
                             stream=None) -> None:
-    _check(load().hw_concurrent_attention(ctx, layer, _dptr(q), _dptr(out), out_dtype, _dptr(lse),
-                                          _stream(stream)), "hw_concurrent_attention")
+    st = (_lib or load()).hw_concurrent_attention(ctx, layer, q.data_ptr(), out.data_ptr(),
+                                                  out_dtype, _dptr(lse), _stream(stream))
+    if st:
+        _check(st, "hw_concurrent_attention")
 
 
 def hw_concurrent_attention_noalloc(ctx: int, layer: int, q, out, out_dtype: int, lse=None,
@@ -197,9 +203,15 @@ def hw_concurrent_attention_noalloc(ctx: int, layer: int, q, out, out_dtype: int
 
 
 def hw_step_end(ctx: int, finished=None, stream=None) -> None:
-    f = None if finished is None else np.ascontiguousarray(np.asarray(finished, dtype=np.uint8))
-    _check(load().hw_step_end(ctx, None if f is None else _ptr(f, ctypes.c_uint8), _stream(stream)),
-           "hw_step_end")
+    if finished is None:
+        f = None
+    elif isinstance(finished, np.ndarray) and finished.dtype == np.uint8 and finished.flags.c_contiguous:
+        f = finished
+    else:
+        f = np.ascontiguousarray(np.asarray(finished, dtype=np.uint8))
+    st = (_lib or load()).hw_step_end(ctx, None if f is None else f.ctypes.data, _stream(stream))
+    if st:
+        _check(st, "hw_step_end")
 
 
 def hw_check_device_errors(ctx: int, stream=None):

@@ -19,6 +19,10 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   // The next kernels of the step (query rotation, attention) may start their own prologue now;
   // they wait for this grid before reading what it writes.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Launched as a programmatic dependent of whatever precedes it on the stream (which may
+  // produce k_raw / v_raw): wait for that grid before reading anything it could write.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  HW_SPAN_BEGIN(0);
   const AppendRun run = a.runs[blockIdx.y];
   const int t0 = blockIdx.x * kTokPerCta;
   if (t0 >= run.ntok) return;
@@ -54,17 +58,28 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
     a.v_layer[dst + i] = a.v_raw[src + i];
     a.v_layer[dst + i + half] = a.v_raw[src + i + half];
   }
+  HW_SPAN_END(0);
 }
 
 }  // namespace
+
+HW_SPAN_EXPORT(append)
 
 void launch_append(const AppendArgs& a, cudaStream_t s) {
   for (int r0 = 0; r0 < a.num_runs; r0 += 65535) {
     AppendArgs b = a;
     b.runs = a.runs + r0;
     b.num_runs = a.num_runs - r0 < 65535 ? a.num_runs - r0 : 65535;
-    dim3 grid((a.max_run + kTokPerCta - 1) / kTokPerCta, b.num_runs);
-    append_kernel<<<grid, kThreads, 0, s>>>(b);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.max_run + kTokPerCta - 1) / kTokPerCta, b.num_runs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, append_kernel, b);
   }
 }
 

@@ -151,51 +151,107 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
 }
 
 // K3: out = sum_u o_u 2^(m_u - M) / sum_u l_u 2^(m_u - M), M = max_u m_u; lse = (M + log2 L) ln 2.
-// One CTA per (group, row), one thread per output column; the loops over units are unrolled so
-// that their loads are in flight together.
+// One warp per (group, query row), lanes across the row as float4 columns.  The units are
+// taken eight at a time with all their loads in flight, merged into a running (M, L, O) that
+// is rescaled when M grows.
+constexpr int kMergeWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(D) merge_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const AttnArgs a) {
   // May be launched as a programmatic dependent of the attention kernel: wait for its writes.
+  HW_SPAN_BEGIN(0);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const Group g = a.groups[blockIdx.x];
-  const int d = threadIdx.x;
-  const int r = blockIdx.y;
-  {
-    const size_t stride = (size_t)a.rows * part_stride(D);
-    const float* base = a.partials + ((size_t)g.unit_begin * a.rows + r) * part_stride(D);
+  HW_SPAN_BEGIN(1);
+  constexpr int PS = part_stride(D);
+  constexpr int kChunk = 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x * kMergeWarps + warp;
+  if (item < a.num_groups * a.rows) {
+    const int gi = item / a.rows, r = item - gi * a.rows;
+    const Group g = a.groups[gi];
+    const bool act = lane < D / 4;
+    const size_t stride = (size_t)a.rows * PS;
+    const float* base = a.partials + ((size_t)g.unit_begin * a.rows + r) * PS;
     const int nu = g.unit_end - g.unit_begin;
-    float M = -CUDART_INF_F;
-#pragma unroll 8
-    for (int k = 0; k < nu; ++k) M = fmaxf(M, base[k * stride + D]);
-    float L = 0.f, O = 0.f;
-    if (M != -CUDART_INF_F) {
-#pragma unroll 8
-      for (int k = 0; k < nu; ++k) {
-        const float* part = base + k * stride;
-        const float sc = exp2f(part[D] - M);
-        L = fmaf(part[D + 1], sc, L);
-        O = fmaf(part[d], sc, O);
+    float M = -CUDART_INF_F, L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < nu; k0 += kChunk) {
+      float2 ml[kChunk];
+      float4 o[kChunk];
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        const int k = k0 + j;
+        ml[j] = make_float2(-CUDART_INF_F, 0.f);
+        o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < nu) {
+          ml[j] = *reinterpret_cast<const float2*>(base + k * stride + D);
+          if (act) o[j] = *reinterpret_cast<const float4*>(base + k * stride + 4 * lane);
+        }
       }
+      float cm = M;
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) cm = fmaxf(cm, ml[j].x);
+      if (cm == -CUDART_INF_F) continue;
+      const float sc = (M == -CUDART_INF_F) ? 0.f : exp2f(M - cm);
+      L *= sc;
+      O.x *= sc;
+      O.y *= sc;
+      O.z *= sc;
+      O.w *= sc;
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        const float wj = (ml[j].x == -CUDART_INF_F) ? 0.f : exp2f(ml[j].x - cm);
+        L = fmaf(ml[j].y, wj, L);
+        O.x = fmaf(o[j].x, wj, O.x);
+        O.y = fmaf(o[j].y, wj, O.y);
+        O.z = fmaf(o[j].z, wj, O.z);
+        O.w = fmaf(o[j].w, wj, O.w);
+      }
+      M = cm;
     }
-    const float res = (L > 0.f) ? O / L : 0.f;
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
     const int w = r / a.G, hq = g.h * a.G + r % a.G;
     const size_t oi = ((size_t)g.p * a.W + w) * a.H_q + hq;
-    if (a.out_f32)
-      reinterpret_cast<float*>(a.out)[oi * D + d] = res;
-    else
-      reinterpret_cast<__nv_bfloat16*>(a.out)[oi * D + d] = __float2bfloat16_rn(res);
-    if (a.lse && d == 0) a.lse[oi] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+    if (act) {
+      if (a.out_f32) {
+        reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + oi * D)[lane] =
+            make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+      } else {
+        const __nv_bfloat162 v0 = __floats2bfloat162_rn(O.x * inv, O.y * inv);
+        const __nv_bfloat162 v1 = __floats2bfloat162_rn(O.z * inv, O.w * inv);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&v0);
+        pk.y = *reinterpret_cast<const uint32_t*>(&v1);
+        reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + oi * D)[lane] = pk;
+      }
+    }
+    if (a.lse && lane == 0) a.lse[oi] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
   }
+  HW_SPAN_END(0);
+}
+
+template <int D>
+constexpr size_t fma_smem_bytes(int rows) {
+  return ((size_t)rows * D + kTile * (D + 1) + kTile * D) * sizeof(float);
 }
 
 template <int D>
 void launch_fma_d(const AttnArgs& a, cudaStream_t s) {
-  const size_t smem = ((size_t)a.rows * D + kTile * (D + 1) + kTile * D) * sizeof(float);
-  cudaFuncSetAttribute(attn_fma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  attn_fma_kernel<D><<<a.num_units, kThreads, smem, s>>>(a);
+  attn_fma_kernel<D><<<a.num_units, kThreads, fma_smem_bytes<D>(a.rows), s>>>(a);
 }
 
 }  // namespace
+
+HW_SPAN_EXPORT(merge)
+
+cudaError_t prepare_attention_fma(int D) {
+  // Shared-memory limit for the largest row count a context may have (128 query rows).
+  if (D == 64)
+    return cudaFuncSetAttribute(attn_fma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)fma_smem_bytes<64>(128));
+  return cudaFuncSetAttribute(attn_fma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)fma_smem_bytes<128>(128));
+}
 
 void launch_attention_fma(const AttnArgs& a, cudaStream_t s) {
   if (a.num_units <= 0) return;
@@ -208,8 +264,8 @@ void launch_attention_fma(const AttnArgs& a, cudaStream_t s) {
 void launch_merge(const AttnArgs& a, cudaStream_t s, bool pdl) {
   if (a.num_groups <= 0) return;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.num_groups, a.rows);
-  cfg.blockDim = dim3(a.D);
+  cfg.gridDim = dim3((a.num_groups * a.rows + kMergeWarps - 1) / kMergeWarps);
+  cfg.blockDim = dim3(32 * kMergeWarps);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -6,14 +6,12 @@
 // group, each through its own rotated query.  The work is split over KV entries and the
 // partial results reduced afterwards (section 9).
 //
-// Two kernels:
-//   rotate_kernel  one CTA per (segment slot, KV head): rotates the group's queries for that
-//                  segment, pre-scales them by log2(e)/sqrt(D) and writes the 128-row bf16 A
-//                  tile in exactly the swizzled layout the MMA reads from shared memory.
-//   attn_tc_kernel one CTA = one unit: a run of pieces (<= 256 tokens of one segment inside one
-//                  page) of one (problem, KV head).  Per 128-token tile:
+// One CTA = one unit: a run of pieces (<= 128 tokens of one segment inside one page) of one
+// (problem, KV head).  Per segment of the unit, the query-rotation warps build the rotated,
+// pre-scaled (log2(e)/sqrt(D)) 128-row bf16 A tile in shared memory, in the swizzled layout the
+// MMA reads.  Per 128-token tile:
 //     S  = Q~ K^T     tcgen05.mma, M = 128 TMEM lanes, N = 128 tokens, K = D; A = rotated
-//                     queries (smem, bulk-copied), B = K tile (smem, TMA, 128-byte swizzle)
+//                     queries (smem), B = K tile (smem, TMA, 128-byte swizzle)
 //     P  = 2^(S - m)  softmax threads, one TMEM lane each.  Every real query row is repeated T
 //                     times in A, once per softmax warp group, and warp group j takes tokens
 //                     [j*128/T, (j+1)*128/T) of every tile: each lane keeps its own running max
@@ -23,14 +21,17 @@
 //     O += P V        tcgen05.mma with A = P from TMEM, B = V tile (smem, MN-major), D = TMEM;
 //                     the epilogue merges the T partial rows of each query row by log-sum-exp
 // T = 4, 2, 1 for up to 32, 64, 128 real rows, so that every SM sub-partition runs softmax.
-// Warp roles: 0 TMA producer (query tiles, K and V tiles), 1 MMA issuer and TMEM owner,
+// Warp roles: 0 TMA producer (K and V tiles), 1 MMA issuer and TMEM owner, 2-3 query rotation,
 // 4-7 softmax / correction / epilogue.  Every K/V element is loaded from HBM once per unit and
 // used by all W*G rows; S is double-buffered so the softmax of tile i overlaps MMA2(i-1) and
-// MMA1(i+1).  All waits are bounded: one that runs out raises a CTA abort flag, records
-// ERR_TIMEOUT in the error word, and the CTA drains the copies and MMAs it issued and frees
-// its TMEM.  Launch chaining: rotate_kernel lets the attention kernel start early
-// (programmatic dependent launch); the attention kernel waits for it only before loading the
-// first query tile, and lets the merge kernel start during its epilogue.
+// MMA1(i+1), and the query tile is double-buffered so the next segment's rotation overlaps
+// the current segment's tiles.  All waits are bounded: one that runs out raises a CTA abort
+// flag, records ERR_TIMEOUT in the error word, and the CTA drains the copies and MMAs it
+// issued and frees its TMEM.  Launch chaining (programmatic dependent launch): the kernel may
+// start while the preceding kernel of the stream (normally the append) still runs; it streams
+// tiles of older tokens meanwhile and waits for that kernel before it reads the queries or a
+// tile holding tokens of the current step, and lets the merge kernel start during its
+// epilogue.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -47,6 +48,7 @@ using namespace tc;
 constexpr int kTile = 128;                  // tokens per tile = N of the first MMA
 constexpr int kRowsM = 128;                 // M of both MMAs (TMEM lanes)
 constexpr int kThreads = 256;
+constexpr int kRotThreads = 64;             // warps 2-3: query rotation
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: two S buffers, O, and two P buffers of their own.  P must not alias S: the
 // MMA that writes S(i+2) is issued right after the one that reads P(i), and the tensor core
@@ -155,90 +157,96 @@ struct TileWalker {
 
 // ---------------------------------------------------------------------------- rotation
 
-// Tile (slot, h): 128 M-rows x D bf16 in the MMA's shared-memory layout (two 64-column atoms
-// for D = 128, 128-byte swizzle: the 16-byte chunk c of M-row m sits at chunk c ^ (m % 8)).
-// M-row m (TMEM lane m, softmax warp q = m / 32) holds query row r = 32 * (q % (4 / T)) +
-// m % 32 of the group: each query row is repeated T times, once per column chunk (see the
-// softmax below).  Rows are rotated by (i_q - view offset) of their worker for this segment
-// and pre-scaled by log2(e)/sqrt(D); rows past W*G, and rows whose worker does not see the
-// segment, are zero.  Two threads per M-row, each owning half of the 8-pair chunks; all loads
-// are issued before any is used.
-template <int D, int T>
-__global__ void __launch_bounds__(256) rotate_kernel(const AttnArgs a) {
-  pdl_launch_dependents();
+// Rotated query tile of segment slot `slot` for the unit's group (p, h): 128 M-rows x D bf16 in
+// the MMA's shared-memory layout (D / 64 atoms of 128-byte rows, 128-byte swizzle: the 16-byte
+// chunk c of M-row m sits at chunk c ^ (m % 8)).  Query row r of the group (worker r / G, head
+// h*G + r % G) is rotated by its worker's delta for the segment and pre-scaled by
+// log2(e)/sqrt(D), and stored at the T M-rows r + j * 128/T (softmax warp group j reads copy
+// j); rows past W*G and rows whose worker does not see the segment are zero.  uniform_delta
+// >= 0 is the rotation of every row (no delta-table load), -1 = look it up per row.  Run by NT
+// threads; each takes (row, 8-pair chunk) items and issues the loads of up to four items
+// before using any.
+template <int D, int T, int NT>
+__device__ __forceinline__ void rotate_tile(const AttnArgs& a, const Group& g, int slot,
+                                            int uniform_delta, uint8_t* tile, int tid) {
   constexpr int half = D / 2;
-  constexpr int CH = half / 8;                 // 8-pair chunks per M-row
-  constexpr int CPT = CH / 2;                  // chunks per thread
-  constexpr int WPC = 4 / T;                   // softmax warps per column chunk
+  constexpr int CH = half / 8;                 // 8-pair chunks per row
+  constexpr int RR = kRowsM / T;               // M-rows per copy
+  constexpr int ITEMS = RR * CH;
+  constexpr int PER = (ITEMS + NT - 1) / NT;   // items per thread
+  constexpr int B = PER < 4 ? PER : (PER % 4 == 0 ? 4 : 3);  // loads in flight together
   constexpr uint32_t kHalfBytes = kTile * 128;
-  const int slot = blockIdx.x / a.H_kv, h = blockIdx.x % a.H_kv;
-  if (slot >= a.num_seg_slots) return;
-  const int p = a.slot_problem[slot];
-  const int m = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * CPT;
-  const int r = 32 * ((m >> 5) % WPC) + (m & 31);
-  int delta = -1;
-  size_t qo = 0;
-  if (r < a.rows && p >= 0 && p < a.P) {
-    const int w = r / a.G, hq = h * a.G + r % a.G;
-    delta = a.delta[(size_t)slot * a.W + w];
-    qo = (((size_t)p * a.W + w) * a.H_q + hq) * D;
-    if (delta >= a.max_position) {
-      record_error(a.err, ERR_POS_RANGE, KID_ATTN_TC, blockIdx.x, delta);
-      delta = -1;
-    }
-  }
-  uint4 q1[CPT], q2[CPT];
-  float4 cs[CPT][2], sn[CPT][2];
-  if (delta >= 0) {
+  static_assert(PER % B == 0, "rotation work split");
+#pragma unroll 1
+  for (int b0 = 0; b0 < PER; b0 += B) {
+    uint4 q1[B], q2[B];
+    float4 cs[B][2], sn[B][2];
+    int dl[B];
 #pragma unroll
-    for (int k = 0; k < CPT; ++k) {
-      const int c = c0 + k;
-      q1[k] = *reinterpret_cast<const uint4*>(a.q + qo + 8 * c);
-      q2[k] = *reinterpret_cast<const uint4*>(a.q + qo + half + 8 * c);
-      const float4* cp = reinterpret_cast<const float4*>(a.rope_cos + (size_t)delta * half + 8 * c);
-      const float4* sp = reinterpret_cast<const float4*>(a.rope_sin + (size_t)delta * half + 8 * c);
-      cs[k][0] = cp[0];
-      cs[k][1] = cp[1];
-      sn[k][0] = sp[0];
-      sn[k][1] = sp[1];
-    }
-  }
-  uint8_t* tile = a.qtiles + ((size_t)slot * a.H_kv + h) * (size_t)(kRowsM * D * 2);
-#pragma unroll
-  for (int k = 0; k < CPT; ++k) {
-    const int c = c0 + k;
-    uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
-    if (delta >= 0) {
-      const __nv_bfloat162* x1p = reinterpret_cast<const __nv_bfloat162*>(&q1[k]);
-      const __nv_bfloat162* x2p = reinterpret_cast<const __nv_bfloat162*>(&q2[k]);
-      const float cv[8] = {cs[k][0].x, cs[k][0].y, cs[k][0].z, cs[k][0].w,
-                           cs[k][1].x, cs[k][1].y, cs[k][1].z, cs[k][1].w};
-      const float sv[8] = {sn[k][0].x, sn[k][0].y, sn[k][0].z, sn[k][0].w,
-                           sn[k][1].x, sn[k][1].y, sn[k][1].z, sn[k][1].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 x1 = __bfloat1622float2(x1p[e]);
-        const float2 x2 = __bfloat1622float2(x2p[e]);
-        const float ca = cv[2 * e], cb = cv[2 * e + 1];
-        const float sa = sv[2 * e], sb = sv[2 * e + 1];
-        const __nv_bfloat162 y1 = __floats2bfloat162_rn((x1.x * ca - x2.x * sa) * a.scale_log2,
-                                                        (x1.y * cb - x2.y * sb) * a.scale_log2);
-        const __nv_bfloat162 y2 = __floats2bfloat162_rn((x2.x * ca + x1.x * sa) * a.scale_log2,
-                                                        (x2.y * cb + x1.y * sb) * a.scale_log2);
-        lo[e] = *reinterpret_cast<const uint32_t*>(&y1);
-        hi[e] = *reinterpret_cast<const uint32_t*>(&y2);
+    for (int k = 0; k < B; ++k) {
+      const int item = tid + NT * (b0 + k);
+      const int r = item / CH, c = item % CH;
+      int delta = -1;
+      size_t qo = 0;
+      if (item < ITEMS && r < a.rows) {
+        const int w = r / a.G, hq = g.h * a.G + r % a.G;
+        delta = uniform_delta >= 0 ? uniform_delta : a.delta[(size_t)slot * a.W + w];
+        qo = (((size_t)g.p * a.W + w) * a.H_q + hq) * D;
+        if (delta >= a.max_position) {
+          record_error(a.err, ERR_POS_RANGE, KID_ATTN_TC, blockIdx.x, delta);
+          delta = -1;
+        }
+      }
+      dl[k] = delta;
+      if (delta >= 0) {
+        q1[k] = *reinterpret_cast<const uint4*>(a.q + qo + 8 * c);
+        q2[k] = *reinterpret_cast<const uint4*>(a.q + qo + half + 8 * c);
+        const float4* cp = reinterpret_cast<const float4*>(a.rope_cos + (size_t)delta * half + 8 * c);
+        const float4* sp = reinterpret_cast<const float4*>(a.rope_sin + (size_t)delta * half + 8 * c);
+        cs[k][0] = cp[0];
+        cs[k][1] = cp[1];
+        sn[k][0] = sp[0];
+        sn[k][1] = sp[1];
       }
     }
-    const int d_lo = 8 * c, d_hi = half + 8 * c;
-    uint8_t* p_lo = tile + (d_lo >> 6) * kHalfBytes + m * 128 + ((((d_lo & 63) >> 3) ^ (m & 7)) << 4);
-    uint8_t* p_hi = tile + (d_hi >> 6) * kHalfBytes + m * 128 + ((((d_hi & 63) >> 3) ^ (m & 7)) << 4);
-    *reinterpret_cast<uint4*>(p_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    *reinterpret_cast<uint4*>(p_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+#pragma unroll
+    for (int k = 0; k < B; ++k) {
+      const int item = tid + NT * (b0 + k);
+      if (item >= ITEMS) break;
+      const int r = item / CH, c = item % CH;
+      uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
+      if (dl[k] >= 0) {
+        const __nv_bfloat162* x1p = reinterpret_cast<const __nv_bfloat162*>(&q1[k]);
+        const __nv_bfloat162* x2p = reinterpret_cast<const __nv_bfloat162*>(&q2[k]);
+        const float cv[8] = {cs[k][0].x, cs[k][0].y, cs[k][0].z, cs[k][0].w,
+                             cs[k][1].x, cs[k][1].y, cs[k][1].z, cs[k][1].w};
+        const float sv[8] = {sn[k][0].x, sn[k][0].y, sn[k][0].z, sn[k][0].w,
+                             sn[k][1].x, sn[k][1].y, sn[k][1].z, sn[k][1].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x1 = __bfloat1622float2(x1p[e]);
+          const float2 x2 = __bfloat1622float2(x2p[e]);
+          const float ca = cv[2 * e], cb = cv[2 * e + 1];
+          const float sa = sv[2 * e], sb = sv[2 * e + 1];
+          const __nv_bfloat162 y1 = __floats2bfloat162_rn((x1.x * ca - x2.x * sa) * a.scale_log2,
+                                                          (x1.y * cb - x2.y * sb) * a.scale_log2);
+          const __nv_bfloat162 y2 = __floats2bfloat162_rn((x2.x * ca + x1.x * sa) * a.scale_log2,
+                                                          (x2.y * cb + x1.y * sb) * a.scale_log2);
+          lo[e] = *reinterpret_cast<const uint32_t*>(&y1);
+          hi[e] = *reinterpret_cast<const uint32_t*>(&y2);
+        }
+      }
+      const int d_lo = 8 * c, d_hi = half + 8 * c;
+#pragma unroll
+      for (int j = 0; j < T; ++j) {
+        const int m = r + j * RR;
+        uint8_t* p_lo = tile + (d_lo >> 6) * kHalfBytes + m * 128 + ((((d_lo & 63) >> 3) ^ (m & 7)) << 4);
+        uint8_t* p_hi = tile + (d_hi >> 6) * kHalfBytes + m * 128 + ((((d_hi & 63) >> 3) ^ (m & 7)) << 4);
+        *reinterpret_cast<uint4*>(p_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(p_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      }
+    }
   }
-  // Launched as a programmatic dependent of the append kernel, whose writes it does not read:
-  // finishing only after that kernel has finished lets the attention kernel's single wait
-  // cover both.
-  pdl_wait();
 }
 
 // ---------------------------------------------------------------------------- attention
@@ -271,7 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Unit u = a.units[blockIdx.x];
-  const Group g = a.groups[u.group];
+  // (problem, KV head) of the unit, from its group index (no dependent load)
+  const Group g{u.group / a.H_kv, u.group % a.H_kv, 0, 0};
   const int R = a.rows;
   int active_softmax_warps = 0;               // softmax warps that own at least one real row
   for (int q = 0; q < 4; ++q) active_softmax_warps += (32 * (q % WPC) < R) ? 1 : 0;
@@ -309,6 +318,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int64_t page_base = (int64_t)layer * a.num_pages;   // first page of this layer's pool
 
+  // The first query tile (segment slot u.seg0, known from the unit without a dependent load) is
+  // built by warps 2-7 together: the softmax warps have nothing to do before the first S.  The
+  // queries may come from the kernel this grid follows: wait for it first.
+  const bool first_q = u.seg0 >= 0 && u.seg0 < a.num_seg_slots;
+  if (warp >= 2) {
+    pdl_wait();
+    if (first_q) {
+      rotate_tile<D, T, kThreads - 64>(a, g, u.seg0, u.delta0, smem + C::kQOff, threadIdx.x - 64);
+      fence_proxy_async_smem();           // generic-proxy writes -> operands of the MMA
+      asm volatile("bar.sync 3, %0;" ::"r"(kThreads - 64) : "memory");
+      if (threadIdx.x == 64) {
+        mbar_arrive(bar_qfull(0));
+        HW_TRACE_EV(2);
+      }
+    }
+  }
+
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -317,52 +343,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tw.init(a, u);
       TileInfo t;
       bool new_seg;
-      uint32_t j = 0, seg = 0;
+      uint32_t j = 0;
       bool ok = true;
-      // The rotated query tiles come from the rotation kernel just before this launch, and the
-      // tiles holding this step's new tokens from the append kernel before that: neither is
-      // read before griddepcontrol.wait.  Tiles of older tokens are streamed before it, so the
-      // ring fills while the previous kernels finish; the first query tile is loaded at the
-      // latest when the ring is full, a fresh tile or a second segment comes up, or the walk ends.
-      int32_t q0_slot = -1;
+      // Tiles holding tokens of the current step come from the append kernel, which may still
+      // run (this grid is its programmatic dependent): wait for it before the first of them.
+      // Tiles of older tokens are streamed right away.
       bool waited = false;
-      uint32_t qloads = 0;         // query tiles issued (load k goes to buffer k & 1)
-      auto load_q = [&](int qb, int32_t slot) {
-        ++qloads;
-        mbar_arrive_expect_tx(bar_qfull(qb), C::kQBytes);
-        bulk_load(q_base + qb * C::kQBytes, a.qtiles + ((size_t)slot * a.H_kv + g.h) * C::kQBytes,
-                  C::kQBytes, bar_qfull(qb));
-      };
-      auto release_q0 = [&]() {
-        if (!waited) {
+      while (ok && tw.next(&t, &new_seg)) {
+        if (t.fresh && !waited) {
           pdl_wait();
           waited = true;
-          if (q0_slot >= 0) load_q(0, q0_slot);
-          HW_TRACE_EV(2);
+          HW_TRACE_EV(248);
         }
-      };
-      while (ok && tw.next(&t, &new_seg)) {
-        if (new_seg) {
-          if (seg == 0) {
-            q0_slot = t.seg_slot;
-          } else {
-            release_q0();
-            const int qb = seg & 1;
-            if (seg >= 2)
-              ok = mbar_wait(bar_qempty(qb), ((seg >> 1) - 1) & 1, abort, kWaitLimitNs);
-            if (!ok) break;
-            load_q(qb, t.seg_slot);
-          }
-          ++seg;
-        }
-        if (t.fresh) release_q0();
         const int32_t y = (int32_t)(((page_base + t.page) * a.H_kv + g.h) * a.S + t.slot0);
         for (int part = 0; part < 2 && ok; ++part, ++j) {
           const int s = j % C::kSlots;
-          if (j >= (uint32_t)C::kSlots) {
-            release_q0();          // the MMA issuer cannot free a slot without the query tile
-            ok = mbar_wait(bar_empty(s), ((j / C::kSlots) - 1) & 1, abort, kWaitLimitNs);
-          }
+          // The first K tile goes out alone with its V: every CTA fills its ring at once at
+          // start-up, and the first tile would otherwise arrive with the last of that burst.
+          if (j == 2) ok = mbar_wait(bar_full(0), 0, abort, kWaitLimitNs);
+          if (j >= (uint32_t)C::kSlots)
+            ok = ok && mbar_wait(bar_empty(s), ((j / C::kSlots) - 1) & 1, abort, kWaitLimitNs);
           if (!ok) break;
           if (part == 0) HW_TRACE_EV(8 + 4 * (j >> 1));
           mbar_arrive_expect_tx(bar_full(s), C::kTileBytes);
@@ -373,16 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         policy);
         }
       }
-      if (ok) release_q0();
       HW_TRACE_EV(3);
       // Drain: every copy issued must have landed before the CTA can exit.
       for (uint32_t s = 0; s < (uint32_t)C::kSlots && s < j; ++s) {
         const uint32_t last = s + ((j - 1 - s) / C::kSlots) * C::kSlots;
         mbar_wait(bar_full(s), (last / C::kSlots) & 1, abort, kWaitLimitNs);
-      }
-      for (uint32_t b = 0; b < 2 && b < qloads; ++b) {
-        const uint32_t last = b + ((qloads - 1 - b) / 2) * 2;
-        mbar_wait(bar_qfull(b), (last >> 1) & 1, abort, kWaitLimitNs);
       }
       if (!ok && (*abort)) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 0);
     }
@@ -455,6 +450,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok && (*abort)) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 1);
     }
+  } else if (warp == 2 || warp == 3) {
+    // ---------------------------------------------------------------- query rotation
+    // The query tiles of the unit's later segments, into the two query buffers in turn.
+    const int tid = threadIdx.x - 64;
+    TileWalker tw;
+    tw.init(a, u);
+    TileInfo t;
+    bool new_seg;
+    uint32_t seg = 0;
+    bool ok = true;
+    while (ok && tw.next(&t, &new_seg)) {
+      if (!new_seg) continue;
+      if (seg == 0 && first_q) {
+        // built above; the plan names the unit's first segment in u.seg0
+        if (t.seg_slot != u.seg0 && tid == 0) record_error(a.err, ERR_PLAN, KID_ATTN_TC, blockIdx.x, 4);
+        ++seg;
+        continue;
+      }
+      const int qb = seg & 1;
+      if (seg >= 2) ok = mbar_wait(bar_qempty(qb), ((seg >> 1) - 1) & 1, abort, kWaitLimitNs);
+      if (!ok) break;
+      rotate_tile<D, T, kRotThreads>(a, g, t.seg_slot, -1, smem + C::kQOff + qb * C::kQBytes, tid);
+      fence_proxy_async_smem();           // generic-proxy writes -> operands of the MMA
+      asm volatile("bar.sync 4, %0;" ::"r"(kRotThreads) : "memory");
+      if (tid == 0) mbar_arrive(bar_qfull(qb));
+      ++seg;
+    }
+    if (!ok && (*abort) && tid == 0) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 3);
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax / epilogue
     // Softmax warp q takes the token columns [cq * 128/T, (cq + 1) * 128/T) of every tile,
@@ -661,15 +684,6 @@ static void launch_tc_dt(const AttnArgs& a, const TcMaps& maps, int layer, cudaS
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t rc = {};
-  rc.gridDim = dim3(a.num_seg_slots * a.H_kv);
-  rc.blockDim = dim3(256);
-  rc.stream = s;
-  rc.attrs = attr;
-  rc.numAttrs = 1;
-  cudaLaunchKernelEx(&rc, rotate_kernel<D, T>, a);
-  cudaFuncSetAttribute(attn_tc_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)C::kSmemBytes);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_units);
   cfg.blockDim = dim3(kThreads);
@@ -692,6 +706,19 @@ static void launch_tc_d(const AttnArgs& a, const TcMaps& maps, int layer, cudaSt
   else
     launch_tc_dt<D, 1>(a, maps, layer, s, e0, e1);
 }
+
+template <int D>
+static cudaError_t prepare_tc_d() {
+  constexpr int smem = (int)Cfg<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_tc_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_tc_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return e;
+}
+
+cudaError_t prepare_attention_tc(int D) { return D == 64 ? prepare_tc_d<64>() : prepare_tc_d<128>(); }
 
 void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s,
                          cudaEvent_t ev_before, cudaEvent_t ev_after) {

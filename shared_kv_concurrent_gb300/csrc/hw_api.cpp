@@ -22,9 +22,10 @@
 
 namespace {
 
-constexpr int kSlots = 8;              // pinned staging / device plan slots in flight
+constexpr int kMaxSlots = 32;          // pinned staging / device plan slots in flight, at most
+constexpr size_t kSlotBudget = 64u << 20;  // ... and at most this many bytes of them (>= 4 slots)
 constexpr size_t kAlign = 256;
-constexpr int kPieceMax = 256;         // tokens per piece (never crosses a page)
+constexpr int kPieceMax = 128;         // tokens per piece = one kernel tile (never crosses a page)
 constexpr int kProfPairs = 4096;       // timed launches kept per hw_profile_read
 
 thread_local int g_cuda_err = 0;
@@ -47,9 +48,10 @@ hw_status cuda_fail(cudaError_t e) {
   } while (0)
 
 struct Layout {
-  size_t err, cos, sin, slots, partials, tickets, qtiles, total;
+  size_t err, cos, sin, slots, partials, tickets, total;
   size_t slot_bytes;
   int32_t max_segments, max_append, max_pieces, max_units, max_seg_slots, rows;
+  int32_t num_slots;
 };
 
 bool valid_config(const hw_config* c) {
@@ -77,8 +79,10 @@ Layout make_layout(const hw_config* c) {
   L.max_segments = c->max_segments ? c->max_segments : (int32_t)(P * (1 + 4 * W));
   const int64_t pool_tokens = (int64_t)c->num_pages * c->page_size;
   L.max_append = c->max_append_tokens ? c->max_append_tokens : (int32_t)pool_tokens;
-  // every visible token sits in a page: pieces <= H * (pool_tokens / 256 + one per segment)
-  L.max_pieces = (int32_t)(H * (pool_tokens / kPieceMax + L.max_segments + 1));
+  // Pieces are listed once per problem (shared by its KV heads); a piece never leaves its
+  // page and pieces start every kPieceMax slots of it, so a page holds at most
+  // ceil(S / kPieceMax) of them.
+  L.max_pieces = (int32_t)((int64_t)c->num_pages * ((c->page_size + kPieceMax - 1) / kPieceMax) + 1);
   L.max_units = (int32_t)(P * H + 2048);
   L.max_seg_slots = L.max_segments;
   const size_t runs = (size_t)P * (W + 1) + (size_t)L.max_append / 128 + 2;
@@ -86,10 +90,11 @@ Layout make_layout(const hw_config* c) {
   const size_t attn_bytes = align_up((size_t)L.max_pieces * sizeof(hw::Piece), 16) +
                             align_up((size_t)L.max_units * sizeof(hw::Unit), 16) +
                             align_up((size_t)P * H * sizeof(hw::Group), 16) +
-                            align_up((size_t)L.max_seg_slots * W * sizeof(int32_t), 16) +
-                            align_up((size_t)L.max_seg_slots * sizeof(int32_t), 16);
+                            align_up((size_t)L.max_seg_slots * W * sizeof(int32_t), 16);
   // A slot holds a step's append runs followed by its attention plan (uploaded together).
   L.slot_bytes = align_up(append_bytes, kAlign) + align_up(attn_bytes, kAlign);
+  // Staging slots let the host run that many calls ahead of the device.
+  L.num_slots = (int32_t)std::max<size_t>(4, std::min<size_t>(kMaxSlots, kSlotBudget / L.slot_bytes));
   size_t off = 0;
   L.err = off;
   off += kAlign;
@@ -99,23 +104,28 @@ Layout make_layout(const hw_config* c) {
   L.sin = off;
   off += tab;
   L.slots = off;
-  off += kSlots * L.slot_bytes;
+  off += (size_t)L.num_slots * L.slot_bytes;
   L.partials = off;
   off += align_up((size_t)L.max_units * L.rows * hw::part_stride(c->head_dim) * sizeof(float), kAlign);
   L.tickets = off;
   off += align_up((size_t)P * H * sizeof(uint32_t), kAlign);
-  // Rotated query tiles of the tensor-core path: one 128-row x D bf16 tile per (segment slot,
-  // KV head), laid out exactly as the kernel's shared-memory operand.
-  L.qtiles = off;
-  off += (size_t)L.max_seg_slots * H * 128 * c->head_dim * 2;
   L.total = off;
   return L;
 }
 
 // Offsets of the arrays of an attention plan inside its buffer, and their sizes.
 struct PlanOffsets {
-  size_t pieces, units, groups, delta, slot_problem, bytes;
+  size_t pieces, units, groups, delta, bytes;
   int32_t num_pieces, num_units, num_groups, num_seg_slots;
+};
+
+// Reused host buffers of the plan builder (no allocation per call once they have grown).
+struct PlanScratch {
+  std::vector<hw::Piece> pieces;
+  std::vector<hw::Unit> units;
+  std::vector<hw::Group> groups;
+  std::vector<int32_t> delta, prob_piece_begin, refs, live_len, live_ref;
+  std::vector<int64_t> prob_tokens;
 };
 
 struct Seg {
@@ -134,9 +144,13 @@ struct hw_ctx {
   __nv_bfloat16* v_pool = nullptr;
   char* ws = nullptr;
   size_t layer_elems = 0;
-  char* h_slots = nullptr;                 // pinned staging, kSlots * slot_bytes
-  cudaEvent_t slot_ev[kSlots] = {};
-  bool slot_used[kSlots] = {};
+  char* h_slots = nullptr;                 // pinned staging, lay.num_slots * slot_bytes
+  cudaEvent_t slot_ev[kMaxSlots] = {};     // compute stream: last kernel reading the slot
+  bool slot_used[kMaxSlots] = {};
+  // Plans go up on a stream of their own, ahead of the compute stream, which waits for them by
+  // event: when the host runs ahead of the device the copy is off the critical path.
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t copy_ev[kMaxSlots] = {};
   int next_slot = 0;
   hw::TcMaps maps{};
   bool use_tc = false;                     // tensor-core attention (W*G >= 16 rows)
@@ -154,6 +168,7 @@ struct hw_ctx {
   size_t step_plan_off = 0;
   bool step_plan_ok = false;
   PlanOffsets step_po{};
+  PlanScratch ps;
   // measurement
   bool prof_on = false;
   int64_t n_launch = 0, n_attn = 0, n_append = 0;
@@ -210,10 +225,18 @@ struct hw_ctx {
     add(live[p][w]);
     return off - 1;
   }
+  // Copy `bytes` of staging slot `slot` to its device copy on the copy stream and make the
+  // compute stream `s` wait for it.  The slot's previous readers have completed (acquire_slot).
+  hw_status upload_slot(int slot, size_t bytes, cudaStream_t s) {
+    HW_CUDA(cudaMemcpyAsync(d_slot(slot), h_slot(slot), bytes, cudaMemcpyHostToDevice, copy_stream));
+    HW_CUDA(cudaEventRecord(copy_ev[slot], copy_stream));
+    HW_CUDA(cudaStreamWaitEvent(s, copy_ev[slot], 0));
+    return HW_OK;
+  }
   // Pick the next staging slot; waits only if the slot's previous use is still in flight.
   hw_status acquire_slot(int* slot) {
     const int i = next_slot;
-    next_slot = (next_slot + 1) % kSlots;
+    next_slot = (next_slot + 1) % lay.num_slots;
     if (slot_used[i]) HW_CUDA(cudaEventSynchronize(slot_ev[i]));
     *slot = i;
     return HW_OK;
@@ -261,11 +284,15 @@ void hw_destroy(hw_ctx* ctx) {
   if (!ctx) return;
   for (cudaEvent_t e : ctx->prof_ev)
     if (e) cudaEventDestroy(e);
-  for (int i = 0; i < kSlots; ++i)
+  for (int i = 0; i < kMaxSlots; ++i)
     if (ctx->slot_ev[i]) {
       cudaEventSynchronize(ctx->slot_ev[i]);
       cudaEventDestroy(ctx->slot_ev[i]);
     }
+  if (ctx->copy_stream) cudaStreamSynchronize(ctx->copy_stream);
+  for (int i = 0; i < kMaxSlots; ++i)
+    if (ctx->copy_ev[i]) cudaEventDestroy(ctx->copy_ev[i]);
+  if (ctx->copy_stream) cudaStreamDestroy(ctx->copy_stream);
   if (ctx->h_slots) cudaFreeHost(ctx->h_slots);
   delete ctx;
 }
@@ -326,10 +353,17 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
                             cfg->page_size;
   c->use_tc = c->rows >= 16 && pool_rows < (1ll << 31);
   if (c->use_tc && !hw::make_tc_maps(*cfg, k_pool, v_pool, &c->maps)) return fail(HW_ERR_UNSUPPORTED);
-  e = cudaHostAlloc((void**)&c->h_slots, kSlots * lay.slot_bytes, cudaHostAllocDefault);
+  e = hw::prepare_attention_fma(cfg->head_dim);
+  if (e == cudaSuccess && c->use_tc) e = hw::prepare_attention_tc(cfg->head_dim);
   if (e != cudaSuccess) return fail(cuda_fail(e));
-  for (int i = 0; i < kSlots; ++i) {
+  e = cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+  e = cudaHostAlloc((void**)&c->h_slots, (size_t)lay.num_slots * lay.slot_bytes,
+                    cudaHostAllocDefault);
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+  for (int i = 0; i < kMaxSlots; ++i) {
     e = cudaEventCreateWithFlags(&c->slot_ev[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->copy_ev[i], cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(cuda_fail(e));
   }
   // RoPE table: cos/sin of p * theta^(-2i/D) in fp64 on the host, stored as fp32.
@@ -362,7 +396,7 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
 }  // extern "C"
 
 namespace {
-bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap,
+bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap,
                           int64_t target_override);
 }  // namespace
 
@@ -470,8 +504,8 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
         plan_off < c->lay.slot_bytes &&
         build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->use_tc ? c->num_sms : 0) &&
         plan_off + po.bytes <= c->lay.slot_bytes;
-    HW_CUDA(cudaMemcpyAsync(c->d_slot(slot), c->h_slot(slot),
-                            plan_off + (plan_ok ? po.bytes : 0), cudaMemcpyHostToDevice, s));
+    st = c->upload_slot(slot, plan_off + (plan_ok ? po.bytes : 0), s);
+    if (st != HW_OK) return st;
     c->step_slot = slot;
     c->step_runs = nr;
     c->step_max_run = max_run;
@@ -515,69 +549,102 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
 namespace {
 
 // Build the attention plan of the current state into host buffer `buf` (slot_bytes long).
-// Returns false if a table would overflow.  Offsets of each array are written to `off`.
-
+// Returns false if a table would overflow.  Offsets of each array are written to `po`.
+//
+// The pieces of a problem are listed once and shared by its KV heads: the units of group
+// (p, h) index the problem's piece list, and the head comes from the group.  Every worker's
+// view holds the same segments (common part, then the live blocks in the worker's order), so
+// i_q is the problem's visible length - 1 and a segment's delta for worker w is i_q minus the
+// segment's offset in w's view.
 // unit_cap > 0 bounds the number of units (one partial result each); 0 = the default split.
-bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0,
+bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0,
                           int64_t target_override = 0) {
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
   const int32_t S = c->cfg.page_size;
   const Layout& L = c->lay;
-  std::vector<hw::Piece> pieces;
-  std::vector<int32_t> delta;
-  std::vector<int32_t> slot_problem;
-  std::vector<int64_t> group_tokens(P * H, 0);
-  std::vector<int32_t> group_piece_begin(P * H + 1, 0);
-  struct SegRef { int32_t sid, slot; };
-  std::vector<hw::Piece> proto;   // per problem: the pieces of one KV head
+  PlanScratch& ps = c->ps;
+  ps.pieces.clear();
+  ps.delta.clear();
+  ps.units.clear();
+  ps.groups.clear();
+  ps.prob_piece_begin.assign(P + 1, 0);
+  ps.prob_tokens.assign(P, 0);
+  const int32_t step = std::min(kPieceMax, S);
   for (int32_t p = 0; p < P; ++p) {
-    // Segments of the problem, in view order of the common part, then worker blocks.
-    std::vector<SegRef> refs;
-    auto add_ref = [&](int32_t sid) {
-      if (c->segs[sid].visible() > 0) refs.push_back({sid, 0});
-    };
-    for (int32_t sid : c->common[p]) add_ref(sid);
-    for (int32_t w = 0; w < W; ++w) add_ref(c->live[p][w]);
-    const int32_t slot_base = (int32_t)(delta.size() / (size_t)W);
-    if (slot_base + (int64_t)refs.size() > L.max_seg_slots) return false;
-    delta.resize(delta.size() + refs.size() * (size_t)W, -1);
-    slot_problem.resize(slot_problem.size() + refs.size(), p);
-    for (size_t r = 0; r < refs.size(); ++r) refs[r].slot = slot_base + (int32_t)r;
-    for (int32_t w = 0; w < W; ++w) {
-      std::vector<int32_t> ids, offs, lens;
-      const int32_t i_q = c->view(p, w, &ids, &offs, &lens);
-      for (size_t e = 0; e < ids.size(); ++e)
-        for (const SegRef& r : refs)
-          if (r.sid == ids[e]) delta[(size_t)r.slot * W + w] = i_q - offs[e];
+    ps.prob_piece_begin[p] = (int32_t)ps.pieces.size();
+    // Visible segments: the common part in commit order, then the live blocks by worker.
+    ps.refs.clear();
+    int64_t common_len = 0;
+    for (int32_t sid : c->common[p]) {
+      const int32_t n = c->segs[sid].visible();
+      if (n > 0) {
+        ps.refs.push_back(sid);
+        common_len += n;
+      }
     }
-    proto.clear();
+    const int32_t n_common_refs = (int32_t)ps.refs.size();
+    ps.live_len.assign(W, 0);
+    ps.live_ref.assign(W, -1);
+    int64_t total = common_len;
+    for (int32_t w = 0; w < W; ++w) {
+      const int32_t sid = c->live[p][w];
+      const int32_t n = c->segs[sid].visible();
+      ps.live_len[w] = n;
+      total += n;
+      if (n > 0) {
+        ps.live_ref[w] = (int32_t)ps.refs.size();
+        ps.refs.push_back(sid);
+      }
+    }
+    const int32_t slot_base = (int32_t)(ps.delta.size() / (size_t)W);
+    if (slot_base + (int64_t)ps.refs.size() > L.max_seg_slots) return false;
+    ps.delta.resize(ps.delta.size() + ps.refs.size() * (size_t)W, -1);
+    int32_t* delta = ps.delta.data() + (size_t)slot_base * W;
+    const int64_t i_q = total - 1;
+    // common segments: the same offset in every view
+    int64_t off = 0;
+    for (int32_t r = 0; r < n_common_refs; ++r) {
+      for (int32_t w = 0; w < W; ++w) delta[(size_t)r * W + w] = (int32_t)(i_q - off);
+      off += c->segs[ps.refs[r]].visible();
+    }
+    // live block of worker u: last in u's own view; in another worker w's view it follows the
+    // common part and the blocks of the workers before u other than w
+    int64_t before_u = common_len;           // common part + blocks of workers 0 .. u-1
+    for (int32_t u = 0; u < W; ++u) {
+      const int32_t r = ps.live_ref[u];
+      if (r >= 0) {
+        for (int32_t w = 0; w < W; ++w) {
+          const int64_t o = (w == u)  ? total - ps.live_len[u]
+                            : (w < u) ? before_u - ps.live_len[w]
+                                      : before_u;
+          delta[(size_t)r * W + w] = (int32_t)(i_q - o);
+        }
+      }
+      before_u += ps.live_len[u];
+    }
     int64_t tok = 0;
-    for (const SegRef& r : refs) {
-      const Seg& sg = c->segs[r.sid];
+    for (size_t r = 0; r < ps.refs.size(); ++r) {
+      const Seg& sg = c->segs[ps.refs[r]];
       const int32_t n = sg.visible();
-      for (int32_t j = 0; j < n; j += std::min(kPieceMax, S)) {
+      for (int32_t j = 0; j < n; j += step) {
         const int32_t pg = c->cfg.contiguous ? sg.pages[0] : sg.pages[j / S];
         const int32_t slot0 = c->cfg.contiguous ? j : j % S;
         const int32_t cnt = std::min(std::min(kPieceMax, S - slot0), n - j);
         // fresh: holds tokens appended in this step (the kernels read it only after the append)
         const int32_t fresh = (sg.pending > 0 && j + cnt > sg.length) ? 1 : 0;
-        proto.push_back(hw::Piece{r.slot, pg, slot0, cnt, fresh});
+        if ((int64_t)ps.pieces.size() >= L.max_pieces) return false;
+        ps.pieces.push_back(hw::Piece{slot_base + (int32_t)r, pg, slot0, cnt, fresh});
         // Balance by 128-token tiles: a partial tile costs the kernels a full one.
         tok += (cnt + 127) / 128 * 128;
       }
     }
-    for (int32_t h = 0; h < H; ++h) {
-      group_piece_begin[p * H + h] = (int32_t)pieces.size();
-      pieces.insert(pieces.end(), proto.begin(), proto.end());
-      group_tokens[p * H + h] = tok;
-    }
+    ps.prob_tokens[p] = tok;
   }
-  group_piece_begin[P * H] = (int32_t)pieces.size();
-  if ((int64_t)pieces.size() > L.max_pieces) return false;
+  ps.prob_piece_begin[P] = (int32_t)ps.pieces.size();
   // Units: split every group into KV-entry-balanced runs of pieces (summary section 9: the
   // kernel balances by KV entries, not by blocks, then reduces the partial results).
   int64_t total_tok = 0;
-  for (int64_t t : group_tokens) total_tok += t;
+  for (int64_t t : ps.prob_tokens) total_tok += t * H;
   int64_t target_units = std::max<int64_t>((int64_t)P * H,
                                            target_override > 0 ? target_override : 4ll * c->num_sms);
   if (unit_cap > 0) {
@@ -585,59 +652,64 @@ bool build_attention_plan(const hw_ctx* c, char* buf, PlanOffsets* po, int64_t u
     // per-group counts are floored and then raised to >= 1: keep room for that raise
     target_units = std::max<int64_t>(0, std::min<int64_t>(target_units, unit_cap - (int64_t)P * H));
   }
-  std::vector<hw::Unit> units;
-  std::vector<hw::Group> groups;
   for (int32_t g = 0; g < P * H; ++g) {
-    const int32_t pb = group_piece_begin[g], pe = group_piece_begin[g + 1];
-    const int64_t T = group_tokens[g];
-    hw::Group gr{g / H, g % H, (int32_t)units.size(), 0};
+    const int32_t p = g / H;
+    const int32_t pb = ps.prob_piece_begin[p], pe = ps.prob_piece_begin[p + 1];
+    const int64_t T = ps.prob_tokens[p];
+    hw::Group gr{p, g % H, (int32_t)ps.units.size(), 0};
     int64_t n_units = total_tok ? (target_units * T + (unit_cap > 0 ? 0 : total_tok / 2)) / total_tok : 1;
     n_units = std::max<int64_t>(1, std::min<int64_t>(n_units, pe - pb));
     if (pe == pb) {
-      units.push_back(hw::Unit{pb, pb, g, 0});
+      ps.units.push_back(hw::Unit{pb, pb, g, -1, -1, {0, 0, 0}});
     } else {
       int64_t cum = 0;
       int32_t cur = -1;
       for (int32_t i = pb; i < pe; ++i) {
-        const int64_t wt = (pieces[i].ntok + 127) / 128 * 128;  // tile-rounded weight
-        const int64_t mid2 = 2 * cum + wt;                      // twice the piece midpoint
+        const int64_t wt = (ps.pieces[i].ntok + 127) / 128 * 128;  // tile-rounded weight
+        const int64_t mid2 = 2 * cum + wt;                         // twice the piece midpoint
         const int32_t k = (int32_t)std::min<int64_t>(n_units - 1, (mid2 * n_units) / (2 * T));
         if (k != cur) {
-          units.push_back(hw::Unit{i, i + 1, g, 0});
+          ps.units.push_back(hw::Unit{i, i + 1, g, ps.pieces[i].seg_slot, -1, {0, 0, 0}});
           cur = k;
         } else {
-          units.back().piece_end = i + 1;
+          ps.units.back().piece_end = i + 1;
         }
         cum += wt;
       }
     }
-    gr.unit_end = (int32_t)units.size();
-    groups.push_back(gr);
+    gr.unit_end = (int32_t)ps.units.size();
+    ps.groups.push_back(gr);
   }
-  if ((int64_t)units.size() > L.max_units) return false;
-  if (unit_cap > 0 && (int64_t)units.size() > unit_cap) return false;
+  if ((int64_t)ps.units.size() > L.max_units) return false;
+  if (unit_cap > 0 && (int64_t)ps.units.size() > unit_cap) return false;
+  // A segment seen by every worker at the same view offset (every common segment) has one
+  // rotation for all query rows: the kernels then need no delta-table load for it.
+  for (hw::Unit& u : ps.units) {
+    if (u.seg0 < 0) continue;
+    const int32_t* row = ps.delta.data() + (size_t)u.seg0 * W;
+    bool same = row[0] >= 0;
+    for (int32_t w = 1; w < W && same; ++w) same = row[w] == row[0];
+    u.delta0 = same ? row[0] : -1;
+  }
   size_t off = 0;
   po->pieces = off;
-  off = align_up(off + pieces.size() * sizeof(hw::Piece), 16);
+  off = align_up(off + ps.pieces.size() * sizeof(hw::Piece), 16);
   po->units = off;
-  off = align_up(off + units.size() * sizeof(hw::Unit), 16);
+  off = align_up(off + ps.units.size() * sizeof(hw::Unit), 16);
   po->groups = off;
-  off = align_up(off + groups.size() * sizeof(hw::Group), 16);
+  off = align_up(off + ps.groups.size() * sizeof(hw::Group), 16);
   po->delta = off;
-  off = align_up(off + delta.size() * sizeof(int32_t), 16);
-  po->slot_problem = off;
-  off = align_up(off + slot_problem.size() * sizeof(int32_t), 16);
+  off = align_up(off + ps.delta.size() * sizeof(int32_t), 16);
   po->bytes = off;
   if (off > L.slot_bytes) return false;
-  std::memcpy(buf + po->pieces, pieces.data(), pieces.size() * sizeof(hw::Piece));
-  std::memcpy(buf + po->units, units.data(), units.size() * sizeof(hw::Unit));
-  std::memcpy(buf + po->groups, groups.data(), groups.size() * sizeof(hw::Group));
-  std::memcpy(buf + po->delta, delta.data(), delta.size() * sizeof(int32_t));
-  std::memcpy(buf + po->slot_problem, slot_problem.data(), slot_problem.size() * sizeof(int32_t));
-  po->num_pieces = (int32_t)pieces.size();
-  po->num_units = (int32_t)units.size();
-  po->num_groups = (int32_t)groups.size();
-  po->num_seg_slots = (int32_t)(delta.size() / (size_t)W);
+  std::memcpy(buf + po->pieces, ps.pieces.data(), ps.pieces.size() * sizeof(hw::Piece));
+  std::memcpy(buf + po->units, ps.units.data(), ps.units.size() * sizeof(hw::Unit));
+  std::memcpy(buf + po->groups, ps.groups.data(), ps.groups.size() * sizeof(hw::Group));
+  std::memcpy(buf + po->delta, ps.delta.data(), ps.delta.size() * sizeof(int32_t));
+  po->num_pieces = (int32_t)ps.pieces.size();
+  po->num_units = (int32_t)ps.units.size();
+  po->num_groups = (int32_t)ps.groups.size();
+  po->num_seg_slots = (int32_t)(ps.delta.size() / (size_t)W);
   return true;
 }
 
@@ -649,6 +721,7 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
                                   int32_t out_dtype, float* lse, void* stream) {
   if (!c || !q || !out || layer < 0 || layer >= c->cfg.num_layers) return HW_ERR_INVALID_ARG;
   if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
+  if (((uintptr_t)q | (uintptr_t)out) % 16) return HW_ERR_INVALID_ARG;
   if (c->step_active && !c->appended[layer]) return HW_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   int slot = 0;
@@ -667,15 +740,14 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
     if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
-    HW_CUDA(cudaMemcpyAsync(dbase, c->h_slot(slot), po.bytes, cudaMemcpyHostToDevice, s));
+    st = c->upload_slot(slot, po.bytes, s);
+    if (st != HW_OK) return st;
   }
   hw::AttnArgs a{};
   a.pieces = reinterpret_cast<const hw::Piece*>(dbase + po.pieces);
   a.units = reinterpret_cast<const hw::Unit*>(dbase + po.units);
   a.groups = reinterpret_cast<const hw::Group*>(dbase + po.groups);
   a.delta = reinterpret_cast<const int32_t*>(dbase + po.delta);
-  a.slot_problem = reinterpret_cast<const int32_t*>(dbase + po.slot_problem);
-  a.qtiles = reinterpret_cast<uint8_t*>(c->ws + c->lay.qtiles);
   a.num_units = po.num_units;
   a.num_groups = po.num_groups;
   a.num_seg_slots = po.num_seg_slots;
@@ -705,7 +777,7 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   cudaEvent_t e0 = pi >= 0 ? c->prof_ev[2 * pi] : nullptr;
   cudaEvent_t e1 = pi >= 0 ? c->prof_ev[2 * pi + 1] : nullptr;
   if (c->use_tc) {
-    // query rotation, then the attention kernel and the merge as programmatic dependents
+    // the attention kernel and the merge, both as programmatic dependents
     hw::launch_attention_tc(a, c->maps, layer, s, e0, e1);
   } else {
     if (e0) cudaEventRecord(e0, s);
@@ -715,7 +787,7 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   HW_CUDA(cudaGetLastError());
   hw::launch_merge(a, s, c->use_tc);
   HW_CUDA(cudaGetLastError());
-  c->n_launch += c->use_tc ? 3 : 2;
+  c->n_launch += 2;
   c->n_attn += 1;
   HW_CUDA(cudaEventRecord(c->slot_ev[slot], s));
   c->slot_used[slot] = true;
@@ -733,6 +805,7 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
   if (!c || !q || !out || !scratch || layer < 0 || layer >= c->cfg.num_layers)
     return HW_ERR_INVALID_ARG;
   if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
+  if (((uintptr_t)q | (uintptr_t)out) % 16) return HW_ERR_INVALID_ARG;
   if (c->step_active && !c->appended[layer]) return HW_ERR_INVALID_ARG;
   const size_t per_unit = (size_t)c->rows * hw::part_stride(c->cfg.head_dim) * sizeof(float);
   const size_t plan_region = align_up(std::min(c->lay.slot_bytes, scratch_bytes / 4), kAlign);
@@ -752,7 +825,6 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
   a.units = reinterpret_cast<const hw::Unit*>(scratch + po.units);
   a.groups = reinterpret_cast<const hw::Group*>(scratch + po.groups);
   a.delta = reinterpret_cast<const int32_t*>(scratch + po.delta);
-  a.slot_problem = reinterpret_cast<const int32_t*>(scratch + po.slot_problem);
   a.num_units = po.num_units;
   a.num_groups = po.num_groups;
   a.num_seg_slots = po.num_seg_slots;

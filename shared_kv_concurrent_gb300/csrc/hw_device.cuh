@@ -19,3 +19,32 @@ __device__ __forceinline__ void record_error(uint32_t* err, uint32_t bits, uint3
 }
 
 }  // namespace hw
+
+// Timeline spans, compiled in only with -DHW_TRACE (a separate debug build of the library):
+// per translation unit, the earliest CTA start and latest CTA end of its kernels, in
+// %globaltimer nanoseconds, read back through hw_span_<name>_read / _clear.
+#ifdef HW_TRACE
+static __device__ unsigned long long g_span[8];
+__device__ __forceinline__ unsigned long long span_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define HW_SPAN_BEGIN(k) \
+  do { if (threadIdx.x == 0) atomicMin(&g_span[2 * (k)], span_now()); } while (0)
+#define HW_SPAN_END(k) \
+  do { if (threadIdx.x == 0) atomicMax(&g_span[2 * (k) + 1], span_now()); } while (0)
+#define HW_SPAN_EXPORT(name)                                                      \
+  extern "C" int hw_span_##name##_read(unsigned long long* dst) {                 \
+    return (int)cudaMemcpyFromSymbol(dst, g_span, sizeof(g_span));                \
+  }                                                                               \
+  extern "C" int hw_span_##name##_clear(void) {                                   \
+    unsigned long long h[8];                                                      \
+    for (int i = 0; i < 8; ++i) h[i] = (i & 1) ? 0ull : ~0ull;                    \
+    return (int)cudaMemcpyToSymbol(g_span, h, sizeof(h));                         \
+  }
+#else
+#define HW_SPAN_BEGIN(k) do { } while (0)
+#define HW_SPAN_END(k) do { } while (0)
+#define HW_SPAN_EXPORT(name)
+#endif

@@ -35,7 +35,7 @@ struct AppendRun {
   int32_t pad;
 };
 
-// A piece: <= 256 consecutive tokens of one segment, inside one page, for one KV head.
+// A piece: <= 128 consecutive tokens (one kernel tile) of one segment, inside one page.
 struct Piece {
   int32_t seg_slot;  // row of the delta table (problem, segment) -> per-worker rotation
   int32_t page;
@@ -51,8 +51,10 @@ __host__ __device__ constexpr int part_stride(int D) { return D + 4; }
 struct Unit {
   int32_t piece_begin;
   int32_t piece_end;
-  int32_t group;
-  int32_t pad;
+  int32_t group;     // p * H_kv + h
+  int32_t seg0;      // seg_slot of the first piece, -1 if the unit has none
+  int32_t delta0;    // the rotation of seg0 if it is the same for every worker, else -1
+  int32_t pad[3];
 };
 
 // A group: one (problem, KV head); its units are [unit_begin, unit_end).
@@ -82,8 +84,6 @@ struct AttnArgs {
   const Unit* units;
   const Group* groups;
   const int32_t* delta;       // [seg_slots][W]: i_q(w) - view offset, or -1 (not visible)
-  const int32_t* slot_problem;  // [seg_slots]: problem of each delta row
-  uint8_t* qtiles;            // [seg_slots][H_kv] rotated query tiles (tensor-core path)
   int32_t num_units, num_groups, num_seg_slots;
   const __nv_bfloat16* k_layer;
   const __nv_bfloat16* v_layer;
@@ -106,10 +106,14 @@ struct TcMaps {
   CUtensorMap v;
 };
 
+// Per-device kernel attributes (shared-memory limits), set once when a context is created.
+cudaError_t prepare_attention_fma(int D);
+cudaError_t prepare_attention_tc(int D);
+
 void launch_append(const AppendArgs& a, cudaStream_t s);
 void launch_attention_fma(const AttnArgs& a, cudaStream_t s);
-// Launches the query rotation and the attention kernel; ev_before / ev_after (optional) are
-// recorded directly around the attention kernel.
+// Launches the attention kernel; ev_before / ev_after (optional) are recorded directly around
+// it (and it is then launched without programmatic chaining).
 void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s,
                          cudaEvent_t ev_before = nullptr, cudaEvent_t ev_after = nullptr);
 // pdl: launch as a programmatic dependent of the preceding kernel (it waits for its writes).

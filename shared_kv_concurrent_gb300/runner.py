@@ -38,7 +38,7 @@ class WorkloadRunner:
             self.cache.append_kv(layer, n, kd, vd)
             del kd, vd
         self.cache.step_end(np.zeros((w.num_problems, w.num_workers), np.uint8))
-        self.n_step = wl.step_n_new(w)
+        self.n_step = np.ascontiguousarray(wl.step_n_new(w), dtype=np.int32)
 
     def step_inputs(self, step: int):
         """Device tensors (k[L], v[L], q[L]) of decode ``step``."""
@@ -50,16 +50,19 @@ class WorkloadRunner:
             qs.append(to_device_bf16(wl.step_q(self.w, layer, step), self.device))
         return ks, vs, qs
 
-    def append(self, inputs) -> None:
+    def append(self, inputs, stream=None) -> None:
+        """``stream``: a torch stream or raw cudaStream_t handle; None = torch's current one."""
         ks, vs, _ = inputs
         for layer in range(self.w.num_layers):
-            self.cache.append_kv(layer, self.n_step, ks[layer], vs[layer])
+            self.cache.append_kv(layer, self.n_step, ks[layer], vs[layer], stream)
 
-    def attend(self, inputs, outs: List, lses: Optional[List] = None, out_dtype="bf16") -> None:
+    def attend(self, inputs, outs: List, lses: Optional[List] = None, out_dtype="bf16",
+               stream=None) -> None:
         _, _, qs = inputs
         for layer in range(self.w.num_layers):
             self.cache.concurrent_attention(layer, qs[layer], outs[layer], out_dtype,
-                                            None if lses is None else lses[layer])
+                                            None if lses is None else lses[layer], stream)
 
-    def end(self, step: int, finished=None) -> None:
-        self.cache.step_end(wl.finished_mask(self.w, step) if finished is None else finished)
+    def end(self, step: int, finished=None, stream=None) -> None:
+        self.cache.step_end(wl.finished_mask(self.w, step) if finished is None else finished,
+                            stream)
