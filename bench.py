@@ -45,6 +45,24 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def captured_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, or None if the kernel's
+    sources changed since that capture (the summary records their hash)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "attn_tc_kernel_w8_common32768.md")) as f:
+            text = f.read()
+        rec = text.split("kernel-source-sha256:")[1].split()[0]
+        traffic = int(text.split("traffic-bytes-per-launch:")[1].split()[0])
+        h = hashlib.sha256()
+        for name in ("attn_tc.cu", "tc_ptx.cuh", "hw_internal.h"):
+            with open(os.path.join(ROOT, "shared_kv_concurrent_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        return traffic if h.hexdigest() == rec else None
+    except Exception:
+        return None
+
+
 def workload_for(name):
     import workload as wl
     return wl.CONFIGS[name]()
@@ -342,7 +360,9 @@ def run_ours(args):
         "pct_of_peak": 100.0 * value / world / peak,
         "worker_tokens_per_s": world * P * W * args.steps / t_total,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "frac": achieved / peak,
+                     "traffic": captured_traffic() if w.name == "w8_common32768_paged" else None,
+                     "peak_kind": peak_kind,
                      "kernel": "concurrent attention (split-K partials)",
                      "kernel_ms": attn_ms,
                      "algorithmic_bytes_per_launch": attn_bytes / args.steps},
