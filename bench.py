@@ -276,6 +276,7 @@ def run_ours(args):
     binding.hw_profile_enable(ctx, True)
     binding.hw_profile_read(ctx)
     attn_bytes = 0
+    torch.cuda._sleep(int(min(0.2, 1.3 * ahead * host_step + 1e-3) * sm_hz))   # queued ahead too
     for i in range(args.steps):
         s = args.warmup + args.steps + i
         flush.zero_()

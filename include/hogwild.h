@@ -112,14 +112,22 @@ void hw_destroy(hw_ctx* ctx);
  *   n_new: host int32[P][W + 1]; n_new[p][0] tokens go to problem p's common block (the last
  *          common segment), n_new[p][1 + w] to worker w's current block.
  *   k_raw, v_raw: device bf16 [sum n_new][H_kv][D], UNROTATED keys and values, ordered
- *          problem-major, then block 0 (common), 1..W, each in position order.
+ *          problem-major, then block 0 (common), 1..W, each in position order; 16-byte
+ *          aligned.  They may be read later than this call (see "When the write happens").
  * Key token j of a block is stored as bf16(rho(k, j)) at (page_of(j), j mod S); values are
  * copied.  The first append of a step allocates pages (FIFO from page_order; problems in
  * order, then the common block, then workers in ascending id; a new page whenever j mod S == 0;
  * in contiguous mode one page at j == 0).  Every layer must append once per step with the same
  * n_new.  Attention in the step sees the appended tokens; lengths advance at hw_step_end().
+ * When the write happens: with the tensor-core attention (W * H_q / H_kv >= 16 query rows) and
+ * at most 16 tokens per block in the step (decode), this call only records k_raw / v_raw and
+ * the layer's hw_concurrent_attention writes the tokens itself, inside its kernel, before it
+ * reads them; if the step ends without that call, hw_step_end writes them.  Otherwise an append
+ * kernel is enqueued here.  Either way k_raw and v_raw must keep their contents, in stream
+ * order, until the layer's attention call or hw_step_end, whichever comes first.
  * Errors: HW_ERR_INVALID_ARG (bad layer, counts differing from the step's first append, layer
- * appended twice), HW_ERR_OUT_OF_PAGES, HW_ERR_CAPACITY (contiguous block full).
+ * appended twice, unaligned k_raw / v_raw), HW_ERR_OUT_OF_PAGES, HW_ERR_CAPACITY (contiguous
+ * block full).
  */
 hw_status hw_append_kv(hw_ctx* ctx, int32_t layer, const int32_t* n_new, const void* k_raw,
                        const void* v_raw, void* stream);
@@ -170,7 +178,8 @@ hw_status hw_concurrent_attention_noalloc(hw_ctx* ctx, int32_t layer, const void
  * re-rotated: the new view offset is absorbed by the query rotation.
  *   finished: host uint8[P][W] or NULL (no commits).
  * Errors: HW_ERR_INVALID_ARG if the step appended some but not all layers; HW_ERR_CAPACITY
- * if the segment table is full.  Enqueues nothing on the GPU.
+ * if the segment table is full.  Enqueues on `stream` only the writes of appended tokens that
+ * no attention call of the step has written (see hw_append_kv); nothing otherwise.
  */
 hw_status hw_step_end(hw_ctx* ctx, const uint8_t* finished, void* stream);
 

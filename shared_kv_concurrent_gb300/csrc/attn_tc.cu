@@ -56,6 +56,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr int kChunkRing = 16;              // published tile ranges in flight (see TileWalker)
 
 template <int D>
 struct Cfg {
@@ -67,10 +68,12 @@ struct Cfg {
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kRingOff = 2 * kQBytes;
   static constexpr uint32_t kBarOff = kRingOff + kSlots * kTileBytes;
-  // barriers: full[S], empty[S], q_full[2], q_empty[2], s_full[2], p_full[2], o_done, fin
-  static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1;
+  // barriers: full[S], empty[S], q_full[2], q_empty[2], s_full[2], p_full[2], o_done, fin,
+  // fresh, chunk_full[kChunkRing], chunk_empty[kChunkRing]
+  static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 2 * kChunkRing;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t kChunkOff = kMiscOff + 16;         // int2[kChunkRing]
+  static constexpr uint32_t kSmemBytes = kChunkOff + 8 * kChunkRing + 1024;  // + alignment slack
 };
 
 // Timeline tracing, compiled in only with -DHW_TRACE (a separate debug build of the library):
@@ -102,55 +105,73 @@ struct TileInfo {
   int32_t seg_slot, page, slot0, nvalid, fresh;
 };
 
-// Walk the tiles of a unit in order; every role runs the same walk.
+// The CTA's sequence of tiles: its static first range of pieces, then the pieces it claims one
+// by one from its group's counter.  The producer publishes each range, {begin, end}, in a
+// shared-memory ring of kChunkRing entries (end < 0 closes the sequence); every other role
+// reads the ring through a TileWalker, so all of them see the same tiles in the same order.
+// A piece is one tile.
+
 struct TileWalker {
   const Piece* pieces;
-  int32_t pi, pe, k, ntiles_piece;
-  Piece pc;
-  int32_t num_pages, S, num_seg_slots;
-  int32_t last_slot;
+  const int2* ring;
+  uint32_t full_bars, empty_bars;             // kChunkRing mbarriers each
+  volatile int* abort;
+  uint32_t ci;                                // ring entries consumed
+  int32_t pi, pe;
+  int32_t num_pages, S, num_seg_slots, last_slot;
+  bool done;
   __device__ bool valid(const Piece& p) const {
-    return p.page >= 0 && p.page < num_pages && p.slot0 >= 0 && p.ntok >= 1 &&
+    return p.page >= 0 && p.page < num_pages && p.slot0 >= 0 && p.ntok >= 1 && p.ntok <= kTile &&
            p.slot0 + p.ntok <= S && (p.slot0 % kTile) == 0 && p.seg_slot >= 0 &&
            p.seg_slot < num_seg_slots;
   }
-  __device__ void init(const AttnArgs& a, const Unit& u) {
+  __device__ void init(const AttnArgs& a, const int2* ring_, uint32_t full_, uint32_t empty_,
+                       volatile int* abort_) {
     pieces = a.pieces;
-    pi = u.piece_begin - 1;
-    pe = u.piece_end;
-    k = 0;
-    ntiles_piece = 0;
+    ring = ring_;
+    full_bars = full_;
+    empty_bars = empty_;
+    abort = abort_;
+    ci = 0;
+    pi = pe = 0;
     num_pages = a.num_pages;
     S = a.S;
     num_seg_slots = a.num_seg_slots;
     last_slot = -1;
+    done = false;
   }
   // Next tile; new_seg is set when the tile starts a new segment (a new query rotation).
+  // False at the end of the sequence, or when a wait gave up (the abort flag is then set).
   __device__ bool next(TileInfo* t, bool* new_seg) {
-    while (k >= ntiles_piece) {
-      if (++pi >= pe) return false;
-      pc = pieces[pi];
-      k = 0;
-      ntiles_piece = valid(pc) ? (pc.ntok + kTile - 1) / kTile : 0;
+    Piece pc;
+    for (;;) {
+      while (pi >= pe) {
+        if (done) return false;
+        const uint32_t e = ci % kChunkRing;
+        if (!mbar_wait(full_bars + 8u * e, (ci / kChunkRing) & 1, abort, kWaitLimitNs)) {
+          done = true;
+          return false;
+        }
+        const int2 r = ring[e];
+        mbar_arrive(empty_bars + 8u * e);
+        ++ci;
+        if (r.y < 0) {
+          done = true;
+          return false;
+        }
+        pi = r.x;
+        pe = r.y;
+      }
+      pc = pieces[pi++];
+      if (valid(pc)) break;
     }
     t->seg_slot = pc.seg_slot;
     t->page = pc.page;
-    t->slot0 = pc.slot0 + k * kTile;
-    t->nvalid = min(kTile, pc.ntok - k * kTile);
+    t->slot0 = pc.slot0;
+    t->nvalid = pc.ntok;
     t->fresh = pc.fresh;
     *new_seg = pc.seg_slot != last_slot;
     last_slot = pc.seg_slot;
-    ++k;
-    return true;
-  }
-  // Whether the tile just returned is the last one of its segment in this unit.
-  __device__ bool last_of_segment() const {
-    if (k < ntiles_piece) return false;
-    for (int32_t j = pi + 1; j < pe; ++j) {
-      const Piece n = pieces[j];
-      if (!valid(n)) continue;
-      return n.seg_slot != pc.seg_slot;
-    }
     return true;
   }
 };
@@ -249,6 +270,58 @@ __device__ __forceinline__ void rotate_tile(const AttnArgs& a, const Group& g, i
   }
 }
 
+// Fused append (Hogwild! Inference summary, section 9: tokens of a block at block-local
+// positions): the unit's appended tokens [f0, f1) of the FreshTok table are written for its KV
+// head h -- key rotated to its position with the fp32 table and stored as bf16, value copied --
+// into the pool, exactly as the append kernel would.  64 threads; each takes 8 rotation pairs
+// (16-byte loads and stores) of one token.
+template <int D>
+__device__ __forceinline__ void append_fresh(const AttnArgs& a, const Group& g, int f0, int f1,
+                                             int tid) {
+  constexpr int half = D / 2;
+  constexpr int CH = half / 8;                 // 8-pair chunks per token
+  constexpr int TPP = kRotThreads / CH;        // tokens per pass
+  const int c = tid % CH;
+#pragma unroll 1
+  for (int f = f0 + tid / CH; f < f1; f += TPP) {
+    const FreshTok ft = a.fresh[f];
+    if (ft.page < 0 || ft.page >= a.num_pages || ft.slot < 0 || ft.slot >= a.S) {
+      if (c == 0) record_error(a.err, ERR_PAGE_RANGE, KID_ATTN_TC, blockIdx.x, ft.page);
+      continue;
+    }
+    if (ft.pos < 0 || ft.pos >= a.max_position || ft.src < 0) {
+      if (c == 0) record_error(a.err, ERR_POS_RANGE, KID_ATTN_TC, blockIdx.x, ft.pos);
+      continue;
+    }
+    const size_t src = ((size_t)ft.src * a.H_kv + g.h) * D + 8 * c;
+    const size_t dst = (((size_t)ft.page * a.H_kv + g.h) * a.S + ft.slot) * D + 8 * c;
+    const size_t tab = (size_t)ft.pos * half + 8 * c;
+    const uint4 k1 = *reinterpret_cast<const uint4*>(a.k_raw + src);
+    const uint4 k2 = *reinterpret_cast<const uint4*>(a.k_raw + src + half);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(a.v_raw + src);
+    const uint4 v2 = *reinterpret_cast<const uint4*>(a.v_raw + src + half);
+    const float4 ca = *reinterpret_cast<const float4*>(a.rope_cos + tab);
+    const float4 cb = *reinterpret_cast<const float4*>(a.rope_cos + tab + 4);
+    const float4 sa = *reinterpret_cast<const float4*>(a.rope_sin + tab);
+    const float4 sb = *reinterpret_cast<const float4*>(a.rope_sin + tab + 4);
+    const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+    const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+    const __nv_bfloat16* x1 = reinterpret_cast<const __nv_bfloat16*>(&k1);
+    const __nv_bfloat16* x2 = reinterpret_cast<const __nv_bfloat16*>(&k2);
+    __align__(16) __nv_bfloat16 y1[8], y2[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float u1 = __bfloat162float(x1[e]), u2 = __bfloat162float(x2[e]);
+      y1[e] = __float2bfloat16_rn(u1 * cv[e] - u2 * sv[e]);
+      y2[e] = __float2bfloat16_rn(u2 * cv[e] + u1 * sv[e]);
+    }
+    *reinterpret_cast<uint4*>(a.k_layer + dst) = *reinterpret_cast<const uint4*>(y1);
+    *reinterpret_cast<uint4*>(a.k_layer + dst + half) = *reinterpret_cast<const uint4*>(y2);
+    *reinterpret_cast<uint4*>(a.v_layer + dst) = v1;
+    *reinterpret_cast<uint4*>(a.v_layer + dst + half) = v2;
+  }
+}
+
 // ---------------------------------------------------------------------------- attention
 
 template <int D, int T>
@@ -274,6 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_pfull = [&](int b) { return bars + 8u * (2 * C::kSlots + 6 + b); };
   const uint32_t bar_odone = bars + 8u * (2 * C::kSlots + 8);
   const uint32_t bar_fin = bars + 8u * (2 * C::kSlots + 9);
+  const uint32_t bar_fresh = bars + 8u * (2 * C::kSlots + 10);   // fused append written
+  const uint32_t bar_cfull0 = bars + 8u * (2 * C::kSlots + 11);   // chunk ring: published
+  const uint32_t bar_cempty0 = bar_cfull0 + 8u * kChunkRing;      // chunk ring: read by all
+  int2* cring = reinterpret_cast<int2*>(smem + C::kChunkOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
@@ -299,6 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_odone, 1);
     mbar_init(bar_fin, 1);
+    mbar_init(bar_fresh, 1);
+    // every tile-walking thread reads each ring entry: MMA issuer, rotation warps, softmax
+    for (int e = 0; e < kChunkRing; ++e) {
+      mbar_init(bar_cfull0 + 8u * e, 1);
+      mbar_init(bar_cempty0 + 8u * e, 1 + kRotThreads + 32 * active_softmax_warps);
+    }
     *abort = 0;
     fence_mbar_init();
   }
@@ -322,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // built by warps 2-7 together: the softmax warps have nothing to do before the first S.  The
   // queries may come from the kernel this grid follows: wait for it first.
   const bool first_q = u.seg0 >= 0 && u.seg0 < a.num_seg_slots;
+  const bool fused = a.k_raw != nullptr;      // this kernel writes the step's appended tokens
   if (warp >= 2) {
     pdl_wait();
     if (first_q) {
@@ -339,40 +423,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t policy = l2_policy_evict_first();
-      TileWalker tw;
-      tw.init(a, u);
-      TileInfo t;
-      bool new_seg;
-      uint32_t j = 0;
+      uint32_t j = 0;          // K/V ring loads issued
+      uint32_t pub = 0;        // chunk-ring entries published
       bool ok = true;
-      // Tiles holding tokens of the current step come from the append kernel, which may still
-      // run (this grid is its programmatic dependent): wait for it before the first of them.
-      // Tiles of older tokens are streamed right away.
+      // Tiles holding tokens of the current step are written by this CTA's rotation warps
+      // (fused append) or by the append kernel, which may still run (this grid is its
+      // programmatic dependent): wait for those writes before the first such tile.  Tiles of
+      // older tokens are streamed right away.
       bool waited = false;
-      while (ok && tw.next(&t, &new_seg)) {
-        if (t.fresh && !waited) {
-          pdl_wait();
-          waited = true;
-          HW_TRACE_EV(248);
-        }
-        const int32_t y = (int32_t)(((page_base + t.page) * a.H_kv + g.h) * a.S + t.slot0);
-        for (int part = 0; part < 2 && ok; ++part, ++j) {
-          const int s = j % C::kSlots;
-          // The first K tile goes out alone with its V: every CTA fills its ring at once at
-          // start-up, and the first tile would otherwise arrive with the last of that burst.
-          if (j == 2) ok = mbar_wait(bar_full(0), 0, abort, kWaitLimitNs);
-          if (j >= (uint32_t)C::kSlots)
-            ok = ok && mbar_wait(bar_empty(s), ((j / C::kSlots) - 1) & 1, abort, kWaitLimitNs);
-          if (!ok) break;
-          if (part == 0) HW_TRACE_EV(8 + 4 * (j >> 1));
-          mbar_arrive_expect_tx(bar_full(s), C::kTileBytes);
-          const CUtensorMap* m = part == 0 ? &maps.k : &maps.v;
+      auto publish = [&](int32_t b, int32_t e) -> bool {
+        const uint32_t slot = pub % kChunkRing;
+        if (pub >= (uint32_t)kChunkRing &&
+            !mbar_wait(bar_cempty0 + 8u * slot, ((pub / kChunkRing) - 1) & 1, abort, kWaitLimitNs))
+          return false;
+        cring[slot] = make_int2(b, e);
+        mbar_arrive(bar_cfull0 + 8u * slot);          // release: the entry is visible to readers
+        ++pub;
+        return true;
+      };
+      auto load_range = [&](int32_t b, int32_t e) -> bool {
+        for (int32_t pi = b; pi < e; ++pi) {
+          const Piece pc = a.pieces[pi];
+          const bool valid = pc.page >= 0 && pc.page < a.num_pages && pc.slot0 >= 0 &&
+                             pc.ntok >= 1 && pc.ntok <= kTile && pc.slot0 + pc.ntok <= a.S &&
+                             (pc.slot0 % kTile) == 0 && pc.seg_slot >= 0 &&
+                             pc.seg_slot < a.num_seg_slots;
+          if (!valid) continue;                        // every role skips it the same way
+          if (pc.fresh && !waited) {
+            if (fused) {
+              if (!mbar_wait(bar_fresh, 0, abort, kWaitLimitNs)) return false;
+            } else {
+              pdl_wait();
+            }
+            waited = true;
+            HW_TRACE_EV(248);
+          }
+          const int32_t y = (int32_t)(((page_base + pc.page) * a.H_kv + g.h) * a.S + pc.slot0);
+          for (int part = 0; part < 2; ++part, ++j) {
+            const int s = j % C::kSlots;
+            // The first K tile goes out alone with its V: every CTA fills its ring at once at
+            // start-up, and the first tile would otherwise arrive with the last of that burst.
+            if (j == 2 && !mbar_wait(bar_full(0), 0, abort, kWaitLimitNs)) return false;
+            if (j >= (uint32_t)C::kSlots &&
+                !mbar_wait(bar_empty(s), ((j / C::kSlots) - 1) & 1, abort, kWaitLimitNs))
+              return false;
+            if (part == 0) HW_TRACE_EV(8 + 4 * (j >> 1));
+            mbar_arrive_expect_tx(bar_full(s), C::kTileBytes);
+            const CUtensorMap* m = part == 0 ? &maps.k : &maps.v;
 #pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_2d(ring + s * C::kTileBytes + h * C::kHalfBytes, m, 64 * h, y, bar_full(s),
-                        policy);
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_2d(ring + s * C::kTileBytes + h * C::kHalfBytes, m, 64 * h, y, bar_full(s),
+                          policy);
+          }
         }
+        return true;
+      };
+      // The static first range, then pieces claimed one by one from the group's counter (the
+      // next claim is issued before the current piece is loaded, hiding its latency).
+      const bool dyn = u.dyn_end > u.dyn_begin;
+      uint32_t* grab = a.tickets + u.group;
+      uint32_t claim = dyn ? atomicAdd(grab, 1u) : 0u;
+      if (u.piece_end > u.piece_begin) ok = publish(u.piece_begin, u.piece_end) && load_range(u.piece_begin, u.piece_end);
+      while (ok && dyn) {
+        const int64_t idx = (int64_t)u.dyn_begin + claim;
+        if (idx >= u.dyn_end) break;
+        claim = atomicAdd(grab, 1u);
+        ok = publish((int32_t)idx, (int32_t)idx + 1) && load_range((int32_t)idx, (int32_t)idx + 1);
       }
+      publish(0, -1);                                  // end of the sequence (also on abort)
       HW_TRACE_EV(3);
       // Drain: every copy issued must have landed before the CTA can exit.
       for (uint32_t s = 0; s < (uint32_t)C::kSlots && s < j; ++s) {
@@ -387,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc1 = idesc_bf16(kRowsM, kTile, 0, 0);
       constexpr uint32_t idesc2 = idesc_bf16(kRowsM, D, 0, 1);
       TileWalker tw;
-      tw.init(a, u);
+      tw.init(a, cring, bar_cfull0, bar_cempty0, abort);
       TileInfo t;
       bool new_seg;
       uint32_t i = 0, seg = 0;
@@ -414,6 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       while (ok && tw.next(&t, &new_seg)) {
         if (new_seg) {
+          // the previous segment's query buffer is free once every MMA issued so far is done
+          if (seg > 0) mma_commit(bar_qempty(qbuf));
           qbuf = seg & 1;
           ok = mbar_wait(bar_qfull(qbuf), (seg >> 1) & 1, abort, kWaitLimitNs);
           ++seg;
@@ -438,7 +558,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         HW_TRACE_EV(9 + 4 * i);
         mma_commit(bar_empty(s));
         mma_commit(bar_sfull(b));
-        if (tw.last_of_segment()) mma_commit(bar_qempty(qbuf));
         if (i > 0) ok = issue_mma2(i - 1);
         ++i;
       }
@@ -452,10 +571,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2 || warp == 3) {
     // ---------------------------------------------------------------- query rotation
-    // The query tiles of the unit's later segments, into the two query buffers in turn.
+    // Fused append first (the producer holds this unit's tiles of new tokens until it is
+    // written), then the query tiles of the unit's later segments, into the two query buffers
+    // in turn.
     const int tid = threadIdx.x - 64;
+    if (fused) {
+      append_fresh<D>(a, g, u.fresh_begin, u.fresh_end, tid);
+      fence_proxy_async_global();         // generic-proxy pool writes -> this CTA's TMA loads
+      asm volatile("bar.sync 4, %0;" ::"r"(kRotThreads) : "memory");
+      if (tid == 0) mbar_arrive(bar_fresh);
+    }
     TileWalker tw;
-    tw.init(a, u);
+    tw.init(a, cring, bar_cfull0, bar_cempty0, abort);
     TileInfo t;
     bool new_seg;
     uint32_t seg = 0;
@@ -500,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float m_run = -CUDART_INF_F, l_sum = 0.f;
       TileWalker tw;
-      tw.init(a, u);
+      tw.init(a, cring, bar_cfull0, bar_cempty0, abort);
       TileInfo t;
       bool new_seg;
       uint32_t i = 0;
@@ -656,6 +783,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && u.dyn_end > u.dyn_begin) {
+    // The last CTA of the group to finish (none claims after that) rewinds its counters for
+    // the next launch.
+    uint32_t* done = a.tickets + a.num_groups + u.group;
+    __threadfence();
+    if (atomicAdd(done, 1u) + 1u == (uint32_t)u.n_group) {
+      atomicExch(a.tickets + u.group, 0u);
+      atomicExch(done, 0u);
+    }
   }
   if (threadIdx.x == 0) HW_TRACE_EV(7);
 }

@@ -27,6 +27,9 @@ constexpr size_t kSlotBudget = 64u << 20;  // ... and at most this many bytes of
 constexpr size_t kAlign = 256;
 constexpr int kPieceMax = 128;         // tokens per piece = one kernel tile (never crosses a page)
 constexpr int kProfPairs = 4096;       // timed launches kept per hw_profile_read
+// A step whose blocks each append at most this many tokens has them written by the
+// tensor-core attention kernel itself (fused append); larger appends use the append kernel.
+constexpr int kFuseTok = 16;
 
 thread_local int g_cuda_err = 0;
 std::mutex g_msg_mu;
@@ -51,7 +54,7 @@ struct Layout {
   size_t err, cos, sin, slots, partials, tickets, total;
   size_t slot_bytes;
   int32_t max_segments, max_append, max_pieces, max_units, max_seg_slots, rows;
-  int32_t num_slots;
+  int32_t num_slots, max_fresh;
 };
 
 bool valid_config(const hw_config* c) {
@@ -85,12 +88,14 @@ Layout make_layout(const hw_config* c) {
   L.max_pieces = (int32_t)((int64_t)c->num_pages * ((c->page_size + kPieceMax - 1) / kPieceMax) + 1);
   L.max_units = (int32_t)(P * H + 2048);
   L.max_seg_slots = L.max_segments;
+  L.max_fresh = (int32_t)(P * (W + 1) * kFuseTok);
   const size_t runs = (size_t)P * (W + 1) + (size_t)L.max_append / 128 + 2;
   const size_t append_bytes = runs * sizeof(hw::AppendRun);
   const size_t attn_bytes = align_up((size_t)L.max_pieces * sizeof(hw::Piece), 16) +
                             align_up((size_t)L.max_units * sizeof(hw::Unit), 16) +
                             align_up((size_t)P * H * sizeof(hw::Group), 16) +
-                            align_up((size_t)L.max_seg_slots * W * sizeof(int32_t), 16);
+                            align_up((size_t)L.max_seg_slots * W * sizeof(int32_t), 16) +
+                            align_up((size_t)L.max_fresh * sizeof(hw::FreshTok), 16);
   // A slot holds a step's append runs followed by its attention plan (uploaded together).
   L.slot_bytes = align_up(append_bytes, kAlign) + align_up(attn_bytes, kAlign);
   // Staging slots let the host run that many calls ahead of the device.
@@ -108,15 +113,15 @@ Layout make_layout(const hw_config* c) {
   L.partials = off;
   off += align_up((size_t)L.max_units * L.rows * hw::part_stride(c->head_dim) * sizeof(float), kAlign);
   L.tickets = off;
-  off += align_up((size_t)P * H * sizeof(uint32_t), kAlign);
+  off += align_up((size_t)2 * P * H * sizeof(uint32_t), kAlign);
   L.total = off;
   return L;
 }
 
 // Offsets of the arrays of an attention plan inside its buffer, and their sizes.
 struct PlanOffsets {
-  size_t pieces, units, groups, delta, bytes;
-  int32_t num_pieces, num_units, num_groups, num_seg_slots;
+  size_t pieces, units, groups, delta, fresh, bytes;
+  int32_t num_pieces, num_units, num_groups, num_seg_slots, num_fresh;
 };
 
 // Reused host buffers of the plan builder (no allocation per call once they have grown).
@@ -124,7 +129,8 @@ struct PlanScratch {
   std::vector<hw::Piece> pieces;
   std::vector<hw::Unit> units;
   std::vector<hw::Group> groups;
-  std::vector<int32_t> delta, prob_piece_begin, refs, live_len, live_ref;
+  std::vector<hw::FreshTok> fresh;
+  std::vector<int32_t> delta, prob_piece_begin, refs, live_len, live_ref, piece_fresh0, src_base;
   std::vector<int64_t> prob_tokens;
 };
 
@@ -169,6 +175,11 @@ struct hw_ctx {
   bool step_plan_ok = false;
   PlanOffsets step_po{};
   PlanScratch ps;
+  // Fused append: when the step's plan lists its appended tokens (step_fused), hw_append_kv
+  // only records the layer's k_raw / v_raw here and the layer's tensor-core attention writes
+  // them; whatever else needs the pool first launches the append kernel (flush_append).
+  bool step_fused = false;
+  std::vector<const void*> pend_k, pend_v;
   // measurement
   bool prof_on = false;
   int64_t n_launch = 0, n_attn = 0, n_append = 0;
@@ -224,6 +235,43 @@ struct hw_ctx {
       if (u != w) add(live[p][u]);
     add(live[p][w]);
     return off - 1;
+  }
+  // Launch the append kernel of `layer` for the step's runs (uploaded with the step's plan).
+  hw_status launch_append(int32_t layer, const void* k_raw, const void* v_raw, cudaStream_t s) {
+    const int slot = step_slot;
+    hw::AppendArgs a{};
+    a.runs = reinterpret_cast<const hw::AppendRun*>(d_slot(slot));
+    a.num_runs = step_runs;
+    a.max_run = step_max_run;
+    a.k_raw = (const __nv_bfloat16*)k_raw;
+    a.v_raw = (const __nv_bfloat16*)v_raw;
+    a.k_layer = k_pool + (size_t)layer * layer_elems;
+    a.v_layer = v_pool + (size_t)layer * layer_elems;
+    a.rope_cos = d_cos();
+    a.rope_sin = d_sin();
+    a.err = d_err();
+    a.H_kv = cfg.num_kv_heads;
+    a.D = cfg.head_dim;
+    a.S = cfg.page_size;
+    a.num_pages = cfg.num_pages;
+    a.max_position = cfg.max_position;
+    const int pi = prof_begin(s, 1);
+    hw::launch_append(a, s);
+    prof_end(pi, s);
+    HW_CUDA(cudaGetLastError());
+    n_launch += (step_runs + 65534) / 65535;
+    n_append += 1;
+    HW_CUDA(cudaEventRecord(slot_ev[slot], s));
+    slot_used[slot] = true;
+    return HW_OK;
+  }
+  // Write a recorded (fused) append of `layer` with the append kernel, if one is pending.
+  hw_status flush_append(int32_t layer, cudaStream_t s) {
+    if (layer < 0 || layer >= (int32_t)pend_k.size() || !pend_k[layer]) return HW_OK;
+    const void* k = pend_k[layer];
+    const void* v = pend_v[layer];
+    pend_k[layer] = pend_v[layer] = nullptr;
+    return launch_append(layer, k, v, s);
   }
   // Copy `bytes` of staging slot `slot` to its device copy on the copy stream and make the
   // compute stream `s` wait for it.  The slot's previous readers have completed (acquire_slot).
@@ -397,7 +445,7 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
 
 namespace {
 bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap,
-                          int64_t target_override);
+                          int64_t target_override, bool fuse, bool dynamic);
 }  // namespace
 
 extern "C" {
@@ -413,6 +461,7 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
     total += n_new[i];
   }
   if (total > 0 && (!k_raw || !v_raw)) return HW_ERR_INVALID_ARG;
+  if (total > 0 && (((uintptr_t)k_raw | (uintptr_t)v_raw) % 16)) return HW_ERR_INVALID_ARG;
   if (total > c->lay.max_append) return HW_ERR_CAPACITY;
   if (!c->step_active) {
     // First append of the step: check, then allocate pages (all-or-nothing).
@@ -462,6 +511,8 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
     ++c->epoch;                            // tables changed: any uploaded plan is stale
     c->step_n.assign(n_new, n_new + P * B);
     c->appended.assign(c->cfg.num_layers, 0);
+    c->pend_k.assign(c->cfg.num_layers, nullptr);
+    c->pend_v.assign(c->cfg.num_layers, nullptr);
   } else {
     if (!std::equal(c->step_n.begin(), c->step_n.end(), n_new)) return HW_ERR_INVALID_ARG;
     if (c->appended[layer]) return HW_ERR_INVALID_ARG;
@@ -500,10 +551,21 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
       }
     const size_t plan_off = align_up((size_t)nr * sizeof(hw::AppendRun), kAlign);
     PlanOffsets po{};
-    const bool plan_ok =
+    // Small appends (decode) are written by the tensor-core attention kernel itself.
+    bool fuse = c->use_tc;
+    for (int32_t i = 0; i < P * B && fuse; ++i) fuse = n_new[i] <= kFuseTok;
+    bool plan_ok =
         plan_off < c->lay.slot_bytes &&
-        build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->use_tc ? c->num_sms : 0) &&
+        build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->use_tc ? c->num_sms : 0,
+                             fuse, false) &&
         plan_off + po.bytes <= c->lay.slot_bytes;
+    if (!plan_ok && fuse) {
+      fuse = false;
+      plan_ok = plan_off < c->lay.slot_bytes &&
+                build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0,
+                                     c->use_tc ? c->num_sms : 0, false, false) &&
+                plan_off + po.bytes <= c->lay.slot_bytes;
+    }
     st = c->upload_slot(slot, plan_off + (plan_ok ? po.bytes : 0), s);
     if (st != HW_OK) return st;
     c->step_slot = slot;
@@ -511,38 +573,22 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
     c->step_max_run = max_run;
     c->step_plan_off = plan_off;
     c->step_plan_ok = plan_ok;
+    c->step_fused = plan_ok && fuse;
     c->step_po = po;
     c->step_epoch = c->epoch;
   }
-  const int slot = c->step_slot;
-  const int32_t nr = c->step_runs;
-  hw::AppendArgs a{};
-  a.runs = reinterpret_cast<const hw::AppendRun*>(c->d_slot(slot));
-  a.num_runs = nr;
-  a.max_run = c->step_max_run;
-  a.k_raw = (const __nv_bfloat16*)k_raw;
-  a.v_raw = (const __nv_bfloat16*)v_raw;
-  a.k_layer = c->k_pool + (size_t)layer * c->layer_elems;
-  a.v_layer = c->v_pool + (size_t)layer * c->layer_elems;
-  a.rope_cos = c->d_cos();
-  a.rope_sin = c->d_sin();
-  a.err = c->d_err();
-  a.H_kv = c->cfg.num_kv_heads;
-  a.D = c->cfg.head_dim;
-  a.S = S;
-  a.num_pages = c->cfg.num_pages;
-  a.max_position = c->cfg.max_position;
-  const int pi = c->prof_begin(s, 1);
-  hw::launch_append(a, s);
-  c->prof_end(pi, s);
-  HW_CUDA(cudaGetLastError());
-  c->n_launch += (nr + 65534) / 65535;
-  c->n_append += 1;
-  HW_CUDA(cudaEventRecord(c->slot_ev[slot], s));
-  c->slot_used[slot] = true;
+  if (c->step_fused) {
+    c->pend_k[layer] = k_raw;
+    c->pend_v[layer] = v_raw;
+    c->appended[layer] = 1;
+    return HW_OK;
+  }
+  const hw_status st = c->launch_append(layer, k_raw, v_raw, s);
+  if (st != HW_OK) return st;
   c->appended[layer] = 1;
   return HW_OK;
 }
+
 
 }  // extern "C"
 
@@ -558,7 +604,7 @@ namespace {
 // segment's offset in w's view.
 // unit_cap > 0 bounds the number of units (one partial result each); 0 = the default split.
 bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0,
-                          int64_t target_override = 0) {
+                          int64_t target_override = 0, bool fuse = false, bool dynamic = false) {
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
   const int32_t S = c->cfg.page_size;
   const Layout& L = c->lay;
@@ -567,6 +613,22 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   ps.delta.clear();
   ps.units.clear();
   ps.groups.clear();
+  ps.fresh.clear();
+  ps.piece_fresh0.clear();
+  // fuse: list the step's appended tokens (k_raw rows in append order: problems, then block 0 =
+  // common, 1 + w = worker w, each in position order) for the attention kernel to write.
+  if (fuse) {
+    if (!c->step_active || c->step_n.size() != (size_t)P * (W + 1)) return false;
+    ps.src_base.assign(c->segs.size(), -1);
+    int32_t run = 0;
+    for (int32_t p = 0; p < P; ++p)
+      for (int32_t b = 0; b <= W; ++b) {
+        const int32_t n = c->step_n[(size_t)p * (W + 1) + b];
+        const int32_t sid = b == 0 ? c->common[p].back() : c->live[p][b - 1];
+        if (n > 0) ps.src_base[sid] = run;
+        run += n;
+      }
+  }
   ps.prob_piece_begin.assign(P + 1, 0);
   ps.prob_tokens.assign(P, 0);
   const int32_t step = std::min(kPieceMax, S);
@@ -633,7 +695,16 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         // fresh: holds tokens appended in this step (the kernels read it only after the append)
         const int32_t fresh = (sg.pending > 0 && j + cnt > sg.length) ? 1 : 0;
         if ((int64_t)ps.pieces.size() >= L.max_pieces) return false;
+        ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
         ps.pieces.push_back(hw::Piece{slot_base + (int32_t)r, pg, slot0, cnt, fresh});
+        if (fuse && fresh) {
+          const int32_t sid = ps.refs[r];
+          if (ps.src_base[sid] < 0) return false;
+          for (int32_t t = std::max<int32_t>(0, sg.length - j); t < cnt; ++t) {
+            if ((int64_t)ps.fresh.size() >= L.max_fresh) return false;
+            ps.fresh.push_back(hw::FreshTok{pg, slot0 + t, j + t, ps.src_base[sid] + (j + t - sg.length)});
+          }
+        }
         // Balance by 128-token tiles: a partial tile costs the kernels a full one.
         tok += (cnt + 127) / 128 * 128;
       }
@@ -641,6 +712,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     ps.prob_tokens[p] = tok;
   }
   ps.prob_piece_begin[P] = (int32_t)ps.pieces.size();
+  ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
   // Units: split every group into KV-entry-balanced runs of pieces (summary section 9: the
   // kernel balances by KV entries, not by blocks, then reduces the partial results).
   int64_t total_tok = 0;
@@ -660,7 +732,18 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     int64_t n_units = total_tok ? (target_units * T + (unit_cap > 0 ? 0 : total_tok / 2)) / total_tok : 1;
     n_units = std::max<int64_t>(1, std::min<int64_t>(n_units, pe - pb));
     if (pe == pb) {
-      ps.units.push_back(hw::Unit{pb, pb, g, -1, -1, {0, 0, 0}});
+      ps.units.push_back(hw::Unit{pb, pb, g, -1, -1, 0, 0, 0, 0, 1, {0, 0}});
+    } else if (dynamic) {
+      // Static first ranges of cs pieces, one per CTA, then the rest claimed dynamically; each
+      // CTA writes all of the problem's appended tokens for its head (identical bytes).
+      const int32_t n = (int32_t)n_units;
+      const int32_t cs = (int32_t)std::max<int64_t>(1, std::min<int64_t>(2, (pe - pb) / n_units));
+      const int32_t f0 = ps.piece_fresh0[pb], f1 = ps.piece_fresh0[pe];
+      for (int32_t k = 0; k < n; ++k) {
+        const int32_t b0 = pb + k * cs, e0 = std::min(pe, b0 + cs);
+        ps.units.push_back(hw::Unit{b0, e0, g, ps.pieces[b0].seg_slot, -1, f0, f1,
+                                    std::min(pe, pb + n * cs), pe, n, {0, 0}});
+      }
     } else {
       int64_t cum = 0;
       int32_t cur = -1;
@@ -669,7 +752,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         const int64_t mid2 = 2 * cum + wt;                         // twice the piece midpoint
         const int32_t k = (int32_t)std::min<int64_t>(n_units - 1, (mid2 * n_units) / (2 * T));
         if (k != cur) {
-          ps.units.push_back(hw::Unit{i, i + 1, g, ps.pieces[i].seg_slot, -1, {0, 0, 0}});
+          ps.units.push_back(hw::Unit{i, i + 1, g, ps.pieces[i].seg_slot, -1, 0, 0, 0, 0, 0, {0, 0}});
           cur = k;
         } else {
           ps.units.back().piece_end = i + 1;
@@ -678,6 +761,13 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
       }
     }
     gr.unit_end = (int32_t)ps.units.size();
+    if (!dynamic)
+      for (int32_t k = gr.unit_begin; k < gr.unit_end; ++k) {
+        hw::Unit& u = ps.units[k];
+        u.fresh_begin = ps.piece_fresh0[u.piece_begin];
+        u.fresh_end = ps.piece_fresh0[u.piece_end];
+        u.n_group = gr.unit_end - gr.unit_begin;
+      }
     ps.groups.push_back(gr);
   }
   if ((int64_t)ps.units.size() > L.max_units) return false;
@@ -700,16 +790,21 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   off = align_up(off + ps.groups.size() * sizeof(hw::Group), 16);
   po->delta = off;
   off = align_up(off + ps.delta.size() * sizeof(int32_t), 16);
+  po->fresh = off;
+  off = align_up(off + ps.fresh.size() * sizeof(hw::FreshTok), 16);
   po->bytes = off;
   if (off > L.slot_bytes) return false;
   std::memcpy(buf + po->pieces, ps.pieces.data(), ps.pieces.size() * sizeof(hw::Piece));
   std::memcpy(buf + po->units, ps.units.data(), ps.units.size() * sizeof(hw::Unit));
   std::memcpy(buf + po->groups, ps.groups.data(), ps.groups.size() * sizeof(hw::Group));
   std::memcpy(buf + po->delta, ps.delta.data(), ps.delta.size() * sizeof(int32_t));
+  if (!ps.fresh.empty())
+    std::memcpy(buf + po->fresh, ps.fresh.data(), ps.fresh.size() * sizeof(hw::FreshTok));
   po->num_pieces = (int32_t)ps.pieces.size();
   po->num_units = (int32_t)ps.units.size();
   po->num_groups = (int32_t)ps.groups.size();
   po->num_seg_slots = (int32_t)(ps.delta.size() / (size_t)W);
+  po->num_fresh = (int32_t)ps.fresh.size();
   return true;
 }
 
@@ -727,7 +822,16 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   int slot = 0;
   PlanOffsets po{};
   char* dbase = nullptr;
-  if (c->step_slot >= 0 && c->step_epoch == c->epoch && c->step_plan_ok) {
+  const bool step_plan = c->step_slot >= 0 && c->step_epoch == c->epoch && c->step_plan_ok;
+  // The layer's recorded append is written by the tensor-core kernel when the step's plan lists
+  // the appended tokens; otherwise by the append kernel, now.
+  const bool fused = c->use_tc && step_plan && c->step_fused && layer < (int32_t)c->pend_k.size() &&
+                     c->pend_k[layer] != nullptr;
+  if (!fused) {
+    const hw_status st = c->flush_append(layer, s);
+    if (st != HW_OK) return st;
+  }
+  if (step_plan) {
     // The plan of this step went up with its first append.
     slot = c->step_slot;
     po = c->step_po;
@@ -737,7 +841,8 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
     if (st != HW_OK) return st;
     // Tensor-core kernel: one CTA per SM holds all of its shared memory and TMEM, so one unit
     // per SM, balanced by KV entries.
-    if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0))
+    if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0, false,
+                              false))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
     st = c->upload_slot(slot, po.bytes, s);
@@ -748,6 +853,9 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   a.units = reinterpret_cast<const hw::Unit*>(dbase + po.units);
   a.groups = reinterpret_cast<const hw::Group*>(dbase + po.groups);
   a.delta = reinterpret_cast<const int32_t*>(dbase + po.delta);
+  a.fresh = reinterpret_cast<const hw::FreshTok*>(dbase + po.fresh);
+  a.k_raw = fused ? (const __nv_bfloat16*)c->pend_k[layer] : nullptr;
+  a.v_raw = fused ? (const __nv_bfloat16*)c->pend_v[layer] : nullptr;
   a.num_units = po.num_units;
   a.num_groups = po.num_groups;
   a.num_seg_slots = po.num_seg_slots;
@@ -758,6 +866,7 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   a.out_f32 = out_dtype == HW_OUT_F32;
   a.lse = lse;
   a.partials = c->d_partials();
+  a.tickets = reinterpret_cast<uint32_t*>(c->ws + c->lay.tickets);
   a.rope_cos = c->d_cos();
   a.rope_sin = c->d_sin();
   a.err = c->d_err();
@@ -785,6 +894,7 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
     if (e1) cudaEventRecord(e1, s);
   }
   HW_CUDA(cudaGetLastError());
+  if (fused) c->pend_k[layer] = c->pend_v[layer] = nullptr;
   hw::launch_merge(a, s, c->use_tc);
   HW_CUDA(cudaGetLastError());
   c->n_launch += 2;
@@ -812,6 +922,10 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
   if (plan_region >= scratch_bytes) return HW_ERR_CAPACITY;
   const int64_t unit_cap = (int64_t)((scratch_bytes - plan_region) / per_unit);
   if (unit_cap < (int64_t)c->cfg.num_problems * c->cfg.num_kv_heads) return HW_ERR_CAPACITY;
+  {
+    const hw_status st = c->flush_append(layer, (cudaStream_t)stream);
+    if (st != HW_OK) return st;
+  }
   int slot = 0;
   hw_status st = c->acquire_slot(&slot);
   if (st != HW_OK) return st;
@@ -825,6 +939,7 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
   a.units = reinterpret_cast<const hw::Unit*>(scratch + po.units);
   a.groups = reinterpret_cast<const hw::Group*>(scratch + po.groups);
   a.delta = reinterpret_cast<const int32_t*>(scratch + po.delta);
+  a.fresh = reinterpret_cast<const hw::FreshTok*>(scratch + po.fresh);
   a.num_units = po.num_units;
   a.num_groups = po.num_groups;
   a.num_seg_slots = po.num_seg_slots;
@@ -863,7 +978,6 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
 extern "C" {
 
 hw_status hw_step_end(hw_ctx* c, const uint8_t* finished, void* stream) {
-  (void)stream;
   if (!c) return HW_ERR_INVALID_ARG;
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers;
   if (c->step_active)
@@ -875,6 +989,13 @@ hw_status hw_step_end(hw_ctx* c, const uint8_t* finished, void* stream) {
       for (int32_t w = 0; w < W; ++w)
         if (finished[p * W + w] && c->segs[c->live[p][w]].visible() > 0) ++commits;
   if ((int64_t)c->segs.size() + commits > c->lay.max_segments) return HW_ERR_CAPACITY;
+  // Appends no attention call has written yet go to the pool now.
+  for (int32_t l = 0; l < (int32_t)c->pend_k.size(); ++l) {
+    const hw_status st = c->flush_append(l, (cudaStream_t)stream);
+    if (st != HW_OK) return st;
+  }
+  c->pend_k.clear();
+  c->pend_v.clear();
   for (Seg& sg : c->segs) {
     sg.length += sg.pending;
     sg.pending = 0;

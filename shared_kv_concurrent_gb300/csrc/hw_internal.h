@@ -44,17 +44,32 @@ struct Piece {
   int32_t fresh;     // 1 if the piece holds tokens appended in the current step
 };
 
+// A token appended in the current step whose K/V the tensor-core attention kernel writes
+// itself (fused append): pool (page, slot), block-local position, row of k_raw / v_raw.
+struct FreshTok {
+  int32_t page;
+  int32_t slot;
+  int32_t pos;
+  int32_t src;
+};
+
 // Row stride (floats) of a partial result: o[D], m, l, 2 pad -- 16-byte aligned rows.
 __host__ __device__ constexpr int part_stride(int D) { return D + 4; }
 
 // A unit: consecutive pieces of one (problem, KV head) group, one CTA, one partial result.
+// The tensor-core kernel gives each CTA a static first range and lets the CTAs of a group claim
+// the pieces [dyn_begin, dyn_end) one by one from a counter (the partial result then covers
+// whatever the CTA processed); the CUDA-core kernel uses the static range only.
 struct Unit {
   int32_t piece_begin;
   int32_t piece_end;
   int32_t group;     // p * H_kv + h
   int32_t seg0;      // seg_slot of the first piece, -1 if the unit has none
   int32_t delta0;    // the rotation of seg0 if it is the same for every worker, else -1
-  int32_t pad[3];
+  int32_t fresh_begin, fresh_end;  // appended tokens it writes, in the FreshTok table
+  int32_t dyn_begin, dyn_end;      // pieces claimed dynamically by the group's CTAs
+  int32_t n_group;                 // CTAs (units) of the group
+  int32_t pad[2];
 };
 
 // A group: one (problem, KV head); its units are [unit_begin, unit_end).
@@ -84,14 +99,19 @@ struct AttnArgs {
   const Unit* units;
   const Group* groups;
   const int32_t* delta;       // [seg_slots][W]: i_q(w) - view offset, or -1 (not visible)
+  const FreshTok* fresh;      // appended tokens, per problem in piece order (fused append)
+  const __nv_bfloat16* k_raw; // fused append: this layer's new keys / values [n][H_kv][D],
+  const __nv_bfloat16* v_raw; //   or null when the append kernel has written them already
   int32_t num_units, num_groups, num_seg_slots;
-  const __nv_bfloat16* k_layer;
-  const __nv_bfloat16* v_layer;
+  __nv_bfloat16* k_layer;     // pool base of this layer: [num_pages][H_kv][S][D]
+  __nv_bfloat16* v_layer;
   const __nv_bfloat16* q;     // [P][W][H_q][D]
   void* out;                  // [P][W][H_q][D] bf16 or fp32
   int32_t out_f32;
   float* lse;                 // [P][W][H_q] or null
   float* partials;            // [units][rows][part_stride(D)]: o[D], m, l (log2 domain), pad
+  uint32_t* tickets;          // [2][groups]: claim counters, finished-CTA counters (zero between
+                              //   launches; the last CTA of a group rewinds them)
   const float* rope_cos;
   const float* rope_sin;
   uint32_t* err;

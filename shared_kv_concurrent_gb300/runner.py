@@ -29,6 +29,7 @@ class WorkloadRunner:
         self.device = device
         self.cache = HogwildCache.from_workload(w, max_segments=max_segments, device=device)
         n = wl.prefill_block_lengths(w)
+        keep = []          # k/v stay alive until the step end has written them (hw_append_kv)
         for layer in range(w.num_layers):
             k, v = wl.prefill_kv(w, layer)
             if k.shape[0] == 0:
@@ -36,8 +37,9 @@ class WorkloadRunner:
                 continue
             kd, vd = to_device_bf16(k, device), to_device_bf16(v, device)
             self.cache.append_kv(layer, n, kd, vd)
-            del kd, vd
+            keep.append((kd, vd))
         self.cache.step_end(np.zeros((w.num_problems, w.num_workers), np.uint8))
+        del keep
         self.n_step = np.ascontiguousarray(wl.step_n_new(w), dtype=np.int32)
 
     def step_inputs(self, step: int):

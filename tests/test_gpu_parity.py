@@ -173,3 +173,51 @@ def test_deterministic_bitwise():
     torch.cuda.synchronize()
     assert torch.equal(o1[0].view(torch.int32), o2[0].view(torch.int32))
     r.cache.close()
+
+
+def test_multi_token_appends_fused_and_deferred():
+    """Tensor-core context (64 query rows): a step appending 17 tokens per worker (append
+    kernel), one appending 16 (written inside the attention kernel), one whose appends no
+    attention call writes (the step end writes them), then a decode step -- each attended step
+    against the oracle, with pools and tables."""
+    import torch
+    import gpu_cases as G
+    from oracle import attention as A
+    from oracle import run as orun
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner, to_device_bf16
+    w = G.small(wl.c4(), common_len=(700,), worker_len=((0, 5, 127, 128, 129, 40, 300, 1),),
+                random_page_order=True, steps=40)     # page budget for the 36 extra tokens
+    r = WorkloadRunner(w)
+    c = orun.prefill(w)
+    P, W, Hq, Hkv, D = w.num_problems, w.num_workers, w.num_q_heads, w.num_kv_heads, w.head_dim
+    rng = np.random.default_rng(7)
+
+    def bits(*shape):
+        return wl.f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32))
+
+    for per_worker, common, attend in ((17, 3, True), (16, 0, True), (2, 1, False), (1, 0, True)):
+        n = np.zeros((P, W + 1), np.int32)
+        n[:, 0] = common
+        n[:, 1:] = per_worker
+        tot = int(n.sum())
+        kb, vb, qb = bits(tot, Hkv, D), bits(tot, Hkv, D), bits(P, W, Hq, D)
+        kd, vd, qd = to_device_bf16(kb), to_device_bf16(vb), to_device_bf16(qb)
+        r.cache.append_kv(0, n, kd, vd)
+        c.append(0, n, orun.bf16(kb), orun.bf16(vb))
+        if attend:
+            out = torch.full((P, W, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+            r.cache.concurrent_attention(0, qd, out, "f32")
+            torch.cuda.synchronize()
+            ref, _ = A.method(c, 0, orun.bf16(qb).astype(np.float64))
+            err = float(np.abs(out.cpu().numpy() - ref).max())
+            assert err <= G.TOL, (per_worker, err)
+        fin = np.zeros((P, W), np.uint8)
+        r.cache.step_end(fin)
+        c.step_end(fin)
+        torch.cuda.synchronize()
+        G.check_pools(r, c, 0)
+        G.dev_tables_equal(r, c)
+    from shared_kv_concurrent_gb300 import binding
+    st, info = r.cache.check_device_errors()
+    assert st == binding.HW_OK, info
+    r.cache.close()
