@@ -105,8 +105,7 @@ struct TileInfo {
   int32_t seg_slot, page, slot0, nvalid, fresh;
 };
 
-// The CTA's sequence of tiles: its static first range of pieces, then the pieces it claims one
-// by one from its group's counter.  The producer publishes each range, {begin, end}, in a
+// The CTA's sequence of tiles: the producer publishes ranges of pieces, {begin, end}, in a
 // shared-memory ring of kChunkRing entries (end < 0 closes the sequence); every other role
 // reads the ring through a TileWalker, so all of them see the same tiles in the same order.
 // A piece is one tile.
@@ -478,18 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      // The static first range, then pieces claimed one by one from the group's counter (the
-      // next claim is issued before the current piece is loaded, hiding its latency).
-      const bool dyn = u.dyn_end > u.dyn_begin;
-      uint32_t* grab = a.tickets + u.group;
-      uint32_t claim = dyn ? atomicAdd(grab, 1u) : 0u;
-      if (u.piece_end > u.piece_begin) ok = publish(u.piece_begin, u.piece_end) && load_range(u.piece_begin, u.piece_end);
-      while (ok && dyn) {
-        const int64_t idx = (int64_t)u.dyn_begin + claim;
-        if (idx >= u.dyn_end) break;
-        claim = atomicAdd(grab, 1u);
-        ok = publish((int32_t)idx, (int32_t)idx + 1) && load_range((int32_t)idx, (int32_t)idx + 1);
-      }
+      // The unit's pieces in plan order, then the end of the sequence.
+      if (u.piece_end > u.piece_begin)
+        ok = publish(u.piece_begin, u.piece_end) && load_range(u.piece_begin, u.piece_end);
       publish(0, -1);                                  // end of the sequence (also on abort)
       HW_TRACE_EV(3);
       // Drain: every copy issued must have landed before the CTA can exit.
@@ -601,9 +591,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       rotate_tile<D, T, kRotThreads>(a, g, t.seg_slot, -1, smem + C::kQOff + qb * C::kQBytes, tid);
       fence_proxy_async_smem();           // generic-proxy writes -> operands of the MMA
       asm volatile("bar.sync 4, %0;" ::"r"(kRotThreads) : "memory");
-      if (tid == 0) mbar_arrive(bar_qfull(qb));
+      if (tid == 0) {
+        mbar_arrive(bar_qfull(qb));
+        HW_TRACE_EV(249);
+      }
       ++seg;
     }
+#ifdef HW_TRACE
+    if (tid == 0 && blockIdx.x < kTraceCtas) g_trace[blockIdx.x][254] = seg;
+#endif
     if (!ok && (*abort) && tid == 0) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 3);
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax / epilogue
@@ -783,16 +779,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
-  }
-  if (threadIdx.x == 0 && u.dyn_end > u.dyn_begin) {
-    // The last CTA of the group to finish (none claims after that) rewinds its counters for
-    // the next launch.
-    uint32_t* done = a.tickets + a.num_groups + u.group;
-    __threadfence();
-    if (atomicAdd(done, 1u) + 1u == (uint32_t)u.n_group) {
-      atomicExch(a.tickets + u.group, 0u);
-      atomicExch(done, 0u);
-    }
   }
   if (threadIdx.x == 0) HW_TRACE_EV(7);
 }

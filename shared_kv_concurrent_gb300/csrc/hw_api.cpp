@@ -16,6 +16,7 @@
 #include <mutex>
 #include <new>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "hw_internal.h"
@@ -113,7 +114,7 @@ Layout make_layout(const hw_config* c) {
   L.partials = off;
   off += align_up((size_t)L.max_units * L.rows * hw::part_stride(c->head_dim) * sizeof(float), kAlign);
   L.tickets = off;
-  off += align_up((size_t)2 * P * H * sizeof(uint32_t), kAlign);
+  off += align_up((size_t)P * H * sizeof(uint32_t), kAlign);
   L.total = off;
   return L;
 }
@@ -126,12 +127,19 @@ struct PlanOffsets {
 
 // Reused host buffers of the plan builder (no allocation per call once they have grown).
 struct PlanScratch {
+  struct Part {
+    int32_t unit, ref, t0, t1;        // tiles [t0, t1) of segment reference `ref` go to `unit`
+  };
   std::vector<hw::Piece> pieces;
   std::vector<hw::Unit> units;
   std::vector<hw::Group> groups;
   std::vector<hw::FreshTok> fresh;
-  std::vector<int32_t> delta, prob_piece_begin, refs, live_len, live_ref, piece_fresh0, src_base;
-  std::vector<int64_t> prob_tokens;
+  std::vector<int32_t> delta, refs, live_len, live_ref, piece_fresh0, src_base;
+  std::vector<int32_t> ref_sid, ref_slot, ref_tiles, prob_ref_begin, prob_common_refs, unit_rem,
+      order;
+  std::vector<int64_t> prob_tiles;
+  std::vector<Part> parts;
+  std::vector<std::pair<int32_t, int32_t>> unit_range;
 };
 
 struct Seg {
@@ -445,7 +453,7 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
 
 namespace {
 bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap,
-                          int64_t target_override, bool fuse, bool dynamic);
+                          int64_t target_override, bool fuse);
 }  // namespace
 
 extern "C" {
@@ -557,13 +565,13 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
     bool plan_ok =
         plan_off < c->lay.slot_bytes &&
         build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->use_tc ? c->num_sms : 0,
-                             fuse, false) &&
+                             fuse) &&
         plan_off + po.bytes <= c->lay.slot_bytes;
     if (!plan_ok && fuse) {
       fuse = false;
       plan_ok = plan_off < c->lay.slot_bytes &&
                 build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0,
-                                     c->use_tc ? c->num_sms : 0, false, false) &&
+                                     c->use_tc ? c->num_sms : 0, false) &&
                 plan_off + po.bytes <= c->lay.slot_bytes;
     }
     st = c->upload_slot(slot, plan_off + (plan_ok ? po.bytes : 0), s);
@@ -604,7 +612,7 @@ namespace {
 // segment's offset in w's view.
 // unit_cap > 0 bounds the number of units (one partial result each); 0 = the default split.
 bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0,
-                          int64_t target_override = 0, bool fuse = false, bool dynamic = false) {
+                          int64_t target_override = 0, bool fuse = false) {
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
   const int32_t S = c->cfg.page_size;
   const Layout& L = c->lay;
@@ -615,6 +623,13 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   ps.groups.clear();
   ps.fresh.clear();
   ps.piece_fresh0.clear();
+  ps.ref_sid.clear();
+  ps.ref_slot.clear();
+  ps.ref_tiles.clear();
+  ps.prob_ref_begin.assign(P + 1, 0);
+  ps.prob_common_refs.assign(P, 0);
+  ps.prob_tiles.assign(P, 0);
+  ps.unit_range.clear();
   // fuse: list the step's appended tokens (k_raw rows in append order: problems, then block 0 =
   // common, 1 + w = worker w, each in position order) for the attention kernel to write.
   if (fuse) {
@@ -629,12 +644,10 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         run += n;
       }
   }
-  ps.prob_piece_begin.assign(P + 1, 0);
-  ps.prob_tokens.assign(P, 0);
-  const int32_t step = std::min(kPieceMax, S);
+  // Pass 1, per problem: the visible segments (common part in commit order, then the live
+  // blocks by worker), their rotation table and their tile counts.
   for (int32_t p = 0; p < P; ++p) {
-    ps.prob_piece_begin[p] = (int32_t)ps.pieces.size();
-    // Visible segments: the common part in commit order, then the live blocks by worker.
+    ps.prob_ref_begin[p] = (int32_t)ps.ref_sid.size();
     ps.refs.clear();
     int64_t common_len = 0;
     for (int32_t sid : c->common[p]) {
@@ -684,39 +697,23 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
       }
       before_u += ps.live_len[u];
     }
-    int64_t tok = 0;
+    int64_t tiles = 0;
     for (size_t r = 0; r < ps.refs.size(); ++r) {
-      const Seg& sg = c->segs[ps.refs[r]];
-      const int32_t n = sg.visible();
-      for (int32_t j = 0; j < n; j += step) {
-        const int32_t pg = c->cfg.contiguous ? sg.pages[0] : sg.pages[j / S];
-        const int32_t slot0 = c->cfg.contiguous ? j : j % S;
-        const int32_t cnt = std::min(std::min(kPieceMax, S - slot0), n - j);
-        // fresh: holds tokens appended in this step (the kernels read it only after the append)
-        const int32_t fresh = (sg.pending > 0 && j + cnt > sg.length) ? 1 : 0;
-        if ((int64_t)ps.pieces.size() >= L.max_pieces) return false;
-        ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
-        ps.pieces.push_back(hw::Piece{slot_base + (int32_t)r, pg, slot0, cnt, fresh});
-        if (fuse && fresh) {
-          const int32_t sid = ps.refs[r];
-          if (ps.src_base[sid] < 0) return false;
-          for (int32_t t = std::max<int32_t>(0, sg.length - j); t < cnt; ++t) {
-            if ((int64_t)ps.fresh.size() >= L.max_fresh) return false;
-            ps.fresh.push_back(hw::FreshTok{pg, slot0 + t, j + t, ps.src_base[sid] + (j + t - sg.length)});
-          }
-        }
-        // Balance by 128-token tiles: a partial tile costs the kernels a full one.
-        tok += (cnt + 127) / 128 * 128;
-      }
+      const int32_t nt = (c->segs[ps.refs[r]].visible() + kPieceMax - 1) / kPieceMax;
+      ps.ref_sid.push_back(ps.refs[r]);
+      ps.ref_slot.push_back(slot_base + (int32_t)r);
+      ps.ref_tiles.push_back(nt);
+      tiles += nt;
     }
-    ps.prob_tokens[p] = tok;
+    ps.prob_common_refs[p] = n_common_refs;
+    ps.prob_tiles[p] = tiles;
   }
-  ps.prob_piece_begin[P] = (int32_t)ps.pieces.size();
-  ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
-  // Units: split every group into KV-entry-balanced runs of pieces (summary section 9: the
-  // kernel balances by KV entries, not by blocks, then reduces the partial results).
-  int64_t total_tok = 0;
-  for (int64_t t : ps.prob_tokens) total_tok += t * H;
+  ps.prob_ref_begin[P] = (int32_t)ps.ref_sid.size();
+  // Units per problem: KV-entry balanced (summary section 9: the kernel balances by KV
+  // entries, not by blocks, then reduces the partial results); every 128-token tile costs the
+  // kernels the same, so the balance is in tiles.
+  int64_t total_tiles = 0;
+  for (int64_t t : ps.prob_tiles) total_tiles += t * H;
   int64_t target_units = std::max<int64_t>((int64_t)P * H,
                                            target_override > 0 ? target_override : 4ll * c->num_sms);
   if (unit_cap > 0) {
@@ -724,51 +721,112 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     // per-group counts are floored and then raised to >= 1: keep room for that raise
     target_units = std::max<int64_t>(0, std::min<int64_t>(target_units, unit_cap - (int64_t)P * H));
   }
-  for (int32_t g = 0; g < P * H; ++g) {
-    const int32_t p = g / H;
-    const int32_t pb = ps.prob_piece_begin[p], pe = ps.prob_piece_begin[p + 1];
-    const int64_t T = ps.prob_tokens[p];
-    hw::Group gr{p, g % H, (int32_t)ps.units.size(), 0};
-    int64_t n_units = total_tok ? (target_units * T + (unit_cap > 0 ? 0 : total_tok / 2)) / total_tok : 1;
-    n_units = std::max<int64_t>(1, std::min<int64_t>(n_units, pe - pb));
-    if (pe == pb) {
-      ps.units.push_back(hw::Unit{pb, pb, g, -1, -1, 0, 0, 0, 0, 1, {0, 0}});
-    } else if (dynamic) {
-      // Static first ranges of cs pieces, one per CTA, then the rest claimed dynamically; each
-      // CTA writes all of the problem's appended tokens for its head (identical bytes).
-      const int32_t n = (int32_t)n_units;
-      const int32_t cs = (int32_t)std::max<int64_t>(1, std::min<int64_t>(2, (pe - pb) / n_units));
-      const int32_t f0 = ps.piece_fresh0[pb], f1 = ps.piece_fresh0[pe];
-      for (int32_t k = 0; k < n; ++k) {
-        const int32_t b0 = pb + k * cs, e0 = std::min(pe, b0 + cs);
-        ps.units.push_back(hw::Unit{b0, e0, g, ps.pieces[b0].seg_slot, -1, f0, f1,
-                                    std::min(pe, pb + n * cs), pe, n, {0, 0}});
-      }
-    } else {
-      int64_t cum = 0;
-      int32_t cur = -1;
-      for (int32_t i = pb; i < pe; ++i) {
-        const int64_t wt = (ps.pieces[i].ntok + 127) / 128 * 128;  // tile-rounded weight
-        const int64_t mid2 = 2 * cum + wt;                         // twice the piece midpoint
-        const int32_t k = (int32_t)std::min<int64_t>(n_units - 1, (mid2 * n_units) / (2 * T));
-        if (k != cur) {
-          ps.units.push_back(hw::Unit{i, i + 1, g, ps.pieces[i].seg_slot, -1, 0, 0, 0, 0, 0, {0, 0}});
-          cur = k;
-        } else {
-          ps.units.back().piece_end = i + 1;
-        }
-        cum += wt;
+  // A piece of segment reference r at tile t (one tile of at most kPieceMax tokens, inside one
+  // page), with the step's appended tokens in it listed for the fused append.
+  auto emit = [&](int32_t r, int32_t t) -> bool {
+    const Seg& sg = c->segs[ps.ref_sid[r]];
+    const int32_t j = t * kPieceMax;
+    const int32_t pg = c->cfg.contiguous ? sg.pages[0] : sg.pages[j / S];
+    const int32_t slot0 = c->cfg.contiguous ? j : j % S;
+    const int32_t cnt = std::min(kPieceMax, sg.visible() - j);
+    // fresh: holds tokens appended in this step (the kernels read it only after the append)
+    const int32_t fresh = (sg.pending > 0 && j + cnt > sg.length) ? 1 : 0;
+    if ((int64_t)ps.pieces.size() >= L.max_pieces) return false;
+    ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
+    ps.pieces.push_back(hw::Piece{ps.ref_slot[r], pg, slot0, cnt, fresh});
+    if (fuse && fresh) {
+      const int32_t sid = ps.ref_sid[r];
+      if (ps.src_base[sid] < 0) return false;
+      for (int32_t k = std::max<int32_t>(0, sg.length - j); k < cnt; ++k) {
+        if ((int64_t)ps.fresh.size() >= L.max_fresh) return false;
+        ps.fresh.push_back(hw::FreshTok{pg, slot0 + k, j + k, ps.src_base[sid] + (j + k - sg.length)});
       }
     }
-    gr.unit_end = (int32_t)ps.units.size();
-    if (!dynamic)
-      for (int32_t k = gr.unit_begin; k < gr.unit_end; ++k) {
-        hw::Unit& u = ps.units[k];
-        u.fresh_begin = ps.piece_fresh0[u.piece_begin];
-        u.fresh_end = ps.piece_fresh0[u.piece_end];
-        u.n_group = gr.unit_end - gr.unit_begin;
+    return true;
+  };
+  for (int32_t p = 0; p < P; ++p) {
+    const int32_t rb = ps.prob_ref_begin[p], re = ps.prob_ref_begin[p + 1];
+    const int32_t rc = rb + ps.prob_common_refs[p];      // first live-block reference
+    const int64_t Tt = ps.prob_tiles[p];
+    int64_t n_units =
+        total_tiles ? (target_units * Tt * H + (unit_cap > 0 ? 0 : total_tiles / 2)) / (total_tiles * H)
+                    : 1;
+    n_units = std::max<int64_t>(1, std::min<int64_t>(n_units, Tt));
+    const int32_t n = (int32_t)n_units;
+    // Layout of the problem's units (the same for every KV head): unit k holds cap_k tiles;
+    // each live block (largest first) goes to the unit with the most room left, split over
+    // units only when it does not fit; the rest of every unit is filled with common-part tiles,
+    // which come first in the unit.  So a unit crosses at most a few segments, its first
+    // segment is usually common (one rotation for every worker), and a block's query tile is
+    // built while the unit's common tiles stream.
+    ps.unit_rem.assign(n, 0);
+    for (int32_t k = 0; k < n; ++k) ps.unit_rem[k] = (int32_t)(Tt / n + (k < Tt % n ? 1 : 0));
+    ps.parts.clear();                                    // (unit, ref, tile begin, tile end)
+    ps.order.clear();
+    for (int32_t r = rc; r < re; ++r) ps.order.push_back(r);
+    std::stable_sort(ps.order.begin(), ps.order.end(),
+                     [&](int32_t x, int32_t y) { return ps.ref_tiles[x] > ps.ref_tiles[y]; });
+    for (int32_t r : ps.order) {
+      int32_t t = 0;
+      const int32_t nt = ps.ref_tiles[r];
+      while (t < nt) {
+        int32_t best = 0;
+        for (int32_t k = 1; k < n; ++k)
+          if (ps.unit_rem[k] > ps.unit_rem[best]) best = k;
+        if (ps.unit_rem[best] <= 0) return false;
+        const int32_t take = std::min(nt - t, ps.unit_rem[best]);
+        ps.parts.push_back({best, r, t, t + take});
+        ps.unit_rem[best] -= take;
+        t += take;
       }
-    ps.groups.push_back(gr);
+    }
+    // pieces, unit by unit: common-part tiles in order, then the unit's live-block parts
+    int32_t cr = rb, ct = 0;                             // common-part cursor
+    for (int32_t k = 0; k < n; ++k) {
+      const int32_t ub = (int32_t)ps.pieces.size();
+      for (int32_t left = ps.unit_rem[k]; left > 0;) {
+        while (cr < rc && ct >= ps.ref_tiles[cr]) {
+          ++cr;
+          ct = 0;
+        }
+        if (cr >= rc) return false;
+        const int32_t take = std::min(left, ps.ref_tiles[cr] - ct);
+        for (int32_t t = ct; t < ct + take; ++t)
+          if (!emit(cr, t)) return false;
+        ct += take;
+        left -= take;
+      }
+      for (const auto& pt : ps.parts) {
+        if (pt.unit != k) continue;
+        for (int32_t t = pt.t0; t < pt.t1; ++t)
+          if (!emit(pt.ref, t)) return false;
+      }
+      ps.unit_range.push_back({ub, (int32_t)ps.pieces.size()});
+    }
+    // units of the problem's groups, one per KV head, over the same pieces
+    const size_t first_range = ps.unit_range.size() - (size_t)n;
+    for (int32_t h = 0; h < H; ++h) {
+      const int32_t g = p * H + h;
+      hw::Group gr{p, h, (int32_t)ps.units.size(), 0};
+      for (int32_t k = 0; k < n; ++k) {
+        const auto rg = ps.unit_range[first_range + k];
+        hw::Unit u{};
+        u.piece_begin = rg.first;
+        u.piece_end = rg.second;
+        u.group = g;
+        u.seg0 = rg.second > rg.first ? ps.pieces[rg.first].seg_slot : -1;
+        u.delta0 = -1;
+        ps.units.push_back(u);
+      }
+      gr.unit_end = (int32_t)ps.units.size();
+      ps.groups.push_back(gr);
+    }
+  }
+  ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
+  // fresh ranges: a unit's appended tokens are those of its pieces
+  for (hw::Unit& u : ps.units) {
+    u.fresh_begin = ps.piece_fresh0[u.piece_begin];
+    u.fresh_end = ps.piece_fresh0[u.piece_end];
   }
   if ((int64_t)ps.units.size() > L.max_units) return false;
   if (unit_cap > 0 && (int64_t)ps.units.size() > unit_cap) return false;
@@ -841,8 +899,7 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
     if (st != HW_OK) return st;
     // Tensor-core kernel: one CTA per SM holds all of its shared memory and TMEM, so one unit
     // per SM, balanced by KV entries.
-    if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0, false,
-                              false))
+    if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
     st = c->upload_slot(slot, po.bytes, s);
@@ -866,7 +923,6 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   a.out_f32 = out_dtype == HW_OUT_F32;
   a.lse = lse;
   a.partials = c->d_partials();
-  a.tickets = reinterpret_cast<uint32_t*>(c->ws + c->lay.tickets);
   a.rope_cos = c->d_cos();
   a.rope_sin = c->d_sin();
   a.err = c->d_err();

@@ -57,9 +57,6 @@ struct FreshTok {
 __host__ __device__ constexpr int part_stride(int D) { return D + 4; }
 
 // A unit: consecutive pieces of one (problem, KV head) group, one CTA, one partial result.
-// The tensor-core kernel gives each CTA a static first range and lets the CTAs of a group claim
-// the pieces [dyn_begin, dyn_end) one by one from a counter (the partial result then covers
-// whatever the CTA processed); the CUDA-core kernel uses the static range only.
 struct Unit {
   int32_t piece_begin;
   int32_t piece_end;
@@ -67,9 +64,7 @@ struct Unit {
   int32_t seg0;      // seg_slot of the first piece, -1 if the unit has none
   int32_t delta0;    // the rotation of seg0 if it is the same for every worker, else -1
   int32_t fresh_begin, fresh_end;  // appended tokens it writes, in the FreshTok table
-  int32_t dyn_begin, dyn_end;      // pieces claimed dynamically by the group's CTAs
-  int32_t n_group;                 // CTAs (units) of the group
-  int32_t pad[2];
+  int32_t pad;
 };
 
 // A group: one (problem, KV head); its units are [unit_begin, unit_end).
@@ -110,8 +105,6 @@ struct AttnArgs {
   int32_t out_f32;
   float* lse;                 // [P][W][H_q] or null
   float* partials;            // [units][rows][part_stride(D)]: o[D], m, l (log2 domain), pad
-  uint32_t* tickets;          // [2][groups]: claim counters, finished-CTA counters (zero between
-                              //   launches; the last CTA of a group rewinds them)
   const float* rope_cos;
   const float* rope_sin;
   uint32_t* err;
