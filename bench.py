@@ -8,9 +8,11 @@ D 128, a 32768-token common block plus 8 worker blocks of 128..2048 tokens in a 
 (page 256, seeded random physical page order).
 
 Reported (one JSON line, rank 0):
-  value  effective HBM GB/s = algorithmic bytes / device time, inputs resident in HBM, L2
-         flushed before every timed step; the algorithmic bytes count every K/V element once
-         (not once per worker), plus q, out and the appended K/V.
+  value  effective HBM GB/s = algorithmic bytes / device time of K consecutive steps (one
+         CUDA event pair), inputs resident in HBM; the steps go in turn to several
+         independent caches of the workload, so each step's K/V come from HBM, not L2.  The
+         algorithmic bytes count every K/V element once (not once per worker), plus q, out
+         and the appended K/V.
   e2e    the same metric through the public API with pinned host buffers: H2D copy of the
          step's new K/V and queries, the step, D2H copy of the outputs, all inside the timer.
   roofline  the attention kernel's algorithmic bytes / its CUDA-event duration vs measured HBM.
@@ -33,7 +35,6 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "concurrent-attn effective HBM GB/s (% of peak) and worker-tokens/s per step"
-PREQUEUE_STEPS = 24        # below the library's staging depth (32 calls in flight)
 
 
 def measured_peaks():
@@ -204,29 +205,46 @@ def run_ours(args):
 
     base = workload_for(args.config)
     e2e_steps = args.e2e_steps
-    total_steps = args.warmup + 2 * args.steps + e2e_steps
-    w = wl.scaled(base, name=base.name, steps=total_steps + 1)
+    R = max(1, args.caches)
+    per_cache = -(-(args.warmup + 2 * args.steps) // R) + 1
+    w = wl.scaled(base, name=base.name, steps=per_cache + e2e_steps + 1)
     P, W, Hq, D, L = w.num_problems, w.num_workers, w.num_q_heads, w.head_dim, w.num_layers
-    runner = WorkloadRunner(w, device=dev)
-    ctx = runner.cache.ctx
-    # Inputs of every step generated up front and resident in HBM.
-    inputs = [runner.step_inputs(s) for s in range(args.warmup + 2 * args.steps)]
-    outs = [torch.empty(P, W, Hq, D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    # R independent caches of the same workload, used in turn: consecutive steps touch
+    # different K/V, and a cache comes back only after the other R-1 have streamed theirs, so
+    # its K/V come from HBM without flushing L2 inside the timed region.
+    kv_mb = w.num_layers * w.view_tokens(0) * w.num_kv_heads * D * 4 / 1e6   # K/V of one cache
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-
+    if (R - 1) * kv_mb * 1e6 < 2 * l2:
+        raise SystemExit(f"--caches {R}: the other caches' {(R - 1) * kv_mb:.0f} MB of K/V do not "
+                         f"evict a cache from the {l2 / 1e6:.0f} MB L2; use more caches")
+    runners = [WorkloadRunner(w, device=dev) for _ in range(R)]
+    ctxs = [r.cache.ctx for r in runners]
+    local = [0] * R                              # next decode step of each cache
+    outs = [torch.empty(P, W, Hq, D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)   # e2e leg
     stream = torch.cuda.current_stream(dev).cuda_stream     # raw handle: no per-call lookup
 
-    def one_step(s, inp):
-        runner.append(inp, stream=stream)
-        runner.attend(inp, outs, stream=stream)
+    n_planned = [0]
+
+    def plan_steps(n):
+        """The next n steps, caches in turn: (cache, its step index, inputs resident in HBM)."""
+        seq = []
+        for _ in range(n):
+            c = n_planned[0] % R
+            n_planned[0] += 1
+            seq.append((c, local[c]))
+            local[c] += 1
+        return [(c, st, runners[c].step_inputs(st)) for c, st in seq]
+
+    def run_step(c, st, inp):
+        runners[c].append(inp, stream=stream)
+        runners[c].attend(inp, outs, stream=stream)
+        runners[c].end(st, stream=stream)
 
     host_s = []
-    for s in range(args.warmup):
-        flush.zero_()
+    for c, st, inp in plan_steps(args.warmup):
         t0 = time.perf_counter()
-        one_step(s, inputs[s])
-        runner.end(s, stream=stream)
+        run_step(c, st, inp)
         host_s.append(time.perf_counter() - t0)
         torch.cuda.synchronize()
     host_step = statistics.median(host_s)      # host time to submit one step (Python + C API)
@@ -236,68 +254,68 @@ def run_ours(args):
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
-    binding.hw_profile_read(ctx)                      # reset the launch counters
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for ctx in ctxs:
+        binding.hw_profile_read(ctx)                  # reset the launch counters
+    timed = plan_steps(args.steps)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(uuid)
     time.sleep(0.3)
-    total_bytes = 0
-    attn_bytes = 0
     # Submission runs ahead of the device: a bounded device-side delay first, long enough for the
-    # host to enqueue the timed steps (up to the library's staging depth), so that the events
-    # time the GPU's work and not the gaps of a slower Python loop.  The host's own cost per
-    # step is reported beside (host_us_per_step) and is inside the e2e number.
+    # host to enqueue every timed step, so that the events time the GPU's work and not the gaps
+    # of a slower Python loop.  The host's own cost per step is reported beside
+    # (host_us_per_step) and is inside the e2e number.
     sm_hz = 2.07e9                             # GB300 maximum SM clock (cycles of the delay)
-    ahead = min(args.steps, PREQUEUE_STEPS)
-    torch.cuda._sleep(int(min(0.2, 1.3 * ahead * host_step + 1e-3) * sm_hz))
-    for i in range(args.steps):
-        s = args.warmup + i
-        flush.zero_()
-        starts[i].record()
-        one_step(s, inputs[s])
-        ends[i].record()
-        runner.end(s, stream=stream)
-        b, ab = step_bytes(w, s)
-        total_bytes += b
-        attn_bytes += ab
+    torch.cuda._sleep(int(min(0.2, 1.3 * args.steps * host_step + 1e-3) * sm_hz))
+    e_start.record()
+    total_bytes = 0
+    for c, st, inp in timed:
+        run_step(c, st, inp)
+        total_bytes += step_bytes(w, st)[0]
+    e_end.record()
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    launches = int(binding.hw_profile_read(ctx)["launches"])
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    launches = sum(int(binding.hw_profile_read(ctx)["launches"]) for ctx in ctxs)
+    t_total = e_start.elapsed_time(e_end) / 1e3
 
     # Kernel timing pass: the same kind of steps again, now with the library recording CUDA
     # events directly around each attention kernel on its stream (kept out of the pass above
     # because an event between launches ends their programmatic chaining).
-    binding.hw_profile_enable(ctx, True)
-    binding.hw_profile_read(ctx)
+    for ctx in ctxs:
+        binding.hw_profile_enable(ctx, True)
+        binding.hw_profile_read(ctx)
+    prof_steps = plan_steps(args.steps)
     attn_bytes = 0
-    torch.cuda._sleep(int(min(0.2, 1.3 * ahead * host_step + 1e-3) * sm_hz))   # queued ahead too
-    for i in range(args.steps):
-        s = args.warmup + args.steps + i
-        flush.zero_()
-        one_step(s, inputs[s])
-        runner.end(s, stream=stream)
-        attn_bytes += step_bytes(w, s)[1]
+    torch.cuda._sleep(int(min(0.2, 1.3 * args.steps * host_step + 1e-3) * sm_hz))
+    for c, st, inp in prof_steps:
+        run_step(c, st, inp)
+        attn_bytes += step_bytes(w, st)[1]
     torch.cuda.synchronize()
-    prof = binding.hw_profile_read(ctx)
-    binding.hw_profile_enable(ctx, False)
-    t_total = sum(step_ms) / 1e3
+    attn_ms_sum, attn_n = 0.0, 0
+    for ctx in ctxs:
+        pr = binding.hw_profile_read(ctx)
+        attn_ms_sum += pr["attention_ms"]
+        attn_n += pr["timed_attention"]
+        binding.hw_profile_enable(ctx, False)
+    prof = {"attention_ms": attn_ms_sum, "timed_attention": attn_n}
     if world > 1:
         t = torch.tensor([t_total], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         t_total = float(t.item())
-
     # End to end through the public API: inputs in pinned host memory.
+    # (cache 0, L2 flushed before every step, one step at a time with a synchronize)
     e2e = None
     if e2e_steps:
+        runner = runners[0]
+        first = local[0]
         host_in = []
         for i in range(e2e_steps):
-            s = args.warmup + 2 * args.steps + i
+            s = first + i
             k, v, q = [], [], []
             for layer in range(L):
                 kb, vb = wl.step_kv(w, layer, s)
@@ -311,7 +329,7 @@ def run_ours(args):
         dq = [torch.empty(P, W, Hq, D, dtype=torch.int16, device=dev) for _ in range(L)]
         e2e_times, e2e_bytes = [], 0
         for i in range(e2e_steps):
-            s = args.warmup + 2 * args.steps + i
+            s = first + i
             flush.zero_()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
@@ -322,7 +340,8 @@ def run_ours(args):
                 dq[layer].copy_(q[layer], non_blocking=True)
             inp = ([x.view(torch.bfloat16) for x in dk], [x.view(torch.bfloat16) for x in dv],
                    [x.view(torch.bfloat16) for x in dq])
-            one_step(s, inp)
+            runner.append(inp, stream=stream)
+            runner.attend(inp, outs, stream=stream)
             for layer in range(L):
                 host_out[layer].copy_(outs[layer], non_blocking=True)
             torch.cuda.synchronize()
@@ -335,9 +354,10 @@ def run_ours(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": 1e3 * sum(e2e_times) / e2e_steps, "steps": e2e_steps}
 
-    st, info = runner.cache.check_device_errors()
-    if st != binding.HW_OK:
-        raise RuntimeError(f"device error word set: {info}")
+    for r in runners:
+        st, info = r.cache.check_device_errors()
+        if st != binding.HW_OK:
+            raise RuntimeError(f"device error word set: {info}")
 
     if rank != 0:
         if world > 1:
@@ -354,9 +374,13 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": w.name, "problems": P, "workers": W, "layers": L, "H_q": Hq,
                    "H_kv": w.num_kv_heads, "head_dim": D, "page_size": w.page_size,
-                   "common_tokens": list(w.common_len), "view_tokens_first_step":
-                   w.view_tokens(args.warmup), "parallelism": f"replicas{world}",
-                   "l2": "flushed (memset of 2x L2) before every timed step",
+                   "common_tokens": list(w.common_len), "view_tokens_first_timed_step":
+                   w.view_tokens(timed[0][1]), "parallelism": f"replicas{world}",
+                   "l2": (f"inputs larger than L2: {R} independent caches of this workload "
+                          f"({kv_mb:.0f} MB of K/V each) used in turn, so a cache returns only "
+                          f"after {(R - 1) * kv_mb:.0f} MB of other K/V; no flush in the timed "
+                          f"region; the e2e leg flushes L2 (2x L2 memset) before every step"),
+                   "timing": "one CUDA event pair around all timed steps",
                    "step": "append 1 token/worker + concurrent attention + step end"},
         "pct_of_peak": 100.0 * value / world / peak,
         "worker_tokens_per_s": world * P * W * args.steps / t_total,
@@ -369,7 +393,6 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": attn_bytes / args.steps},
         "gpu_launches": launches,
         "host_us_per_step": 1e6 * host_step,
-        "prequeued_steps": ahead,
         "clocks": clk,
     }
     if e2e:
@@ -389,11 +412,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="c4")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--caches", type=int, default=4,
+                    help="independent caches of the workload used in turn (>= 2)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.caches < 2:
+        ap.error("--caches must be at least 2")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -152,8 +152,8 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
 
 // K3: out = sum_u o_u 2^(m_u - M) / sum_u l_u 2^(m_u - M), M = max_u m_u; lse = (M + log2 L) ln 2.
 // One warp per (group, query row), lanes across the row as float4 columns.  The units are
-// taken eight at a time with all their loads in flight, merged into a running (M, L, O) that
-// is rescaled when M grows.
+// taken 24 at a time with all their loads in flight, merged into a running (M, L, O) that is
+// rescaled when M grows.
 constexpr int kMergeWarps = 8;
 
 template <int D>
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const AttnArgs 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   HW_SPAN_BEGIN(1);
   constexpr int PS = part_stride(D);
-  constexpr int kChunk = 8;
+  constexpr int kChunk = 24;               // one round of loads for up to 24 units
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item = blockIdx.x * kMergeWarps + warp;
   if (item < a.num_groups * a.rows) {

@@ -751,6 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int Q4 = PS / 4;                               // float4s per row
       float4* part = reinterpret_cast<float4*>(a.partials + (size_t)blockIdx.x * R * PS);
       const float4* st4 = reinterpret_cast<const float4*>(stage);
+#pragma unroll 4
       for (int idx = threadIdx.x - 128; idx < R * Q4; idx += nthr) {
         const int rr = idx / Q4, c4 = idx - rr * Q4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
