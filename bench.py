@@ -221,7 +221,11 @@ def run_ours(args):
     ctxs = [r.cache.ctx for r in runners]
     local = [0] * R                              # next decode step of each cache
     outs = [torch.empty(P, W, Hq, D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)   # e2e leg
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    # Replace the lines the prefills left in L2 (written at normal priority, they would outlive
+    # the kernel's evict-first K/V traffic and serve part of the last-built cache from L2).
+    flush.zero_()
+    torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev).cuda_stream     # raw handle: no per-call lookup
 
     n_planned = [0]
