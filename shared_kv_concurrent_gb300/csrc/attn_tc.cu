@@ -698,9 +698,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_launch_dependents();
       }
       // Epilogue.  Each lane's (O row, max, sum) over its columns goes to shared memory (the
-      // K/V ring is idle once the last MMA has completed) as stage[chunk][row][PS]; then the T
-      // chunks of every row are merged by log-sum-exp and the unit's partials -- unnormalised
-      // o, max and sum in the log2 domain, [rows][PS] fp32 -- are stored with 16-byte writes.
+      // K/V ring is idle once the last MMA has completed) as stage[chunk][row][PS], with the
+      // log-sum-exp weights of the T chunks of every row; after the role branches all warps
+      // merge the chunks and store the unit's partials.
       // Wait for every MMA through the single-use `fin` barrier, not o_done: here o_done may be
       // two phases behind (the last two P.V products can both be in flight), and a parity
       // wait cannot tell that apart from "done".
@@ -732,46 +732,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nthr = 32 * active_softmax_warps;
       asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
       if (threadIdx.x == 128) HW_TRACE_EV(251);
-      // Per row: M = max over the T chunks, and each chunk's weight 2^(m_j - M).
+      // Per row: M = max over the T chunks, each chunk's weight 2^(m_j - M), and the merged
+      // sum L = sum_j l_j 2^(m_j - M); the merged rows are written after the role branches by
+      // all warps.
       float* rowM = stage + (size_t)T * R * PS;
       float* rowW = rowM + R;                                  // [T][R]
+      float* rowL = rowW + T * R;
       for (int rr = threadIdx.x - 128; rr < R; rr += nthr) {
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int j = 0; j < T; ++j) M = fmaxf(M, stage[((size_t)j * R + rr) * PS + D]);
         rowM[rr] = M;
-#pragma unroll
-        for (int j = 0; j < T; ++j)
-          rowW[j * R + rr] = (M == -CUDART_INF_F) ? 0.f : fast_exp2(stage[((size_t)j * R + rr) * PS + D] - M);
-      }
-      asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
-      if (threadIdx.x == 128) HW_TRACE_EV(252);
-      // The unit's [R][PS] block as float4s: o columns are weighted sums over the chunks; the
-      // (m, l, pad, pad) float4 of a row holds M and the weighted sum of the chunks' l.
-      constexpr int Q4 = PS / 4;                               // float4s per row
-      float4* part = reinterpret_cast<float4*>(a.partials + (size_t)blockIdx.x * R * PS);
-      const float4* st4 = reinterpret_cast<const float4*>(stage);
-#pragma unroll 4
-      for (int idx = threadIdx.x - 128; idx < R * Q4; idx += nthr) {
-        const int rr = idx / Q4, c4 = idx - rr * Q4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float Ls = 0.f;
 #pragma unroll
         for (int j = 0; j < T; ++j) {
-          const float wj = rowW[j * R + rr];
-          const float4 x = st4[((size_t)j * R + rr) * Q4 + c4];
-          if (c4 < D / 4) {
-            acc.x = fmaf(x.x, wj, acc.x);
-            acc.y = fmaf(x.y, wj, acc.y);
-            acc.z = fmaf(x.z, wj, acc.z);
-            acc.w = fmaf(x.w, wj, acc.w);
-          } else {
-            acc.y = fmaf(x.y, wj, acc.y);                      // l
-          }
+          const float wj =
+              (M == -CUDART_INF_F) ? 0.f : fast_exp2(stage[((size_t)j * R + rr) * PS + D] - M);
+          rowW[j * R + rr] = wj;
+          Ls = fmaf(stage[((size_t)j * R + rr) * PS + D + 1], wj, Ls);
         }
-        if (c4 == D / 4) acc.x = rowM[rr];
-        part[idx] = acc;
+        rowL[rr] = Ls;
       }
-      if (threadIdx.x == 128) HW_TRACE_EV(6);
+      if (threadIdx.x == 128) HW_TRACE_EV(252);
       if (!ok && (*abort) && lane == 0) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 2);
     }
   }
@@ -780,6 +762,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  {
+    // The unit's partials, [R][PS] fp32 -- unnormalised o, then (M, L, 0, 0) in the log2
+    // domain -- from the T staged chunks of every row: all eight warps, a warp per row and a
+    // float4 column per lane (coalesced 16-byte stores).
+    constexpr int PS = part_stride(D);
+    constexpr int Q4 = PS / 4, DQ = D / 4;
+    const float* stage = reinterpret_cast<const float*>(smem + C::kRingOff);
+    const float4* st4 = reinterpret_cast<const float4*>(stage);
+    const float* rowM = stage + (size_t)T * R * PS;
+    const float* rowW = rowM + R;
+    const float* rowL = rowW + T * R;
+    float4* part = reinterpret_cast<float4*>(a.partials + (size_t)blockIdx.x * R * PS);
+#pragma unroll 2
+    for (int rr = warp; rr < R; rr += kThreads / 32) {
+      if (lane < DQ) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+          const float wj = rowW[j * R + rr];
+          const float4 x = st4[((size_t)j * R + rr) * Q4 + lane];
+          acc.x = fmaf(x.x, wj, acc.x);
+          acc.y = fmaf(x.y, wj, acc.y);
+          acc.z = fmaf(x.z, wj, acc.z);
+          acc.w = fmaf(x.w, wj, acc.w);
+        }
+        part[(size_t)rr * Q4 + lane] = acc;
+      }
+      if (lane == (DQ < 32 ? DQ : 0))                         // a spare lane, else lane 0
+        part[(size_t)rr * Q4 + DQ] = make_float4(rowM[rr], rowL[rr], 0.f, 0.f);
+    }
+    if (threadIdx.x == 128) HW_TRACE_EV(6);
   }
   if (threadIdx.x == 0) HW_TRACE_EV(7);
 }
