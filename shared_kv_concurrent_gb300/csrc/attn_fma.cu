@@ -14,6 +14,7 @@
 #include <math_constants.h>
 
 #include "hw_device.cuh"
+#include "hw_merge.cuh"
 
 namespace hw {
 namespace {
@@ -150,10 +151,9 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
   }
 }
 
-// K3: out = sum_u o_u 2^(m_u - M) / sum_u l_u 2^(m_u - M), M = max_u m_u; lse = (M + log2 L) ln 2.
-// One warp per (group, query row), lanes across the row as float4 columns.  The units are
-// taken 24 at a time with all their loads in flight, merged into a running (M, L, O) that is
-// rescaled when M grows.
+// K3: the log-sum-exp merge of the units' partials (merge_row, hw_merge.cuh), one warp per
+// (group, query row), as a kernel of its own: used after the CUDA-core attention and after the
+// tensor-core attention when that kernel does not merge itself.
 constexpr int kMergeWarps = 8;
 
 template <int D>
@@ -162,71 +162,9 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const AttnArgs 
   HW_SPAN_BEGIN(0);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   HW_SPAN_BEGIN(1);
-  constexpr int PS = part_stride(D);
-  constexpr int kChunk = 24;               // one round of loads for up to 24 units
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item = blockIdx.x * kMergeWarps + warp;
-  if (item < a.num_groups * a.rows) {
-    const int gi = item / a.rows, r = item - gi * a.rows;
-    const Group g = a.groups[gi];
-    const bool act = lane < D / 4;
-    const size_t stride = (size_t)a.rows * PS;
-    const float* base = a.partials + ((size_t)g.unit_begin * a.rows + r) * PS;
-    const int nu = g.unit_end - g.unit_begin;
-    float M = -CUDART_INF_F, L = 0.f;
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = 0; k0 < nu; k0 += kChunk) {
-      float2 ml[kChunk];
-      float4 o[kChunk];
-#pragma unroll
-      for (int j = 0; j < kChunk; ++j) {
-        const int k = k0 + j;
-        ml[j] = make_float2(-CUDART_INF_F, 0.f);
-        o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (k < nu) {
-          ml[j] = *reinterpret_cast<const float2*>(base + k * stride + D);
-          if (act) o[j] = *reinterpret_cast<const float4*>(base + k * stride + 4 * lane);
-        }
-      }
-      float cm = M;
-#pragma unroll
-      for (int j = 0; j < kChunk; ++j) cm = fmaxf(cm, ml[j].x);
-      if (cm == -CUDART_INF_F) continue;
-      const float sc = (M == -CUDART_INF_F) ? 0.f : exp2f(M - cm);
-      L *= sc;
-      O.x *= sc;
-      O.y *= sc;
-      O.z *= sc;
-      O.w *= sc;
-#pragma unroll
-      for (int j = 0; j < kChunk; ++j) {
-        const float wj = (ml[j].x == -CUDART_INF_F) ? 0.f : exp2f(ml[j].x - cm);
-        L = fmaf(ml[j].y, wj, L);
-        O.x = fmaf(o[j].x, wj, O.x);
-        O.y = fmaf(o[j].y, wj, O.y);
-        O.z = fmaf(o[j].z, wj, O.z);
-        O.w = fmaf(o[j].w, wj, O.w);
-      }
-      M = cm;
-    }
-    const float inv = (L > 0.f) ? 1.f / L : 0.f;
-    const int w = r / a.G, hq = g.h * a.G + r % a.G;
-    const size_t oi = ((size_t)g.p * a.W + w) * a.H_q + hq;
-    if (act) {
-      if (a.out_f32) {
-        reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + oi * D)[lane] =
-            make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
-      } else {
-        const __nv_bfloat162 v0 = __floats2bfloat162_rn(O.x * inv, O.y * inv);
-        const __nv_bfloat162 v1 = __floats2bfloat162_rn(O.z * inv, O.w * inv);
-        uint2 pk;
-        pk.x = *reinterpret_cast<const uint32_t*>(&v0);
-        pk.y = *reinterpret_cast<const uint32_t*>(&v1);
-        reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + oi * D)[lane] = pk;
-      }
-    }
-    if (a.lse && lane == 0) a.lse[oi] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
-  }
+  if (item < a.num_groups * a.rows) merge_row<D, 24>(a, item, lane);
   HW_SPAN_END(0);
 }
 

@@ -1,0 +1,84 @@
+// K3 -- merge of the split-K partials (Hogwild! Inference summary, gentlecold.top, section 9:
+// the work is split over KV entries and the partial results reduced; section 5: per-block
+// softmax statistics combine by log-sum-exp):
+//   out = sum_u o_u 2^(m_u - M) / sum_u l_u 2^(m_u - M),  M = max_u m_u,
+//   lse = (M + log2 L) ln 2,
+// with (o_u, m_u, l_u) the unit partials in the log2 domain.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "hw_internal.h"
+
+namespace hw {
+
+// One (group, query row) `item`, by one warp (lane = float4 column).  The units are taken kChunk
+// at a time with all their loads in flight, merged into a running (M, L, O) that is rescaled
+// when M grows.
+template <int D, int kChunk>
+__device__ __forceinline__ void merge_row(const AttnArgs& a, int item, int lane) {
+  constexpr int PS = part_stride(D);
+  const int gi = item / a.rows, r = item - gi * a.rows;
+  const Group g = a.groups[gi];
+  const bool act = lane < D / 4;
+  const size_t stride = (size_t)a.rows * PS;
+  const float* base = a.partials + ((size_t)g.unit_begin * a.rows + r) * PS;
+  const int nu = g.unit_end - g.unit_begin;
+  float M = -CUDART_INF_F, L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < nu; k0 += kChunk) {
+    float2 ml[kChunk];
+    float4 o[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const int k = k0 + j;
+      ml[j] = make_float2(-CUDART_INF_F, 0.f);
+      o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k < nu) {
+        ml[j] = *reinterpret_cast<const float2*>(base + k * stride + D);
+        if (act) o[j] = *reinterpret_cast<const float4*>(base + k * stride + 4 * lane);
+      }
+    }
+    float cm = M;
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) cm = fmaxf(cm, ml[j].x);
+    if (cm == -CUDART_INF_F) continue;
+    const float sc = (M == -CUDART_INF_F) ? 0.f : exp2f(M - cm);
+    L *= sc;
+    O.x *= sc;
+    O.y *= sc;
+    O.z *= sc;
+    O.w *= sc;
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const float wj = (ml[j].x == -CUDART_INF_F) ? 0.f : exp2f(ml[j].x - cm);
+      L = fmaf(ml[j].y, wj, L);
+      O.x = fmaf(o[j].x, wj, O.x);
+      O.y = fmaf(o[j].y, wj, O.y);
+      O.z = fmaf(o[j].z, wj, O.z);
+      O.w = fmaf(o[j].w, wj, O.w);
+    }
+    M = cm;
+  }
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+  const int w = r / a.G, hq = g.h * a.G + r % a.G;
+  const size_t oi = ((size_t)g.p * a.W + w) * a.H_q + hq;
+  if (act) {
+    if (a.out_f32) {
+      reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + oi * D)[lane] =
+          make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    } else {
+      const __nv_bfloat162 v0 = __floats2bfloat162_rn(O.x * inv, O.y * inv);
+      const __nv_bfloat162 v1 = __floats2bfloat162_rn(O.z * inv, O.w * inv);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&v0);
+      pk.y = *reinterpret_cast<const uint32_t*>(&v1);
+      reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + oi * D)[lane] = pk;
+    }
+  }
+  if (a.lse && lane == 0)
+    a.lse[oi] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+}
+
+}  // namespace hw
