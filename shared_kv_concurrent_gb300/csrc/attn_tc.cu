@@ -440,8 +440,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pub;
         return true;
       };
+      // Issue the K and V loads of tile j (two ring slots) at pool row y.
+      auto issue_tile = [&](int32_t y) -> bool {
+        for (int part = 0; part < 2; ++part, ++j) {
+          const int s = j % C::kSlots;
+          // The first K tile goes out alone with its V: every CTA fills its ring at once at
+          // start-up, and the first tile would otherwise arrive with the last of that burst.
+          if (j == 2 && !mbar_wait(bar_full(0), 0, abort, kWaitLimitNs)) return false;
+          if (j >= (uint32_t)C::kSlots &&
+              !mbar_wait(bar_empty(s), ((j / C::kSlots) - 1) & 1, abort, kWaitLimitNs))
+            return false;
+          if (part == 0) HW_TRACE_EV(8 + 4 * (j >> 1));
+          mbar_arrive_expect_tx(bar_full(s), C::kTileBytes);
+          const CUtensorMap* m = part == 0 ? &maps.k : &maps.v;
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_2d(ring + s * C::kTileBytes + h * C::kHalfBytes, m, 64 * h, y, bar_full(s),
+                        policy);
+        }
+        return true;
+      };
+      // The unit's first tile, known from the unit record (page * S + slot of a piece that
+      // holds no token of this step), goes out before anything else is read.
+      const bool early = u.first_tok >= 0;
+      if (early)
+        ok = issue_tile((int32_t)(((page_base + u.first_tok / a.S) * a.H_kv + g.h) * a.S +
+                                  u.first_tok % a.S));
       auto load_range = [&](int32_t b, int32_t e) -> bool {
         for (int32_t pi = b; pi < e; ++pi) {
+          if (early && pi == u.piece_begin) continue;  // issued above
           const Piece pc = a.pieces[pi];
           const bool valid = pc.page >= 0 && pc.page < a.num_pages && pc.slot0 >= 0 &&
                              pc.ntok >= 1 && pc.ntok <= kTile && pc.slot0 + pc.ntok <= a.S &&
@@ -457,28 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             waited = true;
             HW_TRACE_EV(248);
           }
-          const int32_t y = (int32_t)(((page_base + pc.page) * a.H_kv + g.h) * a.S + pc.slot0);
-          for (int part = 0; part < 2; ++part, ++j) {
-            const int s = j % C::kSlots;
-            // The first K tile goes out alone with its V: every CTA fills its ring at once at
-            // start-up, and the first tile would otherwise arrive with the last of that burst.
-            if (j == 2 && !mbar_wait(bar_full(0), 0, abort, kWaitLimitNs)) return false;
-            if (j >= (uint32_t)C::kSlots &&
-                !mbar_wait(bar_empty(s), ((j / C::kSlots) - 1) & 1, abort, kWaitLimitNs))
-              return false;
-            if (part == 0) HW_TRACE_EV(8 + 4 * (j >> 1));
-            mbar_arrive_expect_tx(bar_full(s), C::kTileBytes);
-            const CUtensorMap* m = part == 0 ? &maps.k : &maps.v;
-#pragma unroll
-            for (int h = 0; h < C::kHalves; ++h)
-              tma_load_2d(ring + s * C::kTileBytes + h * C::kHalfBytes, m, 64 * h, y, bar_full(s),
-                          policy);
-          }
+          if (!issue_tile((int32_t)(((page_base + pc.page) * a.H_kv + g.h) * a.S + pc.slot0)))
+            return false;
         }
         return true;
       };
       // The unit's pieces in plan order, then the end of the sequence.
-      if (u.piece_end > u.piece_begin)
+      if (ok && u.piece_end > u.piece_begin)
         ok = publish(u.piece_begin, u.piece_end) && load_range(u.piece_begin, u.piece_end);
       publish(0, -1);                                  // end of the sequence (also on abort)
       HW_TRACE_EV(3);

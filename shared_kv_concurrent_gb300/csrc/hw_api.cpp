@@ -816,6 +816,9 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         u.group = g;
         u.seg0 = rg.second > rg.first ? ps.pieces[rg.first].seg_slot : -1;
         u.delta0 = -1;
+        u.first_tok = -1;
+        if (rg.second > rg.first && !ps.pieces[rg.first].fresh)
+          u.first_tok = ps.pieces[rg.first].page * S + ps.pieces[rg.first].slot0;
         ps.units.push_back(u);
       }
       gr.unit_end = (int32_t)ps.units.size();

@@ -64,7 +64,7 @@ struct Unit {
   int32_t seg0;      // seg_slot of the first piece, -1 if the unit has none
   int32_t delta0;    // the rotation of seg0 if it is the same for every worker, else -1
   int32_t fresh_begin, fresh_end;  // appended tokens it writes, in the FreshTok table
-  int32_t pad;
+  int32_t first_tok;  // page * S + slot of the first piece if it holds no new token, else -1
 };
 
 // A group: one (problem, KV head); its units are [unit_begin, unit_end).
