@@ -23,6 +23,10 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   // produce k_raw / v_raw): wait for that grid before reading anything it could write.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   HW_SPAN_BEGIN(0);
+  __shared__ int plan_ok;
+  if (threadIdx.x == 0) plan_ok = plan_arrived(a.gate, a.err, KID_APPEND);
+  __syncthreads();
+  if (!plan_ok) return;
   const AppendRun run = a.runs[blockIdx.y];
   const int t0 = blockIdx.x * kTokPerCta;
   if (t0 >= run.ntok) return;

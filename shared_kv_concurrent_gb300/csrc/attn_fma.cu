@@ -33,6 +33,10 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
   float* qs = sm;                               // [rows][D] rotated, pre-scaled queries
   float* ks = qs + rows * D;                    // [kTile][D + 1]
   float* vs = ks + kTile * KS;                  // [kTile][D]
+  __shared__ int plan_ok;
+  if (threadIdx.x == 0) plan_ok = plan_arrived(a.gate, a.err, KID_ATTN_FMA);
+  __syncthreads();
+  if (!plan_ok) return;
   const Unit u = a.units[blockIdx.x];
   const Group g = a.groups[u.group];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -159,7 +163,10 @@ constexpr int kMergeWarps = 8;
 template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const AttnArgs a) {
   // May be launched as a programmatic dependent of the attention kernel: wait for its writes.
+  // Whatever follows may start its own prologue now (the library's kernels wait for this grid
+  // before they read anything it writes or overwrite the partials it reads).
   HW_SPAN_BEGIN(0);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   HW_SPAN_BEGIN(1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

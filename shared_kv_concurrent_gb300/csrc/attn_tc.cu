@@ -72,7 +72,8 @@ struct Cfg {
   // fresh, chunk_full[kChunkRing], chunk_empty[kChunkRing]
   static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 2 * kChunkRing;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr uint32_t kChunkOff = kMiscOff + 16;         // int2[kChunkRing]
+  static constexpr uint32_t kUnitOff = (kMiscOff + 8 + 15) / 16 * 16;   // the CTA's Unit
+  static constexpr uint32_t kChunkOff = kUnitOff + 32;         // int2[kChunkRing]
   static constexpr uint32_t kSmemBytes = kChunkOff + 8 * kChunkRing + 1024;  // + alignment slack
 };
 
@@ -354,9 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Unit u = a.units[blockIdx.x];
-  // (problem, KV head) of the unit, from its group index (no dependent load)
-  const Group g{u.group / a.H_kv, u.group % a.H_kv, 0, 0};
+  Unit* u_smem = reinterpret_cast<Unit*>(smem + C::kUnitOff);
   const int R = a.rows;
   int active_softmax_warps = 0;               // softmax warps that own at least one real row
   for (int q = 0; q < 4; ++q) active_softmax_warps += (32 * (q % WPC) < R) ? 1 : 0;
@@ -381,7 +380,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_cfull0 + 8u * e, 1);
       mbar_init(bar_cempty0 + 8u * e, 1 + kRotThreads + 32 * active_softmax_warps);
     }
-    *abort = 0;
+    // The plan of this launch may still be on its way (copy stream): read the unit record
+    // only once its sequence number has arrived.
+    *abort = plan_arrived(a.gate, a.err, KID_ATTN_TC) ? 0 : 1;
+    Unit uu = a.units[blockIdx.x];
+    if (*abort) {                       // no plan: an empty unit (the error word says why)
+      uu.piece_begin = uu.piece_end = 0;
+      uu.seg0 = uu.first_tok = -1;
+      uu.fresh_end = uu.fresh_begin;
+    }
+    *u_smem = uu;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -396,6 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const Unit u = *u_smem;
+  // (problem, KV head) of the unit, from its group index (no dependent load)
+  const Group g{u.group / a.H_kv, u.group % a.H_kv, 0, 0};
   if (threadIdx.x == 0) HW_TRACE_EV(1);
 
   const int64_t page_base = (int64_t)layer * a.num_pages;   // first page of this layer's pool

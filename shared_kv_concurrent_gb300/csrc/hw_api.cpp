@@ -10,6 +10,7 @@
 #include "hogwild.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <deque>
@@ -33,6 +34,9 @@ constexpr int kProfPairs = 4096;       // timed launches kept per hw_profile_rea
 constexpr int kFuseTok = 16;
 
 thread_local int g_cuda_err = 0;
+// Plan sequence numbers, unique in the process: a slot word left by an earlier context in
+// recycled memory never equals a number this context waits for.
+std::atomic<uint64_t> g_upload_seq{0};
 std::mutex g_msg_mu;
 std::string g_cuda_msg;
 
@@ -53,7 +57,7 @@ hw_status cuda_fail(cudaError_t e) {
 
 struct Layout {
   size_t err, cos, sin, slots, partials, tickets, total;
-  size_t slot_bytes;
+  size_t slot_bytes, slot_seq_off;   // a slot ends with the plan's 8-byte sequence number
   int32_t max_segments, max_append, max_pieces, max_units, max_seg_slots, rows;
   int32_t num_slots, max_fresh;
 };
@@ -97,8 +101,10 @@ Layout make_layout(const hw_config* c) {
                             align_up((size_t)P * H * sizeof(hw::Group), 16) +
                             align_up((size_t)L.max_seg_slots * W * sizeof(int32_t), 16) +
                             align_up((size_t)L.max_fresh * sizeof(hw::FreshTok), 16);
-  // A slot holds a step's append runs followed by its attention plan (uploaded together).
-  L.slot_bytes = align_up(append_bytes, kAlign) + align_up(attn_bytes, kAlign);
+  // A slot holds a step's append runs followed by its attention plan (uploaded together), and
+  // last the plan's sequence number.
+  L.slot_seq_off = align_up(append_bytes, kAlign) + align_up(attn_bytes, kAlign);
+  L.slot_bytes = L.slot_seq_off + kAlign;
   // Staging slots let the host run that many calls ahead of the device.
   L.num_slots = (int32_t)std::max<size_t>(4, std::min<size_t>(kMaxSlots, kSlotBudget / L.slot_bytes));
   size_t off = 0;
@@ -161,10 +167,10 @@ struct hw_ctx {
   char* h_slots = nullptr;                 // pinned staging, lay.num_slots * slot_bytes
   cudaEvent_t slot_ev[kMaxSlots] = {};     // compute stream: last kernel reading the slot
   bool slot_used[kMaxSlots] = {};
-  // Plans go up on a stream of their own, ahead of the compute stream, which waits for them by
-  // event: when the host runs ahead of the device the copy is off the critical path.
+  // Plans go up on a stream of their own, each followed by its sequence number, which the
+  // kernels check before reading the plan: the compute stream never waits on the copy stream,
+  // so its kernels stay back to back (programmatic launch chaining across calls).
   cudaStream_t copy_stream = nullptr;
-  cudaEvent_t copy_ev[kMaxSlots] = {};
   int next_slot = 0;
   hw::TcMaps maps{};
   bool use_tc = false;                     // tensor-core attention (W*G >= 16 rows)
@@ -182,6 +188,7 @@ struct hw_ctx {
   size_t step_plan_off = 0;
   bool step_plan_ok = false;
   PlanOffsets step_po{};
+  hw::PlanGate step_gate{};
   PlanScratch ps;
   // Fused append: when the step's plan lists its appended tokens (step_fused), hw_append_kv
   // only records the layer's k_raw / v_raw here and the layer's tensor-core attention writes
@@ -248,6 +255,7 @@ struct hw_ctx {
   hw_status launch_append(int32_t layer, const void* k_raw, const void* v_raw, cudaStream_t s) {
     const int slot = step_slot;
     hw::AppendArgs a{};
+    a.gate = step_gate;
     a.runs = reinterpret_cast<const hw::AppendRun*>(d_slot(slot));
     a.num_runs = step_runs;
     a.max_run = step_max_run;
@@ -281,12 +289,17 @@ struct hw_ctx {
     pend_k[layer] = pend_v[layer] = nullptr;
     return launch_append(layer, k, v, s);
   }
-  // Copy `bytes` of staging slot `slot` to its device copy on the copy stream and make the
-  // compute stream `s` wait for it.  The slot's previous readers have completed (acquire_slot).
-  hw_status upload_slot(int slot, size_t bytes, cudaStream_t s) {
+  // Copy `bytes` of staging slot `slot` to its device copy on the copy stream, then the slot's
+  // new sequence number (*gate is set to check for it).  The slot's previous readers have
+  // completed (acquire_slot), and the next ones check the number before reading.
+  hw_status upload_slot(int slot, size_t bytes, hw::PlanGate* gate) {
+    const uint64_t seq = ++g_upload_seq;
+    std::memcpy(h_slot(slot) + lay.slot_seq_off, &seq, sizeof(seq));
     HW_CUDA(cudaMemcpyAsync(d_slot(slot), h_slot(slot), bytes, cudaMemcpyHostToDevice, copy_stream));
-    HW_CUDA(cudaEventRecord(copy_ev[slot], copy_stream));
-    HW_CUDA(cudaStreamWaitEvent(s, copy_ev[slot], 0));
+    HW_CUDA(cudaMemcpyAsync(d_slot(slot) + lay.slot_seq_off, h_slot(slot) + lay.slot_seq_off,
+                            sizeof(seq), cudaMemcpyHostToDevice, copy_stream));
+    gate->plan_seq = reinterpret_cast<const unsigned long long*>(d_slot(slot) + lay.slot_seq_off);
+    gate->plan_expect = seq;
     return HW_OK;
   }
   // Pick the next staging slot; waits only if the slot's previous use is still in flight.
@@ -345,10 +358,10 @@ void hw_destroy(hw_ctx* ctx) {
       cudaEventSynchronize(ctx->slot_ev[i]);
       cudaEventDestroy(ctx->slot_ev[i]);
     }
-  if (ctx->copy_stream) cudaStreamSynchronize(ctx->copy_stream);
-  for (int i = 0; i < kMaxSlots; ++i)
-    if (ctx->copy_ev[i]) cudaEventDestroy(ctx->copy_ev[i]);
-  if (ctx->copy_stream) cudaStreamDestroy(ctx->copy_stream);
+  if (ctx->copy_stream) {
+    cudaStreamSynchronize(ctx->copy_stream);
+    cudaStreamDestroy(ctx->copy_stream);
+  }
   if (ctx->h_slots) cudaFreeHost(ctx->h_slots);
   delete ctx;
 }
@@ -419,7 +432,6 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
   if (e != cudaSuccess) return fail(cuda_fail(e));
   for (int i = 0; i < kMaxSlots; ++i) {
     e = cudaEventCreateWithFlags(&c->slot_ev[i], cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->copy_ev[i], cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(cuda_fail(e));
   }
   // RoPE table: cos/sin of p * theta^(-2i/D) in fp64 on the host, stored as fp32.
@@ -438,6 +450,8 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
   e = cudaMemsetAsync(k_pool, 0, pool_bytes, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(v_pool, 0, pool_bytes, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->ws + lay.err, 0, kAlign, s);
+  if (e == cudaSuccess)                      // plan slots, with their sequence words
+    e = cudaMemsetAsync(c->ws + lay.slots, 0, (size_t)lay.num_slots * lay.slot_bytes, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->ws + lay.tickets, 0, lay.total - lay.tickets, s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(c->d_cos(), tc.data(), tc.size() * sizeof(float), cudaMemcpyHostToDevice, s);
@@ -537,7 +551,7 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
     hw_status st = c->acquire_slot(&slot);
     if (st != HW_OK) return st;
     hw::AppendRun* runs = reinterpret_cast<hw::AppendRun*>(c->h_slot(slot));
-    const size_t max_runs = (c->lay.slot_bytes / 2) / sizeof(hw::AppendRun);
+    const size_t max_runs = c->lay.slot_seq_off / sizeof(hw::AppendRun);
     int32_t nr = 0, src = 0, max_run = 0;
     for (int32_t p = 0; p < P; ++p)
       for (int32_t b = 0; b < B; ++b) {
@@ -563,18 +577,18 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
     bool fuse = c->use_tc;
     for (int32_t i = 0; i < P * B && fuse; ++i) fuse = n_new[i] <= kFuseTok;
     bool plan_ok =
-        plan_off < c->lay.slot_bytes &&
+        plan_off < c->lay.slot_seq_off &&
         build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->use_tc ? c->num_sms : 0,
                              fuse) &&
-        plan_off + po.bytes <= c->lay.slot_bytes;
+        plan_off + po.bytes <= c->lay.slot_seq_off;
     if (!plan_ok && fuse) {
       fuse = false;
-      plan_ok = plan_off < c->lay.slot_bytes &&
+      plan_ok = plan_off < c->lay.slot_seq_off &&
                 build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0,
                                      c->use_tc ? c->num_sms : 0, false) &&
-                plan_off + po.bytes <= c->lay.slot_bytes;
+                plan_off + po.bytes <= c->lay.slot_seq_off;
     }
-    st = c->upload_slot(slot, plan_off + (plan_ok ? po.bytes : 0), s);
+    st = c->upload_slot(slot, plan_off + (plan_ok ? po.bytes : 0), &c->step_gate);
     if (st != HW_OK) return st;
     c->step_slot = slot;
     c->step_runs = nr;
@@ -854,7 +868,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   po->fresh = off;
   off = align_up(off + ps.fresh.size() * sizeof(hw::FreshTok), 16);
   po->bytes = off;
-  if (off > L.slot_bytes) return false;
+  if (off > L.slot_seq_off) return false;
   std::memcpy(buf + po->pieces, ps.pieces.data(), ps.pieces.size() * sizeof(hw::Piece));
   std::memcpy(buf + po->units, ps.units.data(), ps.units.size() * sizeof(hw::Unit));
   std::memcpy(buf + po->groups, ps.groups.data(), ps.groups.size() * sizeof(hw::Group));
@@ -892,11 +906,13 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
     const hw_status st = c->flush_append(layer, s);
     if (st != HW_OK) return st;
   }
+  hw::PlanGate gate{};
   if (step_plan) {
     // The plan of this step went up with its first append.
     slot = c->step_slot;
     po = c->step_po;
     dbase = c->d_slot(slot) + c->step_plan_off;
+    gate = c->step_gate;
   } else {
     hw_status st = c->acquire_slot(&slot);
     if (st != HW_OK) return st;
@@ -905,10 +921,11 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
     if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
-    st = c->upload_slot(slot, po.bytes, s);
+    st = c->upload_slot(slot, po.bytes, &gate);
     if (st != HW_OK) return st;
   }
   hw::AttnArgs a{};
+  a.gate = gate;
   a.pieces = reinterpret_cast<const hw::Piece*>(dbase + po.pieces);
   a.units = reinterpret_cast<const hw::Unit*>(dbase + po.units);
   a.groups = reinterpret_cast<const hw::Group*>(dbase + po.groups);

@@ -75,7 +75,17 @@ struct Group {
   int32_t unit_end;
 };
 
+// A plan goes up on the library's copy stream, followed by an 8-byte sequence number; a kernel
+// that reads the plan first checks that *plan_seq == plan_expect (spinning, bounded, while the
+// copy is still in flight), so the compute stream needs no wait on the copy stream.  plan_seq
+// is null when the plan was copied in stream order.
+struct PlanGate {
+  const unsigned long long* plan_seq;
+  unsigned long long plan_expect;
+};
+
 struct AppendArgs {
+  PlanGate gate;
   const AppendRun* runs;
   int32_t num_runs;
   int32_t max_run;
@@ -90,6 +100,7 @@ struct AppendArgs {
 };
 
 struct AttnArgs {
+  PlanGate gate;
   const Piece* pieces;
   const Unit* units;
   const Group* groups;
