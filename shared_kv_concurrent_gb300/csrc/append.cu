@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   HW_SPAN_BEGIN(0);
   __shared__ int plan_ok;
-  if (threadIdx.x == 0) plan_ok = plan_arrived(a.gate, a.err, KID_APPEND);
+  if (threadIdx.x == 0) plan_ok = plan_arrived(a.gate, plan_seq_now(a.gate), a.err, KID_APPEND);
   __syncthreads();
   if (!plan_ok) return;
   const AppendRun run = a.runs[blockIdx.y];

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
   float* ks = qs + rows * D;                    // [kTile][D + 1]
   float* vs = ks + kTile * KS;                  // [kTile][D]
   __shared__ int plan_ok;
-  if (threadIdx.x == 0) plan_ok = plan_arrived(a.gate, a.err, KID_ATTN_FMA);
+  if (threadIdx.x == 0) plan_ok = plan_arrived(a.gate, plan_seq_now(a.gate), a.err, KID_ATTN_FMA);
   __syncthreads();
   if (!plan_ok) return;
   const Unit u = a.units[blockIdx.x];

@@ -73,7 +73,7 @@ struct Cfg {
   static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 2 * kChunkRing;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kUnitOff = (kMiscOff + 8 + 15) / 16 * 16;   // the CTA's Unit
-  static constexpr uint32_t kChunkOff = kUnitOff + 32;         // int2[kChunkRing]
+  static constexpr uint32_t kChunkOff = kUnitOff + sizeof(Unit);   // int2[kChunkRing]
   static constexpr uint32_t kSmemBytes = kChunkOff + 8 * kChunkRing + 1024;  // + alignment slack
 };
 
@@ -357,9 +357,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Unit* u_smem = reinterpret_cast<Unit*>(smem + C::kUnitOff);
   const int R = a.rows;
+  const int64_t page_base0 = (int64_t)layer * a.num_pages;  // first page of this layer's pool
   int active_softmax_warps = 0;               // softmax warps that own at least one real row
   for (int q = 0; q < 4; ++q) active_softmax_warps += (32 * (q % WPC) < R) ? 1 : 0;
   if (threadIdx.x == 0) HW_TRACE_EV(0);
+
+  // Warps 2-7 start on the first query tile before set-up is done: a thread whose copy of the
+  // unit record already carries this plan's sequence number (first two vectors) rotates its
+  // items now; the others do after set-up, from the confirmed record (items are per thread, so
+  // the two ways mix freely).
+  bool pre_q = false;
+  if (warp >= 2) {
+    const int4* urec = reinterpret_cast<const int4*>(a.units + blockIdx.x);
+    const int4 h0 = __ldcg(urec), h1 = __ldcg(urec + 1);
+    const uint32_t want = a.gate.plan_seq ? (uint32_t)a.gate.plan_expect : 0u;
+    pdl_wait();                       // the queries may come from the kernel this grid follows
+    if ((uint32_t)h0.z == want && (uint32_t)h1.w == want && h0.w >= 0 && h0.w < a.num_seg_slots) {
+      const Group g0{h0.y / a.H_kv, h0.y % a.H_kv, 0, 0};
+      rotate_tile<D, T, kThreads - 64>(a, g0, h0.w, h1.z, smem + C::kQOff, threadIdx.x - 64);
+      pre_q = true;
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kSlots; ++s) {
@@ -380,22 +398,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_cfull0 + 8u * e, 1);
       mbar_init(bar_cempty0 + 8u * e, 1 + kRotThreads + 32 * active_softmax_warps);
     }
-    // The plan of this launch may still be on its way (copy stream): read the unit record
-    // only once its sequence number has arrived.
-    *abort = plan_arrived(a.gate, a.err, KID_ATTN_TC) ? 0 : 1;
-    Unit uu = a.units[blockIdx.x];
+    fence_mbar_init();
+    // The unit's first tile goes out at once when the first 16 bytes of its record already
+    // carry this plan's sequence number (one vector load: they are all of the current plan);
+    // the rest of the plan is read only once the plan's own sequence word has arrived (it
+    // follows the plan on the copy stream).
+    const int4* urec = reinterpret_cast<const int4*>(a.units + blockIdx.x);
+    int4 uv[3];                                     // (L2, not a stale L1 line)
+#pragma unroll
+    for (int k = 0; k < 3; ++k) uv[k] = __ldcg(urec + k);
+    const unsigned long long seq0 = plan_seq_now(a.gate);   // in flight with the record
+    const uint32_t want = a.gate.plan_seq ? (uint32_t)a.gate.plan_expect : 0u;
+    const int4 head = uv[0];
+    const bool current = (uint32_t)head.z == want;
+    int early = 0;
+    if (current && (uint32_t)uv[1].w == want) {
+      // The first query tile's inputs into L2 before the K/V loads start: the rotation warps
+      // read them right after set-up, and would otherwise queue behind every CTA's tiles.
+      const int p = head.y / a.H_kv, h = head.y % a.H_kv;
+      for (int w = 0; w < a.W; ++w)       // worker w's G query heads of this KV head
+        bulk_prefetch_l2(a.q + (((size_t)p * a.W + w) * a.H_q + (size_t)h * a.G) * D,
+                         (uint32_t)(a.G * D * 2));
+      const int d0 = uv[1].z;             // the first segment's rotation, if shared
+      if (d0 >= 0 && d0 < a.max_position) {
+        bulk_prefetch_l2(a.rope_cos + (size_t)d0 * (D / 2), D / 2 * 4);
+        bulk_prefetch_l2(a.rope_sin + (size_t)d0 * (D / 2), D / 2 * 4);
+      }
+    }
+    if (current && head.x >= 0) {
+      tma_prefetch(&maps.k);
+      tma_prefetch(&maps.v);
+      const int32_t y = (int32_t)(((page_base0 + head.x / a.S) * a.H_kv + head.y % a.H_kv) * a.S +
+                                  head.x % a.S);
+      mbar_arrive_expect_tx(bar_full(0), C::kTileBytes);
+      mbar_arrive_expect_tx(bar_full(1), C::kTileBytes);
+#pragma unroll
+      for (int h = 0; h < C::kHalves; ++h) {
+        tma_load_2d(sbase + C::kRingOff + h * C::kHalfBytes, &maps.k, 64 * h, y, bar_full(0),
+                    l2_policy_evict_first());
+        tma_load_2d(sbase + C::kRingOff + C::kTileBytes + h * C::kHalfBytes, &maps.v, 64 * h, y,
+                    bar_full(1), l2_policy_evict_first());
+      }
+      HW_TRACE_EV(8);
+      early = 1;
+    }
+    *abort = plan_arrived(a.gate, seq0, a.err, KID_ATTN_TC) ? 0 : 1;
+    // a vector read before the plan had landed is read again (the plan is complete now)
+    if ((uint32_t)uv[0].z != want) uv[0] = __ldcg(urec);
+    if ((uint32_t)uv[1].w != want) uv[1] = __ldcg(urec + 1);
+    if ((uint32_t)uv[2].z != want) uv[2] = __ldcg(urec + 2);
+    Unit uu;
+    static_assert(sizeof(Unit) == 48, "unit record: three 16-byte vectors");
+    int4* ud = reinterpret_cast<int4*>(&uu);
+    ud[0] = uv[0];
+    ud[1] = uv[1];
+    ud[2] = uv[2];
+    uu.flags = early;                   // tells the producer that tile 0 is on its way
     if (*abort) {                       // no plan: an empty unit (the error word says why)
       uu.piece_begin = uu.piece_end = 0;
       uu.seg0 = uu.first_tok = -1;
       uu.fresh_end = uu.fresh_begin;
     }
     *u_smem = uu;
-    fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch(&maps.k);
-    tma_prefetch(&maps.v);
-  }
+
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -409,17 +475,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Group g{u.group / a.H_kv, u.group % a.H_kv, 0, 0};
   if (threadIdx.x == 0) HW_TRACE_EV(1);
 
-  const int64_t page_base = (int64_t)layer * a.num_pages;   // first page of this layer's pool
+  const int64_t page_base = page_base0;
 
-  // The first query tile (segment slot u.seg0, known from the unit without a dependent load) is
-  // built by warps 2-7 together: the softmax warps have nothing to do before the first S.  The
-  // queries may come from the kernel this grid follows: wait for it first.
+  // The first query tile (segment slot u.seg0, known from the unit record without a dependent
+  // load), finished by warps 2-7 together (the softmax warps have nothing to do before the
+  // first S).
   const bool first_q = u.seg0 >= 0 && u.seg0 < a.num_seg_slots;
   const bool fused = a.k_raw != nullptr;      // this kernel writes the step's appended tokens
   if (warp >= 2) {
-    pdl_wait();
     if (first_q) {
-      rotate_tile<D, T, kThreads - 64>(a, g, u.seg0, u.delta0, smem + C::kQOff, threadIdx.x - 64);
+      if (!pre_q)
+        rotate_tile<D, T, kThreads - 64>(a, g, u.seg0, u.delta0, smem + C::kQOff, threadIdx.x - 64);
       fence_proxy_async_smem();           // generic-proxy writes -> operands of the MMA
       asm volatile("bar.sync 3, %0;" ::"r"(kThreads - 64) : "memory");
       if (threadIdx.x == 64) {
@@ -471,12 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      // The unit's first tile, known from the unit record (page * S + slot of a piece that
-      // holds no token of this step), goes out before anything else is read.
-      const bool early = u.first_tok >= 0;
-      if (early)
-        ok = issue_tile((int32_t)(((page_base + u.first_tok / a.S) * a.H_kv + g.h) * a.S +
-                                  u.first_tok % a.S));
+      // The unit's first tile may have gone out during set-up (see above): its two ring slots
+      // are then taken.
+      const bool early = u.flags != 0;
+      if (early) j = 2;
       auto load_range = [&](int32_t b, int32_t e) -> bool {
         for (int32_t pi = b; pi < e; ++pi) {
           if (early && pi == u.piece_begin) continue;  // issued above

@@ -289,11 +289,10 @@ struct hw_ctx {
     pend_k[layer] = pend_v[layer] = nullptr;
     return launch_append(layer, k, v, s);
   }
-  // Copy `bytes` of staging slot `slot` to its device copy on the copy stream, then the slot's
-  // new sequence number (*gate is set to check for it).  The slot's previous readers have
+  // Copy `bytes` of staging slot `slot` to its device copy on the copy stream, then the plan's
+  // sequence number `seq` (from next_seq(); *gate is set to check for it).  The slot's previous readers have
   // completed (acquire_slot), and the next ones check the number before reading.
-  hw_status upload_slot(int slot, size_t bytes, hw::PlanGate* gate) {
-    const uint64_t seq = ++g_upload_seq;
+  hw_status upload_slot(int slot, size_t bytes, uint64_t seq, hw::PlanGate* gate) {
     std::memcpy(h_slot(slot) + lay.slot_seq_off, &seq, sizeof(seq));
     HW_CUDA(cudaMemcpyAsync(d_slot(slot), h_slot(slot), bytes, cudaMemcpyHostToDevice, copy_stream));
     HW_CUDA(cudaMemcpyAsync(d_slot(slot) + lay.slot_seq_off, h_slot(slot) + lay.slot_seq_off,
@@ -302,6 +301,7 @@ struct hw_ctx {
     gate->plan_expect = seq;
     return HW_OK;
   }
+  static uint64_t next_seq() { return ++g_upload_seq; }
   // Pick the next staging slot; waits only if the slot's previous use is still in flight.
   hw_status acquire_slot(int* slot) {
     const int i = next_slot;
@@ -467,7 +467,7 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
 
 namespace {
 bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap,
-                          int64_t target_override, bool fuse);
+                          int64_t target_override, bool fuse, uint64_t seq);
 }  // namespace
 
 extern "C" {
@@ -576,19 +576,20 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
     // Small appends (decode) are written by the tensor-core attention kernel itself.
     bool fuse = c->use_tc;
     for (int32_t i = 0; i < P * B && fuse; ++i) fuse = n_new[i] <= kFuseTok;
+    const uint64_t seq = c->next_seq();
     bool plan_ok =
         plan_off < c->lay.slot_seq_off &&
         build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->use_tc ? c->num_sms : 0,
-                             fuse) &&
+                             fuse, seq) &&
         plan_off + po.bytes <= c->lay.slot_seq_off;
     if (!plan_ok && fuse) {
       fuse = false;
       plan_ok = plan_off < c->lay.slot_seq_off &&
                 build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0,
-                                     c->use_tc ? c->num_sms : 0, false) &&
+                                     c->use_tc ? c->num_sms : 0, false, seq) &&
                 plan_off + po.bytes <= c->lay.slot_seq_off;
     }
-    st = c->upload_slot(slot, plan_off + (plan_ok ? po.bytes : 0), &c->step_gate);
+    st = c->upload_slot(slot, plan_off + (plan_ok ? po.bytes : 0), seq, &c->step_gate);
     if (st != HW_OK) return st;
     c->step_slot = slot;
     c->step_runs = nr;
@@ -626,7 +627,7 @@ namespace {
 // segment's offset in w's view.
 // unit_cap > 0 bounds the number of units (one partial result each); 0 = the default split.
 bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0,
-                          int64_t target_override = 0, bool fuse = false) {
+                          int64_t target_override = 0, bool fuse = false, uint64_t seq = 0) {
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
   const int32_t S = c->cfg.page_size;
   const Layout& L = c->lay;
@@ -830,6 +831,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         u.group = g;
         u.seg0 = rg.second > rg.first ? ps.pieces[rg.first].seg_slot : -1;
         u.delta0 = -1;
+        u.seq = u.seq_b = u.seq_c = (uint32_t)seq;
         u.first_tok = -1;
         if (rg.second > rg.first && !ps.pieces[rg.first].fresh)
           u.first_tok = ps.pieces[rg.first].page * S + ps.pieces[rg.first].slot0;
@@ -918,10 +920,11 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
     if (st != HW_OK) return st;
     // Tensor-core kernel: one CTA per SM holds all of its shared memory and TMEM, so one unit
     // per SM, balanced by KV entries.
-    if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0))
+    const uint64_t seq = c->next_seq();
+    if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0, false, seq))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
-    st = c->upload_slot(slot, po.bytes, &gate);
+    st = c->upload_slot(slot, po.bytes, seq, &gate);
     if (st != HW_OK) return st;
   }
   hw::AttnArgs a{};

@@ -18,14 +18,21 @@ __device__ __forceinline__ void record_error(uint32_t* err, uint32_t bits, uint3
   }
 }
 
-// Wait (one thread) until the plan behind `g` has arrived; false, with ERR_TIMEOUT recorded,
-// if it has not after about a second.
-__device__ __forceinline__ bool plan_arrived(const PlanGate& g, uint32_t* err, uint32_t kid) {
+__device__ __forceinline__ unsigned long long plan_seq_now(const PlanGate& g) {
+  unsigned long long v = 0;
+  if (g.plan_seq)
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(g.plan_seq) : "memory");
+  return v;
+}
+
+// Wait (one thread) until the plan behind `g` has arrived, given a first reading `v` of its
+// sequence word; false, with ERR_TIMEOUT recorded, if it has not after about a second.
+__device__ __forceinline__ bool plan_arrived(const PlanGate& g, unsigned long long v, uint32_t* err,
+                                             uint32_t kid) {
   if (!g.plan_seq) return true;
   unsigned long long t0 = 0, t = 0;
   for (int it = 0;; ++it) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(g.plan_seq) : "memory");
+    if (it > 0) v = plan_seq_now(g);
     if (v == g.plan_expect) return true;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     if (it == 0) t0 = t;

@@ -57,14 +57,21 @@ struct FreshTok {
 __host__ __device__ constexpr int part_stride(int D) { return D + 4; }
 
 // A unit: consecutive pieces of one (problem, KV head) group, one CTA, one partial result.
-struct Unit {
+// Read as three 16-byte vectors, possibly before the plan's arrival is confirmed: each vector
+// carries the low 32 bits of the plan's sequence number (seq, seq_b, seq_c; 0 when the plan is
+// not gated), and a vector whose copy matches belongs to the current plan.
+struct __align__(16) Unit {
+  int32_t first_tok;  // page * S + slot of the first piece if it holds no new token, else -1
+  int32_t group;      // p * H_kv + h
+  uint32_t seq;
+  int32_t seg0;       // seg_slot of the first piece, -1 if the unit has none
   int32_t piece_begin;
   int32_t piece_end;
-  int32_t group;     // p * H_kv + h
-  int32_t seg0;      // seg_slot of the first piece, -1 if the unit has none
-  int32_t delta0;    // the rotation of seg0 if it is the same for every worker, else -1
+  int32_t delta0;     // the rotation of seg0 if it is the same for every worker, else -1
+  uint32_t seq_b;
   int32_t fresh_begin, fresh_end;  // appended tokens it writes, in the FreshTok table
-  int32_t first_tok;  // page * S + slot of the first piece if it holds no new token, else -1
+  uint32_t seq_c;
+  int32_t flags;      // kernel-side use
 };
 
 // A group: one (problem, KV head); its units are [unit_begin, unit_end).
