@@ -7,7 +7,7 @@ Hogwild! inference flow (gentlecold.top summary, section 8).
 """
 from __future__ import annotations
 
-from typing import Optional
+from typing import Optional, Sequence
 
 import numpy as np
 
@@ -26,22 +26,29 @@ def new_cache(w: wl.Workload, layers: Optional[int] = None) -> HogwildCache:
                         contiguous=w.contiguous, page_order=w.page_order())
 
 
-def prefill(w: wl.Workload, layers: Optional[int] = None) -> HogwildCache:
-    """Cache holding the workload's pre-step blocks (layer l uses the layer-l draws)."""
-    c = new_cache(w, layers)
+def prefill(w: wl.Workload, layers: Optional[int] = None,
+            layer_ids: Optional[Sequence[int]] = None) -> HogwildCache:
+    """Cache holding the workload's pre-step blocks (layer l uses the layer-l draws).
+
+    ``layer_ids``: keep only these workload layers (cache layer i holds workload layer
+    layer_ids[i]) -- the tables do not depend on the layer, so a few layers pin a deep model."""
+    ids = list(layer_ids) if layer_ids is not None else list(range(layers or w.num_layers))
+    c = new_cache(w, len(ids))
     n = wl.prefill_block_lengths(w)
-    for layer in range(c.L):
+    for i, layer in enumerate(ids):
         k, v = wl.prefill_kv(w, layer)
-        c.append(layer, n, bf16(k), bf16(v))
+        c.append(i, n, bf16(k), bf16(v))
     c.step_end(np.zeros((w.num_problems, w.num_workers), np.uint8))
     return c
 
 
-def append_step(c: HogwildCache, w: wl.Workload, step: int) -> None:
+def append_step(c: HogwildCache, w: wl.Workload, step: int,
+                layer_ids: Optional[Sequence[int]] = None) -> None:
     n = wl.step_n_new(w)
-    for layer in range(c.L):
+    ids = list(layer_ids) if layer_ids is not None else list(range(c.L))
+    for i, layer in enumerate(ids):
         k, v = wl.step_kv(w, layer, step)
-        c.append(layer, n, bf16(k), bf16(v))
+        c.append(i, n, bf16(k), bf16(v))
 
 
 def query(w: wl.Workload, layer: int, step: int) -> np.ndarray:

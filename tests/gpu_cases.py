@@ -31,11 +31,13 @@ def dev_tables_equal(runner, cache):
             assert giq == iq and [tuple(x) for x in ge] == [tuple(x) for x in e]
 
 
-def check_pools(runner, cache, layer, max_tokens_per_seg=None):
+def check_pools(runner, cache, layer, max_tokens_per_seg=None, dev_layer=None):
     """Stored keys within 1 bf16 ulp of the fp64 rotation; values bit-exact; at the oracle's
-    (page, slot) of every token -- so page addressing is checked bit-exactly too."""
+    (page, slot) of every token -- so page addressing is checked bit-exactly too.
+
+    ``layer`` indexes the oracle cache, ``dev_layer`` (default: the same) the library's."""
     import torch
-    kp, vp = runner.cache.pools(layer)
+    kp, vp = runner.cache.pools(layer if dev_layer is None else dev_layer)
     kb = kp.view(torch.int16).cpu().numpy().view(np.uint16)
     vb = vp.view(torch.int16).cpu().numpy().view(np.uint16)
     for sid, seg in enumerate(cache.segments):
@@ -69,12 +71,19 @@ def check_pools(runner, cache, layer, max_tokens_per_seg=None):
 
 
 def run_case(w: wl.Workload, steps: int, out_dtype="f32", bernoulli=None, pools=True,
-             pool_sample=None, tol=TOL):
+             pool_sample=None, tol=TOL, layer_ids=None, check_steps=None):
+    """Run ``steps`` decode steps on both sides; compare tables after every step end.
+
+    ``layer_ids``: the workload layers the oracle computes (default all); the library always
+    runs every layer.  ``check_steps``: the steps whose outputs (and pools) are compared
+    (default all) -- the oracle still appends every step, so later steps see the same cache.
+    """
     import torch
     from shared_kv_concurrent_gb300 import binding
     from shared_kv_concurrent_gb300.runner import WorkloadRunner
     r = WorkloadRunner(w)
-    c = orun.prefill(w)
+    ids = list(range(w.num_layers)) if layer_ids is None else list(layer_ids)
+    c = orun.prefill(w, layer_ids=ids)
     dev_tables_equal(r, c)
     worst = 0.0
     P, W, Hq, D = w.num_problems, w.num_workers, w.num_q_heads, w.head_dim
@@ -82,25 +91,26 @@ def run_case(w: wl.Workload, steps: int, out_dtype="f32", bernoulli=None, pools=
     for step in range(steps):
         inputs = r.step_inputs(step)
         r.append(inputs)
-        orun.append_step(c, w, step)
+        orun.append_step(c, w, step, layer_ids=ids)
         outs = [torch.full((P, W, Hq, D), float("nan"), dtype=dt, device="cuda")
                 for _ in range(w.num_layers)]
         lses = [torch.full((P, W, Hq), float("nan"), dtype=torch.float32, device="cuda")
                 for _ in range(w.num_layers)]
         r.attend(inputs, outs, lses, out_dtype)
         torch.cuda.synchronize()
-        for layer in range(w.num_layers):
-            ref, ref_lse = A.method(c, layer, orun.query(w, layer, step))
-            got = outs[layer].float().cpu().numpy()
-            err = np.abs(got - ref).max()
-            worst = max(worst, float(err))
-            assert err <= tol, (step, layer, err)
-            gl = lses[layer].cpu().numpy()
-            fin = np.isfinite(ref_lse)
-            assert np.array_equal(np.isfinite(gl), fin)
-            assert np.abs(gl[fin] - ref_lse[fin]).max() <= tol
-            if pools:
-                check_pools(r, c, layer, pool_sample)
+        if check_steps is None or step in check_steps:
+            for i, layer in enumerate(ids):
+                ref, ref_lse = A.method(c, i, orun.query(w, layer, step))
+                got = outs[layer].float().cpu().numpy()
+                err = np.abs(got - ref).max()
+                worst = max(worst, float(err))
+                assert err <= tol, (step, layer, err)
+                gl = lses[layer].cpu().numpy()
+                fin = np.isfinite(ref_lse)
+                assert np.array_equal(np.isfinite(gl), fin)
+                assert np.abs(gl[fin] - ref_lse[fin]).max() <= tol
+                if pools:
+                    check_pools(r, c, i, pool_sample, dev_layer=layer)
         fin = wl.finished_mask(w, step, bernoulli)
         r.end(step, fin)
         c.step_end(fin)

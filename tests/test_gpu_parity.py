@@ -96,6 +96,22 @@ def test_full_size_w8_common32768():
     G.run_case(w, steps=1, pool_sample=64)
 
 
+def test_full_size_w4_common16384_64_layers():
+    """All 64 layers run on the device; the oracle computes the first two and the last layer
+    (the tables are shared by every layer, the pools are not)."""
+    import gpu_cases as G
+    G.run_case(wl.c3(), steps=2, layer_ids=(0, 1, 63), pool_sample=64)
+
+
+def test_full_size_16_problems_200_steps_with_commits():
+    """Every step and every commit (after steps 63, 127, 191) runs on the device, the tables are
+    compared after each step end, the outputs on both sides of each commit and at the ends."""
+    import gpu_cases as G
+    w = wl.c5()
+    G.run_case(w, steps=w.steps, check_steps={0, 63, 64, 127, 128, 191, 192, 199},
+               pool_sample=64)
+
+
 def test_empty_view_gives_zero_and_minus_inf():
     import torch
     from shared_kv_concurrent_gb300 import HogwildCache
