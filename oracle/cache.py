@@ -29,6 +29,22 @@ Readings where the pages are silent (each is also listed in the design notes):
 * Segment ids count up in creation order: per problem the prompt segment then workers
   0 .. W-1 at creation; then each fresh block started by a commit, in commit order.
 
+Cache layouts (section 6 compares three; section 10 adds the no-sync baseline of its
+collaboration scores).  The blocks, commits and pages are the same in all of them; only the
+order and the membership of a worker's view change:
+
+* ``combined`` (token-wise, the main method): common history, then the other workers' current
+  blocks, then the own current block -- as above.
+* ``step_wise`` (interleaved): only finished steps are shared -- the common history, then the
+  own current block; other workers' unfinished blocks are not visible.
+* ``contiguous``: each worker's output is one contiguous run -- the prompt, then every other
+  worker's whole output (its committed paragraphs in commit order, then its current block),
+  in ascending id, then the worker's own whole output.
+* ``no_sync``: workers generate independently -- the prompt, the worker's own committed
+  paragraphs in commit order, then its own current block.
+In ``contiguous`` and ``no_sync`` a committed paragraph belongs to the worker that wrote it
+(its segment's origin); tokens appended to the last common segment belong to that segment.
+
 The stored keys are the raw keys rotated to their block-local positions in fp64
 (``rope(k, j)``); the brute-force attention uses the raw keys instead.
 """
@@ -99,10 +115,17 @@ class Segment:
         return self._get("ks", layer)
 
 
+LAYOUTS = ("combined", "step_wise", "contiguous", "no_sync")
+
+
 class HogwildCache:
     def __init__(self, num_problems: int, num_workers: int, num_layers: int, num_kv_heads: int,
                  head_dim: int, rope_theta: float, page_size: int, num_pages: int,
-                 contiguous: bool = False, page_order: Optional[Sequence[int]] = None):
+                 contiguous: bool = False, page_order: Optional[Sequence[int]] = None,
+                 layout: str = "combined"):
+        if layout not in LAYOUTS:
+            raise InvalidArg("unknown cache layout")
+        self.layout = layout
         self.P, self.W, self.L = num_problems, num_workers, num_layers
         self.H_kv, self.D, self.theta = num_kv_heads, head_dim, float(rope_theta)
         self.S, self.contiguous = page_size, bool(contiguous)
@@ -131,12 +154,25 @@ class HogwildCache:
     def view(self, p: int, w: int) -> Tuple[List[Tuple[int, int, int]], int]:
         """Worker w's view: [(segment id, view offset, visible length)], and i_q.
 
-        Order: common segments in commit order, other workers' current blocks in ascending
-        id, own block last; empty segments are skipped.  i_q = view length - 1 (the query is
-        the last token of the worker's own block once this step's token is appended).
+        Order (combined layout): common segments in commit order, other workers' current
+        blocks in ascending id, own block last; the other layouts are listed in the module
+        docstring.  Empty segments are skipped.  i_q = view length - 1 (the query is the last
+        token of the worker's own block once this step's token is appended).
         """
-        order = list(self.common[p]) + [self.live[p][u] for u in range(self.W) if u != w] + \
-            [self.live[p][w]]
+        common, live = self.common[p], self.live[p]
+        others = [u for u in range(self.W) if u != w]
+        if self.layout == "combined":
+            order = list(common) + [live[u] for u in others] + [live[w]]
+        elif self.layout == "step_wise":
+            order = list(common) + [live[w]]
+        else:
+            def output(u):          # worker u's committed paragraphs, then its current block
+                return [s for s in common if self.segments[s].origin == u] + [live[u]]
+            order = [s for s in common if self.segments[s].origin == -1]
+            if self.layout == "contiguous":
+                for u in others:
+                    order += output(u)
+            order += output(w)
         entries, off = [], 0
         for sid in order:
             n = self.segments[sid].visible

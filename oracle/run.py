@@ -23,7 +23,7 @@ def bf16(bits: np.ndarray) -> np.ndarray:
 def new_cache(w: wl.Workload, layers: Optional[int] = None) -> HogwildCache:
     return HogwildCache(w.num_problems, w.num_workers, layers or w.num_layers, w.num_kv_heads,
                         w.head_dim, w.rope_theta, w.page_size, w.num_pages(),
-                        contiguous=w.contiguous, page_order=w.page_order())
+                        contiguous=w.contiguous, page_order=w.page_order(), layout=w.layout)
 
 
 def prefill(w: wl.Workload, layers: Optional[int] = None,

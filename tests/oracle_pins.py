@@ -312,11 +312,87 @@ def check_relabel_two_workers():
     assert np.allclose(o1[0, 0], o2[0, 1], atol=1e-13) and np.allclose(o1[0, 1], o2[0, 0], atol=1e-13)
 
 
+# ------------------------------------------------------------------------- cache layouts
+
+
+def _layout_scenario(layout, D=2, H_kv=1, seed=None):
+    """The hand-worked scenario of views_layouts_w3.json: prompt 4, A 2, B 1, C 3; A commits;
+    then one token for every worker.  Returns the cache and the block -> segment id names."""
+    g = np.random.default_rng(seed)
+    draw = (lambda n: g.standard_normal((n, H_kv, D))) if seed is not None else \
+        (lambda n: np.ones((n, H_kv, D)))
+    c = C.HogwildCache(1, 3, 1, H_kv, D, 1e4, 4, 64, layout=layout)
+    c.append(0, [[4, 2, 1, 3]], draw(10), draw(10))
+    c.step_end([[1, 0, 0]])
+    c.append(0, [[0, 1, 1, 1]], draw(3), draw(3))
+    names = {c.common[0][0]: "P", c.common[0][1]: "A1", c.live[0][0]: "A2", c.live[0][1]: "B",
+             c.live[0][2]: "C"}
+    return c, names
+
+
+def check_layout_views_golden():
+    with open(os.path.join(GOLDEN, "views_layouts_w3.json")) as f:
+        gl = json.load(f)
+    for layout, views in gl["views"].items():
+        c, names = _layout_scenario(layout)
+        for w, who in enumerate("ABC"):
+            entries, i_q = c.view(0, w)
+            got = [[names[sid], off] for sid, off, n in entries]
+            assert got == views[who], (layout, who, got)
+            assert [n for _, _, n in entries] == [gl["lengths"][b] for b, _ in views[who]]
+            assert i_q == gl["i_q"][layout][who], (layout, who, i_q)
+
+
+def check_layouts_textbook_attention():
+    """Every layout: the method equals textbook RoPE attention over the golden's block order
+    (raw keys laid out at positions 0 .. n-1, rotated by the complex form, query at i_q)."""
+    with open(os.path.join(GOLDEN, "views_layouts_w3.json")) as f:
+        gl = json.load(f)
+    D, H_kv, G, theta = 8, 2, 2, 1e4
+    q = np.random.default_rng(31).standard_normal((1, 3, H_kv * G, D))
+    for layout, views in gl["views"].items():
+        c, names = _layout_scenario(layout, D=D, H_kv=H_kv, seed=30)
+        by_name = {v: k for k, v in names.items()}
+        out, lse = A.method(c, 0, q)
+        for w, who in enumerate("ABC"):
+            blocks = [b for b, _ in views[who]]
+            kr = np.concatenate([c.segments[by_name[b]].raw_k(0) for b in blocks])
+            vr = np.concatenate([c.segments[by_name[b]].raw_v(0) for b in blocks])
+            n = kr.shape[0]
+            k = rope_complex(kr, np.arange(n)[:, None], theta)
+            qr = rope_complex(q[0, w], gl["i_q"][layout][who], theta)
+            for h in range(H_kv * G):
+                sc = k[:, h // G, :] @ qr[h] / math.sqrt(D)
+                e = np.exp(sc - sc.max())
+                ref = e @ vr[:, h // G, :] / e.sum()
+                assert np.allclose(out[0, w, h], ref, atol=1e-12), (layout, who, h)
+                assert abs(lse[0, w, h] - (sc.max() + math.log(e.sum()))) < 1e-12
+
+
+def check_layouts_coincide_without_commits():
+    """With no commit yet, the prompt is the whole common history: contiguous equals combined
+    and no-sync equals step-wise (section 6: the layouts differ only in how finished and
+    unfinished steps are shared)."""
+    g = np.random.default_rng(32)
+    k, v = g.standard_normal((14, 1, 8)), g.standard_normal((14, 1, 8))
+    caches = {}
+    for layout in C.LAYOUTS:
+        c = C.HogwildCache(1, 3, 1, 1, 8, 1e4, 4, 64, layout=layout)
+        c.append(0, [[5, 3, 4, 2]], k, v)
+        caches[layout] = c
+    for w in range(3):
+        assert caches["contiguous"].view(0, w) == caches["combined"].view(0, w)
+        assert caches["no_sync"].view(0, w) == caches["step_wise"].view(0, w)
+        assert [s for s, _, _ in caches["step_wise"].view(0, w)[0]] == \
+            [caches["step_wise"].common[0][0], caches["step_wise"].live[0][w]]
+
+
 ALL_CHECKS = [
     check_rope_complex_form, check_rope_d2_textbook, check_inv_freq_values, check_rope_invariants,
     check_views_golden, check_view_offsets_and_query_position, check_pages_hand_example,
     check_simultaneous_commits_in_ascending_id,
     check_two_worker_hand, check_brute_vs_method, check_zero_keys_give_mean_values,
     check_single_token_returns_its_value, check_single_worker_is_textbook_decode,
-    check_relabel_two_workers,
+    check_relabel_two_workers, check_layout_views_golden, check_layouts_textbook_attention,
+    check_layouts_coincide_without_commits,
 ]

@@ -104,6 +104,40 @@ def _step_end_commit_descending(self, finished):
                 self.live[p][w] = self._new_segment(p, w)
 
 
+def _view_layout_ignored(self, p, w):
+    saved = self.layout
+    self.layout = "combined"
+    try:
+        return _orig_view(self, p, w)
+    finally:
+        self.layout = saved
+
+
+def _view_step_wise_shows_others(self, p, w):
+    saved = self.layout
+    if saved == "step_wise":
+        self.layout = "combined"
+    try:
+        return _orig_view(self, p, w)
+    finally:
+        self.layout = saved
+
+
+def _view_contiguous_own_first(self, p, w):
+    entries, i_q = _orig_view(self, p, w)
+    if self.layout != "contiguous" or len(entries) < 3:
+        return entries, i_q
+    own = [e for e in entries if self.segments[e[0]].origin == w]
+    rest = [e for e in entries if self.segments[e[0]].origin != w]
+    out, off = [], 0
+    for sid, _, n in rest[:1] + own + rest[1:]:
+        out.append((sid, off, n))
+        off += n
+    return out, i_q
+
+
+_orig_view = C.HogwildCache.view
+
 MUTATIONS = {
     "rope_rotates_backwards": [(R, "rope", _rope_sign_flip), (A, "rope", _rope_sign_flip),
                                (C, "rope", _rope_sign_flip)],
@@ -119,6 +153,9 @@ MUTATIONS = {
     "merge_forgets_rescale": [(A, "lse_merge", _merge_drop_rescale)],
     "pages_popped_lifo": [(C.HogwildCache, "_allocate", _allocate_lifo)],
     "commits_in_descending_id": [(C.HogwildCache, "step_end", _step_end_commit_descending)],
+    "layout_ignored": [(C.HogwildCache, "view", _view_layout_ignored)],
+    "step_wise_shows_others": [(C.HogwildCache, "view", _view_step_wise_shows_others)],
+    "contiguous_own_output_first": [(C.HogwildCache, "view", _view_contiguous_own_first)],
 }
 
 

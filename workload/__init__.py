@@ -58,6 +58,7 @@ class Workload:
     worker_len: Tuple[Tuple[int, ...], ...]
     steps: int = 1          # decode steps the workload runs
     commit_steps: Tuple[int, ...] = ()  # steps after which every worker commits its block
+    layout: str = "combined"            # cache layout: combined, step_wise, contiguous, no_sync
 
     @property
     def group(self) -> int:
