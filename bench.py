@@ -64,9 +64,15 @@ def captured_traffic():
         return None
 
 
-def workload_for(name):
+def workload_for(name, layout="combined"):
+    """The named workload; another cache layout changes only the views (and the name)."""
+    import dataclasses
+
     import workload as wl
-    return wl.CONFIGS[name]()
+    w = wl.CONFIGS[name]()
+    if layout != "combined":
+        w = dataclasses.replace(w, layout=layout, name=f"{w.name}_{layout}")
+    return w
 
 
 def step_bytes(w, step, out_bytes=2):
@@ -168,7 +174,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    w = workload_for(args.config)
+    w = workload_for(args.config, args.layout)
     per_step, n, threads = oracle_sample(w, seconds=max(10.0, 3.0 * args.steps), max_steps=None)
     b, _ = step_bytes(w, 0)
     v = b / per_step / 1e9
@@ -203,7 +209,7 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    base = workload_for(args.config)
+    base = workload_for(args.config, args.layout)
     e2e_steps = args.e2e_steps
     kv_mb = base.num_layers * base.view_tokens(0) * base.num_kv_heads * base.head_dim * 4 / 1e6
     layer_mb = kv_mb / base.num_layers                     # K/V of one layer of one cache
@@ -384,7 +390,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "problems": P, "workers": W, "layers": L, "H_q": Hq,
+        "config": {"workload": w.name, "layout": w.layout, "problems": P, "workers": W,
+                   "layers": L, "H_q": Hq,
                    "H_kv": w.num_kv_heads, "head_dim": D, "page_size": w.page_size,
                    "common_tokens": list(w.common_len), "view_tokens_first_timed_step":
                    w.view_tokens(timed[0][1]), "parallelism": f"replicas{world}",
@@ -424,6 +431,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="c4")
+    ap.add_argument("--layout", default="combined",
+                    choices=["combined", "step_wise", "contiguous", "no_sync"],
+                    help="cache layout of the workload (the default is the method's own)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--caches", type=int, default=0,
                     help="independent caches of the workload used in turn (0: enough that the "

@@ -55,6 +55,23 @@ typedef enum hw_status {
 
 enum { HW_OUT_BF16 = 0, HW_OUT_F32 = 1 };
 
+/*
+ * Cache layouts (summary section 6 compares the first three; section 10 adds the no-sync
+ * setting): which blocks a worker's view holds, and in what order.  Blocks, commits and pages
+ * are the same in every layout; only the views -- and so the query rotations -- differ.
+ */
+enum {
+  HW_LAYOUT_COMBINED = 0,   /* token-wise (the main method): common history in commit order,
+                               the other workers' current blocks in ascending id, own block */
+  HW_LAYOUT_STEP_WISE = 1,  /* interleaved: common history, own block; the other workers'
+                               unfinished blocks are not visible */
+  HW_LAYOUT_CONTIGUOUS = 2, /* each worker's output is one run: the prompt, every other
+                               worker's committed paragraphs then current block (ascending id),
+                               then the worker's own paragraphs and block */
+  HW_LAYOUT_NO_SYNC = 3     /* independent workers: the prompt, own committed paragraphs, own
+                               block */
+};
+
 typedef struct hw_config {
   int32_t num_problems;      /* P >= 1 independent Hogwild! problems */
   int32_t num_workers;       /* W >= 1 workers per problem */
@@ -69,6 +86,11 @@ typedef struct hw_config {
   int32_t max_segments;      /* segment capacity over all problems (0: P * (1 + 4W)) */
   int32_t max_append_tokens; /* largest sum of n_new in one append (0: num_pages * S) */
   double rope_theta;         /* RoPE base */
+  int32_t layout;            /* HW_LAYOUT_* (0: combined).  In the contiguous and no-sync
+                                layouts a committed paragraph belongs to the worker that wrote
+                                it, and tokens appended to the last common segment belong to
+                                that segment's writer (the prompt's when nothing is committed) */
+  int32_t reserved;          /* 0 */
 } hw_config;
 
 typedef struct hw_ctx hw_ctx;

@@ -14,15 +14,18 @@ import numpy as np
 from . import binding
 from .binding import (HW_OUT_BF16, HW_OUT_F32, HogwildError, hw_config)
 
-__all__ = ["HogwildCache", "HogwildError", "binding", "config_for"]
+__all__ = ["HogwildCache", "HogwildError", "LAYOUTS", "binding", "config_for"]
+
+
+LAYOUTS = {"combined": 0, "step_wise": 1, "contiguous": 2, "no_sync": 3}   # HW_LAYOUT_*
 
 
 def config_for(*, num_problems, num_workers, num_layers, num_q_heads, num_kv_heads, head_dim,
                page_size, num_pages, max_position, rope_theta, contiguous=False,
-               max_segments=0, max_append_tokens=0) -> hw_config:
+               max_segments=0, max_append_tokens=0, layout="combined") -> hw_config:
     return hw_config(num_problems, num_workers, num_layers, num_q_heads, num_kv_heads, head_dim,
                      page_size, int(bool(contiguous)), num_pages, max_position, max_segments,
-                     max_append_tokens, float(rope_theta))
+                     max_append_tokens, float(rope_theta), LAYOUTS[layout], 0)
 
 
 class HogwildCache:
@@ -46,7 +49,8 @@ class HogwildCache:
                          num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
                          page_size=w.page_size, num_pages=w.num_pages(),
                          max_position=w.max_position(), rope_theta=w.rope_theta,
-                         contiguous=w.contiguous, max_segments=max_segments)
+                         contiguous=w.contiguous, max_segments=max_segments,
+                         layout=getattr(w, "layout", "combined"))
         return cls(cfg, page_order=w.page_order(), device=device)
 
     # -- the step protocol ---------------------------------------------------------------

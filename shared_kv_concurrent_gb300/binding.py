@@ -44,7 +44,7 @@ class hw_config(ctypes.Structure):
         ("page_size", ctypes.c_int32), ("contiguous", ctypes.c_int32),
         ("num_pages", ctypes.c_int32), ("max_position", ctypes.c_int32),
         ("max_segments", ctypes.c_int32), ("max_append_tokens", ctypes.c_int32),
-        ("rope_theta", ctypes.c_double),
+        ("rope_theta", ctypes.c_double), ("layout", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 

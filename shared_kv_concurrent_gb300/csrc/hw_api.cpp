@@ -73,6 +73,8 @@ bool valid_config(const hw_config* c) {
   if (c->num_pages < 1 || c->max_position < 1) return false;
   if (c->max_segments < 0 || c->max_append_tokens < 0) return false;
   if (!(c->rope_theta > 1.0) || !std::isfinite(c->rope_theta)) return false;
+  if (c->layout < HW_LAYOUT_COMBINED || c->layout > HW_LAYOUT_NO_SYNC || c->reserved != 0)
+    return false;
   const int64_t rows = (int64_t)c->num_workers * (c->num_q_heads / c->num_kv_heads);
   if (rows > 128) return false;
   const int64_t pool_tokens = (int64_t)c->num_pages * c->page_size;
@@ -140,7 +142,8 @@ struct PlanScratch {
   std::vector<hw::Unit> units;
   std::vector<hw::Group> groups;
   std::vector<hw::FreshTok> fresh;
-  std::vector<int32_t> delta, refs, live_len, live_ref, piece_fresh0, src_base;
+  std::vector<int32_t> delta, refs, piece_fresh0, src_base, ref_of, view_ref;
+  std::vector<int64_t> view_off;
   std::vector<int32_t> ref_sid, ref_slot, ref_tiles, prob_ref_begin, prob_common_refs, unit_rem,
       order;
   std::vector<int64_t> prob_tiles;
@@ -234,22 +237,53 @@ struct hw_ctx {
     return segs[b == 0 ? common[p].back() : live[p][b - 1]];
   }
   // Worker w's view: (segment, offset, visible length); returns i_q.
-  int32_t view(int32_t p, int32_t w, std::vector<int32_t>* ids, std::vector<int32_t>* offs,
-               std::vector<int32_t>* lens) const {
-    int32_t off = 0;
+  // Worker w's view in the context's layout (summary section 6; section 10 for no-sync): calls
+  // f(segment, view offset, visible length) for each non-empty segment in view order and
+  // returns the view length (i_q + 1).  A committed paragraph's writer is its segment origin.
+  template <class F>
+  int64_t for_each_view(int32_t p, int32_t w, F&& f) const {
+    int64_t off = 0;
     auto add = [&](int32_t sid) {
       const int32_t n = segs[sid].visible();
       if (n == 0) return;
-      ids->push_back(sid);
-      offs->push_back(off);
-      lens->push_back(n);
+      f(sid, off, n);
       off += n;
     };
-    for (int32_t sid : common[p]) add(sid);
-    for (int32_t u = 0; u < cfg.num_workers; ++u)
-      if (u != w) add(live[p][u]);
-    add(live[p][w]);
-    return off - 1;
+    auto output = [&](int32_t u) {        // worker u's paragraphs, then its current block
+      for (int32_t sid : common[p])
+        if (segs[sid].origin == u) add(sid);
+      add(live[p][u]);
+    };
+    switch (cfg.layout) {
+      case HW_LAYOUT_STEP_WISE:
+        for (int32_t sid : common[p]) add(sid);
+        add(live[p][w]);
+        break;
+      case HW_LAYOUT_CONTIGUOUS:
+      case HW_LAYOUT_NO_SYNC:
+        for (int32_t sid : common[p])
+          if (segs[sid].origin < 0) add(sid);
+        if (cfg.layout == HW_LAYOUT_CONTIGUOUS)
+          for (int32_t u = 0; u < cfg.num_workers; ++u)
+            if (u != w) output(u);
+        output(w);
+        break;
+      default:                            // HW_LAYOUT_COMBINED
+        for (int32_t sid : common[p]) add(sid);
+        for (int32_t u = 0; u < cfg.num_workers; ++u)
+          if (u != w) add(live[p][u]);
+        add(live[p][w]);
+    }
+    return off;
+  }
+  int32_t view(int32_t p, int32_t w, std::vector<int32_t>* ids, std::vector<int32_t>* offs,
+               std::vector<int32_t>* lens) const {
+    const int64_t total = for_each_view(p, w, [&](int32_t sid, int64_t off, int32_t n) {
+      ids->push_back(sid);
+      offs->push_back((int32_t)off);
+      lens->push_back(n);
+    });
+    return (int32_t)(total - 1);
   }
   // Launch the append kernel of `layer` for the step's runs (uploaded with the step's plan).
   hw_status launch_append(int32_t layer, const void* k_raw, const void* v_raw, cudaStream_t s) {
@@ -621,10 +655,10 @@ namespace {
 // Returns false if a table would overflow.  Offsets of each array are written to `po`.
 //
 // The pieces of a problem are listed once and shared by its KV heads: the units of group
-// (p, h) index the problem's piece list, and the head comes from the group.  Every worker's
-// view holds the same segments (common part, then the live blocks in the worker's order), so
-// i_q is the problem's visible length - 1 and a segment's delta for worker w is i_q minus the
-// segment's offset in w's view.
+// (p, h) index the problem's piece list, and the head comes from the group.  A segment's
+// delta for worker w is i_q(w) minus the segment's offset in w's view (in the context's
+// layout), or -1 when w's view does not hold it; in the combined layout every view holds every
+// segment and i_q is the problem's visible length - 1.
 // unit_cap > 0 bounds the number of units (one partial result each); 0 = the default split.
 bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0,
                           int64_t target_override = 0, bool fuse = false, uint64_t seq = 0) {
@@ -659,58 +693,36 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         run += n;
       }
   }
-  // Pass 1, per problem: the visible segments (common part in commit order, then the live
-  // blocks by worker), their rotation table and their tile counts.
+  // Pass 1, per problem: the non-empty segments (common part in commit order, then the live
+  // blocks by worker), their rotation table and their tile counts.  A segment is streamed once
+  // for every row of its problem; the table says which rows see it, and at what rotation.
+  if (ps.ref_of.size() < c->segs.size()) ps.ref_of.resize(c->segs.size(), -1);
   for (int32_t p = 0; p < P; ++p) {
     ps.prob_ref_begin[p] = (int32_t)ps.ref_sid.size();
     ps.refs.clear();
-    int64_t common_len = 0;
-    for (int32_t sid : c->common[p]) {
-      const int32_t n = c->segs[sid].visible();
-      if (n > 0) {
-        ps.refs.push_back(sid);
-        common_len += n;
-      }
-    }
+    for (int32_t sid : c->common[p])
+      if (c->segs[sid].visible() > 0) ps.refs.push_back(sid);
     const int32_t n_common_refs = (int32_t)ps.refs.size();
-    ps.live_len.assign(W, 0);
-    ps.live_ref.assign(W, -1);
-    int64_t total = common_len;
     for (int32_t w = 0; w < W; ++w) {
       const int32_t sid = c->live[p][w];
-      const int32_t n = c->segs[sid].visible();
-      ps.live_len[w] = n;
-      total += n;
-      if (n > 0) {
-        ps.live_ref[w] = (int32_t)ps.refs.size();
-        ps.refs.push_back(sid);
-      }
+      if (c->segs[sid].visible() > 0) ps.refs.push_back(sid);
     }
     const int32_t slot_base = (int32_t)(ps.delta.size() / (size_t)W);
     if (slot_base + (int64_t)ps.refs.size() > L.max_seg_slots) return false;
     ps.delta.resize(ps.delta.size() + ps.refs.size() * (size_t)W, -1);
     int32_t* delta = ps.delta.data() + (size_t)slot_base * W;
-    const int64_t i_q = total - 1;
-    // common segments: the same offset in every view
-    int64_t off = 0;
-    for (int32_t r = 0; r < n_common_refs; ++r) {
-      for (int32_t w = 0; w < W; ++w) delta[(size_t)r * W + w] = (int32_t)(i_q - off);
-      off += c->segs[ps.refs[r]].visible();
-    }
-    // live block of worker u: last in u's own view; in another worker w's view it follows the
-    // common part and the blocks of the workers before u other than w
-    int64_t before_u = common_len;           // common part + blocks of workers 0 .. u-1
-    for (int32_t u = 0; u < W; ++u) {
-      const int32_t r = ps.live_ref[u];
-      if (r >= 0) {
-        for (int32_t w = 0; w < W; ++w) {
-          const int64_t o = (w == u)  ? total - ps.live_len[u]
-                            : (w < u) ? before_u - ps.live_len[w]
-                                      : before_u;
-          delta[(size_t)r * W + w] = (int32_t)(i_q - o);
-        }
-      }
-      before_u += ps.live_len[u];
+    // Rotation of reference r for worker w: i_q(w) minus r's offset in w's view, or -1 when the
+    // layout keeps r out of that view.
+    for (size_t r = 0; r < ps.refs.size(); ++r) ps.ref_of[ps.refs[r]] = (int32_t)r;
+    for (int32_t w = 0; w < W; ++w) {
+      ps.view_ref.clear();
+      ps.view_off.clear();
+      const int64_t total = c->for_each_view(p, w, [&](int32_t sid, int64_t off, int32_t) {
+        ps.view_ref.push_back(ps.ref_of[sid]);
+        ps.view_off.push_back(off);
+      });
+      for (size_t k = 0; k < ps.view_ref.size(); ++k)
+        delta[(size_t)ps.view_ref[k] * W + w] = (int32_t)(total - 1 - ps.view_off[k]);
     }
     int64_t tiles = 0;
     for (size_t r = 0; r < ps.refs.size(); ++r) {

@@ -64,7 +64,8 @@ def test_sizes(lib, name):
 @pytest.mark.parametrize("field,value", [("head_dim", 96), ("page_size", 100), ("page_size", 0),
                                          ("num_q_heads", 12), ("num_workers", 0),
                                          ("num_workers", 17), ("rope_theta", 0.5),
-                                         ("contiguous", 2), ("num_pages", 0)])
+                                         ("contiguous", 2), ("num_pages", 0), ("layout", 4),
+                                         ("layout", -1), ("reserved", 1)])
 def test_invalid_config_rejected(lib, field, value):
     cfg = _cfg(wl.tiny())
     cfg.num_q_heads, cfg.num_kv_heads = 64, 8
@@ -72,6 +73,15 @@ def test_invalid_config_rejected(lib, field, value):
     with pytest.raises(binding.HogwildError) as e:
         binding.hw_workspace_size(cfg)
     assert e.value.status == binding.HW_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("layout", ["combined", "step_wise", "contiguous", "no_sync"])
+def test_every_layout_accepted(lib, layout):
+    w = wl.tiny()
+    cfg = config_for(num_problems=1, num_workers=2, num_layers=1, num_q_heads=8, num_kv_heads=2,
+                     head_dim=64, page_size=256, num_pages=8, max_position=1024,
+                     rope_theta=1e4, layout=layout)
+    assert binding.hw_workspace_size(cfg) > 0 and w.layout == "combined"
 
 
 def test_null_arguments_rejected_before_cuda(lib):

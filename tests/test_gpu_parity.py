@@ -96,6 +96,16 @@ def test_full_size_w8_common32768():
     G.run_case(w, steps=1, pool_sample=64)
 
 
+@pytest.mark.parametrize("layout", ["combined", "step_wise", "contiguous", "no_sync"])
+def test_cache_layouts_with_commits(layout):
+    """Every cache layout (views differ, kernels do not): 4 workers, random commits, so the
+    views mix the prompt, committed paragraphs of several writers and live blocks."""
+    import gpu_cases as G
+    w = G.small(wl.c4(), num_workers=4, common_len=(900,), worker_len=((130, 0, 257, 40),),
+                steps=6, layout=layout)
+    G.run_case(w, steps=6, bernoulli=0.4)
+
+
 def test_full_size_w4_common16384_64_layers():
     """All 64 layers run on the device; the oracle computes the first two and the last layer
     (the tables are shared by every layer, the pools are not)."""
