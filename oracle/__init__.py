@@ -12,7 +12,8 @@ supplies seeded inputs) and is written from the method's description, not from a
 * ``oracle.attention`` -- the views of each worker and two independent formulations of the
                           concurrent attention: brute force (re-rotate every key at its position
                           in the worker's view) and the method (keys at block-local positions,
-                          one query rotation per block, log-sum-exp merge).
+                          one query rotation per block, log-sum-exp merge); and the same two
+                          for several causal query tokens per worker (``*_mq``).
 
 Source: "Hogwild! Inference: Parallel LLM Generation via Concurrent Attention", summary at
 gentlecold.top, sections 4-6 (views, the RoPE identity, the cache layouts), 10 (the no-sync and

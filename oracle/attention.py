@@ -14,6 +14,14 @@ and 9), with score scale 1/sqrt(D), GQA head h -> KV head floor(h / G), no other
   "aggregate in the softmax weighting" / "partial result reduction" of sections 5 and 9.
 
 Returned ``lse`` is the natural-log log-sum-exp of the scaled scores (-inf for an empty view).
+
+Several query tokens per worker (``*_mq``; the paragraph header a worker prefills after a
+commit, section 8 step 4, or any chunk of tokens a worker appends in one step): the queries of
+worker w are the last n_q[p][w] tokens of its own block, in order.  Query token t sits at view
+position i_q - (n_q - 1 - t) and attends causally -- to every token of the view up to and
+including its own position.  The own block is last in every view (section 6), so only its
+newest tokens are ever masked, and the other workers' tokens of the same step stay visible
+(the inference flow appends every worker's tokens before any attention).
 """
 from __future__ import annotations
 
@@ -131,3 +139,99 @@ def method_rows(cache: HogwildCache, layer: int, q: np.ndarray, rows) -> np.ndar
                                          seg.raw_v(layer)[:n, kh, :], q_rot, scale))
         res[r] = lse_merge(parts)[0][0]
     return res
+
+
+# ------------------------------------------------------------------ several queries per worker
+
+
+def _mq_rows(cache: HogwildCache, n_q):
+    """(p, w, t, back) of every query row in order (problem, worker, token); back = n_q-1-t."""
+    n_q = np.asarray(n_q, dtype=np.int64).reshape(cache.P, cache.W)
+    rows = []
+    for p in range(cache.P):
+        for w in range(cache.W):
+            nq = int(n_q[p, w])
+            if nq < 0:
+                raise ValueError("negative query count")
+            if nq == 0:
+                continue
+            entries, _ = cache.view(p, w)
+            own = cache.live[p][w]
+            if not entries or entries[-1][0] != own or entries[-1][2] < nq:
+                raise ValueError("a worker's queries must be tokens of its own block")
+            rows += [(p, w, t, nq - 1 - t) for t in range(nq)]
+    return rows
+
+
+def _check_q_mq(cache, q, rows):
+    q = np.asarray(q, dtype=np.float64)
+    if q.ndim != 3 or q.shape[0] != len(rows) or q.shape[2] != cache.D or q.shape[1] % cache.H_kv:
+        raise ValueError("q must be [sum n_q][H_q][D]")
+    return q
+
+
+def brute_force_mq(cache: HogwildCache, layer: int, q: np.ndarray, n_q):
+    """Causal textbook attention: view keys re-rotated at positions 0 .. n-1, each query token
+    rotated at its own position and masked to the positions up to it."""
+    rows = _mq_rows(cache, n_q)
+    q = _check_q_mq(cache, q, rows)
+    Hq, D = q.shape[1], q.shape[2]
+    G = Hq // cache.H_kv
+    scale = 1.0 / math.sqrt(D)
+    out = np.zeros(q.shape)
+    lse = np.full(q.shape[:2], -np.inf)
+    for i, (p, w, t, back) in enumerate(rows):
+        entries, i_q = cache.view(p, w)
+        pos = i_q - back
+        kr = np.concatenate([cache.segments[s].raw_k(layer)[:n] for s, _, n in entries])[:pos + 1]
+        vr = np.concatenate([cache.segments[s].raw_v(layer)[:n] for s, _, n in entries])[:pos + 1]
+        k = rope(kr, np.arange(pos + 1)[:, None], cache.theta)
+        qr = rope(q[i], pos, cache.theta)
+        for h in range(Hq):
+            sc = (k[:, h // G, :] @ qr[h]) * scale
+            m = sc.max()
+            e = np.exp(sc - m)
+            out[i, h] = (e @ vr[:, h // G, :]) / e.sum()
+            lse[i, h] = m + math.log(e.sum())
+    return out, lse
+
+
+def query_position(i_q: int, back: int) -> int:
+    """View position of a query token that has ``back`` newer query tokens after it."""
+    return i_q - back
+
+
+def own_visible(n: int, back: int) -> int:
+    """Tokens of the own block (n visible) that a query with ``back`` newer tokens may see."""
+    return n - back
+
+
+def method_mq(cache: HogwildCache, layer: int, q: np.ndarray, n_q):
+    """The method with several causal query tokens per worker: token t is rotated once per
+    block by (its position - the block's view offset); the own block contributes only its
+    tokens up to the query's own; partials merged by log-sum-exp."""
+    rows = _mq_rows(cache, n_q)
+    q = _check_q_mq(cache, q, rows)
+    Hq, D = q.shape[1], q.shape[2]
+    G = Hq // cache.H_kv
+    scale = 1.0 / math.sqrt(D)
+    out = np.zeros(q.shape)
+    lse = np.full(q.shape[:2], -np.inf)
+    for i, (p, w, t, back) in enumerate(rows):
+        entries, i_q = cache.view(p, w)
+        own = cache.live[p][w]
+        pos = query_position(i_q, back)
+        parts = {h: [] for h in range(cache.H_kv)}
+        for sid, off, n in entries:
+            nv = own_visible(n, back) if sid == own else n      # causal cut in the own block
+            seg = cache.segments[sid]
+            q_rot = rope(q[i], pos - off, cache.theta)
+            for kh in range(cache.H_kv):
+                parts[kh].append(segment_partial(seg.stored_k(layer)[:nv, kh, :],
+                                                 seg.raw_v(layer)[:nv, kh, :],
+                                                 q_rot[kh * G:(kh + 1) * G], scale))
+        for kh in range(cache.H_kv):
+            o, l = lse_merge(parts[kh])
+            out[i, kh * G:(kh + 1) * G] = o
+            lse[i, kh * G:(kh + 1) * G] = l
+    return out, lse

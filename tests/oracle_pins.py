@@ -387,6 +387,105 @@ def check_layouts_coincide_without_commits():
             [caches["step_wise"].common[0][0], caches["step_wise"].live[0][w]]
 
 
+# ------------------------------------------------------------- several queries per worker
+
+
+def _mq_counts(g, c):
+    """A random query count per worker: at most its own block's visible length (0 if empty)."""
+    n_q = np.zeros((c.P, c.W), dtype=np.int64)
+    for p in range(c.P):
+        for w in range(c.W):
+            n = c.segments[c.live[p][w]].visible
+            n_q[p, w] = g.integers(0, min(n, 5) + 1) if n else 0
+    return n_q
+
+
+def check_mq_brute_vs_method():
+    """The two causal formulations agree, over random histories, commits and every layout."""
+    for seed in range(4):
+        g = np.random.default_rng(100 + seed)
+        for layout in C.LAYOUTS:
+            for c, _ in random_session(seed, 8, 1 + seed % 3, P=2):
+                c.layout = layout
+                n_q = _mq_counts(g, c)
+                q = g.standard_normal((int(n_q.sum()), 4, 8))
+                ob, lb = A.brute_force_mq(c, 0, q, n_q)
+                om, lm = A.method_mq(c, 0, q, n_q)
+                assert np.allclose(ob, om, rtol=0, atol=1e-10), (seed, layout)
+                assert np.allclose(lb, lm, rtol=0, atol=1e-10)
+
+
+def check_mq_one_query_is_decode():
+    """One query per worker is the decode step: method_mq equals method row for row."""
+    g = np.random.default_rng(110)
+    tried = 0
+    for c, q in random_session(7, 8, 3, P=2, commit_p=0.0):
+        ok = all(c.segments[c.live[p][w]].visible > 0 for p in range(c.P) for w in range(c.W))
+        if not ok:
+            continue
+        tried += 1
+        n_q = np.ones((c.P, c.W), dtype=np.int64)
+        om, lm = A.method_mq(c, 0, q.reshape(-1, q.shape[2], q.shape[3]), n_q)
+        od, ld = A.method(c, 0, q)
+        assert np.allclose(om, od.reshape(om.shape), rtol=0, atol=1e-12)
+        assert np.allclose(lm, ld.reshape(lm.shape), rtol=0, atol=1e-12)
+    assert tried >= 2
+    del g
+
+
+def check_mq_chunk_equals_token_by_token():
+    """Query token t of a chunk sees what a single decode query sees when the worker's block
+    ends at that token (the cache rebuilt with the block cut there)."""
+    g = np.random.default_rng(111)
+    D, H_kv, W = 8, 2, 3
+    lens = [6, 2, 5, 3]                      # common, workers 0..2
+    tot = sum(lens)
+    k, v = g.standard_normal((tot, H_kv, D)), g.standard_normal((tot, H_kv, D))
+    c = C.HogwildCache(1, W, 1, H_kv, D, 1e4, 4, 64)
+    c.append(0, [lens], k, v)
+    n_q = np.array([[0, 4, 2]])
+    q = g.standard_normal((6, 2 * H_kv, D))
+    out, lse = A.method_mq(c, 0, q, n_q)
+    starts = np.cumsum([0] + lens)
+    i = 0
+    for w in range(W):
+        for t in range(int(n_q[0, w])):
+            cut = lens[1 + w] - (int(n_q[0, w]) - 1 - t)
+            sub = [lens[0]] + [lens[1 + u] if u != w else cut for u in range(W)]
+            keep = np.concatenate([np.arange(starts[b], starts[b] + sub[b]) for b in range(W + 1)])
+            c2 = C.HogwildCache(1, W, 1, H_kv, D, 1e4, 4, 64)
+            c2.append(0, [sub], k[keep], v[keep])
+            qd = np.zeros((1, W, 2 * H_kv, D))
+            qd[0, w] = q[i]
+            od, ld = A.method(c2, 0, qd)
+            assert np.allclose(out[i], od[0, w], rtol=0, atol=1e-12), (w, t)
+            assert np.allclose(lse[i], ld[0, w], rtol=0, atol=1e-12)
+            i += 1
+
+
+def check_mq_single_worker_is_causal_prefill():
+    """W = 1 with a chunk of n queries is ordinary causal RoPE attention over prompt + block:
+    torch's scaled_dot_product_attention with a lower-triangular mask on complex-form RoPE."""
+    import torch
+    g = np.random.default_rng(112)
+    D, H_kv, G, theta, nq = 64, 2, 2, 1e4, 5
+    c = C.HogwildCache(1, 1, 1, H_kv, D, theta, 8, 256)
+    k, v = g.standard_normal((19, H_kv, D)), g.standard_normal((19, H_kv, D))
+    c.append(0, [[12, 7]], k, v)
+    q = g.standard_normal((nq, H_kv * G, D))
+    n = 19
+    pos_q = np.arange(n - nq, n)
+    kr = rope_complex(k, np.arange(n)[:, None], theta)
+    qr = np.stack([rope_complex(q[t], pos_q[t], theta) for t in range(nq)])    # [nq][H_q][D]
+    kt = torch.from_numpy(np.repeat(kr.transpose(1, 0, 2), G, axis=0))        # [H_q][n][D]
+    vt = torch.from_numpy(np.repeat(v.transpose(1, 0, 2), G, axis=0))
+    qt = torch.from_numpy(qr.transpose(1, 0, 2).copy())                        # [H_q][nq][D]
+    mask = torch.from_numpy(np.arange(n)[None, :] <= pos_q[:, None])
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask).numpy()
+    out, _ = A.method_mq(c, 0, q, [[nq]])
+    assert np.allclose(out, ref.transpose(1, 0, 2), atol=1e-12), np.abs(out - ref.transpose(1, 0, 2)).max()
+
+
 ALL_CHECKS = [
     check_rope_complex_form, check_rope_d2_textbook, check_inv_freq_values, check_rope_invariants,
     check_views_golden, check_view_offsets_and_query_position, check_pages_hand_example,
@@ -394,5 +493,6 @@ ALL_CHECKS = [
     check_two_worker_hand, check_brute_vs_method, check_zero_keys_give_mean_values,
     check_single_token_returns_its_value, check_single_worker_is_textbook_decode,
     check_relabel_two_workers, check_layout_views_golden, check_layouts_textbook_attention,
-    check_layouts_coincide_without_commits,
+    check_layouts_coincide_without_commits, check_mq_brute_vs_method, check_mq_one_query_is_decode,
+    check_mq_chunk_equals_token_by_token, check_mq_single_worker_is_causal_prefill,
 ]

@@ -138,6 +138,14 @@ def _view_contiguous_own_first(self, p, w):
 
 _orig_view = C.HogwildCache.view
 
+
+def _own_visible_one_more(n, back):
+    return min(n, n - back + 1)
+
+
+def _query_position_unshifted(i_q, back):
+    return i_q
+
 MUTATIONS = {
     "rope_rotates_backwards": [(R, "rope", _rope_sign_flip), (A, "rope", _rope_sign_flip),
                                (C, "rope", _rope_sign_flip)],
@@ -154,6 +162,8 @@ MUTATIONS = {
     "pages_popped_lifo": [(C.HogwildCache, "_allocate", _allocate_lifo)],
     "commits_in_descending_id": [(C.HogwildCache, "step_end", _step_end_commit_descending)],
     "layout_ignored": [(C.HogwildCache, "view", _view_layout_ignored)],
+    "causal_cut_off_by_one": [(A, "own_visible", _own_visible_one_more)],
+    "chunk_queries_share_one_position": [(A, "query_position", _query_position_unshifted)],
     "step_wise_shows_others": [(C.HogwildCache, "view", _view_step_wise_shows_others)],
     "contiguous_own_output_first": [(C.HogwildCache, "view", _view_contiguous_own_first)],
 }
