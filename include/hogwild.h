@@ -173,6 +173,30 @@ hw_status hw_concurrent_attention(hw_ctx* ctx, int32_t layer, const void* q, voi
                                   int32_t out_dtype, float* lse, void* stream);
 
 /*
+ * Several query tokens per worker, attending causally (summary section 8, step 4: after a
+ * commit the worker's new block starts with a paragraph header of several tokens, whose
+ * forward pass needs them all; likewise any chunk of tokens a worker appends in one step).
+ * Worker w's queries are the last n_q[p][w] tokens of its own block (appended before this call,
+ * in this step or earlier), in order.  Query token t sits at view position
+ * i_q(w) - (n_q[p][w] - 1 - t) and attends to every token of w's view up to and including its
+ * own position: the whole view but the own block, which is last in every layout, and the own
+ * block's tokens up to its own.  With n_q = 1 for every worker this is hw_concurrent_attention.
+ *   q:     device bf16 [N][H_q][D], N = sum of n_q, rows in order problem, worker, token;
+ *          16-byte aligned.  Unrotated, as for hw_concurrent_attention.
+ *   n_q:   host int32 [P][W], 0 <= n_q[p][w] <= the worker's own block length (this step's
+ *          appended tokens included).
+ *   out:   device [N][H_q][D], bf16 or fp32 (out_dtype); lse: device fp32 [N][H_q] or NULL.
+ * Limit: every problem's query rows, (sum_w n_q[p][w]) * H_q / H_kv, fit one 128-row tile,
+ * else HW_ERR_CAPACITY and nothing is enqueued.  N = 0 enqueues nothing.  The layer's
+ * recorded append (hw_append_kv) is written first, by the append kernel.
+ * Errors: as hw_concurrent_attention; HW_ERR_INVALID_ARG for a NULL n_q or a count out of
+ * range.
+ */
+hw_status hw_concurrent_attention_mq(hw_ctx* ctx, int32_t layer, const void* q,
+                                     const int32_t* n_q, void* out, int32_t out_dtype, float* lse,
+                                     void* stream);
+
+/*
  * hw_concurrent_attention for callers that cannot allocate device memory when they call it
  * (no counterpart in the paper; a deployment need).  Same arguments, same result as
  * hw_concurrent_attention; the context's pools, tables and RoPE table are used as usual, but

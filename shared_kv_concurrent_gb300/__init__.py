@@ -58,6 +58,17 @@ class HogwildCache:
     def append_kv(self, layer: int, n_new, k_raw, v_raw, stream=None) -> None:
         binding.hw_append_kv(self.ctx, layer, n_new, k_raw, v_raw, stream)
 
+    def concurrent_attention_mq(self, layer: int, q, n_q, out=None, out_dtype: str = "bf16",
+                                lse=None, stream=None):
+        """Several causal query tokens per worker (the last n_q[p][w] tokens of its block)."""
+        import torch
+        dt = HW_OUT_F32 if out_dtype == "f32" else HW_OUT_BF16
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32 if dt == HW_OUT_F32 else torch.bfloat16,
+                              device=q.device)
+        binding.hw_concurrent_attention_mq(self.ctx, layer, q, n_q, out, dt, lse, stream)
+        return out
+
     def concurrent_attention(self, layer: int, q, out=None, out_dtype: str = "bf16", lse=None,
                              stream=None):
         import torch

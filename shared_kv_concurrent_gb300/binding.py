@@ -30,6 +30,7 @@ HW_OUT_F32 = 1
 EXPORTED = (
     "hw_status_string", "hw_last_cuda_error", "hw_pool_size", "hw_workspace_size", "hw_create",
     "hw_destroy", "hw_append_kv", "hw_concurrent_attention", "hw_concurrent_attention_noalloc",
+    "hw_concurrent_attention_mq",
     "hw_step_end",
     "hw_check_device_errors", "hw_profile_enable", "hw_profile_read", "hw_get_counts",
     "hw_get_segment", "hw_get_blocks", "hw_get_view",
@@ -89,6 +90,7 @@ def load() -> ctypes.CDLL:
         "hw_append_kv": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P]),
         "hw_concurrent_attention": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P]),
         "hw_concurrent_attention_noalloc": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P]),
+        "hw_concurrent_attention_mq": (ctypes.c_int, [_P, _I32, _P, _P, _P, _I32, _P, _P]),
         "hw_step_end": (ctypes.c_int, [_P, _P, _P]),
         "hw_check_device_errors": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
         "hw_profile_enable": (ctypes.c_int, [_P, _I32]),
@@ -192,6 +194,15 @@ def hw_concurrent_attention(ctx: int, layer: int, q, out, out_dtype: int, lse=No
                                                   out_dtype, _dptr(lse), _stream(stream))
     if st:
         _check(st, "hw_concurrent_attention")
+
+
+def hw_concurrent_attention_mq(ctx: int, layer: int, q, n_q, out, out_dtype: int, lse=None,
+                               stream=None) -> None:
+    """Several causal query tokens per worker: n_q host int32 [P][W]; q / out [sum n_q][H_q][D]."""
+    nq = np.ascontiguousarray(np.asarray(n_q, dtype=np.int32))
+    _check(load().hw_concurrent_attention_mq(ctx, layer, _dptr(q), nq.ctypes.data, _dptr(out),
+                                             out_dtype, _dptr(lse), _stream(stream)),
+           "hw_concurrent_attention_mq")
 
 
 def hw_concurrent_attention_noalloc(ctx: int, layer: int, q, out, out_dtype: int, lse=None,

@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
         const int delta = dl[w];
         float y1 = 0.f, y2 = 0.f;
         if (delta >= 0 && delta < a.max_position) {
-          const size_t qo = (((size_t)g.p * a.W + w) * a.H_q + hq) * D;
+          const size_t qo = ((size_t)query_row(a, g.p, w) * a.H_q + hq) * D;
           const float q1 = __bfloat162float(a.q[qo + i]);
           const float q2 = __bfloat162float(a.q[qo + i + half]);
           const float c = a.rope_cos[(size_t)delta * half + i];
@@ -113,15 +113,18 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
         const int r = warp + k * kWarps;
         if (r >= rows) continue;
         if (dl[r / a.G] < 0) continue;              // this worker does not see the segment
+        // causal cut (several query tokens per worker): tokens of the segment it may see
+        const int cap = a.vlen ? a.vlen[(size_t)pc.seg_slot * a.W + r / a.G] : pc.pos0 + pc.ntok;
         const float* qr = qs + r * D;
         const float* kr = ks + lane * KS;
         float s = 0.f;
 #pragma unroll 16
         for (int d = 0; d < D; ++d) s = fmaf(qr[d], kr[d], s);
-        if (lane >= nt) s = -CUDART_INF_F;
+        if (lane >= nt || pc.pos0 + t0 + lane >= cap) s = -CUDART_INF_F;
         float tmax = s;
 #pragma unroll
         for (int off = 16; off; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+        if (tmax == -CUDART_INF_F) continue;        // nothing of this tile is visible to the row
         const float mn = fmaxf(m[k], tmax);
         const float alpha = exp2f(m[k] - mn);
         const float p = exp2f(s - mn);

@@ -103,7 +103,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 struct TileInfo {
-  int32_t seg_slot, page, slot0, nvalid, fresh;
+  int32_t seg_slot, page, slot0, nvalid, fresh, pos0;
 };
 
 // The CTA's sequence of tiles: the producer publishes ranges of pieces, {begin, end}, in a
@@ -170,6 +170,7 @@ struct TileWalker {
     t->slot0 = pc.slot0;
     t->nvalid = pc.ntok;
     t->fresh = pc.fresh;
+    t->pos0 = pc.pos0;
     *new_seg = pc.seg_slot != last_slot;
     last_slot = pc.seg_slot;
     return true;
@@ -212,7 +213,7 @@ __device__ __forceinline__ void rotate_tile(const AttnArgs& a, const Group& g, i
       if (item < ITEMS && r < a.rows) {
         const int w = r / a.G, hq = g.h * a.G + r % a.G;
         delta = uniform_delta >= 0 ? uniform_delta : a.delta[(size_t)slot * a.W + w];
-        qo = (((size_t)g.p * a.W + w) * a.H_q + hq) * D;
+        qo = ((size_t)query_row(a, g.p, w) * a.H_q + hq) * D;
         if (delta >= a.max_position) {
           record_error(a.err, ERR_POS_RANGE, KID_ATTN_TC, blockIdx.x, delta);
           delta = -1;
@@ -416,9 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The first query tile's inputs into L2 before the K/V loads start: the rotation warps
       // read them right after set-up, and would otherwise queue behind every CTA's tiles.
       const int p = head.y / a.H_kv, h = head.y % a.H_kv;
-      for (int w = 0; w < a.W; ++w)       // worker w's G query heads of this KV head
-        bulk_prefetch_l2(a.q + (((size_t)p * a.W + w) * a.H_q + (size_t)h * a.G) * D,
-                         (uint32_t)(a.G * D * 2));
+      for (int w = 0; w < a.W; ++w) {     // query row w's G heads of this KV head
+        const int qr = query_row(a, p, w);
+        if (qr >= 0)
+          bulk_prefetch_l2(a.q + ((size_t)qr * a.H_q + (size_t)h * a.G) * D,
+                           (uint32_t)(a.G * D * 2));
+      }
       const int d0 = uv[1].z;             // the first segment's rotation, if shared
       if (d0 >= 0 && d0 < a.max_position) {
         bulk_prefetch_l2(a.rope_cos + (size_t)d0 * (D / 2), D / 2 * 4);
@@ -716,8 +720,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t i = 0;
       bool ok = true;
       bool row_visible = false;
+      int row_cap = 0x7fffffff;
       while (tw.next(&t, &new_seg)) {
-        if (new_seg) row_visible = r < R && a.delta[(size_t)t.seg_slot * a.W + r / a.G] >= 0;
+        if (new_seg) {
+          row_visible = r < R && a.delta[(size_t)t.seg_slot * a.W + r / a.G] >= 0;
+          // causal cut (several query tokens per worker): tokens of the segment it may see
+          row_cap = (row_visible && a.vlen) ? a.vlen[(size_t)t.seg_slot * a.W + r / a.G]
+                                            : 0x7fffffff;
+        }
         const int b = i & 1;
         // (warp-uniform outcome: the TMEM accesses below need every lane)
         if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(b), (i >> 1) & 1, abort, kWaitLimitNs))) {
@@ -733,7 +743,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < CPT; ++k) s[k] = __uint_as_float(v[k]);
         }
-        const int limit = row_visible ? max(0, min(CPT, t.nvalid - cq * CPT)) : 0;
+        const int nv = min(t.nvalid, row_cap - t.pos0);   // (nvalid unless cut)
+        const int limit = row_visible ? max(0, min(CPT, nv - cq * CPT)) : 0;
         float mx = -CUDART_INF_F;
 #pragma unroll
         for (int k = 0; k < CPT; ++k) {

@@ -32,6 +32,7 @@ constexpr int kProfPairs = 4096;       // timed launches kept per hw_profile_rea
 // A step whose blocks each append at most this many tokens has them written by the
 // tensor-core attention kernel itself (fused append); larger appends use the append kernel.
 constexpr int kFuseTok = 16;
+constexpr int kMaxRows = 128;          // query rows of one (problem, KV head): one MMA tile
 
 thread_local int g_cuda_err = 0;
 // Plan sequence numbers, unique in the process: a slot word left by an earlier context in
@@ -98,10 +99,15 @@ Layout make_layout(const hw_config* c) {
   L.max_fresh = (int32_t)(P * (W + 1) * kFuseTok);
   const size_t runs = (size_t)P * (W + 1) + (size_t)L.max_append / 128 + 2;
   const size_t append_bytes = runs * sizeof(hw::AppendRun);
+  // Rotation tables are [segment slot][query rows per problem / G]: W wide for one query per
+  // worker, up to 128 / G wide for several (hw_concurrent_attention_mq), which adds the causal
+  // length table of the same shape and the query-row map.
+  const int64_t Wt = std::max<int64_t>(W, kMaxRows / (c->num_q_heads / c->num_kv_heads));
   const size_t attn_bytes = align_up((size_t)L.max_pieces * sizeof(hw::Piece), 16) +
                             align_up((size_t)L.max_units * sizeof(hw::Unit), 16) +
                             align_up((size_t)P * H * sizeof(hw::Group), 16) +
-                            align_up((size_t)L.max_seg_slots * W * sizeof(int32_t), 16) +
+                            2 * align_up((size_t)L.max_seg_slots * Wt * sizeof(int32_t), 16) +
+                            align_up((size_t)P * Wt * sizeof(int32_t), 16) +
                             align_up((size_t)L.max_fresh * sizeof(hw::FreshTok), 16);
   // A slot holds a step's append runs followed by its attention plan (uploaded together), and
   // last the plan's sequence number.
@@ -129,8 +135,9 @@ Layout make_layout(const hw_config* c) {
 
 // Offsets of the arrays of an attention plan inside its buffer, and their sizes.
 struct PlanOffsets {
-  size_t pieces, units, groups, delta, fresh, bytes;
+  size_t pieces, units, groups, delta, vlen, qrow, fresh, bytes;
   int32_t num_pieces, num_units, num_groups, num_seg_slots, num_fresh;
+  int32_t width;                       // columns of the rotation table (query rows / G)
 };
 
 // Reused host buffers of the plan builder (no allocation per call once they have grown).
@@ -142,7 +149,8 @@ struct PlanScratch {
   std::vector<hw::Unit> units;
   std::vector<hw::Group> groups;
   std::vector<hw::FreshTok> fresh;
-  std::vector<int32_t> delta, refs, piece_fresh0, src_base, ref_of, view_ref;
+  std::vector<int32_t> delta, refs, piece_fresh0, src_base, ref_of, view_ref, vlen, qrow;
+  int32_t qrow_next = 0;
   std::vector<int64_t> view_off;
   std::vector<int32_t> ref_sid, ref_slot, ref_tiles, prob_ref_begin, prob_common_refs, unit_rem,
       order;
@@ -501,7 +509,8 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
 
 namespace {
 bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap,
-                          int64_t target_override, bool fuse, uint64_t seq);
+                          int64_t target_override, bool fuse, uint64_t seq,
+                          const int32_t* n_q = nullptr);
 }  // namespace
 
 extern "C" {
@@ -660,9 +669,22 @@ namespace {
 // layout), or -1 when w's view does not hold it; in the combined layout every view holds every
 // segment and i_q is the problem's visible length - 1.
 // unit_cap > 0 bounds the number of units (one partial result each); 0 = the default split.
+// n_q (host [P][W], or null for one query per worker): several causal query tokens per worker;
+// the rotation table then has one column per query row of a problem (its width WT is the
+// largest count of any problem), with the causal length table and the query-row map.
 bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0,
-                          int64_t target_override = 0, bool fuse = false, uint64_t seq = 0) {
+                          int64_t target_override = 0, bool fuse = false, uint64_t seq = 0,
+                          const int32_t* n_q) {
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
+  int32_t WT = W;                       // rotation-table width: query rows per problem / G
+  if (n_q) {
+    WT = 1;
+    for (int32_t p = 0; p < P; ++p) {
+      int32_t v = 0;
+      for (int32_t w = 0; w < W; ++w) v += n_q[(size_t)p * W + w];
+      WT = std::max(WT, v);
+    }
+  }
   const int32_t S = c->cfg.page_size;
   const Layout& L = c->lay;
   PlanScratch& ps = c->ps;
@@ -679,6 +701,9 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   ps.prob_common_refs.assign(P, 0);
   ps.prob_tiles.assign(P, 0);
   ps.unit_range.clear();
+  ps.vlen.clear();
+  ps.qrow.assign(n_q ? (size_t)P * WT : 0, -1);
+  ps.qrow_next = 0;
   // fuse: list the step's appended tokens (k_raw rows in append order: problems, then block 0 =
   // common, 1 + w = worker w, each in position order) for the attention kernel to write.
   if (fuse) {
@@ -707,22 +732,44 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
       const int32_t sid = c->live[p][w];
       if (c->segs[sid].visible() > 0) ps.refs.push_back(sid);
     }
-    const int32_t slot_base = (int32_t)(ps.delta.size() / (size_t)W);
+    const int32_t slot_base = (int32_t)(ps.delta.size() / (size_t)WT);
     if (slot_base + (int64_t)ps.refs.size() > L.max_seg_slots) return false;
-    ps.delta.resize(ps.delta.size() + ps.refs.size() * (size_t)W, -1);
-    int32_t* delta = ps.delta.data() + (size_t)slot_base * W;
+    ps.delta.resize(ps.delta.size() + ps.refs.size() * (size_t)WT, -1);
+    int32_t* delta = ps.delta.data() + (size_t)slot_base * WT;
+    int32_t* vlen = nullptr;
+    if (n_q) {
+      ps.vlen.resize(ps.delta.size(), 0);
+      vlen = ps.vlen.data() + (size_t)slot_base * WT;
+    }
     // Rotation of reference r for worker w: i_q(w) minus r's offset in w's view, or -1 when the
-    // layout keeps r out of that view.
+    // layout keeps r out of that view.  With several query tokens, worker w's token t (back =
+    // n_q - 1 - t newer tokens after it) is query row v: its rotation is back less, and in the
+    // own block (last in every view) it sees back tokens fewer -- the causal cut.
     for (size_t r = 0; r < ps.refs.size(); ++r) ps.ref_of[ps.refs[r]] = (int32_t)r;
+    int32_t v0 = 0;                        // first query row of worker w
     for (int32_t w = 0; w < W; ++w) {
+      const int32_t nq = n_q ? n_q[(size_t)p * W + w] : 1;
+      if (nq == 0) continue;
       ps.view_ref.clear();
       ps.view_off.clear();
       const int64_t total = c->for_each_view(p, w, [&](int32_t sid, int64_t off, int32_t) {
         ps.view_ref.push_back(ps.ref_of[sid]);
         ps.view_off.push_back(off);
       });
-      for (size_t k = 0; k < ps.view_ref.size(); ++k)
-        delta[(size_t)ps.view_ref[k] * W + w] = (int32_t)(total - 1 - ps.view_off[k]);
+      const int32_t vb = n_q ? v0 : w;
+      for (int32_t t = 0; t < nq; ++t) {
+        const int32_t back = nq - 1 - t, v = vb + t;
+        for (size_t k = 0; k < ps.view_ref.size(); ++k) {
+          const int32_t r = ps.view_ref[k];
+          delta[(size_t)r * WT + v] = (int32_t)(total - 1 - back - ps.view_off[k]);
+          if (vlen) {
+            const int32_t n = c->segs[ps.refs[r]].visible();
+            vlen[(size_t)r * WT + v] = k + 1 == ps.view_ref.size() ? n - back : n;
+          }
+        }
+        if (n_q) ps.qrow[(size_t)p * WT + v] = ps.qrow_next++;
+      }
+      v0 += nq;
     }
     int64_t tiles = 0;
     for (size_t r = 0; r < ps.refs.size(); ++r) {
@@ -760,7 +807,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     const int32_t fresh = (sg.pending > 0 && j + cnt > sg.length) ? 1 : 0;
     if ((int64_t)ps.pieces.size() >= L.max_pieces) return false;
     ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
-    ps.pieces.push_back(hw::Piece{ps.ref_slot[r], pg, slot0, cnt, fresh});
+    ps.pieces.push_back(hw::Piece{ps.ref_slot[r], pg, slot0, cnt, fresh, j});
     if (fuse && fresh) {
       const int32_t sid = ps.ref_sid[r];
       if (ps.src_base[sid] < 0) return false;
@@ -865,9 +912,9 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   // rotation for all query rows: the kernels then need no delta-table load for it.
   for (hw::Unit& u : ps.units) {
     if (u.seg0 < 0) continue;
-    const int32_t* row = ps.delta.data() + (size_t)u.seg0 * W;
-    bool same = row[0] >= 0;
-    for (int32_t w = 1; w < W && same; ++w) same = row[w] == row[0];
+    const int32_t* row = ps.delta.data() + (size_t)u.seg0 * WT;
+    bool same = row[0] >= 0 && !n_q;     // (with a causal cut the rows differ anyway)
+    for (int32_t w = 1; w < WT && same; ++w) same = row[w] == row[0];
     u.delta0 = same ? row[0] : -1;
   }
   size_t off = 0;
@@ -879,6 +926,10 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   off = align_up(off + ps.groups.size() * sizeof(hw::Group), 16);
   po->delta = off;
   off = align_up(off + ps.delta.size() * sizeof(int32_t), 16);
+  po->vlen = off;
+  off = align_up(off + ps.vlen.size() * sizeof(int32_t), 16);
+  po->qrow = off;
+  off = align_up(off + ps.qrow.size() * sizeof(int32_t), 16);
   po->fresh = off;
   off = align_up(off + ps.fresh.size() * sizeof(hw::FreshTok), 16);
   po->bytes = off;
@@ -887,31 +938,55 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   std::memcpy(buf + po->units, ps.units.data(), ps.units.size() * sizeof(hw::Unit));
   std::memcpy(buf + po->groups, ps.groups.data(), ps.groups.size() * sizeof(hw::Group));
   std::memcpy(buf + po->delta, ps.delta.data(), ps.delta.size() * sizeof(int32_t));
+  if (!ps.vlen.empty())
+    std::memcpy(buf + po->vlen, ps.vlen.data(), ps.vlen.size() * sizeof(int32_t));
+  if (!ps.qrow.empty())
+    std::memcpy(buf + po->qrow, ps.qrow.data(), ps.qrow.size() * sizeof(int32_t));
   if (!ps.fresh.empty())
     std::memcpy(buf + po->fresh, ps.fresh.data(), ps.fresh.size() * sizeof(hw::FreshTok));
   po->num_pieces = (int32_t)ps.pieces.size();
   po->num_units = (int32_t)ps.units.size();
   po->num_groups = (int32_t)ps.groups.size();
-  po->num_seg_slots = (int32_t)(ps.delta.size() / (size_t)W);
+  po->num_seg_slots = (int32_t)(ps.delta.size() / (size_t)WT);
+  po->width = WT;
   po->num_fresh = (int32_t)ps.fresh.size();
   return true;
 }
 
-}  // namespace
-
-extern "C" {
-
-hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void* out,
-                                  int32_t out_dtype, float* lse, void* stream) {
-  if (!c || !q || !out || layer < 0 || layer >= c->cfg.num_layers) return HW_ERR_INVALID_ARG;
+// One attention call: one query per worker (n_q null), or n_q[p][w] causal query tokens per
+// worker (the last tokens of its own block).
+static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* n_q, void* out,
+                        int32_t out_dtype, float* lse, void* stream) {
+  if (!c || layer < 0 || layer >= c->cfg.num_layers) return HW_ERR_INVALID_ARG;
   if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
-  if (((uintptr_t)q | (uintptr_t)out) % 16) return HW_ERR_INVALID_ARG;
   if (c->step_active && !c->appended[layer]) return HW_ERR_INVALID_ARG;
+  int64_t width = c->cfg.num_workers;       // query rows per problem / G
+  if (n_q) {
+    const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers;
+    int64_t total = 0;
+    width = 0;
+    for (int32_t p = 0; p < P; ++p) {
+      int64_t rows = 0;
+      for (int32_t w = 0; w < W; ++w) {
+        const int32_t n = n_q[(size_t)p * W + w];
+        if (n < 0 || n > c->segs[c->live[p][w]].visible()) return HW_ERR_INVALID_ARG;
+        rows += n;
+      }
+      total += rows;
+      width = std::max(width, rows);
+    }
+    if (width * c->G > kMaxRows) return HW_ERR_CAPACITY;
+    if (total == 0) return HW_OK;                 // no query: nothing to compute
+  }
+  if (!q || !out) return HW_ERR_INVALID_ARG;
+  if (((uintptr_t)q | (uintptr_t)out) % 16) return HW_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   int slot = 0;
   PlanOffsets po{};
   char* dbase = nullptr;
-  const bool step_plan = c->step_slot >= 0 && c->step_epoch == c->epoch && c->step_plan_ok;
+  // (the step's plan has one query per worker and lists the step's tokens for the kernel)
+  const bool step_plan =
+      !n_q && c->step_slot >= 0 && c->step_epoch == c->epoch && c->step_plan_ok;
   // The layer's recorded append is written by the tensor-core kernel when the step's plan lists
   // the appended tokens; otherwise by the append kernel, now.
   const bool fused = c->use_tc && step_plan && c->step_fused && layer < (int32_t)c->pend_k.size() &&
@@ -933,7 +1008,10 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
     // Tensor-core kernel: one CTA per SM holds all of its shared memory and TMEM, so one unit
     // per SM, balanced by KV entries.
     const uint64_t seq = c->next_seq();
-    if (!build_attention_plan(c, c->h_slot(slot), &po, 0, c->use_tc ? c->num_sms : 0, false, seq))
+    // partials fit the workspace: units * rows stays within its max_units * (W * G) rows
+    const int64_t cap = n_q ? (int64_t)c->lay.max_units * c->rows / (width * c->G) : 0;
+    if (!build_attention_plan(c, c->h_slot(slot), &po, cap, c->use_tc ? c->num_sms : 0, false, seq,
+                              n_q))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
     st = c->upload_slot(slot, po.bytes, seq, &gate);
@@ -945,6 +1023,10 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   a.units = reinterpret_cast<const hw::Unit*>(dbase + po.units);
   a.groups = reinterpret_cast<const hw::Group*>(dbase + po.groups);
   a.delta = reinterpret_cast<const int32_t*>(dbase + po.delta);
+  if (n_q) {
+    a.vlen = reinterpret_cast<const int32_t*>(dbase + po.vlen);
+    a.qrow = reinterpret_cast<const int32_t*>(dbase + po.qrow);
+  }
   a.fresh = reinterpret_cast<const hw::FreshTok*>(dbase + po.fresh);
   a.k_raw = fused ? (const __nv_bfloat16*)c->pend_k[layer] : nullptr;
   a.v_raw = fused ? (const __nv_bfloat16*)c->pend_v[layer] : nullptr;
@@ -962,7 +1044,7 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   a.rope_sin = c->d_sin();
   a.err = c->d_err();
   a.P = c->cfg.num_problems;
-  a.W = c->cfg.num_workers;
+  a.W = po.width;                      // query rows per problem / G (= W for decode)
   a.H_q = c->cfg.num_q_heads;
   a.H_kv = c->cfg.num_kv_heads;
   a.G = c->G;
@@ -970,7 +1052,7 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   a.S = c->cfg.page_size;
   a.num_pages = c->cfg.num_pages;
   a.max_position = c->cfg.max_position;
-  a.rows = c->rows;
+  a.rows = po.width * c->G;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
   // Timing events (when enabled) go directly around the attention kernel only.
   const int pi = c->prof_reserve(0);
@@ -993,6 +1075,21 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
   HW_CUDA(cudaEventRecord(c->slot_ev[slot], s));
   c->slot_used[slot] = true;
   return HW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void* out,
+                                  int32_t out_dtype, float* lse, void* stream) {
+  return attend(c, layer, q, nullptr, out, out_dtype, lse, stream);
+}
+
+hw_status hw_concurrent_attention_mq(hw_ctx* c, int32_t layer, const void* q, const int32_t* n_q,
+                                     void* out, int32_t out_dtype, float* lse, void* stream) {
+  if (!n_q) return HW_ERR_INVALID_ARG;
+  return attend(c, layer, q, n_q, out, out_dtype, lse, stream);
 }
 
 }  // extern "C"
@@ -1045,7 +1142,7 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
   a.rope_sin = c->d_sin();
   a.err = c->d_err();
   a.P = c->cfg.num_problems;
-  a.W = c->cfg.num_workers;
+  a.W = po.width;                      // query rows per problem / G (= W for decode)
   a.H_q = c->cfg.num_q_heads;
   a.H_kv = c->cfg.num_kv_heads;
   a.G = c->G;
@@ -1053,7 +1150,7 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
   a.S = c->cfg.page_size;
   a.num_pages = c->cfg.num_pages;
   a.max_position = c->cfg.max_position;
-  a.rows = c->rows;
+  a.rows = po.width * c->G;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
   hw::launch_attention_fma(a, s);
   HW_CUDA(cudaGetLastError());

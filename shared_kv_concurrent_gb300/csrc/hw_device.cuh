@@ -7,6 +7,12 @@
 
 namespace hw {
 
+// Row of q / out / lse of query row v (worker, or (worker, token) with several query tokens per
+// worker) of problem p; -1 for a padding row.
+__device__ __forceinline__ int query_row(const AttnArgs& a, int p, int v) {
+  return a.qrow ? a.qrow[(size_t)p * a.W + v] : p * a.W + v;
+}
+
 // Record a failed range check without trapping: OR the bits into the error word and keep the
 // details of the first failure.
 __device__ __forceinline__ void record_error(uint32_t* err, uint32_t bits, uint32_t kid,

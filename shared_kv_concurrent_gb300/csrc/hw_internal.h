@@ -42,6 +42,7 @@ struct Piece {
   int32_t slot0;
   int32_t ntok;
   int32_t fresh;     // 1 if the piece holds tokens appended in the current step
+  int32_t pos0;      // block-local position of its first token
 };
 
 // A token appended in the current step whose K/V the tensor-core attention kernel writes
@@ -112,6 +113,11 @@ struct AttnArgs {
   const Unit* units;
   const Group* groups;
   const int32_t* delta;       // [seg_slots][W]: i_q(w) - view offset, or -1 (not visible)
+  // Several query tokens per worker: W counts query rows per problem ("virtual workers"
+  // v = (worker, token)), and the two tables below are set; both are null for one query per
+  // worker (then v = w and q row = p * W + w).
+  const int32_t* qrow;        // [P][W]: row of q / out / lse of (problem, v), or -1 (padding)
+  const int32_t* vlen;        // [seg_slots][W]: tokens of the segment v may see (causal cut)
   const FreshTok* fresh;      // appended tokens, per problem in piece order (fused append)
   const __nv_bfloat16* k_raw; // fused append: this layer's new keys / values [n][H_kv][D],
   const __nv_bfloat16* v_raw; //   or null when the append kernel has written them already

@@ -62,8 +62,9 @@ __device__ __forceinline__ void merge_row(const AttnArgs& a, int item, int lane)
     M = cm;
   }
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  const int w = r / a.G, hq = g.h * a.G + r % a.G;
-  const size_t oi = ((size_t)g.p * a.W + w) * a.H_q + hq;
+  const int qr = query_row(a, g.p, r / a.G), hq = g.h * a.G + r % a.G;
+  if (qr < 0) return;                           // padding row: no output
+  const size_t oi = (size_t)qr * a.H_q + hq;
   if (act) {
     if (a.out_f32) {
       reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + oi * D)[lane] =

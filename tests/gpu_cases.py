@@ -123,3 +123,63 @@ def run_case(w: wl.Workload, steps: int, out_dtype="f32", bernoulli=None, pools=
 
 def small(base: wl.Workload, **kw) -> wl.Workload:
     return dataclasses.replace(base, **kw)
+
+
+def run_mq_case(w: wl.Workload, n_new, n_q, seed=0, tol=TOL, finished=None):
+    """One step with a custom append (n_new [P][W+1]) and several causal query tokens per worker
+    (n_q [P][W]) through hw_concurrent_attention_mq, against the oracle's method_mq; then the
+    step end and one ordinary decode step."""
+    import torch
+    from shared_kv_concurrent_gb300 import binding
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner, to_device_bf16
+    r = WorkloadRunner(w)
+    c = orun.prefill(w)
+    g = np.random.default_rng(seed)
+    n_new = np.asarray(n_new, dtype=np.int32).reshape(w.num_problems, w.num_workers + 1)
+    n_q = np.asarray(n_q, dtype=np.int32).reshape(w.num_problems, w.num_workers)
+    tot = int(n_new.sum())
+    kb = wl.f32_to_bf16_bits(g.standard_normal((tot, w.num_kv_heads, w.head_dim)).astype(np.float32))
+    vb = wl.f32_to_bf16_bits(g.standard_normal((tot, w.num_kv_heads, w.head_dim)).astype(np.float32))
+    N = int(n_q.sum())
+    qb = wl.f32_to_bf16_bits(g.standard_normal((N, w.num_q_heads, w.head_dim)).astype(np.float32))
+    worst = 0.0
+    kd, vd = to_device_bf16(kb), to_device_bf16(vb)   # read until the step's attention
+    for layer in range(w.num_layers):
+        r.cache.append_kv(layer, n_new, kd, vd)
+        c.append(layer, n_new, orun.bf16(kb), orun.bf16(vb))
+    for layer in range(w.num_layers):
+        out = torch.full((N, w.num_q_heads, w.head_dim), float("nan"), dtype=torch.float32,
+                         device="cuda")
+        lse = torch.full((N, w.num_q_heads), float("nan"), dtype=torch.float32, device="cuda")
+        r.cache.concurrent_attention_mq(layer, to_device_bf16(qb), n_q, out, "f32", lse)
+        torch.cuda.synchronize()
+        ref, ref_lse = A.method_mq(c, layer, orun.bf16(qb).astype(np.float64), n_q)
+        got = out.cpu().numpy()
+        err = float(np.abs(got - ref).max()) if N else 0.0
+        worst = max(worst, err)
+        assert err <= tol, (layer, err)
+        if N:
+            assert np.abs(lse.cpu().numpy() - ref_lse).max() <= tol
+        check_pools(r, c, layer, 64)
+    fin = np.zeros((w.num_problems, w.num_workers), np.uint8) if finished is None else finished
+    r.end(0, fin)
+    torch.cuda.synchronize()
+    del kd, vd
+    c.step_end(fin)
+    dev_tables_equal(r, c)
+    # an ordinary decode step afterwards
+    inputs = r.step_inputs(1)
+    r.append(inputs)
+    orun.append_step(c, w, 1)
+    P, W, Hq, D = w.num_problems, w.num_workers, w.num_q_heads, w.head_dim
+    outs = [torch.full((P, W, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+            for _ in range(w.num_layers)]
+    r.attend(inputs, outs, None, "f32")
+    torch.cuda.synchronize()
+    for layer in range(w.num_layers):
+        ref, _ = A.method(c, layer, orun.query(w, layer, 1))
+        assert np.abs(outs[layer].cpu().numpy() - ref).max() <= tol
+    st, info = r.cache.check_device_errors()
+    assert st == binding.HW_OK, info
+    r.cache.close()
+    return worst

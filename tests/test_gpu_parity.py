@@ -106,6 +106,54 @@ def test_cache_layouts_with_commits(layout):
     G.run_case(w, steps=6, bernoulli=0.4)
 
 
+def test_multi_query_paragraph_header():
+    """After a step, two workers append a multi-token header and the others one token; every
+    appended token is a query (tensor-core path, 112 query rows of one KV head)."""
+    import gpu_cases as G
+    w = G.small(wl.c4(), common_len=(1500,), worker_len=((0, 300, 17, 256, 129, 1, 600, 40),),
+                steps=3)
+    n_new = [[0, 5, 1, 1, 3, 1, 1, 1, 1]]
+    G.run_mq_case(w, n_new, [row[1:] for row in n_new], finished=np.array([[0, 1, 0, 0, 1, 0, 0, 0]], np.uint8))
+
+
+def test_multi_query_older_tokens_and_layouts():
+    """Queries that reach back past this step's tokens, in two layouts and two problems."""
+    import gpu_cases as G
+    for layout in ("combined", "step_wise"):
+        w = G.small(wl.c5(), num_problems=2, common_len=(700, 1300),
+                    worker_len=((9, 0, 130, 20), (3, 5, 0, 1)), steps=3, layout=layout)
+        G.run_mq_case(w, [[0, 1, 1, 1, 1], [2, 1, 1, 0, 1]], [[4, 0, 2, 1], [1, 6, 0, 2]],
+                      seed=1)
+
+
+def test_multi_query_cuda_core_path():
+    """Few rows per KV head (2 workers x 4 heads): the CUDA-core kernel with the causal cut."""
+    import gpu_cases as G
+    w = G.small(wl.tiny(), common_len=(300,), worker_len=((70, 5),), steps=3)
+    G.run_mq_case(w, [[0, 3, 1]], [[3, 2]], seed=2)
+
+
+def test_multi_query_over_one_tile_is_refused():
+    import torch
+    from shared_kv_concurrent_gb300 import binding
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner
+    import gpu_cases as G
+    w = G.small(wl.c4(), common_len=(500,), worker_len=((20,) * 8,), steps=2)
+    r = WorkloadRunner(w)
+    n_q = np.full((1, 8), 2, np.int32)
+    n_q[0, 0] = 3                                   # 17 query rows x G 8 > 128
+    q = torch.zeros(17, 64, 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(17, 64, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.HogwildError) as e:
+        r.cache.concurrent_attention_mq(0, q, n_q, out)
+    assert e.value.status == binding.HW_ERR_CAPACITY
+    n_q[0, 0] = 21                                  # more than the block holds
+    with pytest.raises(binding.HogwildError) as e:
+        r.cache.concurrent_attention_mq(0, q, n_q, out)
+    assert e.value.status == binding.HW_ERR_INVALID_ARG
+    r.cache.close()
+
+
 def test_full_size_w4_common16384_64_layers():
     """All 64 layers run on the device; the oracle computes the first two and the last layer
     (the tables are shared by every layer, the pools are not)."""
