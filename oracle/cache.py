@@ -118,6 +118,11 @@ class Segment:
 LAYOUTS = ("combined", "step_wise", "contiguous", "no_sync")
 
 
+def merged_positions(segments) -> np.ndarray:
+    """Position of every token of ``segments`` (in order) in the segment they merge into."""
+    return np.arange(sum(s.length for s in segments))
+
+
 class HogwildCache:
     def __init__(self, num_problems: int, num_workers: int, num_layers: int, num_kv_heads: int,
                  head_dim: int, rope_theta: float, page_size: int, num_pages: int,
@@ -271,6 +276,67 @@ class HogwildCache:
                 if finished[p, w] and self.segments[self.live[p][w]].length > 0:
                     self.common[p].append(self.live[p][w])
                     self.live[p][w] = self._new_segment(p, w)
+
+    def compact(self, p: int, first: int, count: int) -> int:
+        """Merge common segments first .. first+count-1 of problem p into one segment with one
+        RoPE frame (reading 1 of section 8's "correct by RoPE offset": the moved block's keys are
+        re-rotated to their positions in the common history, here relative to the merged
+        segment's start).  Returns the new segment id.
+
+        Readings (the pages name the correction, not its bookkeeping):
+        * only between steps, on committed (common) segments, in commit order; count >= 2;
+        * the merged segment is written into fresh pages taken FIFO from the free list (one per
+          S positions; a contiguous cache takes one page and the merge must fit its capacity);
+          the old segments' pages then go back to the end of the free list, segment by segment
+          in commit order, each in its page order; the old segments stay in the table, empty;
+        * the merged segment's writer is the segments' common origin, or -1 (shared history)
+          when they differ -- which the contiguous and no-sync layouts, whose views depend on
+          the writer, refuse;
+        * keys: the token at merged position j is stored rotated at j (the fp64 oracle re-rotates
+          from the raw key); values unchanged.  Views are unchanged: the merged segment takes the
+          span the old ones had, so every attention output stays the same.
+        """
+        if self.step_pending is not None:
+            raise InvalidArg("compaction between steps only")
+        common = self.common[p]
+        if count < 2 or first < 0 or first + count > len(common):
+            raise InvalidArg("bad segment range")
+        olds = [self.segments[sid] for sid in common[first:first + count]]
+        origins = {s.origin for s in olds}
+        origin = next(iter(origins)) if len(origins) == 1 else -1
+        if len(origins) > 1 and self.layout in ("contiguous", "no_sync"):
+            raise InvalidArg("the layout's views depend on the writer")
+        total = sum(s.length for s in olds)
+        if self.contiguous:
+            if total > self.S:
+                raise Capacity("block capacity exceeded")
+            need = 1 if total else 0
+        else:
+            need = -(-total // self.S)
+        if need > len(self.free):
+            raise OutOfPages("page pool exhausted")
+        new = Segment(len(self.segments), p, origin, self.L)
+        self.segments.append(new)
+        new.pages = [self.free.popleft() for _ in range(need)]
+        new.length = total
+        for layer in range(self.L):
+            kr = [s.raw_k(layer) for s in olds if s.length]
+            vr = [s.raw_v(layer) for s in olds if s.length]
+            if kr:
+                k = np.concatenate(kr)
+                new._raw_k[layer] = [k]
+                new._raw_v[layer] = [np.concatenate(vr)]
+                new._stored_k[layer] = [rope(k, merged_positions(olds)[:, None], self.theta)]
+        for s in olds:
+            self.free.extend(s.pages)
+            s.pages = []
+            s.length = 0
+            for lst in (s._raw_k, s._raw_v, s._stored_k):
+                for layer in range(self.L):
+                    lst[layer] = []
+            s._cat.clear()
+        common[first:first + count] = [new.id]
+        return new.id
 
     # -- exports for bit-exact comparison ------------------------------------------------
 

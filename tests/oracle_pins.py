@@ -486,6 +486,94 @@ def check_mq_single_worker_is_causal_prefill():
     assert np.allclose(out, ref.transpose(1, 0, 2), atol=1e-12), np.abs(out - ref.transpose(1, 0, 2)).max()
 
 
+# ------------------------------------------------------------------------- compaction
+
+
+def _compaction_history(seed, layout="combined", S=4):
+    g = np.random.default_rng(seed)
+    c = C.HogwildCache(1, 3, 2, 2, 8, 1e4, S, 64, layout=layout, page_order=g.permutation(64))
+    for n, fin in (([[5, 3, 2, 4]], [[1, 0, 1]]), ([[1, 2, 1, 1]], [[0, 1, 0]]),
+                   ([[0, 2, 3, 1]], [[1, 1, 0]])):
+        tot = int(np.sum(n))
+        for layer in range(2):
+            c.append(layer, n, g.standard_normal((tot, 2, 8)), g.standard_normal((tot, 2, 8)))
+        c.step_end(fin)
+    return c, g
+
+
+def _next_step(c, g):
+    for layer in range(2):
+        c.append(layer, [[1, 1, 1, 1]], g.standard_normal((4, 2, 8)), g.standard_normal((4, 2, 8)))
+    return g.standard_normal((1, 3, 4, 8))
+
+
+def check_compaction_keeps_outputs():
+    """Re-rotating committed segments into one frame (reading 1) and keeping them in their own
+    frames with the offset absorbed by the query (reading 2) give the same attention."""
+    import copy
+    for layout in ("combined", "step_wise"):
+        for first, count in ((0, 2), (1, 3), (0, 6), (2, 2)):
+            c, g = _compaction_history(40 + first + count, layout)
+            c2 = copy.deepcopy(c)
+            c2.compact(0, first, count)
+            q = _next_step(c, copy.deepcopy(g))
+            q2 = _next_step(c2, g)
+            assert np.array_equal(q, q2)
+            for layer in range(2):
+                o1, l1 = A.method(c, layer, q)
+                o2, l2 = A.method(c2, layer, q2)
+                ob, lb = A.brute_force(c2, layer, q2)
+                assert np.allclose(o1, o2, rtol=0, atol=1e-12) and np.allclose(l1, l2, atol=1e-12)
+                assert np.allclose(o2, ob, rtol=0, atol=1e-12)
+
+
+def check_compaction_rerotates_stored_keys():
+    """The merged keys are the old stored keys turned by their segment's offset in the merge
+    (the rotation composes additively: rho(rho(k, j), o) = rho(k, j + o))."""
+    c, _ = _compaction_history(50)
+    olds = [c.segments[s] for s in c.common[0][1:4]]
+    offs = np.cumsum([0] + [s.length for s in olds])
+    expect = np.concatenate([rope_complex(s.stored_k(1), offs[i], 1e4)
+                             for i, s in enumerate(olds) if s.length])
+    sid = c.compact(0, 1, 3)
+    assert np.allclose(c.segments[sid].stored_k(1), expect, rtol=0, atol=1e-12)
+
+
+def check_compaction_pages_hand():
+    """Worked by hand, page size 4: prompt 5 (pages 9, 8), A's paragraph 3 (page 7), B's 6
+    (pages 6, 5).  Merging all three (14 tokens) takes the next four free pages 4, 3, 2, 1; the
+    old pages return to the end of the free list as 9, 8, 7, 6, 5."""
+    c = C.HogwildCache(1, 2, 1, 1, 2, 1e4, 4, 10, page_order=list(range(9, -1, -1)))
+    c.append(0, [[5, 3, 6]], np.ones((14, 1, 2)), np.ones((14, 1, 2)))
+    c.step_end([[1, 1]])
+    t = c.tables()
+    assert [s[4] for s in t["segments"][:3]] == [[9, 8], [7], [6, 5]]
+    assert t["free_count"] == 5
+    sid = c.compact(0, 0, 3)
+    t = c.tables()
+    assert sid == 5 and t["common"] == [[5]]
+    assert t["segments"][5] == (0, -1, 14, 0, [4, 3, 2, 1])
+    assert [s[2:] for s in t["segments"][:3]] == [(0, 0, [])] * 3
+    assert list(c.free) == [0, 9, 8, 7, 6, 5]
+    entries, i_q = c.view(0, 0)
+    assert entries[0] == (5, 0, 14)
+
+
+def check_compaction_refusals():
+    c, _ = _compaction_history(60, "contiguous")
+    try:
+        c.compact(0, 1, 2)              # A's and C's paragraphs: two writers
+        raise AssertionError("mixed writers merged in the contiguous layout")
+    except C.InvalidArg:
+        pass
+    c.append(0, [[1, 1, 1, 1]], np.ones((4, 2, 8)), np.ones((4, 2, 8)))
+    try:
+        c.compact(0, 0, 2)
+        raise AssertionError("compaction during a step")
+    except C.InvalidArg:
+        pass
+
+
 ALL_CHECKS = [
     check_rope_complex_form, check_rope_d2_textbook, check_inv_freq_values, check_rope_invariants,
     check_views_golden, check_view_offsets_and_query_position, check_pages_hand_example,
@@ -495,4 +583,6 @@ ALL_CHECKS = [
     check_relabel_two_workers, check_layout_views_golden, check_layouts_textbook_attention,
     check_layouts_coincide_without_commits, check_mq_brute_vs_method, check_mq_one_query_is_decode,
     check_mq_chunk_equals_token_by_token, check_mq_single_worker_is_causal_prefill,
+    check_compaction_keeps_outputs, check_compaction_rerotates_stored_keys,
+    check_compaction_pages_hand, check_compaction_refusals,
 ]

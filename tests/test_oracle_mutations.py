@@ -139,6 +139,10 @@ def _view_contiguous_own_first(self, p, w):
 _orig_view = C.HogwildCache.view
 
 
+def _merged_positions_local(segments):
+    return np.concatenate([np.arange(s.length) for s in segments] or [np.zeros(0, int)])
+
+
 def _own_visible_one_more(n, back):
     return min(n, n - back + 1)
 
@@ -163,6 +167,7 @@ MUTATIONS = {
     "commits_in_descending_id": [(C.HogwildCache, "step_end", _step_end_commit_descending)],
     "layout_ignored": [(C.HogwildCache, "view", _view_layout_ignored)],
     "causal_cut_off_by_one": [(A, "own_visible", _own_visible_one_more)],
+    "compaction_keeps_block_local_positions": [(C, "merged_positions", _merged_positions_local)],
     "chunk_queries_share_one_position": [(A, "query_position", _query_position_unshifted)],
     "step_wise_shows_others": [(C.HogwildCache, "view", _view_step_wise_shows_others)],
     "contiguous_own_output_first": [(C.HogwildCache, "view", _view_contiguous_own_first)],
