@@ -230,6 +230,27 @@ hw_status hw_concurrent_attention_noalloc(hw_ctx* ctx, int32_t layer, const void
 hw_status hw_step_end(hw_ctx* ctx, const uint8_t* finished, void* stream);
 
 /*
+ * Compaction (summary section 8: a finished block moves to the end of the common history and
+ * is "corrected by RoPE offset" -- reading 1 of that correction; hw_step_end does reading 2,
+ * an index remap): problem p's common segments first .. first+count-1 (commit order; 0 is
+ * the prompt) merge into one segment with one RoPE frame.  Each key is re-rotated from its
+ * block-local position j to its position in the merge (j plus the segment's offset in it) and,
+ * with its value, copied into fresh pages taken FIFO from the free list; the old pages then
+ * return to the end of the free list (segment by segment in commit order, each in page order)
+ * and the old segments stay in the table, empty.  Views and attention results do not change
+ * (up to the extra bf16 rounding of the re-rotated keys); the segment count and the partial
+ * tiles at segment ends go down.  The merged segment's writer (origin) is the segments'
+ * common writer, or -1 when they differ.
+ *   Between steps only (no hw_append_kv since the last hw_step_end); count >= 2.  Enqueues
+ *   one kernel on `stream`, in stream order after every earlier call of the context.
+ * Errors: HW_ERR_INVALID_ARG (range, during a step, or writers that differ in the contiguous
+ * or no-sync layout, whose views depend on the writer); HW_ERR_OUT_OF_PAGES (nothing changes);
+ * HW_ERR_CAPACITY (segment table full, or a contiguous block's capacity).
+ */
+hw_status hw_compact_segments(hw_ctx* ctx, int32_t problem, int32_t first, int32_t count,
+                              void* stream);
+
+/*
  * Synchronise ``stream`` and read the device error word.  Returns HW_OK, or
  * HW_ERR_DEVICE_CHECK / HW_ERR_DEVICE_TIMEOUT if a kernel recorded one (the word is then
  * cleared).  info: host uint32[4] or NULL: {code, kernel id, detail a, detail b}.

@@ -58,6 +58,10 @@ class HogwildCache:
     def append_kv(self, layer: int, n_new, k_raw, v_raw, stream=None) -> None:
         binding.hw_append_kv(self.ctx, layer, n_new, k_raw, v_raw, stream)
 
+    def compact_segments(self, problem: int, first: int, count: int, stream=None) -> None:
+        """Merge common segments first .. first+count-1 into one RoPE frame (between steps)."""
+        binding.hw_compact_segments(self.ctx, problem, first, count, stream)
+
     def concurrent_attention_mq(self, layer: int, q, n_q, out=None, out_dtype: str = "bf16",
                                 lse=None, stream=None):
         """Several causal query tokens per worker (the last n_q[p][w] tokens of its block)."""

@@ -30,7 +30,7 @@ HW_OUT_F32 = 1
 EXPORTED = (
     "hw_status_string", "hw_last_cuda_error", "hw_pool_size", "hw_workspace_size", "hw_create",
     "hw_destroy", "hw_append_kv", "hw_concurrent_attention", "hw_concurrent_attention_noalloc",
-    "hw_concurrent_attention_mq",
+    "hw_concurrent_attention_mq", "hw_compact_segments",
     "hw_step_end",
     "hw_check_device_errors", "hw_profile_enable", "hw_profile_read", "hw_get_counts",
     "hw_get_segment", "hw_get_blocks", "hw_get_view",
@@ -91,6 +91,7 @@ def load() -> ctypes.CDLL:
         "hw_concurrent_attention": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P]),
         "hw_concurrent_attention_noalloc": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P]),
         "hw_concurrent_attention_mq": (ctypes.c_int, [_P, _I32, _P, _P, _P, _I32, _P, _P]),
+        "hw_compact_segments": (ctypes.c_int, [_P, _I32, _I32, _I32, _P]),
         "hw_step_end": (ctypes.c_int, [_P, _P, _P]),
         "hw_check_device_errors": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
         "hw_profile_enable": (ctypes.c_int, [_P, _I32]),
@@ -211,6 +212,11 @@ def hw_concurrent_attention_noalloc(ctx: int, layer: int, q, out, out_dtype: int
     _check(load().hw_concurrent_attention_noalloc(ctx, layer, _dptr(q), _dptr(out), out_dtype,
                                                   _dptr(lse), _stream(stream)),
            "hw_concurrent_attention_noalloc")
+
+
+def hw_compact_segments(ctx: int, problem: int, first: int, count: int, stream=None) -> None:
+    _check(load().hw_compact_segments(ctx, problem, first, count, _stream(stream)),
+           "hw_compact_segments")
 
 
 def hw_step_end(ctx: int, finished=None, stream=None) -> None:

@@ -1203,6 +1203,95 @@ hw_status hw_step_end(hw_ctx* c, const uint8_t* finished, void* stream) {
   return HW_OK;
 }
 
+hw_status hw_compact_segments(hw_ctx* c, int32_t problem, int32_t first, int32_t count,
+                              void* stream) {
+  if (!c || problem < 0 || problem >= c->cfg.num_problems) return HW_ERR_INVALID_ARG;
+  if (c->step_active) return HW_ERR_INVALID_ARG;          // between steps only
+  std::vector<int32_t>& com = c->common[problem];
+  if (count < 2 || first < 0 || (int64_t)first + count > (int64_t)com.size())
+    return HW_ERR_INVALID_ARG;
+  const int32_t S = c->cfg.page_size;
+  int64_t total = 0;
+  bool mixed = false;
+  const int32_t origin0 = c->segs[com[first]].origin;
+  for (int32_t i = first; i < first + count; ++i) {
+    total += c->segs[com[i]].length;
+    mixed |= c->segs[com[i]].origin != origin0;
+  }
+  if (mixed && (c->cfg.layout == HW_LAYOUT_CONTIGUOUS || c->cfg.layout == HW_LAYOUT_NO_SYNC))
+    return HW_ERR_INVALID_ARG;                            // these views depend on the writer
+  if ((int64_t)c->segs.size() + 1 > c->lay.max_segments) return HW_ERR_CAPACITY;
+  if (c->cfg.contiguous && total > S) return HW_ERR_CAPACITY;
+  const int64_t need = c->cfg.contiguous ? (total > 0 ? 1 : 0) : (total + S - 1) / S;
+  if (need > (int64_t)c->free_pages.size()) return HW_ERR_OUT_OF_PAGES;
+  std::vector<int32_t> dst_pages(c->free_pages.begin(), c->free_pages.begin() + need);
+  // Runs of tokens that stay inside one page on both sides, at most 128 each.
+  std::vector<hw::CompactRun> runs;
+  int64_t pos = 0;                                        // position in the merged segment
+  for (int32_t i = first; i < first + count; ++i) {
+    const Seg& sg = c->segs[com[i]];
+    const int64_t rot = pos;
+    for (int32_t j = 0; j < sg.length;) {
+      const int32_t sp = c->cfg.contiguous ? 0 : j / S, ss = c->cfg.contiguous ? j : j % S;
+      const int64_t d = pos;
+      const int32_t dp = c->cfg.contiguous ? 0 : (int32_t)(d / S);
+      const int32_t ds = c->cfg.contiguous ? (int32_t)d : (int32_t)(d % S);
+      const int32_t n = (int32_t)std::min<int64_t>({(int64_t)S - ss, (int64_t)S - ds,
+                                                    (int64_t)sg.length - j, 128});
+      runs.push_back(hw::CompactRun{sg.pages[sp], ss, dst_pages[dp], ds, n, (int32_t)rot});
+      j += n;
+      pos += n;
+    }
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!runs.empty()) {
+    const size_t bytes = runs.size() * sizeof(hw::CompactRun);
+    if (bytes > c->lay.slot_seq_off) return HW_ERR_CAPACITY;
+    int slot = 0;
+    hw_status st = c->acquire_slot(&slot);
+    if (st != HW_OK) return st;
+    std::memcpy(c->h_slot(slot), runs.data(), bytes);
+    // in stream order: after every earlier call's reads of the old pages, before any later use
+    HW_CUDA(cudaMemcpyAsync(c->d_slot(slot), c->h_slot(slot), bytes, cudaMemcpyHostToDevice, s));
+    hw::CompactArgs a{};
+    a.runs = reinterpret_cast<const hw::CompactRun*>(c->d_slot(slot));
+    a.num_runs = (int32_t)runs.size();
+    a.num_layers = c->cfg.num_layers;
+    a.k_pool = c->k_pool;
+    a.v_pool = c->v_pool;
+    a.layer_elems = c->layer_elems;
+    a.rope_cos = c->d_cos();
+    a.rope_sin = c->d_sin();
+    a.err = c->d_err();
+    a.H_kv = c->cfg.num_kv_heads;
+    a.D = c->cfg.head_dim;
+    a.S = S;
+    a.num_pages = c->cfg.num_pages;
+    a.max_position = c->cfg.max_position;
+    hw::launch_compact(a, s);
+    HW_CUDA(cudaGetLastError());
+    HW_CUDA(cudaEventRecord(c->slot_ev[slot], s));
+    c->slot_used[slot] = true;
+    c->n_launch += 1;
+  }
+  // Tables: the merged segment takes the range's place; the old pages go back to the free list.
+  for (int64_t k = 0; k < need; ++k) c->free_pages.pop_front();
+  int32_t origin = mixed ? -1 : origin0;
+  const int32_t sid = c->new_segment(problem, origin);
+  c->segs[sid].pages = dst_pages;
+  c->segs[sid].length = (int32_t)total;
+  for (int32_t i = first; i < first + count; ++i) {
+    Seg& sg = c->segs[com[i]];
+    for (int32_t pg : sg.pages) c->free_pages.push_back(pg);
+    sg.pages.clear();
+    sg.length = 0;
+  }
+  com.erase(com.begin() + first, com.begin() + first + count);
+  com.insert(com.begin() + first, sid);
+  ++c->epoch;                     // tables changed: no plan of the old state is reused
+  return HW_OK;
+}
+
 hw_status hw_check_device_errors(hw_ctx* c, void* stream, uint32_t* info) {
   if (!c) return HW_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;

@@ -23,7 +23,7 @@ enum : uint32_t {
   ERR_TIMEOUT = 1u << 3,       // a bounded wait gave up
   ERR_PLAN = 1u << 4,          // an inconsistent plan entry
 };
-enum : uint32_t { KID_APPEND = 1, KID_ATTN_FMA = 2, KID_MERGE = 3, KID_ATTN_TC = 4 };
+enum : uint32_t { KID_APPEND = 1, KID_ATTN_FMA = 2, KID_MERGE = 3, KID_ATTN_TC = 4, KID_COMPACT = 5 };
 
 // One run of appended tokens: ntok consecutive tokens of one block that land in one page.
 struct AppendRun {
@@ -33,6 +33,24 @@ struct AppendRun {
   int32_t slot0;     // slot of the first token in the page
   int32_t pos0;      // block-local position of the first token (RoPE angle)
   int32_t pad;
+};
+
+// Compaction: n tokens copied from (src_page, src_slot ..) to (dst_page, dst_slot ..) of every
+// layer, keys turned by rot positions on the way (the run never crosses a page on either side).
+struct CompactRun {
+  int32_t src_page, src_slot, dst_page, dst_slot, n, rot;
+};
+
+struct CompactArgs {
+  const CompactRun* runs;
+  int32_t num_runs, num_layers;
+  __nv_bfloat16* k_pool;      // pool bases: [L][num_pages][H_kv][S][D]
+  __nv_bfloat16* v_pool;
+  size_t layer_elems;
+  const float* rope_cos;
+  const float* rope_sin;
+  uint32_t* err;
+  int32_t H_kv, D, S, num_pages, max_position;
 };
 
 // A piece: <= 128 consecutive tokens (one kernel tile) of one segment, inside one page.
@@ -148,6 +166,7 @@ cudaError_t prepare_attention_fma(int D);
 cudaError_t prepare_attention_tc(int D);
 
 void launch_append(const AppendArgs& a, cudaStream_t s);
+void launch_compact(const CompactArgs& a, cudaStream_t s);
 void launch_attention_fma(const AttnArgs& a, cudaStream_t s);
 // Launches the attention kernel; ev_before / ev_after (optional) are recorded directly around
 // it (and it is then launched without programmatic chaining).

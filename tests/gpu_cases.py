@@ -31,7 +31,7 @@ def dev_tables_equal(runner, cache):
             assert giq == iq and [tuple(x) for x in ge] == [tuple(x) for x in e]
 
 
-def check_pools(runner, cache, layer, max_tokens_per_seg=None, dev_layer=None):
+def check_pools(runner, cache, layer, max_tokens_per_seg=None, dev_layer=None, rerotated=None):
     """Stored keys within 1 bf16 ulp of the fp64 rotation; values bit-exact; at the oracle's
     (page, slot) of every token -- so page addressing is checked bit-exactly too.
 
@@ -65,29 +65,39 @@ def check_pools(runner, cache, layer, max_tokens_per_seg=None, dev_layer=None):
         pair = np.abs(rk[..., :half]) + np.abs(rk[..., half:])
         pair = np.concatenate([pair, pair], axis=-1)
         bound = 2.0 ** -8 * np.abs(sk) + 2.0 ** -21 * pair
+        if rerotated and sid in rerotated:
+            # A compacted key was rounded to bf16 at its block-local position, then turned by
+            # its offset in fp32 and rounded again, once per compaction it went through: each
+            # earlier rounding error (half an ulp of each element) is mixed across the pair by
+            # the rotations after it.
+            bound = 2.0 ** -8 * np.abs(sk) + rerotated[sid] * 2.0 ** -8 * pair
         excess = np.abs(gk - sk) - bound
         assert excess.max() <= 0, (sid, float(np.abs(gk - sk).max()), float(excess.max()))
         assert np.array_equal(gv, ev), sid
 
 
 def run_case(w: wl.Workload, steps: int, out_dtype="f32", bernoulli=None, pools=True,
-             pool_sample=None, tol=TOL, layer_ids=None, check_steps=None):
+             pool_sample=None, tol=TOL, layer_ids=None, check_steps=None, compact_after=None,
+             max_segments=0):
     """Run ``steps`` decode steps on both sides; compare tables after every step end.
 
     ``layer_ids``: the workload layers the oracle computes (default all); the library always
-    runs every layer.  ``check_steps``: the steps whose outputs (and pools) are compared
+    runs every layer.  ``compact_after``: {step: [(problem, first, count), ...]} compactions
+    done on both sides after that step's end (a range that reaches past the common list is
+    cut to it).  ``check_steps``: the steps whose outputs (and pools) are compared
     (default all) -- the oracle still appends every step, so later steps see the same cache.
     """
     import torch
     from shared_kv_concurrent_gb300 import binding
     from shared_kv_concurrent_gb300.runner import WorkloadRunner
-    r = WorkloadRunner(w)
+    r = WorkloadRunner(w, max_segments=max_segments)
     ids = list(range(w.num_layers)) if layer_ids is None else list(layer_ids)
     c = orun.prefill(w, layer_ids=ids)
     dev_tables_equal(r, c)
     worst = 0.0
     P, W, Hq, D = w.num_problems, w.num_workers, w.num_q_heads, w.head_dim
     dt = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    rerotated = {}                        # compacted segment -> compactions its keys went through
     for step in range(steps):
         inputs = r.step_inputs(step)
         r.append(inputs)
@@ -110,11 +120,19 @@ def run_case(w: wl.Workload, steps: int, out_dtype="f32", bernoulli=None, pools=
                 assert np.array_equal(np.isfinite(gl), fin)
                 assert np.abs(gl[fin] - ref_lse[fin]).max() <= tol
                 if pools:
-                    check_pools(r, c, i, pool_sample, dev_layer=layer)
+                    check_pools(r, c, i, pool_sample, dev_layer=layer, rerotated=rerotated)
         fin = wl.finished_mask(w, step, bernoulli)
         r.end(step, fin)
         c.step_end(fin)
         dev_tables_equal(r, c)
+        for p, first, count in (compact_after or {}).get(step, []):
+            count = min(count, len(c.common[p]) - first)
+            if count < 2:
+                continue
+            depth = 1 + max(rerotated.get(sid, 0) for sid in c.common[p][first:first + count])
+            r.cache.compact_segments(p, first, count)
+            rerotated[c.compact(p, first, count)] = depth
+            dev_tables_equal(r, c)
     st, info = r.cache.check_device_errors()
     assert st == binding.HW_OK, info
     r.cache.close()

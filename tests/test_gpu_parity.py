@@ -154,6 +154,34 @@ def test_multi_query_over_one_tile_is_refused():
     r.cache.close()
 
 
+def test_compaction_between_steps():
+    """Commits build up committed segments; compactions merge ranges of them (the prompt with
+    the first paragraphs, then later paragraphs) and the following steps attend to the merged
+    segments: outputs, tables, free list and re-rotated pools against the oracle."""
+    import gpu_cases as G
+    w = G.small(wl.c5(), num_problems=2, common_len=(700, 300), worker_len=((130, 0, 257, 40),
+                (5, 90, 0, 200)), steps=8, num_layers=2,
+                commit_steps=tuple(range(8)))    # (page budget for up to one commit a step)
+    G.run_case(w, steps=8, bernoulli=0.4,
+               compact_after={2: [(0, 0, 3), (1, 1, 4)], 5: [(0, 1, 6), (1, 0, 9)]})
+
+
+def test_compaction_contiguous_cache_and_refusals():
+    import gpu_cases as G
+    from shared_kv_concurrent_gb300 import binding
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner
+    w = G.small(wl.c2(), common_len=(1000,), worker_len=((130, 70),), page_size=2048, steps=4,
+                commit_steps=(0, 1, 2, 3))     # (page budget for a commit every step)
+    G.run_case(w, steps=4, bernoulli=0.6, compact_after={1: [(0, 0, 4)], 2: [(0, 0, 4)]},
+               max_segments=32)         # (each commit and each compaction adds a segment)
+    r = WorkloadRunner(w)
+    for args in ((0, 0, 1), (0, 1, 2), (1, 0, 2)):   # too few, past the list, no such problem
+        with pytest.raises(binding.HogwildError) as e:
+            r.cache.compact_segments(*args)
+        assert e.value.status == binding.HW_ERR_INVALID_ARG
+    r.cache.close()
+
+
 def test_full_size_w4_common16384_64_layers():
     """All 64 layers run on the device; the oracle computes the first two and the last layer
     (the tables are shared by every layer, the pools are not)."""
