@@ -56,7 +56,7 @@ def captured_traffic():
         rec = text.split("kernel-source-sha256:")[1].split()[0]
         traffic = int(text.split("traffic-bytes-per-launch:")[1].split()[0])
         h = hashlib.sha256()
-        for name in ("attn_tc.cu", "tc_ptx.cuh", "hw_internal.h"):
+        for name in ("attn_tc.cu", "tc_ptx.cuh", "hw_internal.h", "hw_device.cuh"):
             with open(os.path.join(ROOT, "shared_kv_concurrent_gb300", "csrc", name), "rb") as f:
                 h.update(f.read())
         return traffic if h.hexdigest() == rec else None
