@@ -170,21 +170,52 @@ def cpu_baseline(w, seconds=12.0):
                       f"per-block query rotation, LSE merge), median {per_step * 1e3:.1f} ms/step"}
 
 
+def workload_config(w):
+    """The workload keys of a bench line's config (both arms)."""
+    return {"workload": w.name, "layout": w.layout, "problems": w.num_problems,
+            "workers": w.num_workers, "layers": w.num_layers, "H_q": w.num_q_heads,
+            "H_kv": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+            "common_tokens": list(w.common_len)}
+
+
 def run_reference(args):
+    """The oracle (as it stands) on the host cores: W untimed decode steps, then exactly K timed
+    ones, each a whole decode step of the same workload (append, method form, step end)."""
+    import workload as wl
+    from oracle import attention as A
+    from oracle import run as orun
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    w = workload_for(args.config, args.layout)
-    per_step, n, threads = oracle_sample(w, seconds=max(10.0, 3.0 * args.steps), max_steps=None)
-    b, _ = step_bytes(w, 0)
-    v = b / per_step / 1e9
+    base = workload_for(args.config, args.layout)
+    w = wl.scaled(base, name=base.name, steps=args.warmup + args.steps + 1)
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    c = orun.prefill(w)
+
+    def one_step(step):
+        orun.append_step(c, w, step)
+        for layer in range(c.L):
+            A.method(c, layer, orun.query(w, layer, step))
+        c.step_end(wl.finished_mask(w, step))
+
+    for step in range(args.warmup):
+        one_step(step)
+    t0 = time.perf_counter()
+    total = 0
+    for step in range(args.warmup, args.warmup + args.steps):
+        one_step(step)
+        total += step_bytes(w, step)[0]
+    t = time.perf_counter() - t0
+    v = total / t / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
-            "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": per_step * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name},
-            "worker_tokens_per_s": w.num_problems * w.num_workers / per_step,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "worker_tokens_per_s": w.num_problems * w.num_workers * args.steps / t,
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{n} decode steps of {w.name}"},
+                             "sample": f"{args.steps} timed decode steps of {w.name} after "
+                                       f"{args.warmup} untimed ones"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -390,10 +421,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "layout": w.layout, "problems": P, "workers": W,
-                   "layers": L, "H_q": Hq,
-                   "H_kv": w.num_kv_heads, "head_dim": D, "page_size": w.page_size,
-                   "common_tokens": list(w.common_len), "view_tokens_first_timed_step":
+        "config": {**workload_config(w), "view_tokens_first_timed_step":
                    w.view_tokens(timed[0][1]), "parallelism": f"replicas{world}",
                    "l2": (f"inputs larger than L2: {R} independent cache(s) of this workload "
                           f"({kv_mb:.0f} MB of K/V each) used in turn, so a layer's K/V return "
