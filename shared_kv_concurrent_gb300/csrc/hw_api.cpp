@@ -57,7 +57,7 @@ hw_status cuda_fail(cudaError_t e) {
   } while (0)
 
 struct Layout {
-  size_t err, cos, sin, slots, partials, tickets, total;
+  size_t err, cos, sin, slots, partials, total;
   size_t slot_bytes, slot_seq_off;   // a slot ends with the plan's 8-byte sequence number
   int32_t max_segments, max_append, max_pieces, max_units, max_seg_slots, rows;
   int32_t num_slots, max_fresh;
@@ -127,8 +127,6 @@ Layout make_layout(const hw_config* c) {
   off += (size_t)L.num_slots * L.slot_bytes;
   L.partials = off;
   off += align_up((size_t)L.max_units * L.rows * hw::part_stride(c->head_dim) * sizeof(float), kAlign);
-  L.tickets = off;
-  off += align_up((size_t)P * H * sizeof(uint32_t), kAlign);
   L.total = off;
   return L;
 }
@@ -494,7 +492,6 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
   if (e == cudaSuccess) e = cudaMemsetAsync(c->ws + lay.err, 0, kAlign, s);
   if (e == cudaSuccess)                      // plan slots, with their sequence words
     e = cudaMemsetAsync(c->ws + lay.slots, 0, (size_t)lay.num_slots * lay.slot_bytes, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(c->ws + lay.tickets, 0, lay.total - lay.tickets, s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(c->d_cos(), tc.data(), tc.size() * sizeof(float), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess)

@@ -143,15 +143,35 @@ def small(base: wl.Workload, **kw) -> wl.Workload:
     return dataclasses.replace(base, **kw)
 
 
-def run_mq_case(w: wl.Workload, n_new, n_q, seed=0, tol=TOL, finished=None):
+def run_mq_case(w: wl.Workload, n_new, n_q, seed=0, tol=TOL, finished=None, pre_steps=0,
+                bernoulli=0.5, compact=(), max_segments=0):
     """One step with a custom append (n_new [P][W+1]) and several causal query tokens per worker
     (n_q [P][W]) through hw_concurrent_attention_mq, against the oracle's method_mq; then the
-    step end and one ordinary decode step."""
+    step end and one ordinary decode step.  Before it: ``pre_steps`` ordinary decode steps with
+    random commits, then the compactions ``compact`` [(problem, first, count)] on both sides."""
     import torch
     from shared_kv_concurrent_gb300 import binding
     from shared_kv_concurrent_gb300.runner import WorkloadRunner, to_device_bf16
-    r = WorkloadRunner(w)
+    r = WorkloadRunner(w, max_segments=max_segments)
     c = orun.prefill(w)
+    for step in range(pre_steps):
+        inputs = r.step_inputs(step)
+        r.append(inputs)
+        orun.append_step(c, w, step)
+        r.attend(inputs, [torch.empty(w.num_problems, w.num_workers, w.num_q_heads, w.head_dim,
+                                      dtype=torch.bfloat16, device="cuda")
+                          for _ in range(w.num_layers)])
+        fin = wl.finished_mask(w, step, bernoulli)
+        r.end(step, fin)
+        c.step_end(fin)
+    rerotated = {}                        # compacted segment -> compactions its keys went through
+    for p, first, count in compact:
+        count = min(count, len(c.common[p]) - first)
+        if count >= 2:
+            depth = 1 + max(rerotated.get(sid, 0) for sid in c.common[p][first:first + count])
+            r.cache.compact_segments(p, first, count)
+            rerotated[c.compact(p, first, count)] = depth
+    dev_tables_equal(r, c)
     g = np.random.default_rng(seed)
     n_new = np.asarray(n_new, dtype=np.int32).reshape(w.num_problems, w.num_workers + 1)
     n_q = np.asarray(n_q, dtype=np.int32).reshape(w.num_problems, w.num_workers)
@@ -178,24 +198,25 @@ def run_mq_case(w: wl.Workload, n_new, n_q, seed=0, tol=TOL, finished=None):
         assert err <= tol, (layer, err)
         if N:
             assert np.abs(lse.cpu().numpy() - ref_lse).max() <= tol
-        check_pools(r, c, layer, 64)
+        check_pools(r, c, layer, 64, rerotated=rerotated)
     fin = np.zeros((w.num_problems, w.num_workers), np.uint8) if finished is None else finished
-    r.end(0, fin)
+    r.end(pre_steps, fin)
     torch.cuda.synchronize()
     del kd, vd
     c.step_end(fin)
     dev_tables_equal(r, c)
     # an ordinary decode step afterwards
-    inputs = r.step_inputs(1)
+    nxt = pre_steps + 1
+    inputs = r.step_inputs(nxt)
     r.append(inputs)
-    orun.append_step(c, w, 1)
+    orun.append_step(c, w, nxt)
     P, W, Hq, D = w.num_problems, w.num_workers, w.num_q_heads, w.head_dim
     outs = [torch.full((P, W, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
             for _ in range(w.num_layers)]
     r.attend(inputs, outs, None, "f32")
     torch.cuda.synchronize()
     for layer in range(w.num_layers):
-        ref, _ = A.method(c, layer, orun.query(w, layer, 1))
+        ref, _ = A.method(c, layer, orun.query(w, layer, nxt))
         assert np.abs(outs[layer].cpu().numpy() - ref).max() <= tol
     st, info = r.cache.check_device_errors()
     assert st == binding.HW_OK, info

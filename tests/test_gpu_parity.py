@@ -133,6 +133,26 @@ def test_multi_query_cuda_core_path():
     G.run_mq_case(w, [[0, 3, 1]], [[3, 2]], seed=2)
 
 
+def test_commits_compaction_then_header_prefill():
+    """Decode steps with random commits, a compaction of the committed paragraphs, then a step
+    in which two workers prefill a header and attend causally to it -- the inference flow of
+    section 8 end to end, on a paged two-layer cache in the step-wise layout."""
+    import gpu_cases as G
+    w = G.small(wl.c5(), num_problems=2, num_layers=2, common_len=(600, 900),
+                worker_len=((40, 0, 130, 7), (12, 300, 1, 0)), steps=12,
+                commit_steps=tuple(range(12)), layout="step_wise")
+    G.run_mq_case(w, [[0, 4, 1, 1, 1], [2, 1, 6, 1, 1]], [[4, 1, 1, 1], [1, 6, 1, 1]], seed=3,
+                  pre_steps=6, bernoulli=0.5, compact=[(0, 0, 5), (1, 1, 4)], max_segments=48)
+
+
+def test_multi_query_head_dim_64_tensor_cores():
+    """The causal cut and the row map on the D = 64 tensor-core kernel."""
+    import gpu_cases as G
+    w = G.small(wl.tiny(), num_workers=4, num_q_heads=16, num_kv_heads=2, common_len=(700,),
+                worker_len=((0, 129, 64, 300),), steps=3)
+    G.run_mq_case(w, [[0, 3, 1, 2, 1]], [[3, 1, 2, 4]], seed=4)
+
+
 def test_multi_query_over_one_tile_is_refused():
     import torch
     from shared_kv_concurrent_gb300 import binding
