@@ -170,6 +170,23 @@ def cpu_baseline(w, seconds=12.0):
                       f"per-block query rotation, LSE merge), median {per_step * 1e3:.1f} ms/step"}
 
 
+def slowest_rank_seconds(t, world, device=None):
+    """The timed region's length on the slowest of the world's ranks (every rank gets it):
+    one max all-reduce, the only collective of a timed run (replicas share no data)."""
+    if world <= 1:
+        return t
+    import torch
+    import torch.distributed as dist
+    x = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(x, op=dist.ReduceOp.MAX)
+    return float(x.item())
+
+
+def job_value(world, bytes_per_rank, t_slowest):
+    """Whole-job GB/s: every rank streams the same workload; the job ends with its slowest rank."""
+    return world * bytes_per_rank / t_slowest / 1e9
+
+
 def workload_config(w):
     """The workload keys of a bench line's config (both arms)."""
     return {"workload": w.name, "layout": w.layout, "problems": w.num_problems,
@@ -351,10 +368,7 @@ def run_ours(args):
         attn_n += pr["timed_attention"]
         binding.hw_profile_enable(ctx, False)
     prof = {"attention_ms": attn_ms_sum, "timed_attention": attn_n}
-    if world > 1:
-        t = torch.tensor([t_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_total = float(t.item())
+    t_total = slowest_rank_seconds(t_total, world, dev)
     # End to end through the public API: inputs in pinned host memory.
     # (cache 0, L2 flushed before every step, one step at a time with a synchronize)
     e2e = None
@@ -412,7 +426,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return
     peak, peak_kind = measured_peaks()
-    value = world * total_bytes / t_total / 1e9
+    value = job_value(world, total_bytes, t_total)
     attn_ms = prof["attention_ms"] / max(1, prof["timed_attention"])
     attn_launch_bytes = attn_bytes / max(1, prof["timed_attention"])   # one launch per layer
     achieved = attn_launch_bytes / (attn_ms / 1e3) / 1e9
