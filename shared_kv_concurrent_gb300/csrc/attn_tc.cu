@@ -64,7 +64,10 @@ struct Cfg {
   static constexpr uint32_t kHalfBytes = kTile * 128;          // one {64, 128} TMA box
   static constexpr uint32_t kTileBytes = kHalves * kHalfBytes; // K or V tile
   static constexpr uint32_t kQBytes = kRowsM * D * 2;          // rotated query tile
-  static constexpr int kSlots = D == 128 ? 5 : 8;
+  // K/V ring slots: at D = 128 two tiles in flight; a fifth slot measured 1 % slower per
+  // chained step (the early fills compete with the previous step's last tiles), a third fewer
+  // starves the MMA.
+  static constexpr int kSlots = D == 128 ? 4 : 8;
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kRingOff = 2 * kQBytes;
   static constexpr uint32_t kBarOff = kRingOff + kSlots * kTileBytes;
