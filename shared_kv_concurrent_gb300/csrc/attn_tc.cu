@@ -528,9 +528,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_tile = [&](int32_t y) -> bool {
         for (int part = 0; part < 2; ++part, ++j) {
           const int s = j % C::kSlots;
-          // The first K tile goes out alone with its V: every CTA fills its ring at once at
-          // start-up, and the first tile would otherwise arrive with the last of that burst.
-          if (j == 2 && !mbar_wait(bar_full(0), 0, abort, kWaitLimitNs)) return false;
           if (j >= (uint32_t)C::kSlots &&
               !mbar_wait(bar_empty(s), ((j / C::kSlots) - 1) & 1, abort, kWaitLimitNs))
             return false;
