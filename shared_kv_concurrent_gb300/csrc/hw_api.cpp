@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstdint>
 #include <cstring>
 #include <deque>
 #include <mutex>
@@ -148,6 +149,7 @@ struct PlanScratch {
   std::vector<hw::Group> groups;
   std::vector<hw::FreshTok> fresh;
   std::vector<int32_t> delta, refs, piece_fresh0, src_base, ref_of, view_ref, vlen, qrow;
+  std::vector<uint8_t> piece_early;     // the piece may be loaded before the programmatic wait
   int32_t qrow_next = 0;
   std::vector<int64_t> view_off;
   std::vector<int32_t> ref_sid, ref_slot, ref_tiles, prob_ref_begin, prob_common_refs, unit_rem,
@@ -160,6 +162,9 @@ struct PlanScratch {
 struct Seg {
   int32_t problem, origin, length, pending;
   std::vector<int32_t> pages;
+  // Positions >= recent_from were written in the last completed step or by a compaction
+  // since: the next attention launch may not load them before its programmatic wait.
+  int32_t recent_from = INT32_MAX;
   int32_t visible() const { return length + pending; }
 };
 
@@ -686,6 +691,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   const Layout& L = c->lay;
   PlanScratch& ps = c->ps;
   ps.pieces.clear();
+  ps.piece_early.clear();
   ps.delta.clear();
   ps.units.clear();
   ps.groups.clear();
@@ -804,6 +810,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     const int32_t fresh = (sg.pending > 0 && j + cnt > sg.length) ? 1 : 0;
     if ((int64_t)ps.pieces.size() >= L.max_pieces) return false;
     ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
+    ps.piece_early.push_back(!fresh && j + cnt <= sg.recent_from ? 1 : 0);
     ps.pieces.push_back(hw::Piece{ps.ref_slot[r], pg, slot0, cnt, fresh, j});
     if (fuse && fresh) {
       const int32_t sid = ps.ref_sid[r];
@@ -889,7 +896,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         u.delta0 = -1;
         u.seq = u.seq_b = u.seq_c = (uint32_t)seq;
         u.first_tok = -1;
-        if (rg.second > rg.first && !ps.pieces[rg.first].fresh)
+        if (rg.second > rg.first && ps.piece_early[rg.first])
           u.first_tok = ps.pieces[rg.first].page * S + ps.pieces[rg.first].slot0;
         ps.units.push_back(u);
       }
@@ -1182,6 +1189,7 @@ hw_status hw_step_end(hw_ctx* c, const uint8_t* finished, void* stream) {
   c->pend_k.clear();
   c->pend_v.clear();
   for (Seg& sg : c->segs) {
+    sg.recent_from = sg.pending > 0 ? sg.length : INT32_MAX;
     sg.length += sg.pending;
     sg.pending = 0;
   }
@@ -1277,6 +1285,7 @@ hw_status hw_compact_segments(hw_ctx* c, int32_t problem, int32_t first, int32_t
   const int32_t sid = c->new_segment(problem, origin);
   c->segs[sid].pages = dst_pages;
   c->segs[sid].length = (int32_t)total;
+  c->segs[sid].recent_from = 0;           // written by the compaction kernel
   for (int32_t i = first; i < first + count; ++i) {
     Seg& sg = c->segs[com[i]];
     for (int32_t pg : sg.pages) c->free_pages.push_back(pg);

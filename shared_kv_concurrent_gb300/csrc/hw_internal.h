@@ -80,7 +80,11 @@ __host__ __device__ constexpr int part_stride(int D) { return D + 4; }
 // carries the low 32 bits of the plan's sequence number (seq, seq_b, seq_c; 0 when the plan is
 // not gated), and a vector whose copy matches belongs to the current plan.
 struct __align__(16) Unit {
-  int32_t first_tok;  // page * S + slot of the first piece if it holds no new token, else -1
+  int32_t first_tok;  // page * S + slot of the first piece if the kernel may load it before
+                      // it waits for the kernel it follows, else -1: a piece with no token of
+                      // this step (the kernel writes or waits for those) and none written by
+                      // the previous step or a compaction since (a launch that may still be in
+                      // flight could have written them)
   int32_t group;      // p * H_kv + h
   uint32_t seq;
   int32_t seg0;       // seg_slot of the first piece, -1 if the unit has none
