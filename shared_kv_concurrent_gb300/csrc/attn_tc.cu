@@ -30,8 +30,8 @@
 // issued and frees its TMEM.  Launch chaining (programmatic dependent launch): the kernel may
 // start while the preceding kernel of the stream (normally the append) still runs; it streams
 // tiles of older tokens meanwhile and waits for that kernel before it reads the queries or a
-// tile holding tokens of the current step, and lets the merge kernel start during its
-// epilogue.
+// tile holding tokens of the current step, and lets the merge kernel launch before its
+// partial results are stored.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -791,10 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 128) HW_TRACE_EV(11 + 4 * i);
         ++i;
       }
-      if (threadIdx.x == 128) {
-        HW_TRACE_EV(5);
-        pdl_launch_dependents();
-      }
+      if (threadIdx.x == 128) HW_TRACE_EV(5);
       // Epilogue.  Each lane's (O row, max, sum) over its columns goes to shared memory (the
       // K/V ring is idle once the last MMA has completed) as stage[chunk][row][PS], with the
       // log-sum-exp weights of the T chunks of every row; after the role branches all warps
@@ -857,6 +854,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // The merge kernel may launch once every CTA is here (it waits for this grid before reading
+  // the partials).  Triggering right after the softmax loop instead measured 1 % slower per
+  // chained step: the merge's CTAs then take the SMs that free up first.
+  if (threadIdx.x == 0) pdl_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
