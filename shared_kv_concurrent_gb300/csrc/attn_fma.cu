@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
 // K3: the log-sum-exp merge of the units' partials (merge_row, hw_merge.cuh), one warp per
 // (group, query row), as a kernel of its own: used after the CUDA-core attention and after the
 // tensor-core attention when that kernel does not merge itself.
-constexpr int kMergeWarps = 8;
+constexpr int kMergeWarps = 4;
 
 template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const AttnArgs a) {
