@@ -343,3 +343,30 @@ def test_multi_token_appends_fused_and_deferred():
     st, info = r.cache.check_device_errors()
     assert st == binding.HW_OK, info
     r.cache.close()
+
+
+def test_readme_example():
+    """The usage example of the README runs as written (and matches the oracle)."""
+    import torch
+    from oracle import attention as A
+    from oracle.cache import HogwildCache as OracleCache
+    from shared_kv_concurrent_gb300 import HogwildCache, config_for
+    g = torch.Generator().manual_seed(7)
+    k_new = torch.randn(8, 8, 128, generator=g).to(torch.bfloat16).cuda()
+    v_new = torch.randn(8, 8, 128, generator=g).to(torch.bfloat16).cuda()
+    q = torch.randn(1, 8, 64, 128, generator=g).to(torch.bfloat16).cuda()
+    cfg = config_for(num_problems=1, num_workers=8, num_layers=1, num_q_heads=64, num_kv_heads=8,
+                     head_dim=128, page_size=256, num_pages=4096, max_position=1 << 17,
+                     rope_theta=1e6)
+    cache = HogwildCache(cfg)
+    n_new = np.ones((1, 9), np.int32)
+    n_new[0, 0] = 0
+    cache.append_kv(0, n_new, k_new, v_new)
+    out = cache.concurrent_attention(0, q)
+    cache.step_end(np.zeros((1, 8), np.uint8))
+    torch.cuda.synchronize()
+    oc = OracleCache(1, 8, 1, 8, 128, 1e6, 256, 4096)
+    oc.append(0, n_new, k_new.float().cpu().numpy(), v_new.float().cpu().numpy())
+    ref, _ = A.method(oc, 0, q.float().cpu().numpy())
+    assert np.abs(out.float().cpu().numpy() - ref).max() <= 1e-2
+    cache.close()
