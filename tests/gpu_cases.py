@@ -5,6 +5,7 @@ from __future__ import annotations
 import dataclasses
 
 import numpy as np
+import pytest
 
 import workload as wl
 from oracle import attention as A
@@ -222,3 +223,106 @@ def run_mq_case(w: wl.Workload, n_new, n_q, seed=0, tol=TOL, finished=None, pre_
     assert st == binding.HW_OK, info
     r.cache.close()
     return worst
+
+
+def run_random_session(seed: int, layout="combined", P=2, W=3, H_q=8, H_kv=2, D=64, L=2,
+                       S=128, steps=10, tol=TOL):
+    """Seeded random use of every entry point against the oracle: appends of 0..3 tokens per
+    block (sometimes a long one, which takes the append kernel), decode or multi-query attention
+    of every layer, random commits, and compactions of random common ranges (a refusal must
+    match on both sides).  Tables after every step end; pools at the end."""
+    import torch
+    from shared_kv_concurrent_gb300 import HogwildCache, binding, config_for
+    from shared_kv_concurrent_gb300.runner import to_device_bf16
+    from oracle import cache as OC
+    g = np.random.default_rng(seed)
+    pages = 2048
+    order = g.permutation(pages).astype(np.int32)
+    cfg = config_for(num_problems=P, num_workers=W, num_layers=L, num_q_heads=H_q,
+                     num_kv_heads=H_kv, head_dim=D, page_size=S, num_pages=pages,
+                     max_position=1 << 14, rope_theta=1e4, max_segments=256, layout=layout)
+    dev = HogwildCache(cfg, page_order=order)
+    c = OC.HogwildCache(P, W, L, H_kv, D, 1e4, S, pages, page_order=order, layout=layout)
+
+    class _R:                               # what dev_tables_equal / check_pools expect
+        cache = dev
+    r = _R()
+    bf = lambda shape: wl.f32_to_bf16_bits(g.standard_normal(shape).astype(np.float32))
+    rerotated = {}
+    worst = 0.0
+    stats = {"decode": 0, "mq": 0, "compacted": 0, "refused": 0, "commits": 0}
+    for step in range(steps):
+        n_new = g.integers(0, 4, size=(P, W + 1)).astype(np.int32)
+        if step == 0 or g.random() < 0.2:
+            n_new[g.integers(P), g.integers(W + 1)] += int(g.integers(17, 60))
+        tot = int(n_new.sum())
+        keep = []
+        for layer in range(L):
+            kb, vb = bf((tot, H_kv, D)), bf((tot, H_kv, D))
+            kd, vd = to_device_bf16(kb), to_device_bf16(vb)
+            keep.append((kd, vd))
+            dev.append_kv(layer, n_new, kd, vd)
+            c.append(layer, n_new, orun.bf16(kb), orun.bf16(vb))
+        own = np.array([[c.segments[c.live[p][w]].visible for w in range(W)] for p in range(P)])
+        use_mq = g.random() < 0.5
+        stats["mq" if use_mq else "decode"] += 1
+        if use_mq:
+            n_q = np.minimum(own, g.integers(0, 4, size=(P, W))).astype(np.int32)
+            while (n_q.sum(axis=1) * (H_q // H_kv)).max() > 128:
+                n_q = n_q // 2
+        for layer in range(L):
+            if use_mq:
+                N = int(n_q.sum())
+                if N == 0:
+                    continue
+                qb = bf((N, H_q, D))
+                out = torch.full((N, H_q, D), float("nan"), device="cuda")
+                lse = torch.full((N, H_q), float("nan"), device="cuda")
+                dev.concurrent_attention_mq(layer, to_device_bf16(qb), n_q, out, "f32", lse)
+                ref, ref_lse = A.method_mq(c, layer, orun.bf16(qb).astype(np.float64), n_q)
+            else:
+                qb = bf((P, W, H_q, D))
+                out = torch.full((P, W, H_q, D), float("nan"), device="cuda")
+                lse = torch.full((P, W, H_q), float("nan"), device="cuda")
+                dev.concurrent_attention(layer, to_device_bf16(qb), out, "f32", lse)
+                ref, ref_lse = A.method(c, layer, orun.bf16(qb).astype(np.float64))
+            torch.cuda.synchronize()
+            got, gl = out.cpu().numpy(), lse.cpu().numpy()
+            err = float(np.abs(got - ref).max())
+            worst = max(worst, err)
+            assert err <= tol, (seed, layout, step, layer, use_mq, err)
+            fin_ = np.isfinite(ref_lse)
+            assert np.array_equal(np.isfinite(gl), fin_)
+            assert np.abs(gl[fin_] - ref_lse[fin_]).max(initial=0.0) <= tol
+        fin = (g.random((P, W)) < 0.3).astype(np.uint8)
+        stats["commits"] += int(fin.sum())
+        dev.step_end(fin)
+        c.step_end(fin)
+        torch.cuda.synchronize()
+        del keep
+        dev_tables_equal(r, c)
+        if g.random() < 0.4:
+            p = int(g.integers(P))
+            n_common = len(c.common[p])
+            if n_common >= 2:
+                first = int(g.integers(0, n_common - 1))
+                count = int(g.integers(2, n_common - first + 1))
+                olds = c.common[p][first:first + count]
+                try:
+                    sid = c.compact(p, first, count)
+                except OC.InvalidArg:
+                    with pytest.raises(binding.HogwildError) as e:
+                        dev.compact_segments(p, first, count)
+                    assert e.value.status == binding.HW_ERR_INVALID_ARG
+                    stats["refused"] += 1
+                else:
+                    dev.compact_segments(p, first, count)
+                    stats["compacted"] += 1
+                    rerotated[sid] = 1 + max(rerotated.get(s_, 0) for s_ in olds)
+                dev_tables_equal(r, c)
+    for layer in range(L):
+        check_pools(r, c, layer, None, rerotated=rerotated)
+    st, info = dev.check_device_errors()
+    assert st == binding.HW_OK, info
+    dev.close()
+    return worst, stats

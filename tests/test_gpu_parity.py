@@ -370,3 +370,17 @@ def test_readme_example():
     ref, _ = A.method(oc, 0, q.float().cpu().numpy())
     assert np.abs(out.float().cpu().numpy() - ref).max() <= 1e-2
     cache.close()
+
+
+@pytest.mark.parametrize("seed,layout,D,H_q,H_kv,S", [
+    (11, "combined", 64, 8, 2, 128), (12, "step_wise", 64, 8, 2, 128),
+    (13, "contiguous", 128, 16, 2, 128), (14, "no_sync", 128, 16, 2, 128),
+    (15, "combined", 128, 32, 4, 256), (16, "step_wise", 128, 64, 8, 256),
+    (17, "contiguous", 64, 16, 4, 256), (18, "combined", 128, 16, 1, 128)])
+def test_random_sessions(seed, layout, D, H_q, H_kv, S):
+    """Every entry point in seeded random order against the oracle (see run_random_session)."""
+    import gpu_cases as G
+    _, stats = G.run_random_session(seed, layout=layout, D=D, H_q=H_q, H_kv=H_kv, S=S, steps=14)
+    assert stats["decode"] and stats["mq"] and stats["commits"], stats
+    assert stats["compacted"] + stats["refused"] > 0, stats
+    print(seed, layout, stats)
