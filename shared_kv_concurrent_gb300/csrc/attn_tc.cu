@@ -28,10 +28,11 @@
 // the current segment's tiles.  All waits are bounded: one that runs out raises a CTA abort
 // flag, records ERR_TIMEOUT in the error word, and the CTA drains the copies and MMAs it
 // issued and frees its TMEM.  Launch chaining (programmatic dependent launch): the kernel may
-// start while the preceding kernel of the stream (normally the append) still runs; it streams
-// tiles of older tokens meanwhile and waits for that kernel before it reads the queries or a
-// tile holding tokens of the current step, and lets the merge kernel launch before its
-// partial results are stored.
+// start while the preceding kernel of the stream (the previous call's merge, or the append
+// kernel) still runs; meanwhile it sets up and loads its first tile, when that tile holds only
+// tokens no launch still in flight can have written, and it waits for that kernel before it
+// reads the queries or any other tile; it lets the merge kernel launch before its partial
+// results are stored.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
