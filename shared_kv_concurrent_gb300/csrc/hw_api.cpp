@@ -34,6 +34,9 @@ constexpr int kProfPairs = 4096;       // timed launches kept per hw_profile_rea
 // tensor-core attention kernel itself (fused append); larger appends use the append kernel.
 constexpr int kFuseTok = 16;
 constexpr int kMaxRows = 128;          // query rows of one (problem, KV head): one MMA tile
+// Tensor-core plans: about this many tiles per SM per wave of units, at most kMaxWaves waves.
+constexpr int64_t kWaveTiles = 24;
+constexpr int64_t kMaxWaves = 4;
 
 thread_local int g_cuda_err = 0;
 // Plan sequence numbers, unique in the process: a slot word left by an earlier context in
@@ -791,8 +794,18 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   // kernels the same, so the balance is in tiles.
   int64_t total_tiles = 0;
   for (int64_t t : ps.prob_tiles) total_tiles += t * H;
+  // target_override: the tensor-core kernel's CTA count per wave (one CTA per SM).  A step with
+  // many tiles per SM gets several waves of smaller units: a unit never spans two groups, so
+  // one wave of units sized by their group leaves some SMs with far more tiles than others,
+  // while the block scheduler hands the next unit of a later wave to whichever SM is free.
+  int64_t waves = 1;
+  if (target_override > 0) {
+    const int64_t per_sm = total_tiles / target_override;
+    waves = std::max<int64_t>(1, std::min<int64_t>(kMaxWaves, (per_sm + kWaveTiles / 2) / kWaveTiles));
+  }
   int64_t target_units = std::max<int64_t>((int64_t)P * H,
-                                           target_override > 0 ? target_override : 4ll * c->num_sms);
+                                           target_override > 0 ? target_override * waves
+                                                               : 4ll * c->num_sms);
   if (unit_cap > 0) {
     if (unit_cap < (int64_t)P * H) return false;
     // per-group counts are floored and then raised to >= 1: keep room for that raise
