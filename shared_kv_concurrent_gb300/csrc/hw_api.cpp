@@ -794,14 +794,26 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   // kernels the same, so the balance is in tiles.
   int64_t total_tiles = 0;
   for (int64_t t : ps.prob_tiles) total_tiles += t * H;
-  // target_override: the tensor-core kernel's CTA count per wave (one CTA per SM).  A step with
-  // many tiles per SM gets several waves of smaller units: a unit never spans two groups, so
-  // one wave of units sized by their group leaves some SMs with far more tiles than others,
-  // while the block scheduler hands the next unit of a later wave to whichever SM is free.
+  // target_override: the tensor-core kernel's CTA count per wave (one CTA per SM).  A unit never
+  // spans two groups, so when groups differ in size one wave of units leaves some SMs with far
+  // more tiles than others; a step with many tiles per SM and such an imbalance gets several
+  // waves of smaller units instead, and the block scheduler hands the next unit to whichever
+  // SM is free.  (With units of about equal size, more waves only add per-unit set-up.)
   int64_t waves = 1;
-  if (target_override > 0) {
+  if (target_override > 0 && total_tiles > 0) {
     const int64_t per_sm = total_tiles / target_override;
-    waves = std::max<int64_t>(1, std::min<int64_t>(kMaxWaves, (per_sm + kWaveTiles / 2) / kWaveTiles));
+    int64_t largest = 0, units1 = 0;                // the one-wave plan, as computed below
+    for (int32_t p = 0; p < P; ++p) {
+      const int64_t Tt = ps.prob_tiles[p];
+      if (Tt == 0) continue;
+      const int64_t n1 = std::max<int64_t>(
+          1, std::min<int64_t>(Tt, (target_override * Tt * H + total_tiles / 2) / (total_tiles * H)));
+      largest = std::max(largest, (Tt + n1 - 1) / n1);
+      units1 += n1 * H;
+    }
+    const bool unbalanced = units1 > 0 && largest * units1 * 4 > total_tiles * 5;  // > 1.25 x mean
+    if (unbalanced)
+      waves = std::max<int64_t>(1, std::min<int64_t>(kMaxWaves, (per_sm + kWaveTiles / 2) / kWaveTiles));
   }
   int64_t target_units = std::max<int64_t>((int64_t)P * H,
                                            target_override > 0 ? target_override * waves
