@@ -257,6 +257,19 @@ hw_status hw_compact_segments(hw_ctx* ctx, int32_t problem, int32_t first, int32
  */
 hw_status hw_check_device_errors(hw_ctx* ctx, void* stream, uint32_t* info);
 
+/*
+ * Fault injection on the host, for tests of the error path: the next `count` plans this
+ * context uploads (a step's plan goes up with its first hw_append_kv; an attention call
+ * outside a step uploads its own) are announced to the kernels with a sequence number that
+ * never arrives.  Every kernel gated on such a plan gives up after its bounded wait (about one
+ * second), skips its work, writes empty partials and records a timeout, so that the next
+ * hw_check_device_errors returns HW_ERR_DEVICE_TIMEOUT.  Outputs of the affected calls are
+ * zero (tensor-core and CUDA-core attention alike), and tokens whose append such a call
+ * carried are not written; the host tables are unaffected and the context stays usable.
+ * count = 0 cancels what is left.  Errors: HW_ERR_INVALID_ARG (null context, count < 0).
+ */
+hw_status hw_debug_expire_plans(hw_ctx* ctx, int32_t count);
+
 /* ---- measurement ------------------------------------------------------------------------ */
 
 typedef struct hw_profile {

@@ -32,8 +32,8 @@ EXPORTED = (
     "hw_destroy", "hw_append_kv", "hw_concurrent_attention", "hw_concurrent_attention_noalloc",
     "hw_concurrent_attention_mq", "hw_compact_segments",
     "hw_step_end",
-    "hw_check_device_errors", "hw_profile_enable", "hw_profile_read", "hw_get_counts",
-    "hw_get_segment", "hw_get_blocks", "hw_get_view",
+    "hw_check_device_errors", "hw_debug_expire_plans", "hw_profile_enable", "hw_profile_read",
+    "hw_get_counts", "hw_get_segment", "hw_get_blocks", "hw_get_view",
 )
 
 
@@ -94,6 +94,7 @@ def load() -> ctypes.CDLL:
         "hw_compact_segments": (ctypes.c_int, [_P, _I32, _I32, _I32, _P]),
         "hw_step_end": (ctypes.c_int, [_P, _P, _P]),
         "hw_check_device_errors": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+        "hw_debug_expire_plans": (ctypes.c_int, [_P, _I32]),
         "hw_profile_enable": (ctypes.c_int, [_P, _I32]),
         "hw_profile_read": (ctypes.c_int, [_P, ctypes.POINTER(hw_profile)]),
         "hw_get_counts": (ctypes.c_int, [_P, _PI32, _PI32]),
@@ -235,6 +236,10 @@ def hw_check_device_errors(ctx: int, stream=None):
     info = (ctypes.c_uint32 * 4)()
     st = load().hw_check_device_errors(ctx, _stream(stream), info)
     return st, list(info)
+
+
+def hw_debug_expire_plans(ctx: int, count: int) -> None:
+    _check(load().hw_debug_expire_plans(ctx, int(count)), "hw_debug_expire_plans")
 
 
 def hw_profile_enable(ctx: int, enable: bool = True) -> None:

@@ -36,7 +36,14 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
   __shared__ int plan_ok;
   if (threadIdx.x == 0) plan_ok = plan_arrived(a.gate, plan_seq_now(a.gate), a.err, KID_ATTN_FMA);
   __syncthreads();
-  if (!plan_ok) return;
+  if (!plan_ok) {
+    // No plan: this unit's partial rows are written empty (m = -inf, l = 0, o = 0), so the
+    // merge gives zero for them; the error word says why.
+    float* part = a.partials + (size_t)blockIdx.x * rows * part_stride(D);
+    for (int e = threadIdx.x; e < rows * part_stride(D); e += blockDim.x)
+      part[e] = (e % part_stride(D) == D) ? -CUDART_INF_F : 0.f;
+    return;
+  }
   const Unit u = a.units[blockIdx.x];
   const Group g = a.groups[u.group];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

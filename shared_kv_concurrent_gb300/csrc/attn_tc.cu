@@ -574,12 +574,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = publish(u.piece_begin, u.piece_end) && load_range(u.piece_begin, u.piece_end);
       publish(0, -1);                                  // end of the sequence (also on abort)
       HW_TRACE_EV(3);
-      // Drain: every copy issued must have landed before the CTA can exit.
+      // Drain: every copy issued must have landed before the CTA can exit, abort or not.
+      bool drained = true;
       for (uint32_t s = 0; s < (uint32_t)C::kSlots && s < j; ++s) {
         const uint32_t last = s + ((j - 1 - s) / C::kSlots) * C::kSlots;
-        mbar_wait(bar_full(s), (last / C::kSlots) & 1, abort, kWaitLimitNs);
+        drained = mbar_wait_drain(bar_full(s), (last / C::kSlots) & 1, kWaitLimitNs) && drained;
       }
-      if (!ok && (*abort)) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 0);
+      if ((!ok && (*abort)) || !drained) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 0);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -645,11 +646,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok && i > 0) ok = issue_mma2(i - 1);
       HW_TRACE_EV(4);
+      // Every MMA issued must have completed before TMEM is freed, abort or not.
+      bool drained = true;
       if (issued_any) {
         mma_commit(bar_fin);
-        mbar_wait(bar_fin, 0, abort, kWaitLimitNs);
+        drained = mbar_wait_drain(bar_fin, 0, kWaitLimitNs);
       }
-      if (!ok && (*abort)) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 1);
+      if ((!ok && (*abort)) || !drained) record_error(a.err, ERR_TIMEOUT, KID_ATTN_TC, blockIdx.x, 1);
     }
   } else if (warp == 2 || warp == 3) {
     // ---------------------------------------------------------------- query rotation

@@ -189,6 +189,7 @@ struct hw_ctx {
   // so its kernels stay back to back (programmatic launch chaining across calls).
   cudaStream_t copy_stream = nullptr;
   int next_slot = 0;
+  int32_t expire_plans = 0;                // fault injection: plans announced with a dead number
   hw::TcMaps maps{};
   bool use_tc = false;                     // tensor-core attention (W*G >= 16 rows)
   std::deque<int32_t> free_pages;
@@ -347,6 +348,12 @@ struct hw_ctx {
                             sizeof(seq), cudaMemcpyHostToDevice, copy_stream));
     gate->plan_seq = reinterpret_cast<const unsigned long long*>(d_slot(slot) + lay.slot_seq_off);
     gate->plan_expect = seq;
+    if (expire_plans > 0) {
+      // ~seq: never a sequence number (those count up from 1), and every 32-bit part of it
+      // differs from seq's, so no unit record looks current either
+      gate->plan_expect = ~seq;
+      --expire_plans;
+    }
     return HW_OK;
   }
   static uint64_t next_seq() { return ++g_upload_seq; }
@@ -1333,6 +1340,12 @@ hw_status hw_check_device_errors(hw_ctx* c, void* stream, uint32_t* info) {
   if (!w[0]) return HW_OK;
   HW_CUDA(cudaMemset(c->d_err(), 0, sizeof(w)));
   return (w[0] & hw::ERR_TIMEOUT) ? HW_ERR_DEVICE_TIMEOUT : HW_ERR_DEVICE_CHECK;
+}
+
+hw_status hw_debug_expire_plans(hw_ctx* c, int32_t count) {
+  if (!c || count < 0) return HW_ERR_INVALID_ARG;
+  c->expire_plans = count;
+  return HW_OK;
 }
 
 hw_status hw_profile_enable(hw_ctx* c, int32_t enable) {

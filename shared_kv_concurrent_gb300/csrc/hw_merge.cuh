@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include "hw_device.cuh"
 #include "hw_internal.h"
 
 namespace hw {
@@ -21,6 +22,11 @@ __device__ __forceinline__ void merge_row(const AttnArgs& a, int item, int lane)
   constexpr int PS = part_stride(D);
   const int gi = item / a.rows, r = item - gi * a.rows;
   const Group g = a.groups[gi];
+  if (g.p < 0 || g.p >= a.P || g.h < 0 || g.h >= a.H_kv || g.unit_begin < 0 ||
+      g.unit_begin > g.unit_end || g.unit_end > a.num_units) {
+    if (lane == 0) record_error(a.err, ERR_PLAN, KID_MERGE, gi, r);   // skipped, not trusted
+    return;
+  }
   const bool act = lane < D / 4;
   const size_t stride = (size_t)a.rows * PS;
   const float* base = a.partials + ((size_t)g.unit_begin * a.rows + r) * PS;

@@ -70,6 +70,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Wait for the completion of work this thread issued itself (its TMA copies, its MMAs) before
+// the CTA leaves or frees TMEM: bounded by `limit_ns` only, since an abort raised elsewhere
+// does not stop copies or MMAs already in flight.  Returns false if the limit ran out.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u && globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // ---- TMA -------------------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {

@@ -95,6 +95,7 @@ def test_null_arguments_rejected_before_cuda(lib):
     assert lib.hw_step_end(None, None, None) == binding.HW_ERR_INVALID_ARG
     a, b = ctypes.c_int32(), ctypes.c_int32()
     assert lib.hw_get_counts(None, ctypes.byref(a), ctypes.byref(b)) == binding.HW_ERR_INVALID_ARG
+    assert lib.hw_debug_expire_plans(None, 1) == binding.HW_ERR_INVALID_ARG
     lib.hw_destroy(None)
 
 

@@ -236,6 +236,59 @@ def G_small_empty():
     return dataclasses.replace(wl.tiny(), common_len=(0,), worker_len=((0, 0),))
 
 
+@pytest.mark.parametrize("H_q,kid", [(16, 4), (4, 2)])      # tensor-core, CUDA-core kernel
+def test_plan_wait_times_out_and_the_context_recovers(H_q, kid):
+    """A plan announced with a sequence number that never arrives (host-side injection): the
+    attention kernel gives up after its bounded wait, outputs zero and reports a timeout; the
+    next calls, outside and inside a step, are correct again."""
+    import torch
+    import gpu_cases as G
+    from oracle import attention as A
+    from oracle import run as orun
+    from shared_kv_concurrent_gb300 import binding
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner, to_device_bf16
+    w = G.small(wl.tiny(), num_workers=4, num_q_heads=H_q, num_kv_heads=2, common_len=(300,),
+                worker_len=((5, 0, 130, 64),), steps=2)
+    r = WorkloadRunner(w)
+    c = orun.prefill(w)
+    P, W, D = w.num_problems, w.num_workers, w.head_dim
+    zeros = np.zeros((P, W), np.uint8)
+    inp = r.step_inputs(0)
+    r.append(inp)
+    orun.append_step(c, w, 0)
+    out = torch.empty(P, W, H_q, D, device="cuda")
+    r.attend(inp, [out], None, "f32")
+    r.end(0, zeros)
+    c.step_end(zeros)
+    assert r.cache.check_device_errors()[0] == binding.HW_OK
+    # outside a step: the call uploads its own plan, which is the one that expires
+    q = to_device_bf16(wl.step_q(w, 0, 1))
+    lse = torch.empty(P, W, H_q, device="cuda")
+    binding.hw_debug_expire_plans(r.cache.ctx, 1)
+    out.fill_(float("nan"))
+    r.cache.concurrent_attention(0, q, out, "f32", lse)
+    st, info = r.cache.check_device_errors()
+    assert st == binding.HW_ERR_DEVICE_TIMEOUT and info[1] == kid, (st, info)
+    assert torch.all(out == 0) and torch.all(torch.isinf(lse) & (lse < 0))
+    ref, ref_lse = A.method(c, 0, orun.query(w, 0, 1))
+    r.cache.concurrent_attention(0, q, out, "f32", lse)
+    assert r.cache.check_device_errors()[0] == binding.HW_OK
+    assert np.abs(out.cpu().numpy() - ref).max() <= G.TOL
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= G.TOL
+    # and a whole decode step after it
+    inp = r.step_inputs(1)
+    r.append(inp)
+    orun.append_step(c, w, 1)
+    r.attend(inp, [out], [lse], "f32")
+    ref, ref_lse = A.method(c, 0, orun.query(w, 0, 1))
+    assert r.cache.check_device_errors()[0] == binding.HW_OK
+    assert np.abs(out.cpu().numpy() - ref).max() <= G.TOL
+    r.end(1, zeros)
+    c.step_end(zeros)
+    G.dev_tables_equal(r, c)
+    r.cache.close()
+
+
 def test_protocol_errors_leave_state_unchanged():
     import torch
     from shared_kv_concurrent_gb300 import HogwildCache, HogwildError, binding
