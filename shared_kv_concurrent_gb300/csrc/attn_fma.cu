@@ -168,20 +168,43 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
 // K3: the log-sum-exp merge of the units' partials (merge_row, hw_merge.cuh), one warp per
 // (group, query row), as a kernel of its own: used after the CUDA-core attention and after the
 // tensor-core attention when that kernel does not merge itself.
+//
+// Register budget: the next call's tensor-core attention kernel (programmatic dependent of the
+// merge) launches while the merge still runs, and an SM can hold one of its CTAs beside a merge
+// CTA only if both fit the SM's 65,536 registers: 8 warps at 182 registers (allocated as 184)
+// plus 4 warps at 144 is exactly 65,536.  At 144 registers a row keeps 20 units' loads in flight
+// at once (the benchmark workload has 19 units per group).  Measured: 32.85 -> 32.63 us per
+// decode step on the 32K-common, 8-worker workload, 1.359 -> 1.326 ms per 64-layer step on the
+// 16K-common one.
 constexpr int kMergeWarps = 4;
+constexpr int kMergeChunk = 20;
 
 template <int D>
-__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const AttnArgs a) {
+__global__ void __maxnreg__(144) merge_kernel(const AttnArgs a) {
   // May be launched as a programmatic dependent of the attention kernel: wait for its writes.
   // Whatever follows may start its own prologue now (the library's kernels wait for this grid
   // before they read anything it writes or overwrite the partials it reads).
   HW_SPAN_BEGIN(0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x * kMergeWarps + warp;
+  const bool valid = item < a.num_groups * a.rows;
+  const int gi = valid ? item / a.rows : 0, r = item - gi * a.rows;
+  // The group entry belongs to the call's plan, not to what the attention kernel writes: it is
+  // read before the wait once the plan's sequence word shows that the plan has arrived (an
+  // acquire load; plans without a word were copied before the attention kernel started).
+  Group g{};
+  bool have_g = false;
+  if (valid && plan_seq_now(a.gate) == a.gate.plan_expect) {
+    g = a.groups[gi];
+    have_g = true;
+  }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   HW_SPAN_BEGIN(1);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x * kMergeWarps + warp;
-  if (item < a.num_groups * a.rows) merge_row<D, 24>(a, item, lane);
+  if (valid) {
+    if (!have_g) g = a.groups[gi];
+    merge_row<D, kMergeChunk>(a, gi, r, g, lane);
+  }
   HW_SPAN_END(0);
 }
 

@@ -14,14 +14,13 @@
 
 namespace hw {
 
-// One (group, query row) `item`, by one warp (lane = float4 column).  The units are taken kChunk
-// at a time with all their loads in flight, merged into a running (M, L, O) that is rescaled
-// when M grows.
+// Query row r of group gi (plan entry g), by one warp (lane = float4 column).  The units are
+// taken kChunk at a time with all their loads in flight, merged into a running (M, L, O) that is
+// rescaled when M grows.
 template <int D, int kChunk>
-__device__ __forceinline__ void merge_row(const AttnArgs& a, int item, int lane) {
+__device__ __forceinline__ void merge_row(const AttnArgs& a, int gi, int r, const Group& g,
+                                          int lane) {
   constexpr int PS = part_stride(D);
-  const int gi = item / a.rows, r = item - gi * a.rows;
-  const Group g = a.groups[gi];
   if (g.p < 0 || g.p >= a.P || g.h < 0 || g.h >= a.H_kv || g.unit_begin < 0 ||
       g.unit_begin > g.unit_end || g.unit_end > a.num_units) {
     if (lane == 0) record_error(a.err, ERR_PLAN, KID_MERGE, gi, r);   // skipped, not trusted
