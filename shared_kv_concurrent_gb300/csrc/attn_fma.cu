@@ -169,13 +169,12 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
 // (group, query row), as a kernel of its own: used after the CUDA-core attention and after the
 // tensor-core attention when that kernel does not merge itself.
 //
-// Register budget: the next call's tensor-core attention kernel (programmatic dependent of the
-// merge) launches while the merge still runs, and an SM can hold one of its CTAs beside a merge
-// CTA only if both fit the SM's 65,536 registers: 8 warps at 182 registers (allocated as 184)
-// plus 4 warps at 144 is exactly 65,536.  At 144 registers a row keeps 20 units' loads in flight
-// at once (the benchmark workload has 19 units per group).  Measured: 32.85 -> 32.63 us per
-// decode step on the 32K-common, 8-worker workload, 1.359 -> 1.326 ms per 64-layer step on the
-// 16K-common one.
+// Register budget: at most 144 registers, with 20 units' loads in flight per row at once (the
+// benchmark workload has 19 units per group).  Measured: 32.85 -> 32.63 us per decode step on
+// the 32K-common, 8-worker workload, 1.359 -> 1.326 ms per 64-layer step on the 16K-common one.
+// (At 144 registers a merge CTA and a CTA of the next call's attention kernel, 8 warps at 184,
+// fit one SM's 65,536 registers; the shared-memory split still keeps them apart, and forcing
+// the large split made the step slower.)
 constexpr int kMergeWarps = 4;
 constexpr int kMergeChunk = 20;
 
