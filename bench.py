@@ -370,7 +370,8 @@ def run_ours(args):
     prof = {"attention_ms": attn_ms_sum, "timed_attention": attn_n}
     t_total = slowest_rank_seconds(t_total, world, dev)
     # End to end through the public API: inputs in pinned host memory.
-    # (cache 0, L2 flushed before every step, one step at a time with a synchronize)
+    # (cache 0, L2 flushed before every step, one whole step -- copies in, append, attention,
+    # copy out, step end -- at a time with a synchronize)
     e2e = None
     if e2e_steps:
         runner = runners[0]
@@ -406,9 +407,9 @@ def run_ours(args):
             runner.attend(inp, outs, stream=stream)
             for layer in range(L):
                 host_out[layer].copy_(outs[layer], non_blocking=True)
+            runner.end(s, stream=stream)
             torch.cuda.synchronize()
             e2e_times.append(time.perf_counter() - t0)
-            runner.end(s, stream=stream)
             e2e_bytes += step_bytes(w, s)[0]
         h2d = sum(x.numel() * 2 for x in dk + dv + dq)
         d2h = sum(x.numel() * 2 for x in host_out)
