@@ -289,6 +289,51 @@ def test_plan_wait_times_out_and_the_context_recovers(H_q, kid):
     r.cache.close()
 
 
+def test_last_rope_position_then_the_position_limit():
+    """Views that reach the RoPE table's last row are exact; the append that would pass it is
+    refused with nothing changed, and attention afterwards still matches."""
+    import dataclasses
+    import torch
+    import gpu_cases as G
+    from oracle import attention as A
+    from oracle import run as orun
+    from shared_kv_concurrent_gb300 import HogwildError, binding
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner, to_device_bf16
+    w = G.small(wl.tiny(), steps=3)
+    limit = w.view_tokens(1)                     # view length after step 1's append
+
+    @dataclasses.dataclass(frozen=True)
+    class Limited(type(w)):
+        def max_position(self) -> int:
+            return limit
+
+    r = WorkloadRunner(Limited(**{f.name: getattr(w, f.name) for f in dataclasses.fields(w)}))
+    c = orun.prefill(w)
+    P, W, Hq, D = w.num_problems, w.num_workers, w.num_q_heads, w.head_dim
+    zeros = np.zeros((P, W), np.uint8)
+    out = torch.empty(P, W, Hq, D, device="cuda")
+    for step in range(2):
+        inp = r.step_inputs(step)
+        r.append(inp)
+        orun.append_step(c, w, step)
+        r.attend(inp, [out], None, "f32")
+        ref, _ = A.method(c, 0, orun.query(w, 0, step))
+        assert np.abs(out.cpu().numpy() - ref).max() <= G.TOL, step
+        r.end(step, zeros)
+        c.step_end(zeros)
+    assert max(c.view(p, wk)[-1] for p in range(P) for wk in range(W)) == limit - 1
+    with pytest.raises(HogwildError) as e:
+        r.append(r.step_inputs(2))
+    assert e.value.status == binding.HW_ERR_CAPACITY
+    G.dev_tables_equal(r, c)
+    q = to_device_bf16(wl.step_q(w, 0, 1))
+    r.cache.concurrent_attention(0, q, out, "f32")
+    ref, _ = A.method(c, 0, orun.query(w, 0, 1))
+    assert np.abs(out.cpu().numpy() - ref).max() <= G.TOL
+    assert r.cache.check_device_errors()[0] == binding.HW_OK
+    r.cache.close()
+
+
 def test_protocol_errors_leave_state_unchanged():
     import torch
     from shared_kv_concurrent_gb300 import HogwildCache, HogwildError, binding
