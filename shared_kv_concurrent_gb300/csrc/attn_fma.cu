@@ -172,9 +172,9 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
 // Register budget: at most 144 registers, with 20 units' loads in flight per row at once (the
 // benchmark workload has 19 units per group).  Measured: 32.85 -> 32.63 us per decode step on
 // the 32K-common, 8-worker workload, 1.359 -> 1.326 ms per 64-layer step on the 16K-common one.
-// (At 144 registers a merge CTA and a CTA of the next call's attention kernel, 8 warps at 184,
-// fit one SM's 65,536 registers; the shared-memory split still keeps them apart, and forcing
-// the large split made the step slower.)
+// (At 144 registers a merge CTA and a CTA of the next call's attention kernel, 8 warps at
+// 184 registers as allocated, fit one SM's 65,536 registers; the shared-memory split still
+// keeps them apart, and forcing the large split made the step slower.)
 constexpr int kMergeWarps = 4;
 constexpr int kMergeChunk = 20;
 

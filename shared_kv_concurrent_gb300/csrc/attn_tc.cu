@@ -32,7 +32,9 @@
 // kernel) still runs; meanwhile it sets up and loads its first tile, when that tile holds only
 // tokens no launch still in flight can have written, and it waits for that kernel before it
 // reads the queries or any other tile; it lets the merge kernel launch before its partial
-// results are stored.
+// results are stored.  What a CTA of the first wave needs before the plan is read (its first
+// tile's row, the first query tile's group, segment and rotation) comes with the launch as a
+// kernel parameter, so that nothing at the start waits on a dependent load.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -331,7 +333,8 @@ __device__ __forceinline__ void append_fresh(const AttnArgs& a, const Group& g, 
 
 template <int D, int T>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const AttnArgs a, const __grid_constant__ TcMaps maps, const int32_t layer) {
+    attn_tc_kernel(const AttnArgs a, const __grid_constant__ TcMaps maps, const int32_t layer,
+                   const __grid_constant__ LaunchUnits lu) {
   using C = Cfg<D>;
   static_assert(T == 1 || T == 2 || T == 4, "T copies of each query row, one per column chunk");
   constexpr int WPC = 4 / T;                  // softmax warps per column chunk
@@ -367,24 +370,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int q = 0; q < 4; ++q) active_softmax_warps += (32 * (q % WPC) < R) ? 1 : 0;
   if (threadIdx.x == 0) HW_TRACE_EV(0);
 
-  // Warps 2-7 start on the first query tile before set-up is done: a thread whose copy of the
-  // unit record already carries this plan's sequence number (first two vectors) rotates its
-  // items now; the others do after set-up, from the confirmed record (items are per thread, so
-  // the two ways mix freely).
+  // The launch parameters describe this CTA's unit before any of the plan is read (first wave).
+  const bool in_lu = blockIdx.x < (unsigned)kLaunchUnits;
+  const int32_t lu_row0 = in_lu ? lu.row0[blockIdx.x] : -1;
+  const int32_t lu_group = in_lu ? lu.group[blockIdx.x] : -1;
+  const int32_t lu_seg0 = in_lu ? lu.seg0[blockIdx.x] : -1;
+  const int32_t lu_delta0 = in_lu ? lu.delta0[blockIdx.x] : -1;
+
+  // Warps 2-7 rotate the first query tile before set-up is done when it needs nothing of the
+  // plan: one rotation for every row (no delta table) and one query per worker (no row map).
+  // Otherwise they do after set-up, once the plan has arrived.
   bool pre_q = false;
   if (warp >= 2) {
-    const int4* urec = reinterpret_cast<const int4*>(a.units + blockIdx.x);
-    const int4 h0 = __ldcg(urec), h1 = __ldcg(urec + 1);
-    const uint32_t want = a.gate.plan_seq ? (uint32_t)a.gate.plan_expect : 0u;
     pdl_wait();                       // the queries may come from the kernel this grid follows
-    if ((uint32_t)h0.z == want && (uint32_t)h1.w == want && h0.w >= 0 && h0.w < a.num_seg_slots) {
-      const Group g0{h0.y / a.H_kv, h0.y % a.H_kv, 0, 0};
-      rotate_tile<D, T, kThreads - 64>(a, g0, h0.w, h1.z, smem + C::kQOff, threadIdx.x - 64);
+    if (lu_delta0 >= 0 && a.qrow == nullptr && lu_group >= 0 && lu_group < a.P * a.H_kv &&
+        lu_seg0 >= 0 && lu_seg0 < a.num_seg_slots) {
+      const Group g0{lu_group / a.H_kv, lu_group % a.H_kv, 0, 0};
+      rotate_tile<D, T, kThreads - 64>(a, g0, lu_seg0, lu_delta0, smem + C::kQOff,
+                                       threadIdx.x - 64);
       pre_q = true;
     }
   }
 
   if (threadIdx.x == 0) {
+    // The unit record (three vectors) and the plan's sequence word are read first and used
+    // once the plan's arrival is confirmed.
+    const int4* urec = reinterpret_cast<const int4*>(a.units + blockIdx.x);
+    int4 uv[3];                                     // (L2, not a stale L1 line)
+#pragma unroll
+    for (int k = 0; k < 3; ++k) uv[k] = __ldcg(urec + k);
+    const unsigned long long seq0 = plan_seq_now(a.gate);   // in flight with the record
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
@@ -404,40 +419,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_cempty0 + 8u * e, 1 + kRotThreads + 32 * active_softmax_warps);
     }
     fence_mbar_init();
-    // The unit's first tile goes out at once when the first 16 bytes of its record already
-    // carry this plan's sequence number (one vector load: they are all of the current plan);
-    // the rest of the plan is read only once the plan's own sequence word has arrived (it
-    // follows the plan on the copy stream).
-    const int4* urec = reinterpret_cast<const int4*>(a.units + blockIdx.x);
-    int4 uv[3];                                     // (L2, not a stale L1 line)
-#pragma unroll
-    for (int k = 0; k < 3; ++k) uv[k] = __ldcg(urec + k);
-    const unsigned long long seq0 = plan_seq_now(a.gate);   // in flight with the record
+    // Meanwhile the first query tile's inputs and the unit's first K/V tile go out from the
+    // launch parameters, which need no load.
     const uint32_t want = a.gate.plan_seq ? (uint32_t)a.gate.plan_expect : 0u;
-    const int4 head = uv[0];
-    const bool current = (uint32_t)head.z == want;
     int early = 0;
-    if (current && (uint32_t)uv[1].w == want) {
+    if (lu_group >= 0 && lu_group < a.P * a.H_kv && a.qrow == nullptr) {
       // The first query tile's inputs into L2 before the K/V loads start: the rotation warps
-      // read them right after set-up, and would otherwise queue behind every CTA's tiles.
-      const int p = head.y / a.H_kv, h = head.y % a.H_kv;
-      for (int w = 0; w < a.W; ++w) {     // query row w's G heads of this KV head
-        const int qr = query_row(a, p, w);
-        if (qr >= 0)
-          bulk_prefetch_l2(a.q + ((size_t)qr * a.H_q + (size_t)h * a.G) * D,
-                           (uint32_t)(a.G * D * 2));
-      }
-      const int d0 = uv[1].z;             // the first segment's rotation, if shared
-      if (d0 >= 0 && d0 < a.max_position) {
-        bulk_prefetch_l2(a.rope_cos + (size_t)d0 * (D / 2), D / 2 * 4);
-        bulk_prefetch_l2(a.rope_sin + (size_t)d0 * (D / 2), D / 2 * 4);
+      // read them right after the wait, and would otherwise queue behind every CTA's tiles.
+      const int p = lu_group / a.H_kv, h = lu_group % a.H_kv;
+      for (int w = 0; w < a.W; ++w)       // query row w's G heads of this KV head
+        bulk_prefetch_l2(a.q + ((size_t)(p * a.W + w) * a.H_q + (size_t)h * a.G) * D,
+                         (uint32_t)(a.G * D * 2));
+      if (lu_delta0 >= 0 && lu_delta0 < a.max_position) {
+        bulk_prefetch_l2(a.rope_cos + (size_t)lu_delta0 * (D / 2), D / 2 * 4);
+        bulk_prefetch_l2(a.rope_sin + (size_t)lu_delta0 * (D / 2), D / 2 * 4);
       }
     }
-    if (current && head.x >= 0) {
+    if (lu_row0 >= 0 && lu_row0 < a.num_pages * a.H_kv * a.S) {
       tma_prefetch(&maps.k);
       tma_prefetch(&maps.v);
-      const int32_t y = (int32_t)(((page_base0 + head.x / a.S) * a.H_kv + head.y % a.H_kv) * a.S +
-                                  head.x % a.S);
+      const int32_t y = (int32_t)(page_base0 * a.H_kv * a.S + lu_row0);
       mbar_arrive_expect_tx(bar_full(0), C::kTileBytes);
       mbar_arrive_expect_tx(bar_full(1), C::kTileBytes);
 #pragma unroll
@@ -466,6 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uu.piece_begin = uu.piece_end = 0;
       uu.seg0 = uu.first_tok = -1;
       uu.fresh_end = uu.fresh_begin;
+    } else if (early) {                 // the launch parameters must name the record's tile
+      const int32_t rec_row = uu.first_tok < 0 ? -1
+          : ((uu.first_tok / a.S) * a.H_kv + uu.group % a.H_kv) * a.S + uu.first_tok % a.S;
+      if (rec_row != lu_row0) record_error(a.err, ERR_PLAN, KID_ATTN_TC, blockIdx.x, 6);
     }
     *u_smem = uu;
   }
@@ -918,8 +923,8 @@ extern "C" int hw_trace_clear(void) {
 #endif
 
 template <int D, int T>
-static void launch_tc_dt(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s,
-                         cudaEvent_t e0, cudaEvent_t e1) {
+static void launch_tc_dt(const AttnArgs& a, const TcMaps& maps, const LaunchUnits& lu, int layer,
+                         cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   using C = Cfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   cudaLaunchAttribute attr[1];
@@ -933,19 +938,19 @@ static void launch_tc_dt(const AttnArgs& a, const TcMaps& maps, int layer, cudaS
   cfg.attrs = attr;
   cfg.numAttrs = e0 ? 0 : 1;        // a timing event in between ends the programmatic chain
   if (e0) cudaEventRecord(e0, s);
-  cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, T>, a, maps, (int32_t)layer);
+  cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, T>, a, maps, (int32_t)layer, lu);
   if (e1) cudaEventRecord(e1, s);
 }
 
 template <int D>
-static void launch_tc_d(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s,
-                        cudaEvent_t e0, cudaEvent_t e1) {
+static void launch_tc_d(const AttnArgs& a, const TcMaps& maps, const LaunchUnits& lu, int layer,
+                        cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   if (a.rows <= 32)
-    launch_tc_dt<D, 4>(a, maps, layer, s, e0, e1);
+    launch_tc_dt<D, 4>(a, maps, lu, layer, s, e0, e1);
   else if (a.rows <= 64)
-    launch_tc_dt<D, 2>(a, maps, layer, s, e0, e1);
+    launch_tc_dt<D, 2>(a, maps, lu, layer, s, e0, e1);
   else
-    launch_tc_dt<D, 1>(a, maps, layer, s, e0, e1);
+    launch_tc_dt<D, 1>(a, maps, lu, layer, s, e0, e1);
 }
 
 template <int D>
@@ -961,13 +966,13 @@ static cudaError_t prepare_tc_d() {
 
 cudaError_t prepare_attention_tc(int D) { return D == 64 ? prepare_tc_d<64>() : prepare_tc_d<128>(); }
 
-void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s,
-                         cudaEvent_t ev_before, cudaEvent_t ev_after) {
+void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, const LaunchUnits& lu, int layer,
+                         cudaStream_t s, cudaEvent_t ev_before, cudaEvent_t ev_after) {
   if (a.num_units <= 0) return;
   if (a.D == 64)
-    launch_tc_d<64>(a, maps, layer, s, ev_before, ev_after);
+    launch_tc_d<64>(a, maps, lu, layer, s, ev_before, ev_after);
   else
-    launch_tc_d<128>(a, maps, layer, s, ev_before, ev_after);
+    launch_tc_d<128>(a, maps, lu, layer, s, ev_before, ev_after);
 }
 
 // ---- tensor maps (host) ------------------------------------------------------------------

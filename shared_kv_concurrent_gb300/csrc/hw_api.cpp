@@ -1032,11 +1032,13 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
     if (st != HW_OK) return st;
   }
   hw::PlanGate gate{};
+  const char* hbase = nullptr;               // host copy of the plan (the staging slot)
   if (step_plan) {
     // The plan of this step went up with its first append.
     slot = c->step_slot;
     po = c->step_po;
     dbase = c->d_slot(slot) + c->step_plan_off;
+    hbase = c->h_slot(slot) + c->step_plan_off;
     gate = c->step_gate;
   } else {
     hw_status st = c->acquire_slot(&slot);
@@ -1050,6 +1052,7 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
                               n_q))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
+    hbase = c->h_slot(slot);
     st = c->upload_slot(slot, po.bytes, seq, &gate);
     if (st != HW_OK) return st;
   }
@@ -1095,8 +1098,22 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
   cudaEvent_t e0 = pi >= 0 ? c->prof_ev[2 * pi] : nullptr;
   cudaEvent_t e1 = pi >= 0 ? c->prof_ev[2 * pi + 1] : nullptr;
   if (c->use_tc) {
+    // What the first CTAs need of their units before reading the plan, as launch parameters.
+    hw::LaunchUnits lu;
+    const hw::Unit* hu = reinterpret_cast<const hw::Unit*>(hbase + po.units);
+    const int32_t S = c->cfg.page_size, H = c->cfg.num_kv_heads;
+    for (int32_t i = 0; i < hw::kLaunchUnits; ++i) {
+      lu.row0[i] = lu.group[i] = lu.seg0[i] = lu.delta0[i] = -1;
+      if (i >= po.num_units) continue;
+      const hw::Unit& u = hu[i];
+      if (u.first_tok >= 0)
+        lu.row0[i] = ((u.first_tok / S) * H + u.group % H) * S + u.first_tok % S;
+      lu.group[i] = u.group;
+      lu.seg0[i] = u.seg0;
+      lu.delta0[i] = u.delta0;
+    }
     // the attention kernel and the merge, both as programmatic dependents
-    hw::launch_attention_tc(a, c->maps, layer, s, e0, e1);
+    hw::launch_attention_tc(a, c->maps, lu, layer, s, e0, e1);
   } else {
     if (e0) cudaEventRecord(e0, s);
     hw::launch_attention_fma(a, s);

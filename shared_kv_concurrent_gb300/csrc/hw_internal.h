@@ -97,6 +97,19 @@ struct __align__(16) Unit {
   int32_t flags;      // kernel-side use
 };
 
+// What the tensor-core kernel needs of its unit before it has read any of the plan, for the
+// first kLaunchUnits CTAs of a launch, passed as a kernel parameter (no load, always current):
+// the layer-relative pool row of the unit's first K/V tile if it may be loaded before the
+// kernel waits for the one it follows (Unit::first_tok), and the group, first segment slot and
+// shared rotation of the unit's first query tile (Unit::group, seg0, delta0).  -1 = none.
+constexpr int kLaunchUnits = 160;
+struct LaunchUnits {
+  int32_t row0[kLaunchUnits];     // ((page * H_kv + h) * S + slot), layer offset not included
+  int32_t group[kLaunchUnits];
+  int32_t seg0[kLaunchUnits];
+  int32_t delta0[kLaunchUnits];
+};
+
 // A group: one (problem, KV head); its units are [unit_begin, unit_end).
 struct Group {
   int32_t p;
@@ -174,8 +187,9 @@ void launch_compact(const CompactArgs& a, cudaStream_t s);
 void launch_attention_fma(const AttnArgs& a, cudaStream_t s);
 // Launches the attention kernel; ev_before / ev_after (optional) are recorded directly around
 // it (and it is then launched without programmatic chaining).
-void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s,
-                         cudaEvent_t ev_before = nullptr, cudaEvent_t ev_after = nullptr);
+void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, const LaunchUnits& lu, int layer,
+                         cudaStream_t s, cudaEvent_t ev_before = nullptr,
+                         cudaEvent_t ev_after = nullptr);
 // pdl: launch as a programmatic dependent of the preceding kernel (it waits for its writes).
 void launch_merge(const AttnArgs& a, cudaStream_t s, bool pdl = false);
 bool make_tc_maps(const hw_config& cfg, void* k_pool, void* v_pool, TcMaps* out);
