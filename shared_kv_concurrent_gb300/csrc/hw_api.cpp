@@ -357,10 +357,13 @@ struct hw_ctx {
     return HW_OK;
   }
   static uint64_t next_seq() { return ++g_upload_seq; }
-  // Pick the next staging slot; waits only if the slot's previous use is still in flight.
+  // Pick the next staging slot; waits only if the slot's previous use is still in flight.  The
+  // current step's plan slot is passed over: every later append flush and attention call of the
+  // step reads it, however many other plans (several-query calls) go up in between.
   hw_status acquire_slot(int* slot) {
-    const int i = next_slot;
-    next_slot = (next_slot + 1) % lay.num_slots;
+    int i = next_slot;
+    if (i == step_slot) i = (i + 1) % lay.num_slots;      // num_slots >= 4
+    next_slot = (i + 1) % lay.num_slots;
     if (slot_used[i]) HW_CUDA(cudaEventSynchronize(slot_ev[i]));
     *slot = i;
     return HW_OK;

@@ -334,6 +334,45 @@ def test_last_rope_position_then_the_position_limit():
     r.cache.close()
 
 
+def test_many_multi_query_calls_inside_one_step():
+    """More several-query calls inside one step than the context has plan slots: the step's own
+    plan (its append runs and decode attention plan) must survive them."""
+    import torch
+    import gpu_cases as G
+    from oracle import attention as A
+    from oracle import run as orun
+    from shared_kv_concurrent_gb300 import binding
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner, to_device_bf16
+    w = G.small(wl.tiny(), steps=2)
+    r = WorkloadRunner(w)
+    c = orun.prefill(w)
+    P, W, Hq, D = w.num_problems, w.num_workers, w.num_q_heads, w.head_dim
+    inputs = r.step_inputs(0)
+    r.append(inputs)
+    orun.append_step(c, w, 0)
+    q = orun.query(w, 0, 0)
+    ref, _ = A.method(c, 0, q)
+    n_q = np.ones((P, W), np.int32)                 # each worker's newest token: the decode query
+    qd = to_device_bf16(wl.step_q(w, 0, 0).reshape(P * W, Hq, D))
+    out = torch.empty(P * W, Hq, D, device="cuda")
+    for _ in range(70):                              # more than the at most 32 plan slots
+        r.cache.concurrent_attention_mq(0, qd, n_q, out, "f32")
+    torch.cuda.synchronize()
+    assert np.abs(out.cpu().numpy().reshape(P, W, Hq, D) - ref).max() <= G.TOL
+    outs = [torch.empty(P, W, Hq, D, device="cuda")]
+    r.attend(inputs, outs, None, "f32")             # the step's own plan
+    torch.cuda.synchronize()
+    assert np.abs(outs[0].cpu().numpy() - ref).max() <= G.TOL
+    zeros = np.zeros((P, W), np.uint8)
+    r.end(0, zeros)
+    c.step_end(zeros)
+    G.dev_tables_equal(r, c)
+    G.check_pools(r, c, 0)
+    st, info = r.cache.check_device_errors()
+    assert st == binding.HW_OK, info
+    r.cache.close()
+
+
 def test_protocol_errors_leave_state_unchanged():
     import torch
     from shared_kv_concurrent_gb300 import HogwildCache, HogwildError, binding
