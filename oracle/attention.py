@@ -119,28 +119,6 @@ def method(cache: HogwildCache, layer: int, q: np.ndarray) -> Tuple[np.ndarray, 
     return out, lse
 
 
-def method_rows(cache: HogwildCache, layer: int, q: np.ndarray, rows) -> np.ndarray:
-    """``method`` for selected (p, w, h) rows only; returns out [len(rows)][D] (sampled checks)."""
-    P, W, Hq, D = np.asarray(q).shape
-    q = _check_q(cache, q, Hq)
-    G = Hq // cache.H_kv
-    scale = 1.0 / math.sqrt(D)
-    res = np.zeros((len(rows), D))
-    for r, (p, w, h) in enumerate(rows):
-        entries, i_q = cache.view(p, w)
-        if not entries:
-            continue
-        kh = h // G
-        parts = []
-        for sid, off, n in entries:
-            seg = cache.segments[sid]
-            q_rot = rope(q[p, w, h][None, :], i_q - off, cache.theta)
-            parts.append(segment_partial(seg.stored_k(layer)[:n, kh, :],
-                                         seg.raw_v(layer)[:n, kh, :], q_rot, scale))
-        res[r] = lse_merge(parts)[0][0]
-    return res
-
-
 # ------------------------------------------------------------------ several queries per worker
 
 
