@@ -203,15 +203,23 @@ hw_status hw_concurrent_attention_mq(hw_ctx* ctx, int32_t layer, const void* q,
  * the call's plan and its split-K partial results live in a fixed 16 MiB array in device global
  * memory that the library defines, instead of in the workspace.  Nothing is allocated: no
  * cudaMalloc, cudaFree or allocating library routine is called.
+ *   - Speed: it always runs the CUDA-core attention kernel and a separate merge kernel, also
+ *     on contexts whose regular call uses the tensor cores (16 or more query rows per KV
+ *     head), so it is several times slower there; the regular call remains the fast path.
  *   - Limit: the plan plus one partial result per (problem, KV head) group, i.e.
  *     P * H_kv * rows * (D + 4) * 4 bytes with rows = W * H_q / H_kv, must fit in 16 MiB, else
  *     HW_ERR_CAPACITY and nothing is enqueued.  The KV split adapts to the space left.
+ *   - Not on a capturing stream: a call on a stream that is capturing a CUDA graph returns
+ *     HW_ERR_UNSUPPORTED with nothing enqueued (the plan is copied from a host staging slot
+ *     that later calls reuse).  A capture on another stream is no obstacle.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- *     with that device current); make that first call before any stream capture.
+ *     with that device current).
  *   - Every call, from every context, shares the one array, which keeps the last call's
  *     contents; nothing in it needs to start at zero (each call writes its plan and every
  *     partial before reading them).  Calls whose GPU work overlaps -- on different streams,
  *     or from different contexts -- race on the array: order them on one stream.
+ *   - A recorded append of the layer (hw_append_kv) is written first, by the append kernel,
+ *     once the call's plan has been checked; on HW_ERR_CAPACITY nothing is enqueued.
  */
 hw_status hw_concurrent_attention_noalloc(hw_ctx* ctx, int32_t layer, const void* q, void* out,
                                           int32_t out_dtype, float* lse, void* stream);

@@ -1166,17 +1166,17 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
   if (plan_region >= scratch_bytes) return HW_ERR_CAPACITY;
   const int64_t unit_cap = (int64_t)((scratch_bytes - plan_region) / per_unit);
   if (unit_cap < (int64_t)c->cfg.num_problems * c->cfg.num_kv_heads) return HW_ERR_CAPACITY;
-  {
-    const hw_status st = c->flush_append(layer, (cudaStream_t)stream);
-    if (st != HW_OK) return st;
-  }
   int slot = 0;
   hw_status st = c->acquire_slot(&slot);
   if (st != HW_OK) return st;
+  // The plan is built and checked before anything is enqueued: a refusal leaves the stream and
+  // the layer's recorded append untouched.
   PlanOffsets po{};
   if (!build_attention_plan(c, c->h_slot(slot), &po, unit_cap) || po.bytes > plan_region)
     return HW_ERR_CAPACITY;
   cudaStream_t s = (cudaStream_t)stream;
+  st = c->flush_append(layer, s);
+  if (st != HW_OK) return st;
   HW_CUDA(cudaMemcpyAsync(scratch, c->h_slot(slot), po.bytes, cudaMemcpyHostToDevice, s));
   hw::AttnArgs a{};
   a.pieces = reinterpret_cast<const hw::Piece*>(scratch + po.pieces);

@@ -16,7 +16,7 @@
 namespace {
 
 // 16 MiB: room for the plan and the partial results of well over 200 units of 64 rows at
-// head_dim 128 (one unit needs rows * (head_dim + 2) * 4 bytes).
+// head_dim 128 (one unit needs rows * (head_dim + 4) * 4 bytes: o, m, l and two pad floats).
 constexpr size_t kScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
@@ -49,6 +49,15 @@ extern "C" hw_status hw_concurrent_attention_noalloc(hw_ctx* ctx, int32_t layer,
                                                      void* out, int32_t out_dtype, float* lse,
                                                      void* stream) {
   if (!ctx || !q || !out) return HW_ERR_INVALID_ARG;
+  // Each call copies its plan from a pinned staging slot that later calls reuse, and may wait
+  // on events recorded on `stream`: neither can be replayed from a graph, so a capturing stream
+  // is refused before anything is enqueued.  (Another stream's capture does not matter.)
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing((cudaStream_t)stream, &cap) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return HW_ERR_UNSUPPORTED;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return HW_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   const hw_status st = scratch_address(&scratch);
   if (st != HW_OK) return st;

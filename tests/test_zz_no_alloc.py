@@ -62,7 +62,7 @@ def test_matches_regular_entry_point_on_two_calls_in_a_row():
 def test_refuses_partials_beyond_the_array():
     import torch
     from shared_kv_concurrent_gb300 import HogwildCache, HogwildError, binding, config_for
-    # 40 problems x 8 KV heads x 128 rows x 130 floats = 21 MB of partials > 16 MiB.
+    # 40 problems x 8 KV heads x 128 rows x 132 floats x 4 B = 21.6 MB of partials > 16 MiB.
     cfg = config_for(num_problems=40, num_workers=16, num_layers=1, num_q_heads=64,
                      num_kv_heads=8, head_dim=128, page_size=128, num_pages=4,
                      max_position=1024, rope_theta=1e6)
@@ -73,3 +73,73 @@ def test_refuses_partials_beyond_the_array():
         binding.hw_concurrent_attention_noalloc(c.ctx, 0, q, out, binding.HW_OUT_F32)
     assert e.value.status == binding.HW_ERR_CAPACITY
     c.close()
+
+
+def test_first_in_its_step_then_the_regular_call():
+    """The allocation-free call made first in a step, right after the append, so that it writes
+    the layer's recorded append itself; a second cache fed the same inputs gives the reference
+    through the regular call.  The regular call made afterwards in the same step still
+    matches."""
+    import torch
+    from shared_kv_concurrent_gb300 import binding
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner
+    w = _small_w8()
+    r1, r2 = WorkloadRunner(w), WorkloadRunner(w)
+    shape = (w.num_problems, w.num_workers, w.num_q_heads, w.head_dim)
+    for step in range(2):
+        inputs = r1.step_inputs(step)
+        r1.append(inputs)
+        r2.append(inputs)
+        q = inputs[2][0]
+        got = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+        got_lse = torch.full(shape[:3], float("nan"), dtype=torch.float32, device="cuda")
+        binding.hw_concurrent_attention_noalloc(r1.cache.ctx, 0, q, got, binding.HW_OUT_F32,
+                                                got_lse)
+        ref = torch.full_like(got, float("nan"))
+        ref_lse = torch.full_like(got_lse, float("nan"))
+        binding.hw_concurrent_attention(r2.cache.ctx, 0, q, ref, binding.HW_OUT_F32, ref_lse)
+        after = torch.full_like(got, float("nan"))
+        binding.hw_concurrent_attention(r1.cache.ctx, 0, q, after, binding.HW_OUT_F32)
+        torch.cuda.synchronize()
+        assert (got - ref).abs().max().item() <= TOL
+        assert (got_lse - ref_lse).abs().max().item() <= TOL
+        assert (after - ref).abs().max().item() <= TOL
+        r1.end(step)
+        r2.end(step)
+    for r in (r1, r2):
+        st, info = r.cache.check_device_errors()
+        assert st == binding.HW_OK, info
+        r.cache.close()
+
+
+def test_refused_on_a_capturing_stream():
+    """A stream that is capturing a CUDA graph is refused before anything is enqueued; the
+    same call on the same stream after the capture works."""
+    import torch
+    from shared_kv_concurrent_gb300 import HogwildError, binding
+    from shared_kv_concurrent_gb300.runner import WorkloadRunner
+    w = _small_w8()
+    r = WorkloadRunner(w)
+    inputs = r.step_inputs(0)
+    r.append(inputs)
+    q = inputs[2][0]
+    shape = (w.num_problems, w.num_workers, w.num_q_heads, w.head_dim)
+    out = torch.zeros(shape, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    status = None
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        try:
+            binding.hw_concurrent_attention_noalloc(r.cache.ctx, 0, q, out, binding.HW_OUT_F32,
+                                                    None, s)
+        except HogwildError as e:
+            status = e.status
+    assert status == binding.HW_ERR_UNSUPPORTED
+    binding.hw_concurrent_attention_noalloc(r.cache.ctx, 0, q, out, binding.HW_OUT_F32, None, s)
+    s.synchronize()
+    assert torch.isfinite(out).all()
+    r.end(0)
+    st, info = r.cache.check_device_errors()
+    assert st == binding.HW_OK, info
+    r.cache.close()
