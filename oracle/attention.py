@@ -213,3 +213,119 @@ def method_mq(cache: HogwildCache, layer: int, q: np.ndarray, n_q):
             out[i, kh * G:(kh + 1) * G] = o
             lse[i, kh * G:(kh + 1) * G] = l
     return out, lse
+
+
+# ------------------------------------------------------------------ split over KV entries
+#
+# The work of one decode step can be split over KV entries and the partial results reduced
+# afterwards (summary section 9: the kernel is balanced by KV entries, then the partial results
+# are reduced) -- also across GPUs, each taking a range of the entries.  The entries of a
+# problem are numbered in segment order: the common segments in commit order, then the
+# workers' current blocks in ascending id.  Every view holds whole segments of that list in its
+# own order, so an entry's number does not depend on the worker; a worker attends to the
+# selected entries of its view, each still at its position in the worker's view.
+
+
+def entry_spans(cache: HogwildCache, p: int):
+    """Problem p's entry numbering: {segment id: number of its first token} and the total."""
+    first, n = {}, 0
+    for sid in list(cache.common[p]) + list(cache.live[p]):
+        first[sid] = n
+        n += cache.segments[sid].visible
+    return first, n
+
+
+def selected(first_entry: int, n: int, begin: int, end: int):
+    """Block-local tokens [a, b) of a segment holding entries [first_entry, first_entry + n)
+    that lie in the entry range [begin, end) (a == b when none do)."""
+    a = min(max(begin - first_entry, 0), n)
+    b = min(max(end - first_entry, 0), n)
+    return a, max(a, b)
+
+
+def brute_force_range(cache: HogwildCache, layer: int, q: np.ndarray, ranges):
+    """Plain definition of the attention over selected entries: worker w's view laid out with
+    every raw key rotated at its view position, and softmax attention of rho(q, i_q) over the
+    keys whose entry number lies in ranges[p] = (begin, end) only.  Returns (out, lse); a worker
+    that selects no key gets out = 0 and lse = -inf."""
+    P, W, Hq, D = np.asarray(q).shape
+    q = _check_q(cache, q, Hq)
+    G = Hq // cache.H_kv
+    scale = 1.0 / math.sqrt(D)
+    out = np.zeros((P, W, Hq, D))
+    lse = np.full((P, W, Hq), -np.inf)
+    for p in range(P):
+        first, _ = entry_spans(cache, p)
+        begin, end = (int(x) for x in ranges[p])
+        for w in range(W):
+            entries, i_q = cache.view(p, w)
+            if not entries:
+                continue
+            kr = np.concatenate([cache.segments[s].raw_k(layer)[:n] for s, _, n in entries])
+            vr = np.concatenate([cache.segments[s].raw_v(layer)[:n] for s, _, n in entries])
+            number = np.concatenate([first[s] + np.arange(n) for s, _, n in entries])
+            keep = (number >= begin) & (number < end)
+            if not keep.any():
+                continue
+            pos = np.arange(kr.shape[0])
+            k = rope(kr, pos[:, None], cache.theta)[keep]
+            v = vr[keep]
+            qr = rope(q[p, w], i_q, cache.theta)
+            for h in range(Hq):
+                s = (k[:, h // G, :] @ qr[h]) * scale
+                m = s.max()
+                e = np.exp(s - m)
+                out[p, w, h] = (e @ v[:, h // G, :]) / e.sum()
+                lse[p, w, h] = m + math.log(e.sum())
+    return out, lse
+
+
+def method_range(cache: HogwildCache, layer: int, q: np.ndarray, ranges):
+    """The method over selected entries: for each segment of worker w's view, its tokens in the
+    range, stored at block-local positions, attended with the query rotated once by
+    (i_q - the segment's view offset); the per-segment partials merged by log-sum-exp."""
+    P, W, Hq, D = np.asarray(q).shape
+    q = _check_q(cache, q, Hq)
+    G = Hq // cache.H_kv
+    scale = 1.0 / math.sqrt(D)
+    out = np.zeros((P, W, Hq, D))
+    lse = np.full((P, W, Hq), -np.inf)
+    for p in range(P):
+        first, _ = entry_spans(cache, p)
+        begin, end = (int(x) for x in ranges[p])
+        for w in range(W):
+            entries, i_q = cache.view(p, w)
+            parts = {h: [] for h in range(cache.H_kv)}
+            for sid, off, n in entries:
+                a, b = selected(first[sid], n, begin, end)
+                if a == b:
+                    continue
+                seg = cache.segments[sid]
+                q_rot = rope(q[p, w], i_q - off, cache.theta)
+                for kh in range(cache.H_kv):
+                    parts[kh].append(segment_partial(seg.stored_k(layer)[a:b, kh, :],
+                                                     seg.raw_v(layer)[a:b, kh, :],
+                                                     q_rot[kh * G:(kh + 1) * G], scale))
+            if not parts[0]:
+                continue
+            for kh in range(cache.H_kv):
+                o, l = lse_merge(parts[kh])
+                out[p, w, kh * G:(kh + 1) * G] = o
+                lse[p, w, kh * G:(kh + 1) * G] = l
+    return out, lse
+
+
+def merge_parts(outs, lses):
+    """Merge normalised partial results of the same queries over disjoint sets of keys:
+    LSE = log sum_i exp(lse_i), out = sum_i exp(lse_i - LSE) out_i (out = 0, LSE = -inf when
+    every part is empty).  outs: [n][...][D], lses: [n][...] (natural log)."""
+    outs = np.asarray(outs, dtype=np.float64)
+    lses = np.asarray(lses, dtype=np.float64)
+    M = lses.max(axis=0)
+    finite = np.isfinite(M)
+    Ms = np.where(finite, M, 0.0)
+    wts = np.where(np.isfinite(lses), np.exp(lses - Ms), 0.0)
+    L = wts.sum(axis=0)
+    out = np.where(finite[..., None], (wts[..., None] * outs).sum(axis=0) /
+                   np.where(finite, L, 1.0)[..., None], 0.0)
+    return out, np.where(finite, Ms + np.log(np.where(finite, L, 1.0)), -np.inf)

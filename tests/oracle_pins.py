@@ -574,6 +574,93 @@ def check_compaction_refusals():
         pass
 
 
+# ------------------------------------------------------------- split over KV entries
+
+
+def _random_ranges(g, total, k):
+    """k ranges that partition [0, total) at random cut points (some of them empty)."""
+    cuts = np.sort(g.integers(0, total + 1, size=k - 1)) if k > 1 else np.array([], int)
+    edges = np.concatenate([[0], cuts, [total]]).astype(int)
+    return [(int(edges[i]), int(edges[i + 1])) for i in range(k)]
+
+
+def check_range_brute_vs_method(seeds=range(4)):
+    """The method over selected entries (per-segment query rotation, LSE merge) against the
+    plain definition (every key re-rotated at its view position, softmax over the selected
+    keys), for random histories with commits and ranges cutting segments anywhere."""
+    for seed in seeds:
+        g = np.random.default_rng(100 + seed)
+        for D in (2, 64):
+            for c, q in random_session(seed, D, 1 + seed % 4):
+                tot = [A.entry_spans(c, p)[1] for p in range(c.P)]
+                for _ in range(3):
+                    rg = []
+                    for t in tot:
+                        b = int(g.integers(0, t + 1))
+                        rg.append((b, int(g.integers(b, t + 1))))
+                    ob, lb = A.brute_force_range(c, 0, q, rg)
+                    om, lm = A.method_range(c, 0, q, rg)
+                    assert np.allclose(ob, om, rtol=0, atol=1e-10), (seed, D, rg)
+                    fin = np.isfinite(lb)
+                    assert (fin == np.isfinite(lm)).all()
+                    assert np.allclose(lb[fin], lm[fin], rtol=0, atol=1e-10)
+
+
+def check_range_partition_merges_to_full(seeds=range(4)):
+    """Results over ranges that partition every problem's entries, merged by log-sum-exp,
+    equal the attention over the whole view (the brute-force definition, pinned above)."""
+    for seed in seeds:
+        g = np.random.default_rng(200 + seed)
+        for D in (2, 64):
+            for c, q in random_session(seed, D, 1 + seed % 4):
+                tot = [A.entry_spans(c, p)[1] for p in range(c.P)]
+                k = int(g.integers(1, 5))
+                per = [_random_ranges(g, t, k) for t in tot]
+                parts = [A.method_range(c, 0, q, [per[p][i] for p in range(c.P)]) for i in range(k)]
+                out, lse = A.merge_parts([o for o, _ in parts], [l for _, l in parts])
+                ob, lb = A.brute_force(c, 0, q)
+                assert np.allclose(out, ob, rtol=0, atol=1e-10), (seed, D, k)
+                fin = np.isfinite(lb)
+                assert (fin == np.isfinite(lse)).all()
+                assert np.allclose(lse[fin], lb[fin], rtol=0, atol=1e-10)
+
+
+def check_range_selects_segment_order_hand():
+    """Entries are numbered common first, then the workers' blocks by id, whatever the view:
+    prompt C (3 tokens) = entries 0-2, Alice's block (2) = 3-4, Bob's (2) = 5-6.  With all
+    keys zero every score is 0, so a worker's output is the mean of the selected values and
+    lse = log(count), for both workers alike."""
+    c = _tiny_cache(W=2, S=4, pages=32, H_kv=1, D=2)
+    n = np.array([[3, 2, 2]])
+    vals = np.array([[10.0, 0.0], [20.0, 0.0], [30.0, 0.0],      # prompt
+                     [1.0, 0.0], [0.0, 1.0],                     # Alice
+                     [5.0, 5.0], [7.0, 9.0]])                    # Bob
+    c.append(0, n, np.zeros((7, 1, 2)), vals[:, None, :])
+    q = np.array([[[[0.3, -0.2]], [[1.1, 0.4]]]])
+    for (b, e), mean in (((3, 5), [0.5, 0.5]), ((5, 7), [6.0, 7.0]), ((2, 4), [15.5, 0.0]),
+                         ((0, 3), [20.0, 0.0]), ((4, 6), [2.5, 3.0])):
+        for fn in (A.method_range, A.brute_force_range):
+            out, lse = fn(c, 0, q, [(b, e)])
+            for w in range(2):
+                assert np.allclose(out[0, w, 0], mean, atol=1e-13), (fn.__name__, b, e, w, out[0, w, 0])
+                assert abs(lse[0, w, 0] - math.log(e - b)) < 1e-13
+    out, lse = A.method_range(c, 0, q, [(4, 4)])
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def check_merge_parts_closed_form():
+    """Two parts with sums of exponentials 1 and 3 (lse 0 and log 3): weights 1/4 and 3/4, and
+    merged lse log 4; an empty part (lse -inf) changes nothing; all parts empty give 0, -inf."""
+    a, b = np.array([[2.0, -4.0]]), np.array([[6.0, 8.0]])
+    out, lse = A.merge_parts([a, b], [np.array([0.0]), np.array([math.log(3.0)])])
+    assert np.allclose(out, [[5.0, 5.0]], atol=1e-14) and abs(lse[0] - math.log(4.0)) < 1e-14
+    out2, lse2 = A.merge_parts([a, b, np.full((1, 2), 99.0)],
+                               [np.array([0.0]), np.array([math.log(3.0)]), np.array([-np.inf])])
+    assert np.allclose(out2, out, atol=1e-14) and abs(lse2[0] - lse[0]) < 1e-14
+    out3, lse3 = A.merge_parts([a, b], [np.array([-np.inf]), np.array([-np.inf])])
+    assert np.all(out3 == 0) and np.isneginf(lse3[0])
+
+
 ALL_CHECKS = [
     check_rope_complex_form, check_rope_d2_textbook, check_inv_freq_values, check_rope_invariants,
     check_views_golden, check_view_offsets_and_query_position, check_pages_hand_example,
@@ -585,4 +672,6 @@ ALL_CHECKS = [
     check_mq_chunk_equals_token_by_token, check_mq_single_worker_is_causal_prefill,
     check_compaction_keeps_outputs, check_compaction_rerotates_stored_keys,
     check_compaction_pages_hand, check_compaction_refusals,
+    check_range_brute_vs_method, check_range_partition_merges_to_full,
+    check_range_selects_segment_order_hand, check_merge_parts_closed_form,
 ]

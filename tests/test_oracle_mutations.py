@@ -150,7 +150,66 @@ def _own_visible_one_more(n, back):
 def _query_position_unshifted(i_q, back):
     return i_q
 
+def _entry_spans_live_descending(cache, p):
+    first, n = {}, 0
+    for sid in list(cache.common[p]) + list(reversed(cache.live[p])):
+        first[sid] = n
+        n += cache.segments[sid].visible
+    return first, n
+
+
+def _selected_end_inclusive(first_entry, n, begin, end):
+    a = min(max(begin - first_entry, 0), n)
+    b = min(max(end + 1 - first_entry, 0), n)
+    return a, max(a, b)
+
+
+def _merge_parts_unweighted(outs, lses):
+    outs = np.asarray(outs, dtype=np.float64)
+    lses = np.asarray(lses, dtype=np.float64)
+    return outs.mean(axis=0), np.log(np.exp(lses).sum(axis=0))
+
+
+def _method_range_rotated_from_range_start(cache, layer, q, ranges):
+    """method_range with each segment's query rotated from the first selected token."""
+    import math
+    P, W, Hq, D = np.asarray(q).shape
+    q = np.asarray(q, dtype=np.float64)
+    G = Hq // cache.H_kv
+    scale = 1.0 / math.sqrt(D)
+    out = np.zeros((P, W, Hq, D))
+    lse = np.full((P, W, Hq), -np.inf)
+    for p in range(P):
+        first, _ = A.entry_spans(cache, p)
+        begin, end = ranges[p]
+        for w in range(W):
+            entries, i_q = cache.view(p, w)
+            parts = {h: [] for h in range(cache.H_kv)}
+            for sid, off, n in entries:
+                a, b = A.selected(first[sid], n, begin, end)
+                if a == b:
+                    continue
+                seg = cache.segments[sid]
+                q_rot = A.rope(q[p, w], i_q - off - a, cache.theta)
+                for kh in range(cache.H_kv):
+                    parts[kh].append(A.segment_partial(seg.stored_k(layer)[a:b, kh, :],
+                                                       seg.raw_v(layer)[a:b, kh, :],
+                                                       q_rot[kh * G:(kh + 1) * G], scale))
+            if not parts[0]:
+                continue
+            for kh in range(cache.H_kv):
+                o, l = A.lse_merge(parts[kh])
+                out[p, w, kh * G:(kh + 1) * G] = o
+                lse[p, w, kh * G:(kh + 1) * G] = l
+    return out, lse
+
+
 MUTATIONS = {
+    "entry_numbering_live_descending": [(A, "entry_spans", _entry_spans_live_descending)],
+    "range_end_inclusive": [(A, "selected", _selected_end_inclusive)],
+    "merge_parts_unweighted": [(A, "merge_parts", _merge_parts_unweighted)],
+    "range_query_rotated_from_range_start": [(A, "method_range",
+                                              _method_range_rotated_from_range_start)],
     "rope_rotates_backwards": [(R, "rope", _rope_sign_flip), (A, "rope", _rope_sign_flip),
                                (C, "rope", _rope_sign_flip)],
     "rope_interleaved_pairs": [(R, "rope", _rope_interleaved), (A, "rope", _rope_interleaved),
