@@ -197,6 +197,49 @@ hw_status hw_concurrent_attention_mq(hw_ctx* ctx, int32_t layer, const void* q,
                                      void* stream);
 
 /*
+ * Concurrent attention over a range of KV entries, for splitting one step's attention into
+ * parts (summary section 9: the work is split over KV entries and the partial results are
+ * reduced afterwards) -- on one GPU, or across GPUs that each take a range and exchange their
+ * results.  A problem's entries are numbered in segment order: its common segments in commit
+ * order, then the workers' current blocks in ascending worker id (entry e of a segment with
+ * first number f is its block-local token e - f).  Every view holds whole segments of that
+ * list in its own order, so the numbering is the same for every worker.
+ *   q:      as hw_concurrent_attention.
+ *   ranges: host int64 [P][2]: problem p's entries [ranges[p][0], ranges[p][1]); 0 <= begin <=
+ *           end (an end past the last entry stops there).
+ *   out:    device fp32 [P][W][H_q][D], 16-byte aligned: each worker's softmax attention over
+ *           the selected entries of its view, each key still at its position in the worker's
+ *           view (the query rotation is the full call's), normalised over those keys.
+ *   lse:    device fp32 [P][W][H_q] (required): natural-log log-sum-exp of the selected
+ *           scaled scores; -inf (and out = 0) where a worker selects nothing.
+ * Merging, with hw_merge_attention, the results of ranges that partition every problem's
+ * entries gives hw_concurrent_attention's out and lse.  The layer's recorded append is
+ * written first, by the append kernel.  Errors: as hw_concurrent_attention; HW_ERR_INVALID_ARG
+ * for a NULL ranges or lse, or a range with begin < 0 or end < begin.
+ */
+hw_status hw_concurrent_attention_range(hw_ctx* ctx, int32_t layer, const void* q,
+                                        const int64_t* ranges, float* out, float* lse,
+                                        void* stream);
+
+/*
+ * Merge of n partial attention results of the same query rows over disjoint sets of keys
+ * (summary section 9, "partial result reduction"; section 5: by log-sum-exp):
+ *   LSE = log sum_i exp(lse_i),   out = sum_i exp(lse_i - LSE) out_i,
+ * parts with lse_i = -inf count as empty; out = 0 and LSE = -inf when every part is.  Needs no
+ * context: the parts may come from hw_concurrent_attention_range calls on this GPU, or be
+ * gathered from GPUs that attended to other ranges.
+ *   n_parts: 1 .. 4096.  rows: query rows per part (P * W * H_q for one query per worker).
+ *   head_dim: D, a multiple of 4.
+ *   parts_out: device fp32 [n_parts][rows][D], 16-byte aligned; parts_lse: device fp32
+ *   [n_parts][rows].  out: device [rows][D], bf16 or fp32 (out_dtype), 16-byte aligned; lse:
+ *   device fp32 [rows] or NULL.  One kernel on `stream`.
+ * Errors: HW_ERR_INVALID_ARG (counts, NULL or misaligned pointers), HW_ERR_CUDA.
+ */
+hw_status hw_merge_attention(int32_t n_parts, int64_t rows, int32_t head_dim,
+                             const float* parts_out, const float* parts_lse, void* out,
+                             int32_t out_dtype, float* lse, void* stream);
+
+/*
  * hw_concurrent_attention for callers that cannot allocate device memory when they call it
  * (no counterpart in the paper; a deployment need).  Same arguments, same result as
  * hw_concurrent_attention; the context's pools, tables and RoPE table are used as usual, but
@@ -288,12 +331,15 @@ typedef struct hw_profile {
   double append_ms;          /* summed CUDA-event time of the append kernels (enabled only) */
   int64_t timed_attention;   /* how many attention launches attention_ms covers */
   int64_t timed_append;
+  double merge_ms;           /* summed CUDA-event time of the merge kernels (enabled only) */
+  int64_t timed_merge;
 } hw_profile;
 
 /*
  * Turn kernel timing on or off.  When on, every attention and append call records a pair of
- * CUDA events on its stream directly around its main kernel (up to 4096 pairs per read).
- * Launch counting is always on.
+ * CUDA events on its stream directly around each of its kernels -- the attention kernel, the
+ * merge kernel, the append kernel -- (up to 4096 pairs per read); the kernels are then launched
+ * without programmatic chaining.  Launch counting is always on.
  */
 hw_status hw_profile_enable(hw_ctx* ctx, int32_t enable);
 

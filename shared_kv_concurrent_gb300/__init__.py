@@ -83,6 +83,32 @@ class HogwildCache:
         binding.hw_concurrent_attention(self.ctx, layer, q, out, dt, lse, stream)
         return out
 
+    def concurrent_attention_range(self, layer: int, q, ranges, out=None, lse=None, stream=None):
+        """Attention over entries [ranges[p][0], ranges[p][1]) of each problem (segment order):
+        returns (out fp32, lse fp32), normalised over the selected keys."""
+        import torch
+        P, W, Hq = q.shape[0], q.shape[1], q.shape[2]
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        if lse is None:
+            lse = torch.empty((P, W, Hq), dtype=torch.float32, device=q.device)
+        binding.hw_concurrent_attention_range(self.ctx, layer, q, ranges, out, lse, stream)
+        return out, lse
+
+    def entry_totals(self):
+        """Entries of every problem in segment order (common segments, then the workers'
+        blocks), this step's appended tokens included: the extent hw_concurrent_attention_range
+        numbers."""
+        totals = []
+        for p in range(self.cfg.num_problems):
+            common, live = binding.hw_get_blocks(self.ctx, p, self.cfg.num_workers)
+            n = 0
+            for sid in common + live:
+                _, _, length, pending, _ = binding.hw_get_segment(self.ctx, sid)
+                n += length + pending
+            totals.append(n)
+        return totals
+
     def step_end(self, finished=None, stream=None) -> None:
         binding.hw_step_end(self.ctx, finished, stream)
 

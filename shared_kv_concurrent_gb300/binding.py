@@ -30,7 +30,8 @@ HW_OUT_F32 = 1
 EXPORTED = (
     "hw_status_string", "hw_last_cuda_error", "hw_pool_size", "hw_workspace_size", "hw_create",
     "hw_destroy", "hw_append_kv", "hw_concurrent_attention", "hw_concurrent_attention_noalloc",
-    "hw_concurrent_attention_mq", "hw_compact_segments",
+    "hw_concurrent_attention_mq", "hw_concurrent_attention_range", "hw_merge_attention",
+    "hw_compact_segments",
     "hw_step_end",
     "hw_check_device_errors", "hw_debug_expire_plans", "hw_profile_enable", "hw_profile_read",
     "hw_get_counts", "hw_get_segment", "hw_get_blocks", "hw_get_view",
@@ -54,7 +55,8 @@ class hw_profile(ctypes.Structure):
         ("launches", ctypes.c_int64), ("attention_launches", ctypes.c_int64),
         ("append_launches", ctypes.c_int64), ("attention_ms", ctypes.c_double),
         ("append_ms", ctypes.c_double), ("timed_attention", ctypes.c_int64),
-        ("timed_append", ctypes.c_int64),
+        ("timed_append", ctypes.c_int64), ("merge_ms", ctypes.c_double),
+        ("timed_merge", ctypes.c_int64),
     ]
 
 
@@ -91,6 +93,9 @@ def load() -> ctypes.CDLL:
         "hw_concurrent_attention": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P]),
         "hw_concurrent_attention_noalloc": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P]),
         "hw_concurrent_attention_mq": (ctypes.c_int, [_P, _I32, _P, _P, _P, _I32, _P, _P]),
+        "hw_concurrent_attention_range": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P]),
+        "hw_merge_attention": (ctypes.c_int, [_I32, ctypes.c_int64, _I32, _P, _P, _P, _I32, _P,
+                                              _P]),
         "hw_compact_segments": (ctypes.c_int, [_P, _I32, _I32, _I32, _P]),
         "hw_step_end": (ctypes.c_int, [_P, _P, _P]),
         "hw_check_device_errors": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -205,6 +210,27 @@ def hw_concurrent_attention_mq(ctx: int, layer: int, q, n_q, out, out_dtype: int
     _check(load().hw_concurrent_attention_mq(ctx, layer, _dptr(q), nq.ctypes.data, _dptr(out),
                                              out_dtype, _dptr(lse), _stream(stream)),
            "hw_concurrent_attention_mq")
+
+
+def hw_concurrent_attention_range(ctx: int, layer: int, q, ranges, out, lse,
+                                  stream=None) -> None:
+    """Attention over entries [ranges[p][0], ranges[p][1]) of each problem (host int64 [P][2]);
+    out fp32 [P][W][H_q][D] normalised over those keys, lse fp32 [P][W][H_q]."""
+    rg = np.ascontiguousarray(np.asarray(ranges, dtype=np.int64))
+    _check(load().hw_concurrent_attention_range(ctx, layer, _dptr(q), rg.ctypes.data, _dptr(out),
+                                                _dptr(lse), _stream(stream)),
+           "hw_concurrent_attention_range")
+
+
+def hw_merge_attention(parts_out, parts_lse, out, out_dtype: int, lse=None, stream=None) -> None:
+    """Log-sum-exp merge of partial results: parts_out fp32 [n][..][D], parts_lse fp32 [n][..]
+    (the same query rows in every part); out [..][D] bf16 or fp32, lse fp32 [..] or None."""
+    n = int(parts_out.shape[0])
+    rows = int(parts_lse.numel() // n)
+    _check(load().hw_merge_attention(n, rows, int(parts_out.shape[-1]), _dptr(parts_out),
+                                     _dptr(parts_lse), _dptr(out), out_dtype, _dptr(lse),
+                                     _stream(stream)),
+           "hw_merge_attention")
 
 
 def hw_concurrent_attention_noalloc(ctx: int, layer: int, q, out, out_dtype: int, lse=None,

@@ -128,7 +128,7 @@ struct TileWalker {
   bool done;
   __device__ bool valid(const Piece& p) const {
     return p.page >= 0 && p.page < num_pages && p.slot0 >= 0 && p.ntok >= 1 && p.ntok <= kTile &&
-           p.slot0 + p.ntok <= S && (p.slot0 % kTile) == 0 && p.seg_slot >= 0 &&
+           p.slot0 + p.ntok <= S && p.seg_slot >= 0 &&
            p.seg_slot < num_seg_slots;
   }
   __device__ void init(const AttnArgs& a, const int2* ring_, uint32_t full_, uint32_t empty_,
@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const Piece pc = a.pieces[pi];
           const bool valid = pc.page >= 0 && pc.page < a.num_pages && pc.slot0 >= 0 &&
                              pc.ntok >= 1 && pc.ntok <= kTile && pc.slot0 + pc.ntok <= a.S &&
-                             (pc.slot0 % kTile) == 0 && pc.seg_slot >= 0 &&
+                             pc.seg_slot >= 0 &&
                              pc.seg_slot < a.num_seg_slots;
           if (!valid) continue;                        // every role skips it the same way
           if (pc.fresh && !waited) {

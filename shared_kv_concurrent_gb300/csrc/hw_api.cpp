@@ -155,6 +155,9 @@ struct PlanScratch {
   std::vector<uint8_t> piece_early;     // the piece may be loaded before the programmatic wait
   int32_t qrow_next = 0;
   std::vector<int64_t> view_off;
+  // per segment reference: its tokens [ref_lo, ref_hi) are attended (the whole segment, or its
+  // part inside an entry range), in ref_tiles tiles starting at tile ref_lo / kPieceMax
+  std::vector<int32_t> ref_lo, ref_hi;
   std::vector<int32_t> ref_sid, ref_slot, ref_tiles, prob_ref_begin, prob_common_refs, unit_rem,
       order;
   std::vector<int64_t> prob_tiles;
@@ -217,7 +220,7 @@ struct hw_ctx {
   bool prof_on = false;
   int64_t n_launch = 0, n_attn = 0, n_append = 0;
   std::vector<cudaEvent_t> prof_ev;       // 2 * kProfPairs, created on first enable
-  std::vector<int8_t> prof_kind;          // 0 = attention, 1 = append, per recorded pair
+  std::vector<int8_t> prof_kind;          // 0 = attention, 1 = append, 2 = merge, per pair
   int prof_next = 0;
 
   // Reserve an event pair for a timed launch (the caller records it); -1 when not timing.
@@ -525,7 +528,7 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
 namespace {
 bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap,
                           int64_t target_override, bool fuse, uint64_t seq,
-                          const int32_t* n_q = nullptr);
+                          const int32_t* n_q = nullptr, const int64_t* ranges = nullptr);
 }  // namespace
 
 extern "C" {
@@ -689,7 +692,7 @@ namespace {
 // largest count of any problem), with the causal length table and the query-row map.
 bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0,
                           int64_t target_override = 0, bool fuse = false, uint64_t seq = 0,
-                          const int32_t* n_q) {
+                          const int32_t* n_q, const int64_t* ranges) {
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
   int32_t WT = W;                       // rotation-table width: query rows per problem / G
   if (n_q) {
@@ -713,6 +716,8 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   ps.ref_sid.clear();
   ps.ref_slot.clear();
   ps.ref_tiles.clear();
+  ps.ref_lo.clear();
+  ps.ref_hi.clear();
   ps.prob_ref_begin.assign(P + 1, 0);
   ps.prob_common_refs.assign(P, 0);
   ps.prob_tiles.assign(P, 0);
@@ -787,12 +792,25 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
       }
       v0 += nq;
     }
-    int64_t tiles = 0;
+    // Tokens attended of each reference: all of them, or, with an entry range, those whose
+    // entry number (segment order: the common segments in commit order, then the workers'
+    // blocks by id -- the order of the references) lies in [begin, end).
+    int64_t tiles = 0, entry = 0;
     for (size_t r = 0; r < ps.refs.size(); ++r) {
-      const int32_t nt = (c->segs[ps.refs[r]].visible() + kPieceMax - 1) / kPieceMax;
+      const int32_t vis = c->segs[ps.refs[r]].visible();
+      int32_t lo = 0, hi = vis;
+      if (ranges) {
+        const int64_t b = ranges[2 * (size_t)p], e = ranges[2 * (size_t)p + 1];
+        lo = (int32_t)std::min<int64_t>(std::max<int64_t>(b - entry, 0), vis);
+        hi = (int32_t)std::max<int64_t>(lo, std::min<int64_t>(std::max<int64_t>(e - entry, 0), vis));
+      }
+      entry += vis;
+      const int32_t nt = hi > lo ? (hi + kPieceMax - 1) / kPieceMax - lo / kPieceMax : 0;
       ps.ref_sid.push_back(ps.refs[r]);
       ps.ref_slot.push_back(slot_base + (int32_t)r);
       ps.ref_tiles.push_back(nt);
+      ps.ref_lo.push_back(lo);
+      ps.ref_hi.push_back(hi);
       tiles += nt;
     }
     ps.prob_common_refs[p] = n_common_refs;
@@ -833,26 +851,47 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     // per-group counts are floored and then raised to >= 1: keep room for that raise
     target_units = std::max<int64_t>(0, std::min<int64_t>(target_units, unit_cap - (int64_t)P * H));
   }
-  // A piece of segment reference r at tile t (one tile of at most kPieceMax tokens, inside one
-  // page), with the step's appended tokens in it listed for the fused append.
-  auto emit = [&](int32_t r, int32_t t) -> bool {
-    const Seg& sg = c->segs[ps.ref_sid[r]];
-    const int32_t j = t * kPieceMax;
-    const int32_t pg = c->cfg.contiguous ? sg.pages[0] : sg.pages[j / S];
-    const int32_t slot0 = c->cfg.contiguous ? j : j % S;
-    const int32_t cnt = std::min(kPieceMax, sg.visible() - j);
-    // fresh: holds tokens appended in this step (the kernels read it only after the append)
-    const int32_t fresh = (sg.pending > 0 && j + cnt > sg.length) ? 1 : 0;
-    if ((int64_t)ps.pieces.size() >= L.max_pieces) return false;
-    ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
-    ps.piece_early.push_back(!fresh && j + cnt <= sg.recent_from ? 1 : 0);
-    ps.pieces.push_back(hw::Piece{ps.ref_slot[r], pg, slot0, cnt, fresh, j});
-    if (fuse && fresh) {
-      const int32_t sid = ps.ref_sid[r];
-      if (ps.src_base[sid] < 0) return false;
-      for (int32_t k = std::max<int32_t>(0, sg.length - j); k < cnt; ++k) {
-        if ((int64_t)ps.fresh.size() >= L.max_fresh) return false;
-        ps.fresh.push_back(hw::FreshTok{pg, slot0 + k, j + k, ps.src_base[sid] + (j + k - sg.length)});
+  // The pieces of segment reference r at its tiles [t0, t1) (counted from the reference's
+  // first tile): the reference's tokens inside one kPieceMax-aligned tile each -- so inside one
+  // page -- with the step's appended tokens in it listed for the fused append.  Only the first
+  // piece of a reference can start inside its tile (an entry range that cuts the segment).
+  // (Segment data is read once per run; the page index advances with the tile.)
+  const bool contiguous = c->cfg.contiguous != 0;
+  const int32_t tiles_per_page = S / kPieceMax;
+  auto emit = [&](int32_t r, int32_t t0, int32_t t1) -> bool {
+    if (t1 <= t0) return true;
+    if ((int64_t)ps.pieces.size() + (t1 - t0) > L.max_pieces) return false;
+    const int32_t sid = ps.ref_sid[r];
+    const Seg& sg = c->segs[sid];
+    const int32_t* pages = sg.pages.data();
+    const int32_t seg_slot = ps.ref_slot[r], len = sg.length;
+    const int32_t lo = ps.ref_lo[r], hi = ps.ref_hi[r];
+    const int32_t recent = sg.recent_from;
+    const bool pending = sg.pending > 0;
+    const int32_t T0 = lo / kPieceMax + t0, T1 = lo / kPieceMax + t1;   // tiles of the segment
+    int32_t pi = contiguous ? 0 : T0 / tiles_per_page;     // page of tile T
+    int32_t sub = contiguous ? 0 : T0 - pi * tiles_per_page;  // tile T's place in it
+    for (int32_t T = T0; T < T1; ++T) {
+      const int32_t j = std::max(lo, T * kPieceMax);              // first token of the piece
+      const int32_t end = std::min(hi, (T + 1) * kPieceMax);      // one past its last
+      const int32_t pg = pages[pi];
+      const int32_t slot0 = contiguous ? j : sub * kPieceMax + (j - T * kPieceMax);
+      const int32_t cnt = end - j;
+      // fresh: holds tokens appended in this step (the kernels read it only after the append)
+      const int32_t fresh = (pending && end > len) ? 1 : 0;
+      ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
+      ps.piece_early.push_back(!fresh && end <= recent ? 1 : 0);
+      ps.pieces.push_back(hw::Piece{seg_slot, pg, slot0, cnt, fresh, j});
+      if (fuse && fresh) {
+        if (ps.src_base[sid] < 0) return false;
+        for (int32_t k = std::max<int32_t>(0, len - j); k < cnt; ++k) {
+          if ((int64_t)ps.fresh.size() >= L.max_fresh) return false;
+          ps.fresh.push_back(hw::FreshTok{pg, slot0 + k, j + k, ps.src_base[sid] + (j + k - len)});
+        }
+      }
+      if (!contiguous && ++sub == tiles_per_page) {
+        sub = 0;
+        ++pi;
       }
     }
     return true;
@@ -904,15 +943,13 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         }
         if (cr >= rc) return false;
         const int32_t take = std::min(left, ps.ref_tiles[cr] - ct);
-        for (int32_t t = ct; t < ct + take; ++t)
-          if (!emit(cr, t)) return false;
+        if (!emit(cr, ct, ct + take)) return false;
         ct += take;
         left -= take;
       }
       for (const auto& pt : ps.parts) {
         if (pt.unit != k) continue;
-        for (int32_t t = pt.t0; t < pt.t1; ++t)
-          if (!emit(pt.ref, t)) return false;
+        if (!emit(pt.ref, pt.t0, pt.t1)) return false;
       }
       ps.unit_range.push_back({ub, (int32_t)ps.pieces.size()});
     }
@@ -995,7 +1032,8 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
 // One attention call: one query per worker (n_q null), or n_q[p][w] causal query tokens per
 // worker (the last tokens of its own block).
 static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* n_q, void* out,
-                        int32_t out_dtype, float* lse, void* stream) {
+                        int32_t out_dtype, float* lse, void* stream,
+                        const int64_t* ranges = nullptr) {
   if (!c || layer < 0 || layer >= c->cfg.num_layers) return HW_ERR_INVALID_ARG;
   if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
   if (c->step_active && !c->appended[layer]) return HW_ERR_INVALID_ARG;
@@ -1025,7 +1063,7 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
   char* dbase = nullptr;
   // (the step's plan has one query per worker and lists the step's tokens for the kernel)
   const bool step_plan =
-      !n_q && c->step_slot >= 0 && c->step_epoch == c->epoch && c->step_plan_ok;
+      !n_q && !ranges && c->step_slot >= 0 && c->step_epoch == c->epoch && c->step_plan_ok;
   // The layer's recorded append is written by the tensor-core kernel when the step's plan lists
   // the appended tokens; otherwise by the append kernel, now.
   const bool fused = c->use_tc && step_plan && c->step_fused && layer < (int32_t)c->pend_k.size() &&
@@ -1052,7 +1090,7 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
     // partials fit the workspace: units * rows stays within its max_units * (W * G) rows
     const int64_t cap = n_q ? (int64_t)c->lay.max_units * c->rows / (width * c->G) : 0;
     if (!build_attention_plan(c, c->h_slot(slot), &po, cap, c->use_tc ? c->num_sms : 0, false, seq,
-                              n_q))
+                              n_q, ranges))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
     hbase = c->h_slot(slot);
@@ -1124,7 +1162,9 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
   }
   HW_CUDA(cudaGetLastError());
   if (fused) c->pend_k[layer] = c->pend_v[layer] = nullptr;
-  hw::launch_merge(a, s, c->use_tc);
+  const int pm = c->prof_begin(s, 2);      // (a timed merge is not chained to the attention)
+  hw::launch_merge(a, s, c->use_tc && pm < 0);
+  c->prof_end(pm, s);
   HW_CUDA(cudaGetLastError());
   c->n_launch += 2;
   c->n_attn += 1;
@@ -1148,7 +1188,19 @@ hw_status hw_concurrent_attention_mq(hw_ctx* c, int32_t layer, const void* q, co
   return attend(c, layer, q, n_q, out, out_dtype, lse, stream);
 }
 
+hw_status hw_concurrent_attention_range(hw_ctx* c, int32_t layer, const void* q,
+                                        const int64_t* ranges, float* out, float* lse,
+                                        void* stream) {
+  if (!c || !ranges || !lse) return HW_ERR_INVALID_ARG;
+  for (int32_t p = 0; p < c->cfg.num_problems; ++p)
+    if (ranges[2 * p] < 0 || ranges[2 * p + 1] < ranges[2 * p]) return HW_ERR_INVALID_ARG;
+  if ((uintptr_t)lse % 4) return HW_ERR_INVALID_ARG;
+  return attend(c, layer, q, nullptr, out, HW_OUT_F32, lse, stream, ranges);
+}
+
 }  // extern "C"
+
+hw_status hw::cuda_status(cudaError_t e) { return e == cudaSuccess ? HW_OK : cuda_fail(e); }
 
 // Same computation as hw_concurrent_attention, with the call's plan and the split-K partials
 // placed in caller-given device scratch instead of the workspace (used by the allocation-free
@@ -1392,6 +1444,9 @@ hw_status hw_profile_read(hw_ctx* c, hw_profile* out) {
     if (c->prof_kind[i] == 0) {
       r.attention_ms += ms;
       r.timed_attention += 1;
+    } else if (c->prof_kind[i] == 2) {
+      r.merge_ms += ms;
+      r.timed_merge += 1;
     } else {
       r.append_ms += ms;
       r.timed_append += 1;

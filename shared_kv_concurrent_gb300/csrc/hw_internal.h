@@ -194,6 +194,10 @@ void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, const LaunchUnit
 void launch_merge(const AttnArgs& a, cudaStream_t s, bool pdl = false);
 bool make_tc_maps(const hw_config& cfg, void* k_pool, void* v_pool, TcMaps* out);
 
+// HW_OK for cudaSuccess; otherwise records the error for hw_last_cuda_error and returns
+// HW_ERR_CUDA.
+hw_status cuda_status(cudaError_t e);
+
 // hw_concurrent_attention with the plan and the partial results in `scratch` (device).
 hw_status attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, void* out,
                                  int32_t out_dtype, float* lse, void* stream, char* scratch,
