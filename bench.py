@@ -87,12 +87,15 @@ def captured_share():
         return None
 
 
-def workload_for(name, layout="combined"):
-    """The named workload; another cache layout changes only the views (and the name)."""
+def workload_for(name, layout="combined", seed=None):
+    """The named workload; another cache layout changes only the views (and the name); another
+    master seed redraws the block lengths, the page order and every tensor (and the name)."""
     import dataclasses
 
     import workload as wl
-    w = wl.CONFIGS[name]()
+    w = wl.CONFIGS[name]() if seed is None else wl.CONFIGS[name](seed=seed)
+    if seed is not None:
+        w = dataclasses.replace(w, name=f"{w.name}_seed{seed}")
     if layout != "combined":
         w = dataclasses.replace(w, layout=layout, name=f"{w.name}_{layout}")
     return w
@@ -227,7 +230,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    base = workload_for(args.config, args.layout)
+    base = workload_for(args.config, args.layout, args.seed)
     w = wl.scaled(base, name=base.name, steps=args.warmup + args.steps + 1)
     threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
     c = orun.prefill(w)
@@ -280,7 +283,7 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    base = workload_for(args.config, args.layout)
+    base = workload_for(args.config, args.layout, args.seed)
     e2e_steps = args.e2e_steps
     kv_mb = base.num_layers * base.view_tokens(0) * base.num_kv_heads * base.head_dim * 4 / 1e6
     layer_mb = kv_mb / base.num_layers                     # K/V of one layer of one cache
@@ -523,6 +526,9 @@ def main():
     ap.add_argument("--layout", default="combined",
                     choices=["combined", "step_wise", "contiguous", "no_sync"],
                     help="cache layout of the workload (the default is the method's own)")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="another master seed for the workload (block lengths, page order, "
+                         "tensors); the default is the workload's own")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--caches", type=int, default=0,
                     help="independent caches of the workload used in turn (0: enough that the "

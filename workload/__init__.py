@@ -210,51 +210,51 @@ def _uniform_lengths(seed: int, P: int, W: int, lo: int, hi: int, stream: int = 
     return tuple(tuple(int(x) for x in g.integers(lo, hi + 1, size=W)) for _ in range(P))
 
 
-def tiny(contiguous: bool = False) -> Workload:
+def tiny(contiguous: bool = False, seed: int = 1000) -> Workload:
     """W=2, H_q 8, H_kv 2, D 64, theta 1e4; common 512, each worker block 64; views C+B+A / C+A+B."""
     return Workload(name="tiny_w2_c512" + ("_contig" if contiguous else ""), num_problems=1,
                     num_workers=2, num_layers=1, num_q_heads=8, num_kv_heads=2, head_dim=64,
                     rope_theta=1e4, page_size=(640 if contiguous else 256), contiguous=contiguous,
-                    random_page_order=False, seed=1000, common_len=(512,),
+                    random_page_order=False, seed=seed, common_len=(512,),
                     worker_len=((64, 64),), steps=4)
 
 
-def c2() -> Workload:
+def c2(seed: int = 1001) -> Workload:
     """W=2, H_q 40, H_kv 8, D 128, theta 1e6; common 4096, worker blocks 256; contiguous cache."""
     return Workload(name="w2_common4096_contig", num_problems=1, num_workers=2, num_layers=1,
                     num_q_heads=40, num_kv_heads=8, head_dim=128, rope_theta=1e6,
-                    page_size=4224, contiguous=True, random_page_order=False, seed=1001,
+                    page_size=4224, contiguous=True, random_page_order=False, seed=seed,
                     common_len=(4096,), worker_len=((256, 256),), steps=64)
 
 
-def c3() -> Workload:
+def c3(seed: int = 1002) -> Workload:
     """W=4, H_q 64, H_kv 8, D 128; common 16384, worker blocks U[0,1024]; 64 layers."""
     return Workload(name="w4_common16384_64layers", num_problems=1, num_workers=4, num_layers=64,
                     num_q_heads=64, num_kv_heads=8, head_dim=128, rope_theta=1e6,
-                    page_size=256, contiguous=False, random_page_order=False, seed=1002,
-                    common_len=(16384,), worker_len=_uniform_lengths(1002, 1, 4, 0, 1024),
+                    page_size=256, contiguous=False, random_page_order=False, seed=seed,
+                    common_len=(16384,), worker_len=_uniform_lengths(seed, 1, 4, 0, 1024),
                     steps=16)
 
 
-def c4() -> Workload:
+def c4(seed: int = 1003) -> Workload:
     """W=8, H_q 64, H_kv 8, D 128; common 32768 + worker blocks U[128,2048]; paged, permuted."""
     return Workload(name="w8_common32768_paged", num_problems=1, num_workers=8, num_layers=1,
                     num_q_heads=64, num_kv_heads=8, head_dim=128, rope_theta=1e6,
-                    page_size=256, contiguous=False, random_page_order=True, seed=1003,
-                    common_len=(32768,), worker_len=_uniform_lengths(1003, 1, 8, 128, 2048),
+                    page_size=256, contiguous=False, random_page_order=True, seed=seed,
+                    common_len=(32768,), worker_len=_uniform_lengths(seed, 1, 8, 128, 2048),
                     steps=400)
 
 
-def c5() -> Workload:
+def c5(seed: int = 1004) -> Workload:
     """16 problems x W=4, H_q 32, H_kv 8, D 128; lognormal common lengths; 200 steps."""
-    g = _rng(1004, TAG_LENGTHS, 1)
+    g = _rng(seed, TAG_LENGTHS, 1)
     common = np.clip(np.round(g.lognormal(mean=math.log(8192.0), sigma=0.7, size=16)),
                      1024, 65536).astype(int)
     return Workload(name="p16_w4_lognormal_200steps", num_problems=16, num_workers=4,
                     num_layers=1, num_q_heads=32, num_kv_heads=8, head_dim=128,
                     rope_theta=1e6, page_size=256, contiguous=False, random_page_order=False,
-                    seed=1004, common_len=tuple(int(c) for c in common),
-                    worker_len=_uniform_lengths(1004, 16, 4, 0, 512), steps=200,
+                    seed=seed, common_len=tuple(int(c) for c in common),
+                    worker_len=_uniform_lengths(seed, 16, 4, 0, 512), steps=200,
                     commit_steps=(63, 127, 191))
 
 
