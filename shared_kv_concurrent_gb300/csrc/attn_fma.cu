@@ -1,5 +1,6 @@
-// K2 (FMA form) and K3 -- concurrent attention with per-(worker, block) query rotation, and
-// the log-sum-exp merge of the per-unit partial results.
+// K2 (CUDA-core form) and K3 -- concurrent attention with per-(worker, block) query rotation
+// for fewer than 16 query rows per KV head, and the log-sum-exp merge of the per-unit partial
+// results.
 //
 // Method (Hogwild! Inference summary, gentlecold.top): keys are stored rotated at block-local
 // positions; for a block at offset o in worker w's view the query is rotated by (i_q - o)
@@ -7,70 +8,193 @@
 // with its own rotated query.  Work is split over KV entries, not over blocks, and the partial
 // results are reduced afterwards (section 9, Flash-Decoding style kernel).
 //
-// This form uses FP32 FMA and is meant for small row counts (W * G below a 16-row tile); one
-// CTA per unit (a run of pieces of one (problem, KV head)), 8 warps, each warp owning rows
-// r = warp, warp + 8, ...; lane = token of a 32-token tile staged in shared memory.
+// One CTA per unit (a run of pieces of one (problem, KV head)), 8 warps.  Each piece's K and V
+// tiles (128 rows x D bf16 from the pool, the same 128-byte-swizzled TMA boxes the tensor-core
+// kernel loads) are staged once into a ring of one or two slots in shared memory, completion
+// on an mbarrier, and kept in bf16; the rotated, pre-scaled queries (log2(e)/sqrt(D)) and the
+// running output O of every row stay in shared memory in fp32.  Per tile and per chunk of 16
+// query rows: S = Q~ K^T with a thread per (token, half of the rows); the online softmax with a
+// warp per row (running max and sum, rescale factor); O = alpha O + P V with a thread per (row
+// pair, 4 columns).  Every wait is bounded (about a second): one that runs out records
+// ERR_TIMEOUT, and the CTA waits (bounded by the clock) for its copies in flight, then writes
+// empty partials.  The kernel is launched as a programmatic dependent: it waits for the grid
+// it follows (which may write the queries or this step's tokens) before it reads anything.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
 #include "hw_device.cuh"
 #include "hw_merge.cuh"
+#include "tc_ptx.cuh"
+
+#include <algorithm>
 
 namespace hw {
 namespace {
 
+using tc::fence_mbar_init;
+using tc::fence_proxy_async_smem;
+using tc::mbar_arrive_expect_tx;
+using tc::mbar_init;
+using tc::mbar_wait;
+using tc::mbar_wait_drain;
+using tc::smem_u32;
+using tc::tma_load_2d;
+
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTile = 32;
-constexpr int kMaxRowsPerWarp = 16;   // rows <= 128
+constexpr int kTile = 128;            // tokens per tile (one TMA box of rows)
+constexpr int kChunkRows = 16;        // query rows per pass over a tile, at most
+constexpr uint64_t kWaitNs = 1000000000ull;
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
-  extern __shared__ float sm[];
-  constexpr int DJ = D / 32;
-  constexpr int KS = D + 1;                     // padded key row: conflict-free lane = token
-  const int rows = a.rows;
-  float* qs = sm;                               // [rows][D] rotated, pre-scaled queries
-  float* ks = qs + rows * D;                    // [kTile][D + 1]
-  float* vs = ks + kTile * KS;                  // [kTile][D]
-  __shared__ int plan_ok;
-  if (threadIdx.x == 0) plan_ok = plan_arrived(a.gate, plan_seq_now(a.gate), a.err, KID_ATTN_FMA);
+struct FmaCfg {
+  static constexpr int kHalves = D / 64;                       // 128-byte swizzle atoms per row
+  static constexpr uint32_t kHalfBytes = kTile * 128;          // one {64, 128} TMA box
+  static constexpr uint32_t kTileBytes = kHalves * kHalfBytes; // K or V tile
+  static constexpr uint32_t kSlotBytes = 2 * kTileBytes;       // K then V
+};
+
+// Shared-memory layout for R query rows and `slots` ring slots (offsets from a 1024-byte
+// aligned base): ring, Q~ [R][D] f32, O [R][D] f32, S/P [16][128] f32, M/L/alpha [R] f32, row
+// cut [R] i32, barriers, flags.
+template <int D>
+struct FmaLayout {
+  uint32_t q, o, s, m, l, al, cut, bars, flags, total;
+  __host__ __device__ FmaLayout(int R, int slots) {
+    uint32_t off = (uint32_t)slots * FmaCfg<D>::kSlotBytes;
+    q = off;    off += (uint32_t)R * D * 4;
+    o = off;    off += (uint32_t)R * D * 4;
+    s = off;    off += kChunkRows * kTile * 4;
+    m = off;    off += (uint32_t)R * 4;
+    l = off;    off += (uint32_t)R * 4;
+    al = off;   off += (uint32_t)R * 4;
+    cut = off;  off += (uint32_t)R * 4;
+    off = (off + 7) / 8 * 8;
+    bars = off; off += 8 * 2;
+    flags = off; off += 16;
+    total = off + 1024;                  // + alignment slack
+  }
+};
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Byte offset, inside a {64, 128} swizzled box pair, of the 16-byte chunk holding elements
+// 8c .. 8c + 7 (c = d / 8) of tile row j.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int j, int c) {
+  return (uint32_t)(c >> 3) * FmaCfg<D>::kHalfBytes + (uint32_t)j * 128 +
+         ((uint32_t)((c & 7) ^ (j & 7)) << 4);
+}
+
+__device__ __forceinline__ bool piece_ok(const AttnArgs& a, const Piece& pc) {
+  return pc.page >= 0 && pc.page < a.num_pages && pc.slot0 >= 0 && pc.ntok >= 1 &&
+         pc.ntok <= kTile && pc.slot0 + pc.ntok <= a.S && pc.seg_slot >= 0 &&
+         pc.seg_slot < a.num_seg_slots;
+}
+
+// RPT: query rows per thread in S = Q~ K^T (the chunk of 2 * RPT rows a pass over a tile
+// takes; 1 .. 8, so that no thread issues FMAs for rows a short chunk does not have).
+template <int D, int RPT>
+__global__ void __launch_bounds__(kThreads, 2)
+    attn_fma_kernel(const AttnArgs a, const __grid_constant__ TcMaps maps, const int32_t layer,
+                    const int32_t slots) {
+  using C = FmaCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int R = a.rows;
+  const FmaLayout<D> L(R, slots);
+  float* Qs = reinterpret_cast<float*>(smem + L.q);
+  float* Os = reinterpret_cast<float*>(smem + L.o);
+  float* Ss = reinterpret_cast<float*>(smem + L.s);
+  float* Ms = reinterpret_cast<float*>(smem + L.m);
+  float* Ls = reinterpret_cast<float*>(smem + L.l);
+  float* As = reinterpret_cast<float*>(smem + L.al);
+  int* cut = reinterpret_cast<int*>(smem + L.cut);     // tokens of the segment a row sees (-1: none)
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + L.flags);   // [0] plan ok, [1] abort
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + L.bars;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int PS = part_stride(D);
+
+  // Wait for the grid this one follows (it may write the queries, this step's tokens, or read
+  // the partials this grid overwrites) before anything is read or written.
+  tc::pdl_wait();
+  if (tid == 0) {
+    for (int k = 0; k < slots; ++k) mbar_init(bars + 8u * k, 1);
+    fence_mbar_init();
+    flags[0] = plan_arrived(a.gate, plan_seq_now(a.gate), a.err, KID_ATTN_FMA) ? 1 : 0;
+    flags[1] = 0;
+  }
+  for (int i = tid; i < R * D; i += kThreads) Os[i] = 0.f;
+  for (int r = tid; r < R; r += kThreads) {
+    Ms[r] = -CUDART_INF_F;
+    Ls[r] = 0.f;
+  }
   __syncthreads();
-  if (!plan_ok) {
-    // No plan: this unit's partial rows are written empty (m = -inf, l = 0, o = 0), so the
-    // merge gives zero for them; the error word says why.
-    float* part = a.partials + (size_t)blockIdx.x * rows * part_stride(D);
-    for (int e = threadIdx.x; e < rows * part_stride(D); e += blockDim.x)
-      part[e] = (e % part_stride(D) == D) ? -CUDART_INF_F : 0.f;
-    return;
-  }
-  const Unit u = a.units[blockIdx.x];
-  const Group g = a.groups[u.group];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  float m[kMaxRowsPerWarp], l[kMaxRowsPerWarp], o[kMaxRowsPerWarp][DJ];
-#pragma unroll
-  for (int k = 0; k < kMaxRowsPerWarp; ++k) {
-    m[k] = -CUDART_INF_F;
-    l[k] = 0.f;
-#pragma unroll
-    for (int j = 0; j < DJ; ++j) o[k][j] = 0.f;
-  }
-
-  int cur_slot = -1;
-  for (int pi = u.piece_begin; pi < u.piece_end; ++pi) {
-    const Piece pc = a.pieces[pi];
-    if (pc.page < 0 || pc.page >= a.num_pages || pc.slot0 < 0 || pc.ntok < 1 ||
-        pc.slot0 + pc.ntok > a.S || pc.seg_slot < 0 || pc.seg_slot >= a.num_seg_slots) {
-      if (threadIdx.x == 0) record_error(a.err, ERR_PLAN, KID_ATTN_FMA, blockIdx.x, pi);
-      continue;
+  const bool plan_ok = flags[0] != 0;
+  Unit u{};
+  Group g{};
+  bool unit_ok = false;
+  if (plan_ok) {
+    u = a.units[blockIdx.x];
+    if (u.group >= 0 && u.group < a.num_groups) {
+      g = a.groups[u.group];
+      unit_ok = g.p >= 0 && g.p < a.P && g.h >= 0 && g.h < a.H_kv && u.piece_begin >= 0 &&
+                u.piece_begin <= u.piece_end;
     }
-    const int* dl = a.delta + (size_t)pc.seg_slot * a.W;
-    if (pc.seg_slot != cur_slot) {
-      // New segment: rotate every row's query by (i_q - view offset) of this segment.
-      __syncthreads();
-      const int half = D / 2;
-      for (int idx = threadIdx.x; idx < rows * half; idx += kThreads) {
+    if (!unit_ok && tid == 0) record_error(a.err, ERR_PLAN, KID_ATTN_FMA, blockIdx.x, 0);
+  }
+  const int pb = unit_ok ? u.piece_begin : 0, pe = unit_ok ? u.piece_end : 0;
+  const int64_t page_base = (int64_t)layer * a.num_pages;   // first page of this layer's pool
+
+  // Producer (thread 0): the first valid piece at or after `from`, its K and V tiles into ring
+  // slot `slot` (pool rows ((page_base + page) * H_kv + h) * S + slot0 ..).  Returns the index
+  // of the piece it loaded, or -1 when none is left.
+  auto issue = [&](int from, int slot) -> int {
+    for (int pi = from; pi < pe; ++pi) {
+      const Piece pc = a.pieces[pi];
+      if (!piece_ok(a, pc)) continue;
+      const uint32_t dst = sbase + (uint32_t)slot * C::kSlotBytes;
+      const int32_t y = (int32_t)(((page_base + pc.page) * a.H_kv + g.h) * a.S + pc.slot0);
+      mbar_arrive_expect_tx(bars + 8u * slot, C::kSlotBytes);
+#pragma unroll
+      for (int hh = 0; hh < C::kHalves; ++hh) {
+        tma_load_2d(dst + hh * C::kHalfBytes, &maps.k, 64 * hh, y, bars + 8u * slot,
+                    tc::l2_policy_evict_first());
+        tma_load_2d(dst + C::kTileBytes + hh * C::kHalfBytes, &maps.v, 64 * hh, y,
+                    bars + 8u * slot, tc::l2_policy_evict_first());
+      }
+      return pi;
+    }
+    return -1;
+  };
+  int next_issue = pb;            // (thread 0) first piece not yet looked at
+  uint32_t issued = 0;            // (thread 0) tiles issued
+  if (tid == 0 && pb < pe) {
+    tc::tma_prefetch(&maps.k);
+    tc::tma_prefetch(&maps.v);
+    for (int k = 0; k < slots && next_issue < pe; ++k) {
+      const int got = issue(next_issue, k);
+      next_issue = got < 0 ? pe : got + 1;
+      if (got >= 0) ++issued;
+    }
+  }
+
+  int cur_seg = -1;
+  uint32_t tile = 0;              // tiles consumed
+  for (int pi = pb; pi < pe; ++pi) {
+    const Piece pc = a.pieces[pi];
+    if (!piece_ok(a, pc)) continue;                 // every thread skips it the same way
+    if (pc.seg_slot != cur_seg) {
+      // New segment: every row's query rotated by (i_q - the segment's view offset), pre-scaled;
+      // rows of workers that do not see it are zero and cut = -1.
+      cur_seg = pc.seg_slot;
+      const int* dl = a.delta + (size_t)pc.seg_slot * a.W;
+      constexpr int half = D / 2;
+      for (int idx = tid; idx < R * half; idx += kThreads) {
         const int r = idx / half, i = idx % half;
         const int w = r / a.G, hq = g.h * a.G + r % a.G;
         const int delta = dl[w];
@@ -80,88 +204,189 @@ __global__ void __launch_bounds__(kThreads) attn_fma_kernel(const AttnArgs a) {
           const float q1 = __bfloat162float(a.q[qo + i]);
           const float q2 = __bfloat162float(a.q[qo + i + half]);
           const float c = a.rope_cos[(size_t)delta * half + i];
-          const float s = a.rope_sin[(size_t)delta * half + i];
-          y1 = (q1 * c - q2 * s) * a.scale_log2;
-          y2 = (q2 * c + q1 * s) * a.scale_log2;
+          const float sn = a.rope_sin[(size_t)delta * half + i];
+          y1 = (q1 * c - q2 * sn) * a.scale_log2;
+          y2 = (q2 * c + q1 * sn) * a.scale_log2;
         } else if (delta >= a.max_position && i == 0) {
           record_error(a.err, ERR_POS_RANGE, KID_ATTN_FMA, blockIdx.x, delta);
         }
-        qs[r * D + i] = y1;
-        qs[r * D + i + half] = y2;
+        Qs[r * D + i] = y1;
+        Qs[r * D + i + half] = y2;
+        if (i == 0) {
+          const bool vis = delta >= 0 && delta < a.max_position;
+          // causal cut (several query tokens per worker): tokens of the segment it may see
+          cut[r] = !vis ? -1
+                        : (a.vlen ? a.vlen[(size_t)pc.seg_slot * a.W + w] : 0x7fffffff);
+        }
       }
-      cur_slot = pc.seg_slot;
     }
-    const size_t base = (((size_t)pc.page * a.H_kv + g.h) * a.S + pc.slot0) * D;
-    for (int t0 = 0; t0 < pc.ntok; t0 += kTile) {
-      const int nt = min(kTile, pc.ntok - t0);
-      __syncthreads();
-      for (int idx = threadIdx.x; idx < kTile * (D / 8); idx += kThreads) {
-        const int tok = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
-        uint4 kr = make_uint4(0, 0, 0, 0), vr = make_uint4(0, 0, 0, 0);
-        if (tok < nt) {
-          kr = *reinterpret_cast<const uint4*>(a.k_layer + base + (size_t)(t0 + tok) * D + c8);
-          vr = *reinterpret_cast<const uint4*>(a.v_layer + base + (size_t)(t0 + tok) * D + c8);
-        }
-        const __nv_bfloat162* kp = reinterpret_cast<const __nv_bfloat162*>(&kr);
-        const __nv_bfloat162* vp = reinterpret_cast<const __nv_bfloat162*>(&vr);
+    const int slot = (int)(tile % (uint32_t)slots);
+    const uint32_t parity = (tile / (uint32_t)slots) & 1u;
+    // every thread waits for the tile (bounded); an expiry anywhere ends the loop for all
+    if (!mbar_wait(bars + 8u * slot, parity, flags + 1, kWaitNs)) flags[1] = 1;
+    __syncthreads();                                // also: the rotated queries are written
+    if (flags[1]) break;
+    const uint8_t* kt = smem + (uint32_t)slot * C::kSlotBytes;
+    const uint8_t* vt = kt + C::kTileBytes;
+    const int nv = pc.ntok;
+    for (int r0 = 0; r0 < R; r0 += 2 * RPT) {
+      const int CR = min(2 * RPT, R - r0);
+      {
+        // S = Q~ K^T: thread (token j, row parity hf) takes rows hf, hf + 2, ... of the chunk
+        // (two accumulators per row, and a chunk's queries loaded before its FMAs: the chains
+        // are short and the shared loads in flight together)
+        const int j = tid & (kTile - 1), hf = tid >> 7;
+        float acc0[RPT], acc1[RPT];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 kf = __bfloat1622float2(kp[j]);
-          const float2 vf = __bfloat1622float2(vp[j]);
-          ks[tok * KS + c8 + 2 * j] = kf.x;
-          ks[tok * KS + c8 + 2 * j + 1] = kf.y;
-          vs[tok * D + c8 + 2 * j] = vf.x;
-          vs[tok * D + c8 + 2 * j + 1] = vf.y;
+        for (int i = 0; i < RPT; ++i) acc0[i] = acc1[i] = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 kw = *reinterpret_cast<const uint4*>(kt + swz<D>(j, c));
+          float4 qa[RPT], qb[RPT];
+#pragma unroll
+          for (int i = 0; i < RPT; ++i) {
+            const int rr = min(hf + 2 * i, CR - 1);         // (rows past the chunk: ignored)
+            qa[i] = *reinterpret_cast<const float4*>(Qs + (size_t)(r0 + rr) * D + 8 * c);
+            qb[i] = *reinterpret_cast<const float4*>(Qs + (size_t)(r0 + rr) * D + 8 * c + 4);
+          }
+          const float k0 = bf_lo(kw.x), k1 = bf_hi(kw.x), k2 = bf_lo(kw.y), k3 = bf_hi(kw.y);
+          const float k4 = bf_lo(kw.z), k5 = bf_hi(kw.z), k6 = bf_lo(kw.w), k7 = bf_hi(kw.w);
+#pragma unroll
+          for (int i = 0; i < RPT; ++i) {
+            acc0[i] = fmaf(qa[i].x, k0, acc0[i]);
+            acc1[i] = fmaf(qa[i].y, k1, acc1[i]);
+            acc0[i] = fmaf(qa[i].z, k2, acc0[i]);
+            acc1[i] = fmaf(qa[i].w, k3, acc1[i]);
+            acc0[i] = fmaf(qb[i].x, k4, acc0[i]);
+            acc1[i] = fmaf(qb[i].y, k5, acc1[i]);
+            acc0[i] = fmaf(qb[i].z, k6, acc0[i]);
+            acc1[i] = fmaf(qb[i].w, k7, acc1[i]);
+          }
         }
+#pragma unroll
+        for (int i = 0; i < RPT; ++i)
+          if (hf + 2 * i < CR) Ss[(hf + 2 * i) * kTile + j] = acc0[i] + acc1[i];
       }
       __syncthreads();
+      // Online softmax: warp w takes rows w and w + 8 of the chunk, a lane four tokens.
+      for (int rr = warp; rr < CR; rr += kWarps) {
+        const int r = r0 + rr;
+        const int cap = cut[r];                     // -1: the row does not see the segment
+        const int lim = cap < 0 ? 0 : min(nv, cap - pc.pos0);
+        float4 sv = reinterpret_cast<const float4*>(Ss + rr * kTile)[lane];
+        float s4[4] = {sv.x, sv.y, sv.z, sv.w};
+        float mx = -CUDART_INF_F;
 #pragma unroll
-      for (int k = 0; k < kMaxRowsPerWarp; ++k) {
-        const int r = warp + k * kWarps;
-        if (r >= rows) continue;
-        if (dl[r / a.G] < 0) continue;              // this worker does not see the segment
-        // causal cut (several query tokens per worker): tokens of the segment it may see
-        const int cap = a.vlen ? a.vlen[(size_t)pc.seg_slot * a.W + r / a.G] : pc.pos0 + pc.ntok;
-        const float* qr = qs + r * D;
-        const float* kr = ks + lane * KS;
-        float s = 0.f;
-#pragma unroll 16
-        for (int d = 0; d < D; ++d) s = fmaf(qr[d], kr[d], s);
-        if (lane >= nt || pc.pos0 + t0 + lane >= cap) s = -CUDART_INF_F;
-        float tmax = s;
+        for (int e = 0; e < 4; ++e) {
+          if (4 * lane + e >= lim) s4[e] = -CUDART_INF_F;
+          mx = fmaxf(mx, s4[e]);
+        }
 #pragma unroll
-        for (int off = 16; off; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-        if (tmax == -CUDART_INF_F) continue;        // nothing of this tile is visible to the row
-        const float mn = fmaxf(m[k], tmax);
-        const float alpha = exp2f(m[k] - mn);
-        const float p = exp2f(s - mn);
-        float ps = p;
+        for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_old = Ms[r];
+        const float m_new = fmaxf(m_old, mx);
+        float alpha = 1.f, ps = 0.f;
+        float p4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (m_new != -CUDART_INF_F) {
+          alpha = (m_old == -CUDART_INF_F) ? 0.f : exp2f(m_old - m_new);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            p4[e] = (s4[e] == -CUDART_INF_F) ? 0.f : exp2f(s4[e] - m_new);
+            ps += p4[e];
+          }
+        }
 #pragma unroll
         for (int off = 16; off; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-        l[k] = l[k] * alpha + ps;
-#pragma unroll
-        for (int j = 0; j < DJ; ++j) o[k][j] *= alpha;
-        for (int t = 0; t < nt; ++t) {
-          const float pt = __shfl_sync(0xffffffffu, p, t);
-#pragma unroll
-          for (int j = 0; j < DJ; ++j) o[k][j] = fmaf(pt, vs[t * D + lane + 32 * j], o[k][j]);
+        reinterpret_cast<float4*>(Ss + rr * kTile)[lane] = make_float4(p4[0], p4[1], p4[2], p4[3]);
+        __syncwarp();
+        if (lane == 0) {
+          Ms[r] = m_new;
+          Ls[r] = Ls[r] * alpha + ps;
+          As[r] = alpha;
         }
-        m[k] = mn;
       }
+      __syncthreads();
+      {
+        // O = alpha O + P V: thread (row pair rp, columns 4 dg .. 4 dg + 3)
+        const int rp = tid >> 5, dg = lane;
+        const int ra = 2 * rp, rb = 2 * rp + 1;
+        if (dg < D / 4 && ra < CR) {
+          const bool has_b = rb < CR;
+          float4* oa = reinterpret_cast<float4*>(Os + (size_t)(r0 + ra) * D) + dg;
+          float4* ob = reinterpret_cast<float4*>(Os + (size_t)(r0 + (has_b ? rb : ra)) * D) + dg;
+          float4 xa = *oa, xb = *ob;
+          const float aa = As[r0 + ra], ab = has_b ? As[r0 + rb] : 1.f;
+          xa = make_float4(xa.x * aa, xa.y * aa, xa.z * aa, xa.w * aa);
+          xb = make_float4(xb.x * ab, xb.y * ab, xb.z * ab, xb.w * ab);
+          const float* pa = Ss + ra * kTile;
+          const float* pbr = Ss + (has_b ? rb : ra) * kTile;
+          const int d = 4 * dg;
+          const uint8_t* vcol = vt + (uint32_t)(d >> 6) * C::kHalfBytes + (uint32_t)((d & 7) * 2);
+          const int vc = (d & 63) >> 3;
+          // four tokens at a time: their P values (one float4 per row) and V words loaded first
+          // (P is zero past the piece's tokens, so the tail of the last group adds nothing)
+          const int nv4 = (nv + 3) & ~3;
+#pragma unroll 1
+          for (int k = 0; k < nv4; k += 4) {
+            const float4 p4 = *reinterpret_cast<const float4*>(pa + k);
+            const float4 q4 = *reinterpret_cast<const float4*>(pbr + k);
+            uint2 vw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              vw[e] = *reinterpret_cast<const uint2*>(
+                  vcol + (uint32_t)(k + e) * 128 + ((uint32_t)(vc ^ ((k + e) & 7)) << 4));
+            const float pp[4] = {p4.x, p4.y, p4.z, p4.w}, qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float v0 = bf_lo(vw[e].x), v1 = bf_hi(vw[e].x);
+              const float v2 = bf_lo(vw[e].y), v3 = bf_hi(vw[e].y);
+              xa.x = fmaf(pp[e], v0, xa.x);
+              xa.y = fmaf(pp[e], v1, xa.y);
+              xa.z = fmaf(pp[e], v2, xa.z);
+              xa.w = fmaf(pp[e], v3, xa.w);
+              xb.x = fmaf(qq[e], v0, xb.x);
+              xb.y = fmaf(qq[e], v1, xb.y);
+              xb.z = fmaf(qq[e], v2, xb.z);
+              xb.w = fmaf(qq[e], v3, xb.w);
+            }
+          }
+          *oa = xa;
+          if (has_b) *ob = xb;
+        }
+      }
+      __syncthreads();
+    }
+    ++tile;
+    // the slot is free: its next piece goes out (the generic reads of the slot are ordered
+    // before the copy's writes)
+    if (tid == 0 && next_issue < pe) {
+      fence_proxy_async_smem();
+      const int got = issue(next_issue, slot);
+      next_issue = got < 0 ? pe : got + 1;
+      if (got >= 0) ++issued;
     }
   }
-  // Partial result of this unit: o (unnormalised), m, l in the log2 domain.
-#pragma unroll
-  for (int k = 0; k < kMaxRowsPerWarp; ++k) {
-    const int r = warp + k * kWarps;
-    if (r >= rows) continue;
-    float* part = a.partials + ((size_t)blockIdx.x * rows + r) * part_stride(D);
-#pragma unroll
-    for (int j = 0; j < DJ; ++j) part[lane + 32 * j] = o[k][j];
-    if (lane == 0) {
-      part[D] = m[k];
-      part[D + 1] = l[k];
+  if (tid == 0) tc::pdl_launch_dependents();       // the merge may start its prologue
+  if (flags[1] || !plan_ok) {
+    // A wait ran out (or the plan never arrived): the copies in flight land before the CTA
+    // leaves, and the unit's partials are written empty.
+    if (tid == 0) {
+      if (flags[1]) record_error(a.err, ERR_TIMEOUT, KID_ATTN_FMA, blockIdx.x, 1);
+      for (uint32_t k = tile; k < issued; ++k)
+        mbar_wait_drain(bars + 8u * (k % (uint32_t)slots), (k / (uint32_t)slots) & 1u, kWaitNs);
     }
+    float* part = a.partials + (size_t)blockIdx.x * R * PS;
+    for (int e = tid; e < R * PS; e += kThreads) part[e] = (e % PS == D) ? -CUDART_INF_F : 0.f;
+    return;
+  }
+  // Partial result of this unit: o (unnormalised), m, l in the log2 domain.
+  float* part = a.partials + (size_t)blockIdx.x * R * PS;
+  for (int r = warp; r < R; r += kWarps) {
+    if (lane < D / 4)
+      reinterpret_cast<float4*>(part + (size_t)r * PS)[lane] =
+          reinterpret_cast<const float4*>(Os + (size_t)r * D)[lane];
+    if (lane == 0)
+      *reinterpret_cast<float4*>(part + (size_t)r * PS + D) = make_float4(Ms[r], Ls[r], 0.f, 0.f);
   }
 }
 
@@ -207,14 +432,61 @@ __global__ void __maxnreg__(144) merge_kernel(const AttnArgs a) {
   HW_SPAN_END(0);
 }
 
+// Ring slots for R query rows: one, so that two CTAs share an SM (each computes while the
+// other's tile lands); the occupancy, not a second slot, hides the load latency.
 template <int D>
-constexpr size_t fma_smem_bytes(int rows) {
-  return ((size_t)rows * D + kTile * (D + 1) + kTile * D) * sizeof(float);
+int fma_slots(int rows) {
+  (void)rows;
+  return 1;
+}
+
+template <int D, int RPT>
+void launch_fma_dr(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
+  const int slots = fma_slots<D>(a.rows);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_units);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = FmaLayout<D>(a.rows, slots).total;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, attn_fma_kernel<D, RPT>, a, maps, (int32_t)layer, (int32_t)slots);
 }
 
 template <int D>
-void launch_fma_d(const AttnArgs& a, cudaStream_t s) {
-  attn_fma_kernel<D><<<a.num_units, kThreads, fma_smem_bytes<D>(a.rows), s>>>(a);
+void launch_fma_d(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
+  switch (a.rows >= 16 ? 8 : (a.rows + 1) / 2) {
+    case 1: launch_fma_dr<D, 1>(a, maps, layer, s); break;
+    case 2: launch_fma_dr<D, 2>(a, maps, layer, s); break;
+    case 3: launch_fma_dr<D, 3>(a, maps, layer, s); break;
+    case 4: launch_fma_dr<D, 4>(a, maps, layer, s); break;
+    case 5: launch_fma_dr<D, 5>(a, maps, layer, s); break;
+    case 6: launch_fma_dr<D, 6>(a, maps, layer, s); break;
+    case 7: launch_fma_dr<D, 7>(a, maps, layer, s); break;
+    default: launch_fma_dr<D, 8>(a, maps, layer, s); break;
+  }
+}
+
+template <int D, int RPT>
+cudaError_t prepare_fma_dr(int smem) {
+  return cudaFuncSetAttribute(attn_fma_kernel<D, RPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem);
+}
+
+template <int D>
+cudaError_t prepare_fma_d(int smem) {
+  cudaError_t e = prepare_fma_dr<D, 1>(smem);
+  if (e == cudaSuccess) e = prepare_fma_dr<D, 2>(smem);
+  if (e == cudaSuccess) e = prepare_fma_dr<D, 3>(smem);
+  if (e == cudaSuccess) e = prepare_fma_dr<D, 4>(smem);
+  if (e == cudaSuccess) e = prepare_fma_dr<D, 5>(smem);
+  if (e == cudaSuccess) e = prepare_fma_dr<D, 6>(smem);
+  if (e == cudaSuccess) e = prepare_fma_dr<D, 7>(smem);
+  if (e == cudaSuccess) e = prepare_fma_dr<D, 8>(smem);
+  return e;
 }
 
 }  // namespace
@@ -222,20 +494,20 @@ void launch_fma_d(const AttnArgs& a, cudaStream_t s) {
 HW_SPAN_EXPORT(merge)
 
 cudaError_t prepare_attention_fma(int D) {
-  // Shared-memory limit for the largest row count a context may have (128 query rows).
-  if (D == 64)
-    return cudaFuncSetAttribute(attn_fma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)fma_smem_bytes<64>(128));
-  return cudaFuncSetAttribute(attn_fma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)fma_smem_bytes<128>(128));
+  // Shared-memory limit: the largest layout any row count up to 128 uses.
+  int most = 0;
+  for (int r = 1; r <= 128; ++r)
+    most = std::max(most, (int)(D == 64 ? FmaLayout<64>(r, fma_slots<64>(r)).total
+                                        : FmaLayout<128>(r, fma_slots<128>(r)).total));
+  return D == 64 ? prepare_fma_d<64>(most) : prepare_fma_d<128>(most);
 }
 
-void launch_attention_fma(const AttnArgs& a, cudaStream_t s) {
+void launch_attention_fma(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
   if (a.num_units <= 0) return;
   if (a.D == 64)
-    launch_fma_d<64>(a, s);
+    launch_fma_d<64>(a, maps, layer, s);
   else
-    launch_fma_d<128>(a, s);
+    launch_fma_d<128>(a, maps, layer, s);
 }
 
 void launch_merge(const AttnArgs& a, cudaStream_t s, bool pdl) {

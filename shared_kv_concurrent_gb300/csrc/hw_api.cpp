@@ -195,6 +195,9 @@ struct hw_ctx {
   int32_t expire_plans = 0;                // fault injection: plans announced with a dead number
   hw::TcMaps maps{};
   bool use_tc = false;                     // tensor-core attention (W*G >= 16 rows)
+  // CTAs of one wave of units: the tensor-core kernel holds an SM alone (its shared memory and
+  // TMEM); the CUDA-core kernel runs two CTAs per SM, one computing while the other's tile lands.
+  int64_t wave_ctas() const { return use_tc ? num_sms : 2 * (int64_t)num_sms; }
   std::deque<int32_t> free_pages;
   std::vector<Seg> segs;
   std::vector<std::vector<int32_t>> common, live;
@@ -481,8 +484,11 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
   // row coordinate of the pools must fit in int32.
   const int64_t pool_rows = (int64_t)cfg->num_layers * cfg->num_pages * cfg->num_kv_heads *
                             cfg->page_size;
-  c->use_tc = c->rows >= 16 && pool_rows < (1ll << 31);
-  if (c->use_tc && !hw::make_tc_maps(*cfg, k_pool, v_pool, &c->maps)) return fail(HW_ERR_UNSUPPORTED);
+  // Both attention kernels stage K/V tiles through TMA tensor maps of the pools, whose row
+  // coordinate must fit in int32.
+  if (pool_rows >= (1ll << 31)) return fail(HW_ERR_UNSUPPORTED);
+  c->use_tc = c->rows >= 16;
+  if (!hw::make_tc_maps(*cfg, k_pool, v_pool, &c->maps)) return fail(HW_ERR_UNSUPPORTED);
   e = hw::prepare_attention_fma(cfg->head_dim);
   if (e == cudaSuccess && c->use_tc) e = hw::prepare_attention_tc(cfg->head_dim);
   if (e != cudaSuccess) return fail(cuda_fail(e));
@@ -640,14 +646,13 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
     const uint64_t seq = c->next_seq();
     bool plan_ok =
         plan_off < c->lay.slot_seq_off &&
-        build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->use_tc ? c->num_sms : 0,
-                             fuse, seq) &&
+        build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->wave_ctas(), fuse, seq) &&
         plan_off + po.bytes <= c->lay.slot_seq_off;
     if (!plan_ok && fuse) {
       fuse = false;
       plan_ok = plan_off < c->lay.slot_seq_off &&
-                build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0,
-                                     c->use_tc ? c->num_sms : 0, false, seq) &&
+                build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->wave_ctas(), false,
+                                     seq) &&
                 plan_off + po.bytes <= c->lay.slot_seq_off;
     }
     st = c->upload_slot(slot, plan_off + (plan_ok ? po.bytes : 0), seq, &c->step_gate);
@@ -1084,13 +1089,13 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
   } else {
     hw_status st = c->acquire_slot(&slot);
     if (st != HW_OK) return st;
-    // Tensor-core kernel: one CTA per SM holds all of its shared memory and TMEM, so one unit
-    // per SM, balanced by KV entries.
+    // One CTA per SM holds all of its shared memory (and, tensor-core kernel, TMEM), so one
+    // unit per SM, balanced by KV entries.
     const uint64_t seq = c->next_seq();
     // partials fit the workspace: units * rows stays within its max_units * (W * G) rows
     const int64_t cap = n_q ? (int64_t)c->lay.max_units * c->rows / (width * c->G) : 0;
-    if (!build_attention_plan(c, c->h_slot(slot), &po, cap, c->use_tc ? c->num_sms : 0, false, seq,
-                              n_q, ranges))
+    if (!build_attention_plan(c, c->h_slot(slot), &po, cap, c->wave_ctas(), false, seq, n_q,
+                              ranges))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
     hbase = c->h_slot(slot);
@@ -1157,13 +1162,13 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
     hw::launch_attention_tc(a, c->maps, lu, layer, s, e0, e1);
   } else {
     if (e0) cudaEventRecord(e0, s);
-    hw::launch_attention_fma(a, s);
+    hw::launch_attention_fma(a, c->maps, layer, s);
     if (e1) cudaEventRecord(e1, s);
   }
   HW_CUDA(cudaGetLastError());
   if (fused) c->pend_k[layer] = c->pend_v[layer] = nullptr;
   const int pm = c->prof_begin(s, 2);      // (a timed merge is not chained to the attention)
-  hw::launch_merge(a, s, c->use_tc && pm < 0);
+  hw::launch_merge(a, s, pm < 0);
   c->prof_end(pm, s);
   HW_CUDA(cudaGetLastError());
   c->n_launch += 2;
@@ -1260,7 +1265,7 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
   a.max_position = c->cfg.max_position;
   a.rows = po.width * c->G;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
-  hw::launch_attention_fma(a, s);
+  hw::launch_attention_fma(a, c->maps, layer, s);
   HW_CUDA(cudaGetLastError());
   hw::launch_merge(a, s);
   HW_CUDA(cudaGetLastError());

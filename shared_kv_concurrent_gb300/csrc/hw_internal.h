@@ -184,7 +184,9 @@ cudaError_t prepare_attention_tc(int D);
 
 void launch_append(const AppendArgs& a, cudaStream_t s);
 void launch_compact(const CompactArgs& a, cudaStream_t s);
-void launch_attention_fma(const AttnArgs& a, cudaStream_t s);
+// The CUDA-core attention kernel (fewer than 16 query rows), K/V tiles staged through the same
+// tensor maps as the tensor-core kernel; a programmatic dependent of whatever precedes it.
+void launch_attention_fma(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s);
 // Launches the attention kernel; ev_before / ev_after (optional) are recorded directly around
 // it (and it is then launched without programmatic chaining).
 void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, const LaunchUnits& lu, int layer,
