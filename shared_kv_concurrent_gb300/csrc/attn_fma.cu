@@ -80,6 +80,18 @@ struct FmaLayout {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// c + a * b on two fp32 lanes at once (packed FMA, each lane rounded as fma.rn.f32).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long ar, br, cr;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ar) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(br) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(cr) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(cr) : "l"(ar), "l"(br));
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(cr));
+  return r;
+}
+
 // Byte offset, inside a {64, 128} swizzled box pair, of the 16-byte chunk holding elements
 // 8c .. 8c + 7 (c = d / 8) of tile row j.
 template <int D>
@@ -94,9 +106,7 @@ __device__ __forceinline__ bool piece_ok(const AttnArgs& a, const Piece& pc) {
          pc.seg_slot < a.num_seg_slots;
 }
 
-// RPT: query rows per thread in S = Q~ K^T (the chunk of 2 * RPT rows a pass over a tile
-// takes; 1 .. 8, so that no thread issues FMAs for rows a short chunk does not have).
-template <int D, int RPT>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     attn_fma_kernel(const AttnArgs a, const __grid_constant__ TcMaps maps, const int32_t layer,
                     const int32_t slots) {
@@ -229,43 +239,39 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint8_t* kt = smem + (uint32_t)slot * C::kSlotBytes;
     const uint8_t* vt = kt + C::kTileBytes;
     const int nv = pc.ntok;
-    for (int r0 = 0; r0 < R; r0 += 2 * RPT) {
-      const int CR = min(2 * RPT, R - r0);
+    for (int r0 = 0; r0 < R; r0 += kChunkRows) {
+      const int CR = min(kChunkRows, R - r0);
       {
         // S = Q~ K^T: thread (token j, row parity hf) takes rows hf, hf + 2, ... of the chunk
-        // (two accumulators per row, and a chunk's queries loaded before its FMAs: the chains
-        // are short and the shared loads in flight together)
-        const int j = tid & (kTile - 1), hf = tid >> 7;
-        float acc0[RPT], acc1[RPT];
+        // S = Q~ K^T: thread (row r of the chunk, token group tg) takes tokens tg + 16 k, k < 8.
+        // A row's 8-element query chunk is loaded once into registers and used for all eight
+        // tokens (shared-memory broadcasts deliver 4 bytes per wavefront, so re-reading the
+        // queries per token would cost more than the K tile itself); the 16 threads of a row
+        // read 16 consecutive tokens' chunks (swizzled rows: no bank conflict).
+        const int r = tid >> 4, tg = tid & 15;
+        if (r < CR) {
+          float2 acc[kTile / 16];           // per token: (even, odd) element accumulators
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) acc0[i] = acc1[i] = 0.f;
+          for (int k = 0; k < kTile / 16; ++k) acc[k] = make_float2(0.f, 0.f);
+          const float* qrow = Qs + (size_t)(r0 + r) * D;
 #pragma unroll 1
-        for (int c = 0; c < D / 8; ++c) {
-          const uint4 kw = *reinterpret_cast<const uint4*>(kt + swz<D>(j, c));
-          float4 qa[RPT], qb[RPT];
+          for (int c = 0; c < D / 8; ++c) {
+            const float4 qa = *reinterpret_cast<const float4*>(qrow + 8 * c);
+            const float4 qb = *reinterpret_cast<const float4*>(qrow + 8 * c + 4);
+            const float2 q01 = make_float2(qa.x, qa.y), q23 = make_float2(qa.z, qa.w);
+            const float2 q45 = make_float2(qb.x, qb.y), q67 = make_float2(qb.z, qb.w);
 #pragma unroll
-          for (int i = 0; i < RPT; ++i) {
-            const int rr = min(hf + 2 * i, CR - 1);         // (rows past the chunk: ignored)
-            qa[i] = *reinterpret_cast<const float4*>(Qs + (size_t)(r0 + rr) * D + 8 * c);
-            qb[i] = *reinterpret_cast<const float4*>(Qs + (size_t)(r0 + rr) * D + 8 * c + 4);
+            for (int k = 0; k < kTile / 16; ++k) {
+              const uint4 kw = *reinterpret_cast<const uint4*>(kt + swz<D>(tg + 16 * k, c));
+              acc[k] = fma2(q01, make_float2(bf_lo(kw.x), bf_hi(kw.x)), acc[k]);
+              acc[k] = fma2(q23, make_float2(bf_lo(kw.y), bf_hi(kw.y)), acc[k]);
+              acc[k] = fma2(q45, make_float2(bf_lo(kw.z), bf_hi(kw.z)), acc[k]);
+              acc[k] = fma2(q67, make_float2(bf_lo(kw.w), bf_hi(kw.w)), acc[k]);
+            }
           }
-          const float k0 = bf_lo(kw.x), k1 = bf_hi(kw.x), k2 = bf_lo(kw.y), k3 = bf_hi(kw.y);
-          const float k4 = bf_lo(kw.z), k5 = bf_hi(kw.z), k6 = bf_lo(kw.w), k7 = bf_hi(kw.w);
 #pragma unroll
-          for (int i = 0; i < RPT; ++i) {
-            acc0[i] = fmaf(qa[i].x, k0, acc0[i]);
-            acc1[i] = fmaf(qa[i].y, k1, acc1[i]);
-            acc0[i] = fmaf(qa[i].z, k2, acc0[i]);
-            acc1[i] = fmaf(qa[i].w, k3, acc1[i]);
-            acc0[i] = fmaf(qb[i].x, k4, acc0[i]);
-            acc1[i] = fmaf(qb[i].y, k5, acc1[i]);
-            acc0[i] = fmaf(qb[i].z, k6, acc0[i]);
-            acc1[i] = fmaf(qb[i].w, k7, acc1[i]);
-          }
+          for (int k = 0; k < kTile / 16; ++k) Ss[r * kTile + tg + 16 * k] = acc[k].x + acc[k].y;
         }
-#pragma unroll
-        for (int i = 0; i < RPT; ++i)
-          if (hf + 2 * i < CR) Ss[(hf + 2 * i) * kTile + j] = acc0[i] + acc1[i];
       }
       __syncthreads();
       // Online softmax: warp w takes rows w and w + 8 of the chunk, a lane four tokens.
@@ -326,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           // four tokens at a time: their P values (one float4 per row) and V words loaded first
           // (P is zero past the piece's tokens, so the tail of the last group adds nothing)
           const int nv4 = (nv + 3) & ~3;
+          float2 xa01 = make_float2(xa.x, xa.y), xa23 = make_float2(xa.z, xa.w);
+          float2 xb01 = make_float2(xb.x, xb.y), xb23 = make_float2(xb.z, xb.w);
 #pragma unroll 1
           for (int k = 0; k < nv4; k += 4) {
             const float4 p4 = *reinterpret_cast<const float4*>(pa + k);
@@ -338,20 +346,17 @@ __global__ void __launch_bounds__(kThreads, 2)
             const float pp[4] = {p4.x, p4.y, p4.z, p4.w}, qq[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float v0 = bf_lo(vw[e].x), v1 = bf_hi(vw[e].x);
-              const float v2 = bf_lo(vw[e].y), v3 = bf_hi(vw[e].y);
-              xa.x = fmaf(pp[e], v0, xa.x);
-              xa.y = fmaf(pp[e], v1, xa.y);
-              xa.z = fmaf(pp[e], v2, xa.z);
-              xa.w = fmaf(pp[e], v3, xa.w);
-              xb.x = fmaf(qq[e], v0, xb.x);
-              xb.y = fmaf(qq[e], v1, xb.y);
-              xb.z = fmaf(qq[e], v2, xb.z);
-              xb.w = fmaf(qq[e], v3, xb.w);
+              const float2 v01 = make_float2(bf_lo(vw[e].x), bf_hi(vw[e].x));
+              const float2 v23 = make_float2(bf_lo(vw[e].y), bf_hi(vw[e].y));
+              const float2 pe = make_float2(pp[e], pp[e]), qe = make_float2(qq[e], qq[e]);
+              xa01 = fma2(pe, v01, xa01);
+              xa23 = fma2(pe, v23, xa23);
+              xb01 = fma2(qe, v01, xb01);
+              xb23 = fma2(qe, v23, xb23);
             }
           }
-          *oa = xa;
-          if (has_b) *ob = xb;
+          *oa = make_float4(xa01.x, xa01.y, xa23.x, xa23.y);
+          if (has_b) *ob = make_float4(xb01.x, xb01.y, xb23.x, xb23.y);
         }
       }
       __syncthreads();
@@ -440,8 +445,8 @@ int fma_slots(int rows) {
   return 1;
 }
 
-template <int D, int RPT>
-void launch_fma_dr(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
+template <int D>
+void launch_fma_d(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
   const int slots = fma_slots<D>(a.rows);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -453,40 +458,7 @@ void launch_fma_dr(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaLaunchKernelEx(&cfg, attn_fma_kernel<D, RPT>, a, maps, (int32_t)layer, (int32_t)slots);
-}
-
-template <int D>
-void launch_fma_d(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
-  switch (a.rows >= 16 ? 8 : (a.rows + 1) / 2) {
-    case 1: launch_fma_dr<D, 1>(a, maps, layer, s); break;
-    case 2: launch_fma_dr<D, 2>(a, maps, layer, s); break;
-    case 3: launch_fma_dr<D, 3>(a, maps, layer, s); break;
-    case 4: launch_fma_dr<D, 4>(a, maps, layer, s); break;
-    case 5: launch_fma_dr<D, 5>(a, maps, layer, s); break;
-    case 6: launch_fma_dr<D, 6>(a, maps, layer, s); break;
-    case 7: launch_fma_dr<D, 7>(a, maps, layer, s); break;
-    default: launch_fma_dr<D, 8>(a, maps, layer, s); break;
-  }
-}
-
-template <int D, int RPT>
-cudaError_t prepare_fma_dr(int smem) {
-  return cudaFuncSetAttribute(attn_fma_kernel<D, RPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              smem);
-}
-
-template <int D>
-cudaError_t prepare_fma_d(int smem) {
-  cudaError_t e = prepare_fma_dr<D, 1>(smem);
-  if (e == cudaSuccess) e = prepare_fma_dr<D, 2>(smem);
-  if (e == cudaSuccess) e = prepare_fma_dr<D, 3>(smem);
-  if (e == cudaSuccess) e = prepare_fma_dr<D, 4>(smem);
-  if (e == cudaSuccess) e = prepare_fma_dr<D, 5>(smem);
-  if (e == cudaSuccess) e = prepare_fma_dr<D, 6>(smem);
-  if (e == cudaSuccess) e = prepare_fma_dr<D, 7>(smem);
-  if (e == cudaSuccess) e = prepare_fma_dr<D, 8>(smem);
-  return e;
+  cudaLaunchKernelEx(&cfg, attn_fma_kernel<D>, a, maps, (int32_t)layer, (int32_t)slots);
 }
 
 }  // namespace
@@ -499,7 +471,11 @@ cudaError_t prepare_attention_fma(int D) {
   for (int r = 1; r <= 128; ++r)
     most = std::max(most, (int)(D == 64 ? FmaLayout<64>(r, fma_slots<64>(r)).total
                                         : FmaLayout<128>(r, fma_slots<128>(r)).total));
-  return D == 64 ? prepare_fma_d<64>(most) : prepare_fma_d<128>(most);
+  if (D == 64)
+    return cudaFuncSetAttribute(attn_fma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                most);
+  return cudaFuncSetAttribute(attn_fma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              most);
 }
 
 void launch_attention_fma(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t s) {
