@@ -188,8 +188,10 @@ def hw_destroy(ctx: int) -> None:
 
 
 def hw_append_kv(ctx: int, layer: int, n_new, k_raw, v_raw, stream=None) -> None:
-    n = _i32(n_new)
-    st = (_lib or load()).hw_append_kv(ctx, layer, n.ctypes.data, _dptr(k_raw), _dptr(v_raw),
+    """n_new: host int32 [P][W + 1] (array-like), or the address (int) of such an array that
+    stays alive for the call (saves the per-call conversion in a decode loop)."""
+    nptr = n_new if isinstance(n_new, int) else _i32(n_new).ctypes.data
+    st = (_lib or load()).hw_append_kv(ctx, layer, nptr, _dptr(k_raw), _dptr(v_raw),
                                        _stream(stream))
     if st:
         _check(st, "hw_append_kv")
@@ -247,13 +249,14 @@ def hw_compact_segments(ctx: int, problem: int, first: int, count: int, stream=N
 
 
 def hw_step_end(ctx: int, finished=None, stream=None) -> None:
-    if finished is None:
-        f = None
+    """finished: host uint8 [P][W] (array-like), None, or the address (int) of such an array."""
+    if finished is None or isinstance(finished, int):
+        fptr = finished
     elif isinstance(finished, np.ndarray) and finished.dtype == np.uint8 and finished.flags.c_contiguous:
-        f = finished
+        fptr = finished.ctypes.data
     else:
-        f = np.ascontiguousarray(np.asarray(finished, dtype=np.uint8))
-    st = (_lib or load()).hw_step_end(ctx, None if f is None else f.ctypes.data, _stream(stream))
+        fptr = np.ascontiguousarray(np.asarray(finished, dtype=np.uint8)).ctypes.data
+    st = (_lib or load()).hw_step_end(ctx, fptr, _stream(stream))
     if st:
         _check(st, "hw_step_end")
 

@@ -142,17 +142,42 @@ struct PlanOffsets {
   int32_t width;                       // columns of the rotation table (query rows / G)
 };
 
+// An append-only array that keeps its storage across plans: `grow(k)` hands out k slots to be
+// written by index (no per-element capacity check, no zero-fill of slots that are written).
+template <class T>
+struct Buf {
+  std::vector<T> v;
+  size_t n = 0;
+  void clear() { n = 0; }
+  T* grow(size_t k) {
+    if (n + k > v.size()) v.resize(std::max<size_t>(2 * v.size(), n + k + 64));
+    T* p = v.data() + n;
+    n += k;
+    return p;
+  }
+  void push_back(const T& x) { *grow(1) = x; }
+  size_t size() const { return n; }
+  bool empty() const { return n == 0; }
+  T* data() { return v.data(); }
+  const T* data() const { return v.data(); }
+  T& operator[](size_t i) { return v[i]; }
+  const T& operator[](size_t i) const { return v[i]; }
+  T* begin() { return v.data(); }
+  T* end() { return v.data() + n; }
+};
+
 // Reused host buffers of the plan builder (no allocation per call once they have grown).
 struct PlanScratch {
   struct Part {
     int32_t unit, ref, t0, t1;        // tiles [t0, t1) of segment reference `ref` go to `unit`
   };
-  std::vector<hw::Piece> pieces;
-  std::vector<hw::Unit> units;
+  Buf<hw::Piece> pieces;
+  Buf<hw::Unit> units;
   std::vector<hw::Group> groups;
-  std::vector<hw::FreshTok> fresh;
-  std::vector<int32_t> delta, refs, piece_fresh0, src_base, ref_of, view_ref, vlen, qrow;
-  std::vector<uint8_t> piece_early;     // the piece may be loaded before the programmatic wait
+  Buf<hw::FreshTok> fresh;
+  Buf<int32_t> piece_fresh0;
+  std::vector<int32_t> delta, refs, src_base, ref_of, view_ref, vlen, qrow;
+  Buf<uint8_t> piece_early;             // the piece may be loaded before the programmatic wait
   int32_t qrow_next = 0;
   std::vector<int64_t> view_off;
   // per segment reference: its tokens [ref_lo, ref_hi) are attended (the whole segment, or its
@@ -165,9 +190,18 @@ struct PlanScratch {
   std::vector<std::pair<int32_t, int32_t>> unit_range;
 };
 
+// The pieces of a segment as the planner last emitted them, with what they depend on: a plan
+// reuses them while all of it is unchanged (common segments between decode steps).
+struct PieceCache {
+  int32_t seg_slot = -1, lo = -1, hi = -1, len = -1, recent = -1, npages = -1;
+  std::vector<hw::Piece> pieces;
+  std::vector<uint8_t> early;
+};
+
 struct Seg {
   int32_t problem, origin, length, pending;
   std::vector<int32_t> pages;
+  PieceCache cache;
   // Positions >= recent_from were written in the last completed step or by a compaction
   // since: the next attention launch may not load them before its programmatic wait.
   int32_t recent_from = INT32_MAX;
@@ -867,7 +901,47 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     if (t1 <= t0) return true;
     if ((int64_t)ps.pieces.size() + (t1 - t0) > L.max_pieces) return false;
     const int32_t sid = ps.ref_sid[r];
-    const Seg& sg = c->segs[sid];
+    Seg& sg = c->segs[sid];
+    if (sg.pending == 0) {
+      // No token of this step in it: its pieces are those of the last plan while the segment,
+      // its slot in the rotation table and the attended range are unchanged.
+      PieceCache& pc = sg.cache;
+      if (pc.seg_slot != ps.ref_slot[r] || pc.lo != ps.ref_lo[r] || pc.hi != ps.ref_hi[r] ||
+          pc.len != sg.length || pc.recent != sg.recent_from ||
+          pc.npages != (int32_t)sg.pages.size()) {
+        const int32_t nt = ps.ref_tiles[r];
+        const int32_t lo = ps.ref_lo[r], hi = ps.ref_hi[r];
+        pc.pieces.resize((size_t)nt);
+        pc.early.resize((size_t)nt);
+        const int32_t Tb = lo / kPieceMax;
+        int32_t pi = contiguous ? 0 : Tb / tiles_per_page;
+        int32_t sub = contiguous ? 0 : Tb - pi * tiles_per_page;
+        for (int32_t T = Tb; T < Tb + nt; ++T) {
+          const int32_t j = std::max(lo, T * kPieceMax);
+          const int32_t end = std::min(hi, (T + 1) * kPieceMax);
+          const int32_t slot0 = contiguous ? j : sub * kPieceMax + (j - T * kPieceMax);
+          pc.pieces[T - Tb] = hw::Piece{ps.ref_slot[r], sg.pages[pi], slot0, end - j, 0, j};
+          pc.early[T - Tb] = end <= sg.recent_from ? 1 : 0;
+          if (!contiguous && ++sub == tiles_per_page) {
+            sub = 0;
+            ++pi;
+          }
+        }
+        pc.seg_slot = ps.ref_slot[r];
+        pc.lo = lo;
+        pc.hi = hi;
+        pc.len = sg.length;
+        pc.recent = sg.recent_from;
+        pc.npages = (int32_t)sg.pages.size();
+      }
+      const size_t n = (size_t)(t1 - t0);
+      std::memcpy(ps.pieces.grow(n), pc.pieces.data() + t0, n * sizeof(hw::Piece));
+      std::memcpy(ps.piece_early.grow(n), pc.early.data() + t0, n);
+      int32_t* f0 = ps.piece_fresh0.grow(n);
+      const int32_t nf = (int32_t)ps.fresh.size();
+      for (size_t k = 0; k < n; ++k) f0[k] = nf;
+      return true;
+    }
     const int32_t* pages = sg.pages.data();
     const int32_t seg_slot = ps.ref_slot[r], len = sg.length;
     const int32_t lo = ps.ref_lo[r], hi = ps.ref_hi[r];
@@ -876,6 +950,9 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     const int32_t T0 = lo / kPieceMax + t0, T1 = lo / kPieceMax + t1;   // tiles of the segment
     int32_t pi = contiguous ? 0 : T0 / tiles_per_page;     // page of tile T
     int32_t sub = contiguous ? 0 : T0 - pi * tiles_per_page;  // tile T's place in it
+    hw::Piece* out = ps.pieces.grow((size_t)(T1 - T0));
+    uint8_t* early = ps.piece_early.grow((size_t)(T1 - T0));
+    int32_t* fresh0 = ps.piece_fresh0.grow((size_t)(T1 - T0));
     for (int32_t T = T0; T < T1; ++T) {
       const int32_t j = std::max(lo, T * kPieceMax);              // first token of the piece
       const int32_t end = std::min(hi, (T + 1) * kPieceMax);      // one past its last
@@ -884,9 +961,10 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
       const int32_t cnt = end - j;
       // fresh: holds tokens appended in this step (the kernels read it only after the append)
       const int32_t fresh = (pending && end > len) ? 1 : 0;
-      ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
-      ps.piece_early.push_back(!fresh && end <= recent ? 1 : 0);
-      ps.pieces.push_back(hw::Piece{seg_slot, pg, slot0, cnt, fresh, j});
+      const int32_t at = T - T0;
+      fresh0[at] = (int32_t)ps.fresh.size();
+      early[at] = !fresh && end <= recent ? 1 : 0;
+      out[at] = hw::Piece{seg_slot, pg, slot0, cnt, fresh, j};
       if (fuse && fresh) {
         if (ps.src_base[sid] < 0) return false;
         for (int32_t k = std::max<int32_t>(0, len - j); k < cnt; ++k) {
@@ -963,9 +1041,11 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     for (int32_t h = 0; h < H; ++h) {
       const int32_t g = p * H + h;
       hw::Group gr{p, h, (int32_t)ps.units.size(), 0};
+      hw::Unit* us = ps.units.grow((size_t)n);
       for (int32_t k = 0; k < n; ++k) {
         const auto rg = ps.unit_range[first_range + k];
-        hw::Unit u{};
+        hw::Unit& u = us[k];
+        u = hw::Unit{};
         u.piece_begin = rg.first;
         u.piece_end = rg.second;
         u.group = g;
@@ -975,7 +1055,6 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         u.first_tok = -1;
         if (rg.second > rg.first && ps.piece_early[rg.first])
           u.first_tok = ps.pieces[rg.first].page * S + ps.pieces[rg.first].slot0;
-        ps.units.push_back(u);
       }
       gr.unit_end = (int32_t)ps.units.size();
       ps.groups.push_back(gr);

@@ -41,6 +41,9 @@ class WorkloadRunner:
         self.cache.step_end(np.zeros((w.num_problems, w.num_workers), np.uint8))
         del keep
         self.n_step = np.ascontiguousarray(wl.step_n_new(w), dtype=np.int32)
+        self._n_step_ptr = self.n_step.ctypes.data          # (the arrays live with the runner)
+        self._no_commit = np.zeros((w.num_problems, w.num_workers), np.uint8)
+        self._no_commit_ptr = self._no_commit.ctypes.data
 
     def step_inputs(self, step: int):
         """Device tensors (k[L], v[L], q[L]) of decode ``step``."""
@@ -56,7 +59,7 @@ class WorkloadRunner:
         """``stream``: a torch stream or raw cudaStream_t handle; None = torch's current one."""
         ks, vs, _ = inputs
         for layer in range(self.w.num_layers):
-            self.cache.append_kv(layer, self.n_step, ks[layer], vs[layer], stream)
+            self.cache.append_kv(layer, self._n_step_ptr, ks[layer], vs[layer], stream)
 
     def attend(self, inputs, outs: List, lses: Optional[List] = None, out_dtype="bf16",
                stream=None) -> None:
@@ -66,5 +69,7 @@ class WorkloadRunner:
                                             None if lses is None else lses[layer], stream)
 
     def end(self, step: int, finished=None, stream=None) -> None:
-        self.cache.step_end(wl.finished_mask(self.w, step) if finished is None else finished,
-                            stream)
+        if finished is None:
+            finished = (wl.finished_mask(self.w, step) if step in self.w.commit_steps
+                        else self._no_commit_ptr)
+        self.cache.step_end(finished, stream)
