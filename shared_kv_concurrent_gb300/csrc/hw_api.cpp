@@ -171,11 +171,6 @@ struct PlanScratch {
   struct Part {
     int32_t unit, ref, t0, t1;        // tiles [t0, t1) of segment reference `ref` go to `unit`
   };
-  Buf<hw::Piece> pieces;
-  Buf<hw::Unit> units;
-  std::vector<hw::Group> groups;
-  Buf<hw::FreshTok> fresh;
-  Buf<int32_t> piece_fresh0;
   std::vector<int32_t> delta, refs, src_base, ref_of, view_ref, vlen, qrow;
   Buf<uint8_t> piece_early;             // the piece may be loaded before the programmatic wait
   int32_t qrow_next = 0;
@@ -184,10 +179,9 @@ struct PlanScratch {
   // part inside an entry range), in ref_tiles tiles starting at tile ref_lo / kPieceMax
   std::vector<int32_t> ref_lo, ref_hi;
   std::vector<int32_t> ref_sid, ref_slot, ref_tiles, prob_ref_begin, prob_common_refs, unit_rem,
-      order;
+      order, prob_units;
   std::vector<int64_t> prob_tiles;
   std::vector<Part> parts;
-  std::vector<std::pair<int32_t, int32_t>> unit_range;
 };
 
 // The pieces of a segment as the planner last emitted them, with what they depend on: a plan
@@ -566,7 +560,7 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
 }  // extern "C"
 
 namespace {
-bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap,
+bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int64_t unit_cap,
                           int64_t target_override, bool fuse, uint64_t seq,
                           const int32_t* n_q = nullptr, const int64_t* ranges = nullptr);
 }  // namespace
@@ -678,16 +672,14 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
     bool fuse = c->use_tc;
     for (int32_t i = 0; i < P * B && fuse; ++i) fuse = n_new[i] <= kFuseTok;
     const uint64_t seq = c->next_seq();
-    bool plan_ok =
-        plan_off < c->lay.slot_seq_off &&
-        build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->wave_ctas(), fuse, seq) &&
-        plan_off + po.bytes <= c->lay.slot_seq_off;
+    bool plan_ok = plan_off < c->lay.slot_seq_off &&
+                   build_attention_plan(c, c->h_slot(slot) + plan_off, c->lay.slot_seq_off - plan_off,
+                                        &po, 0, c->wave_ctas(), fuse, seq);
     if (!plan_ok && fuse) {
       fuse = false;
       plan_ok = plan_off < c->lay.slot_seq_off &&
-                build_attention_plan(c, c->h_slot(slot) + plan_off, &po, 0, c->wave_ctas(), false,
-                                     seq) &&
-                plan_off + po.bytes <= c->lay.slot_seq_off;
+                build_attention_plan(c, c->h_slot(slot) + plan_off, c->lay.slot_seq_off - plan_off,
+                                     &po, 0, c->wave_ctas(), false, seq);
     }
     st = c->upload_slot(slot, plan_off + (plan_ok ? po.bytes : 0), seq, &c->step_gate);
     if (st != HW_OK) return st;
@@ -717,8 +709,9 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
 
 namespace {
 
-// Build the attention plan of the current state into host buffer `buf` (slot_bytes long).
-// Returns false if a table would overflow.  Offsets of each array are written to `po`.
+// Build the attention plan of the current state into host buffer `buf` (`cap` bytes long).
+// Returns false if a table would overflow (the buffer's contents are then undefined).  Offsets
+// of each array are written to `po`.
 //
 // The pieces of a problem are listed once and shared by its KV heads: the units of group
 // (p, h) index the problem's piece list, and the head comes from the group.  A segment's
@@ -729,7 +722,7 @@ namespace {
 // n_q (host [P][W], or null for one query per worker): several causal query tokens per worker;
 // the rotation table then has one column per query row of a problem (its width WT is the
 // largest count of any problem), with the causal length table and the query-row map.
-bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_cap = 0,
+bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int64_t unit_cap = 0,
                           int64_t target_override = 0, bool fuse = false, uint64_t seq = 0,
                           const int32_t* n_q, const int64_t* ranges) {
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
@@ -745,13 +738,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   const int32_t S = c->cfg.page_size;
   const Layout& L = c->lay;
   PlanScratch& ps = c->ps;
-  ps.pieces.clear();
-  ps.piece_early.clear();
   ps.delta.clear();
-  ps.units.clear();
-  ps.groups.clear();
-  ps.fresh.clear();
-  ps.piece_fresh0.clear();
   ps.ref_sid.clear();
   ps.ref_slot.clear();
   ps.ref_tiles.clear();
@@ -760,7 +747,6 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   ps.prob_ref_begin.assign(P + 1, 0);
   ps.prob_common_refs.assign(P, 0);
   ps.prob_tiles.assign(P, 0);
-  ps.unit_range.clear();
   ps.vlen.clear();
   ps.qrow.assign(n_q ? (size_t)P * WT : 0, -1);
   ps.qrow_next = 0;
@@ -890,6 +876,47 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     // per-group counts are floored and then raised to >= 1: keep room for that raise
     target_units = std::max<int64_t>(0, std::min<int64_t>(target_units, unit_cap - (int64_t)P * H));
   }
+  // Sizes, known before anything is written: every tile of a problem is one piece, and a
+  // problem's units (the same for every KV head) follow from its share of the tiles.  The plan
+  // is written straight into `buf`; only the fresh-token list, last, grows while it is built.
+  ps.prob_units.resize((size_t)P);
+  int64_t n_pieces = 0, n_units_all = 0;
+  for (int32_t p = 0; p < P; ++p) {
+    const int64_t Tt = ps.prob_tiles[p];
+    int64_t nu = total_tiles ? (target_units * Tt * H + (unit_cap > 0 ? 0 : total_tiles / 2)) /
+                                   (total_tiles * H)
+                             : 1;
+    nu = std::max<int64_t>(1, std::min<int64_t>(nu, Tt));
+    ps.prob_units[p] = (int32_t)nu;
+    n_pieces += Tt;
+    n_units_all += nu * H;
+  }
+  if (n_pieces > L.max_pieces || n_units_all > L.max_units) return false;
+  if (unit_cap > 0 && n_units_all > unit_cap) return false;
+  size_t off = 0;
+  po->pieces = off;
+  off = align_up(off + (size_t)n_pieces * sizeof(hw::Piece), 16);
+  po->units = off;
+  off = align_up(off + (size_t)n_units_all * sizeof(hw::Unit), 16);
+  po->groups = off;
+  off = align_up(off + (size_t)P * H * sizeof(hw::Group), 16);
+  po->delta = off;
+  off = align_up(off + ps.delta.size() * sizeof(int32_t), 16);
+  po->vlen = off;
+  off = align_up(off + ps.vlen.size() * sizeof(int32_t), 16);
+  po->qrow = off;
+  off = align_up(off + ps.qrow.size() * sizeof(int32_t), 16);
+  po->fresh = off;
+  if (off > cap) return false;
+  hw::Piece* const pieces = reinterpret_cast<hw::Piece*>(buf + po->pieces);
+  hw::Unit* const units = reinterpret_cast<hw::Unit*>(buf + po->units);
+  hw::Group* const groups = reinterpret_cast<hw::Group*>(buf + po->groups);
+  hw::FreshTok* const fresh = reinterpret_cast<hw::FreshTok*>(buf + po->fresh);
+  const int64_t max_fresh =
+      std::min<int64_t>(L.max_fresh, (int64_t)((cap - off) / sizeof(hw::FreshTok)));
+  int32_t np = 0, nf = 0, nu_done = 0;                 // pieces, fresh tokens, units written
+  ps.piece_early.clear();
+  uint8_t* const early_all = ps.piece_early.grow((size_t)n_pieces);
   // The pieces of segment reference r at its tiles [t0, t1) (counted from the reference's
   // first tile): the reference's tokens inside one kPieceMax-aligned tile each -- so inside one
   // page -- with the step's appended tokens in it listed for the fused append.  Only the first
@@ -899,7 +926,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
   const int32_t tiles_per_page = S / kPieceMax;
   auto emit = [&](int32_t r, int32_t t0, int32_t t1) -> bool {
     if (t1 <= t0) return true;
-    if ((int64_t)ps.pieces.size() + (t1 - t0) > L.max_pieces) return false;
+    if ((int64_t)np + (t1 - t0) > n_pieces) return false;
     const int32_t sid = ps.ref_sid[r];
     Seg& sg = c->segs[sid];
     if (sg.pending == 0) {
@@ -935,24 +962,18 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         pc.npages = (int32_t)sg.pages.size();
       }
       const size_t n = (size_t)(t1 - t0);
-      std::memcpy(ps.pieces.grow(n), pc.pieces.data() + t0, n * sizeof(hw::Piece));
-      std::memcpy(ps.piece_early.grow(n), pc.early.data() + t0, n);
-      int32_t* f0 = ps.piece_fresh0.grow(n);
-      const int32_t nf = (int32_t)ps.fresh.size();
-      for (size_t k = 0; k < n; ++k) f0[k] = nf;
+      std::memcpy(pieces + np, pc.pieces.data() + t0, n * sizeof(hw::Piece));
+      std::memcpy(early_all + np, pc.early.data() + t0, n);
+      np += (int32_t)n;
       return true;
     }
     const int32_t* pages = sg.pages.data();
     const int32_t seg_slot = ps.ref_slot[r], len = sg.length;
     const int32_t lo = ps.ref_lo[r], hi = ps.ref_hi[r];
     const int32_t recent = sg.recent_from;
-    const bool pending = sg.pending > 0;
     const int32_t T0 = lo / kPieceMax + t0, T1 = lo / kPieceMax + t1;   // tiles of the segment
     int32_t pi = contiguous ? 0 : T0 / tiles_per_page;     // page of tile T
     int32_t sub = contiguous ? 0 : T0 - pi * tiles_per_page;  // tile T's place in it
-    hw::Piece* out = ps.pieces.grow((size_t)(T1 - T0));
-    uint8_t* early = ps.piece_early.grow((size_t)(T1 - T0));
-    int32_t* fresh0 = ps.piece_fresh0.grow((size_t)(T1 - T0));
     for (int32_t T = T0; T < T1; ++T) {
       const int32_t j = std::max(lo, T * kPieceMax);              // first token of the piece
       const int32_t end = std::min(hi, (T + 1) * kPieceMax);      // one past its last
@@ -960,16 +981,14 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
       const int32_t slot0 = contiguous ? j : sub * kPieceMax + (j - T * kPieceMax);
       const int32_t cnt = end - j;
       // fresh: holds tokens appended in this step (the kernels read it only after the append)
-      const int32_t fresh = (pending && end > len) ? 1 : 0;
-      const int32_t at = T - T0;
-      fresh0[at] = (int32_t)ps.fresh.size();
-      early[at] = !fresh && end <= recent ? 1 : 0;
-      out[at] = hw::Piece{seg_slot, pg, slot0, cnt, fresh, j};
-      if (fuse && fresh) {
+      const int32_t is_fresh = end > len ? 1 : 0;
+      early_all[np] = !is_fresh && end <= recent ? 1 : 0;
+      pieces[np++] = hw::Piece{seg_slot, pg, slot0, cnt, is_fresh, j};
+      if (fuse && is_fresh) {
         if (ps.src_base[sid] < 0) return false;
         for (int32_t k = std::max<int32_t>(0, len - j); k < cnt; ++k) {
-          if ((int64_t)ps.fresh.size() >= L.max_fresh) return false;
-          ps.fresh.push_back(hw::FreshTok{pg, slot0 + k, j + k, ps.src_base[sid] + (j + k - len)});
+          if (nf >= max_fresh) return false;
+          fresh[nf++] = hw::FreshTok{pg, slot0 + k, j + k, ps.src_base[sid] + (j + k - len)};
         }
       }
       if (!contiguous && ++sub == tiles_per_page) {
@@ -983,11 +1002,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     const int32_t rb = ps.prob_ref_begin[p], re = ps.prob_ref_begin[p + 1];
     const int32_t rc = rb + ps.prob_common_refs[p];      // first live-block reference
     const int64_t Tt = ps.prob_tiles[p];
-    int64_t n_units =
-        total_tiles ? (target_units * Tt * H + (unit_cap > 0 ? 0 : total_tiles / 2)) / (total_tiles * H)
-                    : 1;
-    n_units = std::max<int64_t>(1, std::min<int64_t>(n_units, Tt));
-    const int32_t n = (int32_t)n_units;
+    const int32_t n = ps.prob_units[p];
     // Layout of the problem's units (the same for every KV head): unit k holds cap_k tiles;
     // each live block (largest first) goes to the unit with the most room left, split over
     // units only when it does not fit; the rest of every unit is filled with common-part tiles,
@@ -998,9 +1013,17 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
     for (int32_t k = 0; k < n; ++k) ps.unit_rem[k] = (int32_t)(Tt / n + (k < Tt % n ? 1 : 0));
     ps.parts.clear();                                    // (unit, ref, tile begin, tile end)
     ps.order.clear();
-    for (int32_t r = rc; r < re; ++r) ps.order.push_back(r);
-    std::stable_sort(ps.order.begin(), ps.order.end(),
-                     [&](int32_t x, int32_t y) { return ps.ref_tiles[x] > ps.ref_tiles[y]; });
+    // live blocks by tile count, largest first, ties in worker order (a stable insertion sort:
+    // W is small)
+    for (int32_t r = rc; r < re; ++r) {
+      size_t i = ps.order.size();
+      ps.order.push_back(r);
+      while (i > 0 && ps.ref_tiles[ps.order[i - 1]] < ps.ref_tiles[r]) {
+        ps.order[i] = ps.order[i - 1];
+        --i;
+      }
+      ps.order[i] = r;
+    }
     for (int32_t r : ps.order) {
       int32_t t = 0;
       const int32_t nt = ps.ref_tiles[r];
@@ -1015,10 +1038,12 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         t += take;
       }
     }
-    // pieces, unit by unit: common-part tiles in order, then the unit's live-block parts
+    // Pieces, unit by unit (common-part tiles in order, then the unit's live-block parts), and
+    // the units of KV head 0 over them; every other head's units are copies (but the group).
+    hw::Unit* const us = units + nu_done;
     int32_t cr = rb, ct = 0;                             // common-part cursor
     for (int32_t k = 0; k < n; ++k) {
-      const int32_t ub = (int32_t)ps.pieces.size();
+      const int32_t ub = np, fb = nf;
       for (int32_t left = ps.unit_rem[k]; left > 0;) {
         while (cr < rc && ct >= ps.ref_tiles[cr]) {
           ++cr;
@@ -1034,82 +1059,50 @@ bool build_attention_plan(hw_ctx* c, char* buf, PlanOffsets* po, int64_t unit_ca
         if (pt.unit != k) continue;
         if (!emit(pt.ref, pt.t0, pt.t1)) return false;
       }
-      ps.unit_range.push_back({ub, (int32_t)ps.pieces.size()});
-    }
-    // units of the problem's groups, one per KV head, over the same pieces
-    const size_t first_range = ps.unit_range.size() - (size_t)n;
-    for (int32_t h = 0; h < H; ++h) {
-      const int32_t g = p * H + h;
-      hw::Group gr{p, h, (int32_t)ps.units.size(), 0};
-      hw::Unit* us = ps.units.grow((size_t)n);
-      for (int32_t k = 0; k < n; ++k) {
-        const auto rg = ps.unit_range[first_range + k];
-        hw::Unit& u = us[k];
-        u = hw::Unit{};
-        u.piece_begin = rg.first;
-        u.piece_end = rg.second;
-        u.group = g;
-        u.seg0 = rg.second > rg.first ? ps.pieces[rg.first].seg_slot : -1;
-        u.delta0 = -1;
-        u.seq = u.seq_b = u.seq_c = (uint32_t)seq;
-        u.first_tok = -1;
-        if (rg.second > rg.first && ps.piece_early[rg.first])
-          u.first_tok = ps.pieces[rg.first].page * S + ps.pieces[rg.first].slot0;
+      hw::Unit& u = us[k];
+      u = hw::Unit{};
+      u.piece_begin = ub;
+      u.piece_end = np;
+      u.group = p * H;
+      u.seg0 = np > ub ? pieces[ub].seg_slot : -1;
+      u.seq = u.seq_b = u.seq_c = (uint32_t)seq;
+      u.first_tok = np > ub && early_all[ub] ? pieces[ub].page * S + pieces[ub].slot0 : -1;
+      // a unit's appended tokens are those of its pieces
+      u.fresh_begin = fb;
+      u.fresh_end = nf;
+      // A segment seen by every worker at the same view offset (every common segment) has one
+      // rotation for all query rows: the kernels then need no delta-table load for it.
+      u.delta0 = -1;
+      if (u.seg0 >= 0 && !n_q) {           // (with a causal cut the rows differ anyway)
+        const int32_t* row = ps.delta.data() + (size_t)u.seg0 * WT;
+        bool same = row[0] >= 0;
+        for (int32_t w = 1; w < WT && same; ++w) same = row[w] == row[0];
+        if (same) u.delta0 = row[0];
       }
-      gr.unit_end = (int32_t)ps.units.size();
-      ps.groups.push_back(gr);
     }
+    for (int32_t h = 0; h < H; ++h) {
+      hw::Unit* const uh = us + (size_t)h * n;
+      if (h > 0) {
+        std::memcpy(uh, us, (size_t)n * sizeof(hw::Unit));
+        for (int32_t k = 0; k < n; ++k) uh[k].group = p * H + h;
+      }
+      groups[p * H + h] = hw::Group{p, h, nu_done + h * n, nu_done + (h + 1) * n};
+    }
+    nu_done += n * H;
   }
-  ps.piece_fresh0.push_back((int32_t)ps.fresh.size());
-  // fresh ranges: a unit's appended tokens are those of its pieces
-  for (hw::Unit& u : ps.units) {
-    u.fresh_begin = ps.piece_fresh0[u.piece_begin];
-    u.fresh_end = ps.piece_fresh0[u.piece_end];
-  }
-  if ((int64_t)ps.units.size() > L.max_units) return false;
-  if (unit_cap > 0 && (int64_t)ps.units.size() > unit_cap) return false;
-  // A segment seen by every worker at the same view offset (every common segment) has one
-  // rotation for all query rows: the kernels then need no delta-table load for it.
-  for (hw::Unit& u : ps.units) {
-    if (u.seg0 < 0) continue;
-    const int32_t* row = ps.delta.data() + (size_t)u.seg0 * WT;
-    bool same = row[0] >= 0 && !n_q;     // (with a causal cut the rows differ anyway)
-    for (int32_t w = 1; w < WT && same; ++w) same = row[w] == row[0];
-    u.delta0 = same ? row[0] : -1;
-  }
-  size_t off = 0;
-  po->pieces = off;
-  off = align_up(off + ps.pieces.size() * sizeof(hw::Piece), 16);
-  po->units = off;
-  off = align_up(off + ps.units.size() * sizeof(hw::Unit), 16);
-  po->groups = off;
-  off = align_up(off + ps.groups.size() * sizeof(hw::Group), 16);
-  po->delta = off;
-  off = align_up(off + ps.delta.size() * sizeof(int32_t), 16);
-  po->vlen = off;
-  off = align_up(off + ps.vlen.size() * sizeof(int32_t), 16);
-  po->qrow = off;
-  off = align_up(off + ps.qrow.size() * sizeof(int32_t), 16);
-  po->fresh = off;
-  off = align_up(off + ps.fresh.size() * sizeof(hw::FreshTok), 16);
-  po->bytes = off;
-  if (off > L.slot_seq_off) return false;
-  std::memcpy(buf + po->pieces, ps.pieces.data(), ps.pieces.size() * sizeof(hw::Piece));
-  std::memcpy(buf + po->units, ps.units.data(), ps.units.size() * sizeof(hw::Unit));
-  std::memcpy(buf + po->groups, ps.groups.data(), ps.groups.size() * sizeof(hw::Group));
+  if (np != n_pieces || nu_done != n_units_all) return false;
   std::memcpy(buf + po->delta, ps.delta.data(), ps.delta.size() * sizeof(int32_t));
   if (!ps.vlen.empty())
     std::memcpy(buf + po->vlen, ps.vlen.data(), ps.vlen.size() * sizeof(int32_t));
   if (!ps.qrow.empty())
     std::memcpy(buf + po->qrow, ps.qrow.data(), ps.qrow.size() * sizeof(int32_t));
-  if (!ps.fresh.empty())
-    std::memcpy(buf + po->fresh, ps.fresh.data(), ps.fresh.size() * sizeof(hw::FreshTok));
-  po->num_pieces = (int32_t)ps.pieces.size();
-  po->num_units = (int32_t)ps.units.size();
-  po->num_groups = (int32_t)ps.groups.size();
+  po->bytes = align_up(off + (size_t)nf * sizeof(hw::FreshTok), 16);
+  po->num_pieces = np;
+  po->num_units = nu_done;
+  po->num_groups = P * H;
   po->num_seg_slots = (int32_t)(ps.delta.size() / (size_t)WT);
   po->width = WT;
-  po->num_fresh = (int32_t)ps.fresh.size();
+  po->num_fresh = nf;
   return true;
 }
 
@@ -1173,8 +1166,8 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
     const uint64_t seq = c->next_seq();
     // partials fit the workspace: units * rows stays within its max_units * (W * G) rows
     const int64_t cap = n_q ? (int64_t)c->lay.max_units * c->rows / (width * c->G) : 0;
-    if (!build_attention_plan(c, c->h_slot(slot), &po, cap, c->wave_ctas(), false, seq, n_q,
-                              ranges))
+    if (!build_attention_plan(c, c->h_slot(slot), c->lay.slot_seq_off, &po, cap, c->wave_ctas(),
+                              false, seq, n_q, ranges))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
     hbase = c->h_slot(slot);
@@ -1308,7 +1301,8 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
   // The plan is built and checked before anything is enqueued: a refusal leaves the stream and
   // the layer's recorded append untouched.
   PlanOffsets po{};
-  if (!build_attention_plan(c, c->h_slot(slot), &po, unit_cap) || po.bytes > plan_region)
+  if (!build_attention_plan(c, c->h_slot(slot), std::min(plan_region, c->lay.slot_seq_off), &po,
+                            unit_cap))
     return HW_ERR_CAPACITY;
   cudaStream_t s = (cudaStream_t)stream;
   st = c->flush_append(layer, s);
