@@ -13,8 +13,9 @@ Reported (one JSON line, rank 0):
          independent caches of the workload, so each step's K/V come from HBM, not L2.  The
          algorithmic bytes count every K/V element once (not once per worker), plus q, out
          and the appended K/V.
-  e2e    the same metric through the public API with pinned host buffers: H2D copy of the
-         step's new K/V and queries, the step, D2H copy of the outputs, all inside the timer.
+  e2e    the same metric through the public API with pinned host buffers
+         (hw_decode_step_host): one H2D copy of the step's new K/V and queries, the step, one
+         D2H copy of the outputs and a stream synchronize, all inside the timer.
   roofline  the attention kernel's algorithmic bytes / its duration in the timed chain (the
          chained step time x the kernel's share of the step's kernel time, from CUDA events
          around every kernel in a second pass) vs measured HBM; the unchained per-launch figure
@@ -360,7 +361,7 @@ def run_ours(args):
     # of a slower Python loop.  The host's own cost per step is reported beside
     # (host_us_per_step) and is inside the e2e number.
     sm_hz = 2.07e9                             # GB300 maximum SM clock (cycles of the delay)
-    torch.cuda._sleep(int(min(0.2, 1.3 * args.steps * host_step + 1e-3) * sm_hz))
+    torch.cuda._sleep(int(min(0.2, 3 * args.steps * host_step + 2e-3) * sm_hz))
     e_start.record()
     total_bytes = 0
     for c, st, inp in timed:
@@ -382,7 +383,7 @@ def run_ours(args):
         binding.hw_profile_read(ctx)
     prof_steps = plan_steps(args.steps)
     attn_bytes = 0
-    torch.cuda._sleep(int(min(0.2, 1.3 * args.steps * host_step + 1e-3) * sm_hz))
+    torch.cuda._sleep(int(min(0.2, 3 * args.steps * host_step + 2e-3) * sm_hz))
     for c, st, inp in prof_steps:
         run_step(c, st, inp)
         attn_bytes += step_bytes(w, st)[1]
@@ -400,52 +401,32 @@ def run_ours(args):
             "share": attn_ms_sum / max(1e-12, attn_ms_sum + other_ms_sum)}
     t_total = slowest_rank_seconds(t_total, world, dev)
     # End to end through the public API: inputs in pinned host memory.
-    # (cache 0, L2 flushed before every step, one whole step -- copies in, append, attention,
-    # copy out, step end -- at a time with a synchronize)
+    # (cache 0, L2 flushed before every step; one whole step at a time through
+    # hw_decode_step_host: the packed K/V/Q copy in, append, attention, the output copy out,
+    # step end and a stream synchronize)
     e2e = None
     if e2e_steps:
         runner = runners[0]
         first = local[0]
-        host_in = []
-        for i in range(e2e_steps):
-            s = first + i
-            k, v, q = [], [], []
-            for layer in range(L):
-                kb, vb = wl.step_kv(w, layer, s)
-                k.append(torch.from_numpy(kb.view(np.int16)).pin_memory())
-                v.append(torch.from_numpy(vb.view(np.int16)).pin_memory())
-                q.append(torch.from_numpy(wl.step_q(w, layer, s).view(np.int16)).pin_memory())
-            host_in.append((k, v, q))
-        host_out = [torch.empty(P, W, Hq, D, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
-        dk = [torch.empty(P * W, w.num_kv_heads, D, dtype=torch.int16, device=dev) for _ in range(L)]
-        dv = [torch.empty_like(x) for x in dk]
-        dq = [torch.empty(P, W, Hq, D, dtype=torch.int16, device=dev) for _ in range(L)]
+        host_in = [runner.packed_inputs(first + i) for i in range(e2e_steps)]
+        host_out = torch.empty(L * P * W * Hq * D, dtype=torch.bfloat16).pin_memory()
+        runner.cache.reserve_step_scratch(runner.n_step)
         e2e_times, e2e_bytes = [], 0
         for i in range(e2e_steps):
             s = first + i
             flush.zero_()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-            k, v, q = host_in[i]
-            for layer in range(L):
-                dk[layer].copy_(k[layer], non_blocking=True)
-                dv[layer].copy_(v[layer], non_blocking=True)
-                dq[layer].copy_(q[layer], non_blocking=True)
-            inp = ([x.view(torch.bfloat16) for x in dk], [x.view(torch.bfloat16) for x in dv],
-                   [x.view(torch.bfloat16) for x in dq])
-            runner.append(inp, stream=stream)
-            runner.attend(inp, outs, stream=stream)
-            for layer in range(L):
-                host_out[layer].copy_(outs[layer], non_blocking=True)
-            runner.end(s, stream=stream)
-            torch.cuda.synchronize()
+            runner.cache.decode_step_host(runner._n_step_ptr, host_in[i], host_out,
+                                          runner.finished_for(s), sync=True, stream=stream)
             e2e_times.append(time.perf_counter() - t0)
             e2e_bytes += step_bytes(w, s)[0]
-        h2d = sum(x.numel() * 2 for x in dk + dv + dq)
-        d2h = sum(x.numel() * 2 for x in host_out)
+        h2d = host_in[0].numel()
+        d2h = host_out.numel() * 2
         e2e = {"value": e2e_bytes / sum(e2e_times) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": 1e3 * sum(e2e_times) / e2e_steps, "steps": e2e_steps}
+               "ms_per_step": 1e3 * sum(e2e_times) / e2e_steps, "steps": e2e_steps,
+               "call": "hw_decode_step_host (one packed host-to-device copy, one copy back)"}
 
     for r in runners:
         st, info = r.cache.check_device_errors()

@@ -281,6 +281,44 @@ hw_status hw_concurrent_attention_noalloc(hw_ctx* ctx, int32_t layer, const void
 hw_status hw_step_end(hw_ctx* ctx, const uint8_t* finished, void* stream);
 
 /*
+ * One whole decode step from host memory (section 8's inference flow: every worker appends its
+ * token, attends to the shared cache, and the step ends with the commits), for callers whose
+ * inputs and outputs are in host memory.  Every layer's K, V and queries go to the device in
+ * one host-to-device copy and every layer's output comes back in one device-to-host copy;
+ * in between, hw_append_kv for every layer, hw_concurrent_attention for every layer and
+ * hw_step_end, all on `stream`.
+ *   n_new:    host int32[P][W + 1], as hw_append_kv (the same counts for every layer).
+ *   in_host:  host, packed [K][V][Q]: K and V bf16 [L][sum n_new][H_kv][D] each (layer-major;
+ *             within a layer as hw_append_kv's k_raw / v_raw), then Q bf16 [L][P][W][H_q][D]
+ *             (unrotated, as hw_concurrent_attention's q).
+ *   in_bytes: must equal 2 * L * D * (2 * sum(n_new) * H_kv + P * W * H_q).
+ *   out_host: host, [L][P][W][H_q][D] of out_dtype (HW_OUT_BF16 or HW_OUT_F32).
+ *   finished: host uint8[P][W] or NULL, as hw_step_end.
+ *   scratch:  device, >= hw_step_scratch_size() bytes, 256-byte aligned, caller-owned: the
+ *             device copies of the inputs and outputs.  Not to be shared with GPU work that
+ *             may overlap the step.
+ *   sync:     nonzero: return once the step's GPU work and the output copy have completed
+ *             (cudaStreamSynchronize); zero: return after enqueueing, and in_host, out_host
+ *             and scratch must then stay untouched until the stream has passed the step.
+ * Host buffers should be page-locked (cudaHostAlloc or cudaHostRegister) for the copies to be
+ * asynchronous.  Between steps only (HW_ERR_INVALID_ARG if a step is open).
+ * Errors: HW_ERR_INVALID_ARG (NULL pointer, bad out_dtype, a negative count, in_bytes not as
+ * above, unaligned scratch, a step open) and HW_ERR_CAPACITY (scratch too small) with nothing
+ * enqueued; otherwise those of hw_append_kv (the first append's errors leave no open step),
+ * hw_concurrent_attention (every layer is appended by then: hw_step_end can close the step)
+ * and hw_step_end.
+ */
+hw_status hw_decode_step_host(hw_ctx* ctx, const int32_t* n_new, const void* in_host,
+                              size_t in_bytes, void* out_host, int32_t out_dtype,
+                              const uint8_t* finished, void* scratch, size_t scratch_bytes,
+                              int32_t sync, void* stream);
+
+/* Device scratch bytes hw_decode_step_host needs for the counts n_new (host int32[P][W + 1])
+ * and the output type.  Errors: HW_ERR_INVALID_ARG (NULL, bad out_dtype, a negative count). */
+hw_status hw_step_scratch_size(const hw_ctx* ctx, const int32_t* n_new, int32_t out_dtype,
+                               size_t* bytes);
+
+/*
  * Compaction (summary section 8: a finished block moves to the end of the common history and
  * is "corrected by RoPE offset" -- reading 1 of that correction; hw_step_end does reading 2,
  * an index remap): problem p's common segments first .. first+count-1 (commit order; 0 is

@@ -112,6 +112,32 @@ class HogwildCache:
     def step_end(self, finished=None, stream=None) -> None:
         binding.hw_step_end(self.ctx, finished, stream)
 
+    def decode_step_host(self, n_new, in_host, out_host, finished=None, out_dtype: str = "bf16",
+                         sync: bool = True, stream=None) -> None:
+        """One decode step from host memory (hw_decode_step_host): ``in_host`` a page-locked
+        uint8 CPU tensor holding the packed [K][V][Q] input, ``out_host`` a page-locked CPU
+        tensor of L*P*W*H_q*D elements of out_dtype.  The device scratch is kept between calls
+        (grown when a step needs more)."""
+        dt = HW_OUT_F32 if out_dtype == "f32" else HW_OUT_BF16
+        scratch = self.reserve_step_scratch(n_new, out_dtype)
+        binding.hw_decode_step_host(self.ctx, n_new, in_host.data_ptr(),
+                                    in_host.numel() * in_host.element_size(), out_host.data_ptr(),
+                                    dt, finished, scratch.data_ptr(), scratch.numel(), sync,
+                                    stream)
+
+    def reserve_step_scratch(self, n_new, out_dtype: str = "bf16"):
+        """The device scratch of decode_step_host for the counts n_new, allocated (or grown)
+        now rather than inside the first step."""
+        import torch
+        dt = HW_OUT_F32 if out_dtype == "f32" else HW_OUT_BF16
+        need = binding.hw_step_scratch_size(self.ctx, n_new, dt)
+        scratch = getattr(self, "_step_scratch", None)
+        if scratch is None or scratch.numel() < need:
+            # (a larger buffer may only replace the old one once no step still uses it)
+            torch.cuda.synchronize(self.device)
+            scratch = self._step_scratch = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return scratch
+
     def check_device_errors(self, stream=None):
         return binding.hw_check_device_errors(self.ctx, stream)
 

@@ -32,7 +32,7 @@ EXPORTED = (
     "hw_destroy", "hw_append_kv", "hw_concurrent_attention", "hw_concurrent_attention_noalloc",
     "hw_concurrent_attention_mq", "hw_concurrent_attention_range", "hw_merge_attention",
     "hw_compact_segments",
-    "hw_step_end",
+    "hw_step_end", "hw_decode_step_host", "hw_step_scratch_size",
     "hw_check_device_errors", "hw_debug_expire_plans", "hw_profile_enable", "hw_profile_read",
     "hw_get_counts", "hw_get_segment", "hw_get_blocks", "hw_get_view",
 )
@@ -98,6 +98,9 @@ def load() -> ctypes.CDLL:
                                               _P]),
         "hw_compact_segments": (ctypes.c_int, [_P, _I32, _I32, _I32, _P]),
         "hw_step_end": (ctypes.c_int, [_P, _P, _P]),
+        "hw_decode_step_host": (ctypes.c_int, [_P, _P, _P, ctypes.c_size_t, _P, _I32, _P, _P,
+                                               ctypes.c_size_t, _I32, _P]),
+        "hw_step_scratch_size": (ctypes.c_int, [_P, _P, _I32, ctypes.POINTER(ctypes.c_size_t)]),
         "hw_check_device_errors": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
         "hw_debug_expire_plans": (ctypes.c_int, [_P, _I32]),
         "hw_profile_enable": (ctypes.c_int, [_P, _I32]),
@@ -259,6 +262,33 @@ def hw_step_end(ctx: int, finished=None, stream=None) -> None:
     st = (_lib or load()).hw_step_end(ctx, fptr, _stream(stream))
     if st:
         _check(st, "hw_step_end")
+
+
+def hw_step_scratch_size(ctx: int, n_new, out_dtype: int) -> int:
+    n = ctypes.c_size_t()
+    nptr = n_new if isinstance(n_new, int) else _i32(n_new).ctypes.data
+    _check(load().hw_step_scratch_size(ctx, nptr, out_dtype, ctypes.byref(n)),
+           "hw_step_scratch_size")
+    return n.value
+
+
+def hw_decode_step_host(ctx: int, n_new, in_host: int, in_bytes: int, out_host: int,
+                        out_dtype: int, finished, scratch: int, scratch_bytes: int,
+                        sync: bool = True, stream=None) -> None:
+    """One decode step from host memory.  in_host / out_host: host addresses (ints) of the
+    packed [K][V][Q] input and the [L][P][W][H_q][D] output (page-locked for asynchronous
+    copies); scratch: device address; n_new and finished as hw_append_kv and hw_step_end
+    (array-likes, or addresses of arrays that stay alive for the call)."""
+    nptr = n_new if isinstance(n_new, int) else _i32(n_new).ctypes.data
+    if finished is None or isinstance(finished, int):
+        fptr = finished
+    else:
+        fptr = np.ascontiguousarray(np.asarray(finished, dtype=np.uint8)).ctypes.data
+    st = (_lib or load()).hw_decode_step_host(ctx, nptr, in_host, in_bytes, out_host, out_dtype,
+                                              fptr, scratch, scratch_bytes, int(bool(sync)),
+                                              _stream(stream))
+    if st:
+        _check(st, "hw_decode_step_host")
 
 
 def hw_check_device_errors(ctx: int, stream=None):

@@ -1589,3 +1589,99 @@ hw_status hw_get_view(const hw_ctx* c, int32_t problem, int32_t worker, int32_t*
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------- decode step from host
+
+namespace {
+// Device scratch of hw_decode_step_host: [K][V][Q][out], each 256-byte aligned.
+struct StepScratch {
+  size_t k, v, q, out, bytes;
+};
+StepScratch step_scratch_layout(const hw_config& cfg, int64_t total_new, int32_t out_elem) {
+  const size_t L = (size_t)cfg.num_layers, D = (size_t)cfg.head_dim;
+  const size_t kv = L * (size_t)total_new * cfg.num_kv_heads * D * sizeof(__nv_bfloat16);
+  const size_t rows = (size_t)cfg.num_problems * cfg.num_workers * cfg.num_q_heads;
+  StepScratch s{};
+  s.k = 0;
+  s.v = align_up(kv, kAlign);
+  s.q = s.v + align_up(kv, kAlign);
+  s.out = s.q + align_up(L * rows * D * sizeof(__nv_bfloat16), kAlign);
+  s.bytes = s.out + align_up(L * rows * D * out_elem, kAlign);
+  return s;
+}
+}  // namespace
+
+extern "C" {
+
+hw_status hw_step_scratch_size(const hw_ctx* c, const int32_t* n_new, int32_t out_dtype,
+                               size_t* bytes) {
+  if (!c || !n_new || !bytes) return HW_ERR_INVALID_ARG;
+  if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
+  int64_t total = 0;
+  for (int32_t i = 0; i < c->cfg.num_problems * (c->cfg.num_workers + 1); ++i) {
+    if (n_new[i] < 0) return HW_ERR_INVALID_ARG;
+    total += n_new[i];
+  }
+  *bytes = step_scratch_layout(c->cfg, total, out_dtype == HW_OUT_F32 ? 4 : 2).bytes;
+  return HW_OK;
+}
+
+hw_status hw_decode_step_host(hw_ctx* c, const int32_t* n_new, const void* in_host,
+                              size_t in_bytes, void* out_host, int32_t out_dtype,
+                              const uint8_t* finished, void* scratch, size_t scratch_bytes,
+                              int32_t sync, void* stream) {
+  if (!c || !n_new || !in_host || !out_host || !scratch) return HW_ERR_INVALID_ARG;
+  if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
+  if (c->step_active || (uintptr_t)scratch % kAlign) return HW_ERR_INVALID_ARG;
+  const hw_config& cfg = c->cfg;
+  int64_t total = 0;
+  for (int32_t i = 0; i < cfg.num_problems * (cfg.num_workers + 1); ++i) {
+    if (n_new[i] < 0) return HW_ERR_INVALID_ARG;
+    total += n_new[i];
+  }
+  const int32_t out_elem = out_dtype == HW_OUT_F32 ? 4 : 2;
+  const StepScratch sl = step_scratch_layout(cfg, total, out_elem);
+  if (scratch_bytes < sl.bytes) return HW_ERR_CAPACITY;
+  const size_t L = (size_t)cfg.num_layers, D = (size_t)cfg.head_dim;
+  const size_t kv_layer = (size_t)total * cfg.num_kv_heads * D * sizeof(__nv_bfloat16);
+  const size_t q_layer = (size_t)cfg.num_problems * cfg.num_workers * cfg.num_q_heads * D *
+                         sizeof(__nv_bfloat16);
+  const size_t out_layer = q_layer / sizeof(__nv_bfloat16) * out_elem;
+  if (in_bytes != L * (2 * kv_layer + q_layer)) return HW_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* dev = (char*)scratch;
+  const char* in = (const char*)in_host;
+  // Inputs up: one copy when the scratch holds K, V and Q back to back (no alignment gaps),
+  // else one copy per part.
+  if (sl.v == L * kv_layer && sl.q == 2 * L * kv_layer) {
+    HW_CUDA(cudaMemcpyAsync(dev, in, in_bytes, cudaMemcpyHostToDevice, s));
+  } else {
+    if (kv_layer) {
+      HW_CUDA(cudaMemcpyAsync(dev + sl.k, in, L * kv_layer, cudaMemcpyHostToDevice, s));
+      HW_CUDA(cudaMemcpyAsync(dev + sl.v, in + L * kv_layer, L * kv_layer,
+                              cudaMemcpyHostToDevice, s));
+    }
+    HW_CUDA(cudaMemcpyAsync(dev + sl.q, in + 2 * L * kv_layer, L * q_layer,
+                            cudaMemcpyHostToDevice, s));
+  }
+  // Every layer's append, then every layer's attention: an error from an attention call leaves
+  // a step that hw_step_end can close.  (An append after the first one fails only on the
+  // arguments checked above.)
+  for (int32_t l = 0; l < cfg.num_layers; ++l) {
+    const hw_status st = hw_append_kv(c, l, n_new, total ? dev + sl.k + l * kv_layer : nullptr,
+                                      total ? dev + sl.v + l * kv_layer : nullptr, stream);
+    if (st != HW_OK) return st;
+  }
+  for (int32_t l = 0; l < cfg.num_layers; ++l) {
+    const hw_status st = attend(c, l, dev + sl.q + l * q_layer, nullptr,
+                                dev + sl.out + l * out_layer, out_dtype, nullptr, stream);
+    if (st != HW_OK) return st;
+  }
+  HW_CUDA(cudaMemcpyAsync(out_host, dev + sl.out, L * out_layer, cudaMemcpyDeviceToHost, s));
+  const hw_status st = hw_step_end(c, finished, stream);
+  if (st != HW_OK) return st;
+  if (sync) HW_CUDA(cudaStreamSynchronize(s));
+  return HW_OK;
+}
+
+}  // extern "C"

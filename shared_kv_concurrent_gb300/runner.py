@@ -68,8 +68,24 @@ class WorkloadRunner:
             self.cache.concurrent_attention(layer, qs[layer], outs[layer], out_dtype,
                                             None if lses is None else lses[layer], stream)
 
+    def finished_for(self, step: int):
+        """The workload's commit mask after ``step`` (the address of a zero mask if none)."""
+        return wl.finished_mask(self.w, step) if step in self.w.commit_steps else self._no_commit_ptr
+
+    def packed_inputs(self, step: int):
+        """Page-locked uint8 CPU tensor [K(L)][V(L)][Q(L)] of decode ``step``: the input of
+        hw_decode_step_host."""
+        import torch
+        parts_k, parts_v, parts_q = [], [], []
+        for layer in range(self.w.num_layers):
+            k, v = wl.step_kv(self.w, layer, step)
+            parts_k.append(np.ascontiguousarray(k).ravel())
+            parts_v.append(np.ascontiguousarray(v).ravel())
+            parts_q.append(np.ascontiguousarray(wl.step_q(self.w, layer, step)).ravel())
+        flat = np.concatenate(parts_k + parts_v + parts_q).astype(np.uint16).view(np.uint8)
+        return torch.from_numpy(flat.copy()).pin_memory()
+
     def end(self, step: int, finished=None, stream=None) -> None:
         if finished is None:
-            finished = (wl.finished_mask(self.w, step) if step in self.w.commit_steps
-                        else self._no_commit_ptr)
+            finished = self.finished_for(step)
         self.cache.step_end(finished, stream)
