@@ -141,10 +141,9 @@ void hw_destroy(hw_ctx* ctx);
  * order, then the common block, then workers in ascending id; a new page whenever j mod S == 0;
  * in contiguous mode one page at j == 0).  Every layer must append once per step with the same
  * n_new.  Attention in the step sees the appended tokens; lengths advance at hw_step_end().
- * When the write happens: with the tensor-core attention (W * H_q / H_kv >= 16 query rows) and
- * at most 16 tokens per block in the step (decode), this call only records k_raw / v_raw and
- * the layer's hw_concurrent_attention writes the tokens itself, inside its kernel, before it
- * reads them; if the step ends without that call, hw_step_end writes them.  Otherwise an append
+ * When the write happens: with at most 16 tokens per block in the step (decode), this call
+ * only records k_raw / v_raw and the layer's hw_concurrent_attention writes the tokens itself,
+ * inside its kernel (either attention kernel), before it reads them; if the step ends without that call, hw_step_end writes them.  Otherwise an append
  * kernel is enqueued here.  Either way k_raw and v_raw must keep their contents, in stream
  * order, until the layer's attention call or hw_step_end, whichever comes first.
  * Errors: HW_ERR_INVALID_ARG (bad layer, counts differing from the step's first append, layer

@@ -13,9 +13,10 @@
 // kernel loads) are staged once into a ring of one or two slots in shared memory, completion
 // on an mbarrier, and kept in bf16; the rotated, pre-scaled queries (log2(e)/sqrt(D)) and the
 // running output O of every row stay in shared memory in fp32.  Per tile and per chunk of 16
-// query rows: S = Q~ K^T with a thread per (token, half of the rows); the online softmax with a
-// warp per row (running max and sum, rescale factor); O = alpha O + P V with a thread per (row
-// pair, 4 columns).  Every wait is bounded (about a second): one that runs out records
+// query rows: S = Q~ K^T and the online softmax (running max and sum, rescale factor) with a
+// thread per (row, 8 tokens), a row's 16 threads reducing by shuffles; O = alpha O + P V with a
+// thread per (row pair, 4 columns).  In a decode step the CTA first writes its unit's appended
+// tokens itself (fused append).  Every wait is bounded (about a second): one that runs out records
 // ERR_TIMEOUT, and the CTA waits (bounded by the clock) for its copies in flight, then writes
 // empty partials.  The kernel is launched as a programmatic dependent: it waits for the grid
 // it follows (which may write the queries or this step's tokens) before it reads anything.
@@ -33,6 +34,7 @@ namespace hw {
 namespace {
 
 using tc::fence_mbar_init;
+using tc::fence_proxy_async_global;
 using tc::fence_proxy_async_smem;
 using tc::mbar_arrive_expect_tx;
 using tc::mbar_init;
@@ -45,6 +47,7 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 128;            // tokens per tile (one TMA box of rows)
 constexpr int kChunkRows = 16;        // query rows per pass over a tile, at most
+constexpr int kSStride = kTile + 4;   // floats per row of P (padded: two rows' stores share no bank)
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 template <int D>
@@ -56,7 +59,7 @@ struct FmaCfg {
 };
 
 // Shared-memory layout for R query rows and `slots` ring slots (offsets from a 1024-byte
-// aligned base): ring, Q~ [R][D] f32, O [R][D] f32, S/P [16][128] f32, M/L/alpha [R] f32, row
+// aligned base): ring, Q~ [R][D] f32, O [R][D] f32, P [16][132] f32, M/L/alpha [R] f32, row
 // cut [R] i32, barriers, flags.
 template <int D>
 struct FmaLayout {
@@ -65,7 +68,7 @@ struct FmaLayout {
     uint32_t off = (uint32_t)slots * FmaCfg<D>::kSlotBytes;
     q = off;    off += (uint32_t)R * D * 4;
     o = off;    off += (uint32_t)R * D * 4;
-    s = off;    off += kChunkRows * kTile * 4;
+    s = off;    off += kChunkRows * kSStride * 4;
     m = off;    off += (uint32_t)R * 4;
     l = off;    off += (uint32_t)R * 4;
     al = off;   off += (uint32_t)R * 4;
@@ -181,6 +184,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     return -1;
   };
+  // Fused append (decode steps): the unit's appended tokens of its KV head are written here,
+  // before any tile is loaded (the async-proxy fence orders these writes before the CTA's TMA
+  // reads of them).  Each (token, KV head) belongs to exactly one unit.
+  if (unit_ok && a.k_raw != nullptr && u.fresh_end > u.fresh_begin) {
+    append_fresh<D, kThreads>(a, g.h, u.fresh_begin, u.fresh_end, tid, KID_ATTN_FMA);
+    fence_proxy_async_global();
+    __syncthreads();
+  }
   int next_issue = pb;            // (thread 0) first piece not yet looked at
   uint32_t issued = 0;            // (thread 0) tiles issued
   if (tid == 0 && pb < pe) {
@@ -242,14 +253,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int r0 = 0; r0 < R; r0 += kChunkRows) {
       const int CR = min(kChunkRows, R - r0);
       {
-        // S = Q~ K^T: thread (token j, row parity hf) takes rows hf, hf + 2, ... of the chunk
-        // S = Q~ K^T: thread (row r of the chunk, token group tg) takes tokens tg + 16 k, k < 8.
-        // A row's 8-element query chunk is loaded once into registers and used for all eight
-        // tokens (shared-memory broadcasts deliver 4 bytes per wavefront, so re-reading the
-        // queries per token would cost more than the K tile itself); the 16 threads of a row
-        // read 16 consecutive tokens' chunks (swizzled rows: no bank conflict).
+        // S = Q~ K^T and the online softmax of the tile, fused: thread (row r of the chunk, token
+        // group tg) takes tokens tg + 16 k, k < 8, and the 16 threads of a row (one half-warp)
+        // reduce its maximum and sum with shuffles.  A row's 8-element query chunk is loaded
+        // once into registers and used for all eight tokens (shared-memory broadcasts deliver
+        // 4 bytes per wavefront, so re-reading the queries per token would cost more than the
+        // K tile itself); the 16 threads of a row read 16 consecutive tokens' chunks (swizzled
+        // rows: no bank conflict).
         const int r = tid >> 4, tg = tid & 15;
         if (r < CR) {
+          const unsigned hmask = (lane < 16) ? 0x0000ffffu : 0xffff0000u;   // this row's lanes
           float2 acc[kTile / 16];           // per token: (even, odd) element accumulators
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k) acc[k] = make_float2(0.f, 0.f);
@@ -269,46 +282,38 @@ __global__ void __launch_bounds__(kThreads, 2)
               acc[k] = fma2(q67, make_float2(bf_lo(kw.w), bf_hi(kw.w)), acc[k]);
             }
           }
+          // Online softmax of the row over this tile: tokens past the piece or past the row's
+          // causal cut (cut -1: the row does not see the segment) score -inf.
+          const int rr = r0 + r;
+          const int cap = cut[rr];
+          const int lim = cap < 0 ? 0 : min(nv, cap - pc.pos0);
+          const float m_old = Ms[rr];
+          float sv[kTile / 16];
+          float mx = -CUDART_INF_F;
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k) Ss[r * kTile + tg + 16 * k] = acc[k].x + acc[k].y;
-        }
-      }
-      __syncthreads();
-      // Online softmax: warp w takes rows w and w + 8 of the chunk, a lane four tokens.
-      for (int rr = warp; rr < CR; rr += kWarps) {
-        const int r = r0 + rr;
-        const int cap = cut[r];                     // -1: the row does not see the segment
-        const int lim = cap < 0 ? 0 : min(nv, cap - pc.pos0);
-        float4 sv = reinterpret_cast<const float4*>(Ss + rr * kTile)[lane];
-        float s4[4] = {sv.x, sv.y, sv.z, sv.w};
-        float mx = -CUDART_INF_F;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (4 * lane + e >= lim) s4[e] = -CUDART_INF_F;
-          mx = fmaxf(mx, s4[e]);
-        }
-#pragma unroll
-        for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float m_old = Ms[r];
-        const float m_new = fmaxf(m_old, mx);
-        float alpha = 1.f, ps = 0.f;
-        float p4[4] = {0.f, 0.f, 0.f, 0.f};
-        if (m_new != -CUDART_INF_F) {
-          alpha = (m_old == -CUDART_INF_F) ? 0.f : exp2f(m_old - m_new);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            p4[e] = (s4[e] == -CUDART_INF_F) ? 0.f : exp2f(s4[e] - m_new);
-            ps += p4[e];
+          for (int k = 0; k < kTile / 16; ++k) {
+            sv[k] = (tg + 16 * k < lim) ? acc[k].x + acc[k].y : -CUDART_INF_F;
+            mx = fmaxf(mx, sv[k]);
           }
-        }
 #pragma unroll
-        for (int off = 16; off; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-        reinterpret_cast<float4*>(Ss + rr * kTile)[lane] = make_float4(p4[0], p4[1], p4[2], p4[3]);
-        __syncwarp();
-        if (lane == 0) {
-          Ms[r] = m_new;
-          Ls[r] = Ls[r] * alpha + ps;
-          As[r] = alpha;
+          for (int off = 8; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(hmask, mx, off));
+          const float m_new = fmaxf(m_old, mx);
+          float alpha = 1.f, ps = 0.f;
+          float* prow = Ss + r * kSStride;
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k) {
+            const float pk = (sv[k] == -CUDART_INF_F) ? 0.f : exp2f(sv[k] - m_new);
+            ps += pk;
+            prow[tg + 16 * k] = pk;
+          }
+          if (m_new != -CUDART_INF_F) alpha = (m_old == -CUDART_INF_F) ? 0.f : exp2f(m_old - m_new);
+#pragma unroll
+          for (int off = 8; off; off >>= 1) ps += __shfl_xor_sync(hmask, ps, off);
+          if (tg == 0) {               // (every lane of the row has read Ms above)
+            Ms[rr] = m_new;
+            Ls[rr] = Ls[rr] * alpha + ps;
+            As[rr] = alpha;
+          }
         }
       }
       __syncthreads();
@@ -324,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           const float aa = As[r0 + ra], ab = has_b ? As[r0 + rb] : 1.f;
           xa = make_float4(xa.x * aa, xa.y * aa, xa.z * aa, xa.w * aa);
           xb = make_float4(xb.x * ab, xb.y * ab, xb.z * ab, xb.w * ab);
-          const float* pa = Ss + ra * kTile;
-          const float* pbr = Ss + (has_b ? rb : ra) * kTile;
+          const float* pa = Ss + ra * kSStride;
+          const float* pbr = Ss + (has_b ? rb : ra) * kSStride;
           const int d = 4 * dg;
           const uint8_t* vcol = vt + (uint32_t)(d >> 6) * C::kHalfBytes + (uint32_t)((d & 7) * 2);
           const int vc = (d & 63) >> 3;

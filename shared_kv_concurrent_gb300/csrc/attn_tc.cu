@@ -277,58 +277,6 @@ __device__ __forceinline__ void rotate_tile(const AttnArgs& a, const Group& g, i
   }
 }
 
-// Fused append (Hogwild! Inference summary, section 9: tokens of a block at block-local
-// positions): the unit's appended tokens [f0, f1) of the FreshTok table are written for its KV
-// head h -- key rotated to its position with the fp32 table and stored as bf16, value copied --
-// into the pool, exactly as the append kernel would.  64 threads; each takes 8 rotation pairs
-// (16-byte loads and stores) of one token.
-template <int D>
-__device__ __forceinline__ void append_fresh(const AttnArgs& a, const Group& g, int f0, int f1,
-                                             int tid) {
-  constexpr int half = D / 2;
-  constexpr int CH = half / 8;                 // 8-pair chunks per token
-  constexpr int TPP = kRotThreads / CH;        // tokens per pass
-  const int c = tid % CH;
-#pragma unroll 1
-  for (int f = f0 + tid / CH; f < f1; f += TPP) {
-    const FreshTok ft = a.fresh[f];
-    if (ft.page < 0 || ft.page >= a.num_pages || ft.slot < 0 || ft.slot >= a.S) {
-      if (c == 0) record_error(a.err, ERR_PAGE_RANGE, KID_ATTN_TC, blockIdx.x, ft.page);
-      continue;
-    }
-    if (ft.pos < 0 || ft.pos >= a.max_position || ft.src < 0) {
-      if (c == 0) record_error(a.err, ERR_POS_RANGE, KID_ATTN_TC, blockIdx.x, ft.pos);
-      continue;
-    }
-    const size_t src = ((size_t)ft.src * a.H_kv + g.h) * D + 8 * c;
-    const size_t dst = (((size_t)ft.page * a.H_kv + g.h) * a.S + ft.slot) * D + 8 * c;
-    const size_t tab = (size_t)ft.pos * half + 8 * c;
-    const uint4 k1 = *reinterpret_cast<const uint4*>(a.k_raw + src);
-    const uint4 k2 = *reinterpret_cast<const uint4*>(a.k_raw + src + half);
-    const uint4 v1 = *reinterpret_cast<const uint4*>(a.v_raw + src);
-    const uint4 v2 = *reinterpret_cast<const uint4*>(a.v_raw + src + half);
-    const float4 ca = *reinterpret_cast<const float4*>(a.rope_cos + tab);
-    const float4 cb = *reinterpret_cast<const float4*>(a.rope_cos + tab + 4);
-    const float4 sa = *reinterpret_cast<const float4*>(a.rope_sin + tab);
-    const float4 sb = *reinterpret_cast<const float4*>(a.rope_sin + tab + 4);
-    const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
-    const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-    const __nv_bfloat16* x1 = reinterpret_cast<const __nv_bfloat16*>(&k1);
-    const __nv_bfloat16* x2 = reinterpret_cast<const __nv_bfloat16*>(&k2);
-    __align__(16) __nv_bfloat16 y1[8], y2[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float u1 = __bfloat162float(x1[e]), u2 = __bfloat162float(x2[e]);
-      y1[e] = __float2bfloat16_rn(u1 * cv[e] - u2 * sv[e]);
-      y2[e] = __float2bfloat16_rn(u2 * cv[e] + u1 * sv[e]);
-    }
-    *reinterpret_cast<uint4*>(a.k_layer + dst) = *reinterpret_cast<const uint4*>(y1);
-    *reinterpret_cast<uint4*>(a.k_layer + dst + half) = *reinterpret_cast<const uint4*>(y2);
-    *reinterpret_cast<uint4*>(a.v_layer + dst) = v1;
-    *reinterpret_cast<uint4*>(a.v_layer + dst + half) = v2;
-  }
-}
-
 // ---------------------------------------------------------------------------- attention
 
 template <int D, int T>
@@ -666,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // in turn.
     const int tid = threadIdx.x - 64;
     if (fused) {
-      append_fresh<D>(a, g, u.fresh_begin, u.fresh_end, tid);
+      append_fresh<D, kRotThreads>(a, g.h, u.fresh_begin, u.fresh_end, tid, KID_ATTN_TC);
       fence_proxy_async_global();         // generic-proxy pool writes -> this CTA's TMA loads
       asm volatile("bar.sync 4, %0;" ::"r"(kRotThreads) : "memory");
       if (tid == 0) mbar_arrive(bar_fresh);

@@ -30,8 +30,8 @@ constexpr size_t kSlotBudget = 64u << 20;  // ... and at most this many bytes of
 constexpr size_t kAlign = 256;
 constexpr int kPieceMax = 128;         // tokens per piece = one kernel tile (never crosses a page)
 constexpr int kProfPairs = 4096;       // timed launches kept per hw_profile_read
-// A step whose blocks each append at most this many tokens has them written by the
-// tensor-core attention kernel itself (fused append); larger appends use the append kernel.
+// A step whose blocks each append at most this many tokens has them written by the attention
+// kernel itself (fused append, either kernel); larger appends use the append kernel.
 constexpr int kFuseTok = 16;
 constexpr int kMaxRows = 128;          // query rows of one (problem, KV head): one MMA tile
 // Tensor-core plans: about this many tiles per SM per wave of units, at most kMaxWaves waves.
@@ -171,6 +171,13 @@ struct PlanScratch {
   struct Part {
     int32_t unit, ref, t0, t1;        // tiles [t0, t1) of segment reference `ref` go to `unit`
   };
+  // The plan's arrays are built here (memory the planner keeps warm) and copied into the
+  // staging slot in one pass at the end: a slot comes back only after the others have been
+  // used, and stores scattered over its cold lines cost more than the copy.
+  Buf<hw::Piece> pieces;
+  Buf<hw::Unit> units;
+  Buf<hw::Group> groups;
+  Buf<hw::FreshTok> fresh;
   std::vector<int32_t> delta, refs, src_base, ref_of, view_ref, vlen, qrow;
   Buf<uint8_t> piece_early;             // the piece may be loaded before the programmatic wait
   int32_t qrow_next = 0;
@@ -243,8 +250,8 @@ struct hw_ctx {
   hw::PlanGate step_gate{};
   PlanScratch ps;
   // Fused append: when the step's plan lists its appended tokens (step_fused), hw_append_kv
-  // only records the layer's k_raw / v_raw here and the layer's tensor-core attention writes
-  // them; whatever else needs the pool first launches the append kernel (flush_append).
+  // only records the layer's k_raw / v_raw here and the layer's attention kernel writes them;
+  // whatever else needs the pool first launches the append kernel (flush_append).
   bool step_fused = false;
   std::vector<const void*> pend_k, pend_v;
   // measurement
@@ -668,8 +675,8 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
       }
     const size_t plan_off = align_up((size_t)nr * sizeof(hw::AppendRun), kAlign);
     PlanOffsets po{};
-    // Small appends (decode) are written by the tensor-core attention kernel itself.
-    bool fuse = c->use_tc;
+    // Small appends (decode) are written by the attention kernel itself.
+    bool fuse = true;
     for (int32_t i = 0; i < P * B && fuse; ++i) fuse = n_new[i] <= kFuseTok;
     const uint64_t seq = c->next_seq();
     bool plan_ok = plan_off < c->lay.slot_seq_off &&
@@ -876,9 +883,8 @@ bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int
     // per-group counts are floored and then raised to >= 1: keep room for that raise
     target_units = std::max<int64_t>(0, std::min<int64_t>(target_units, unit_cap - (int64_t)P * H));
   }
-  // Sizes, known before anything is written: every tile of a problem is one piece, and a
-  // problem's units (the same for every KV head) follow from its share of the tiles.  The plan
-  // is written straight into `buf`; only the fresh-token list, last, grows while it is built.
+  // Sizes, known before anything is built: every tile of a problem is one piece, and a
+  // problem's units (the same for every KV head) follow from its share of the tiles.
   ps.prob_units.resize((size_t)P);
   int64_t n_pieces = 0, n_units_all = 0;
   for (int32_t p = 0; p < P; ++p) {
@@ -908,15 +914,19 @@ bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int
   off = align_up(off + ps.qrow.size() * sizeof(int32_t), 16);
   po->fresh = off;
   if (off > cap) return false;
-  hw::Piece* const pieces = reinterpret_cast<hw::Piece*>(buf + po->pieces);
-  hw::Unit* const units = reinterpret_cast<hw::Unit*>(buf + po->units);
-  hw::Group* const groups = reinterpret_cast<hw::Group*>(buf + po->groups);
-  hw::FreshTok* const fresh = reinterpret_cast<hw::FreshTok*>(buf + po->fresh);
   const int64_t max_fresh =
       std::min<int64_t>(L.max_fresh, (int64_t)((cap - off) / sizeof(hw::FreshTok)));
-  int32_t np = 0, nf = 0, nu_done = 0;                 // pieces, fresh tokens, units written
+  ps.pieces.clear();
+  ps.units.clear();
+  ps.groups.clear();
+  ps.fresh.clear();
   ps.piece_early.clear();
+  hw::Piece* const pieces = ps.pieces.grow((size_t)n_pieces);
+  hw::Unit* const units = ps.units.grow((size_t)n_units_all);
+  hw::Group* const groups = ps.groups.grow((size_t)P * H);
+  hw::FreshTok* const fresh = ps.fresh.grow((size_t)max_fresh);
   uint8_t* const early_all = ps.piece_early.grow((size_t)n_pieces);
+  int32_t np = 0, nf = 0, nu_done = 0;                 // pieces, fresh tokens, units written
   // The pieces of segment reference r at its tiles [t0, t1) (counted from the reference's
   // first tile): the reference's tokens inside one kPieceMax-aligned tile each -- so inside one
   // page -- with the step's appended tokens in it listed for the fused append.  Only the first
@@ -1091,6 +1101,10 @@ bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int
     nu_done += n * H;
   }
   if (np != n_pieces || nu_done != n_units_all) return false;
+  std::memcpy(buf + po->pieces, pieces, (size_t)np * sizeof(hw::Piece));
+  std::memcpy(buf + po->units, units, (size_t)nu_done * sizeof(hw::Unit));
+  std::memcpy(buf + po->groups, groups, (size_t)P * H * sizeof(hw::Group));
+  if (nf) std::memcpy(buf + po->fresh, fresh, (size_t)nf * sizeof(hw::FreshTok));
   std::memcpy(buf + po->delta, ps.delta.data(), ps.delta.size() * sizeof(int32_t));
   if (!ps.vlen.empty())
     std::memcpy(buf + po->vlen, ps.vlen.data(), ps.vlen.size() * sizeof(int32_t));
@@ -1141,9 +1155,9 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
   // (the step's plan has one query per worker and lists the step's tokens for the kernel)
   const bool step_plan =
       !n_q && !ranges && c->step_slot >= 0 && c->step_epoch == c->epoch && c->step_plan_ok;
-  // The layer's recorded append is written by the tensor-core kernel when the step's plan lists
+  // The layer's recorded append is written by the attention kernel when the step's plan lists
   // the appended tokens; otherwise by the append kernel, now.
-  const bool fused = c->use_tc && step_plan && c->step_fused && layer < (int32_t)c->pend_k.size() &&
+  const bool fused = step_plan && c->step_fused && layer < (int32_t)c->pend_k.size() &&
                      c->pend_k[layer] != nullptr;
   if (!fused) {
     const hw_status st = c->flush_append(layer, s);
