@@ -79,7 +79,7 @@ def captured_share():
         rec = text.split("kernel-source-sha256:")[1].split()[0]
         share = float(text.split("attention-share-of-step:")[1].split()[0])
         h = hashlib.sha256()
-        for name in ("attn_tc.cu", "attn_fma.cu", "hw_merge.cuh", "tc_ptx.cuh", "hw_internal.h",
+        for name in ("attn_tc.cu", "merge.cu", "hw_merge.cuh", "tc_ptx.cuh", "hw_internal.h",
                      "hw_device.cuh"):
             with open(os.path.join(ROOT, "shared_kv_concurrent_gb300", "csrc", name), "rb") as f:
                 h.update(f.read())

@@ -1,6 +1,5 @@
-// K2 (CUDA-core form) and K3 -- concurrent attention with per-(worker, block) query rotation
-// for fewer than 16 query rows per KV head, and the log-sum-exp merge of the per-unit partial
-// results.
+// K2 (CUDA-core form) -- concurrent attention with per-(worker, block) query rotation for fewer
+// than 16 query rows per KV head; the per-unit partial results are merged by K3 (merge.cu).
 //
 // Method (Hogwild! Inference summary, gentlecold.top): keys are stored rotated at block-local
 // positions; for a block at offset o in worker w's view the query is rotated by (i_q - o)
@@ -25,7 +24,6 @@
 #include <math_constants.h>
 
 #include "hw_device.cuh"
-#include "hw_merge.cuh"
 #include "tc_ptx.cuh"
 
 #include <algorithm>
@@ -132,13 +130,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int PS = part_stride(D);
 
-  // Wait for the grid this one follows (it may write the queries, this step's tokens, or read
-  // the partials this grid overwrites) before anything is read or written.
-  tc::pdl_wait();
+  // Set-up that touches no global memory: barriers, running output and row statistics.
   if (tid == 0) {
     for (int k = 0; k < slots; ++k) mbar_init(bars + 8u * k, 1);
     fence_mbar_init();
-    flags[0] = plan_arrived(a.gate, plan_seq_now(a.gate), a.err, KID_ATTN_FMA) ? 1 : 0;
     flags[1] = 0;
   }
   for (int i = tid; i < R * D; i += kThreads) Os[i] = 0.f;
@@ -146,6 +141,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     Ms[r] = -CUDART_INF_F;
     Ls[r] = 0.f;
   }
+  // Wait for the grid this one follows (it may write the queries, this step's tokens, or read
+  // the partials this grid overwrites) before anything global is read or written.
+  tc::pdl_wait();
+  if (tid == 0) flags[0] = plan_arrived(a.gate, plan_seq_now(a.gate), a.err, KID_ATTN_FMA) ? 1 : 0;
   __syncthreads();
   const bool plan_ok = flags[0] != 0;
   Unit u{};
@@ -153,23 +152,29 @@ __global__ void __launch_bounds__(kThreads, 2)
   bool unit_ok = false;
   if (plan_ok) {
     u = a.units[blockIdx.x];
+    // (problem, KV head) from the group index (groups are numbered p * H_kv + h): no dependent
+    // load of the group record
     if (u.group >= 0 && u.group < a.num_groups) {
-      g = a.groups[u.group];
-      unit_ok = g.p >= 0 && g.p < a.P && g.h >= 0 && g.h < a.H_kv && u.piece_begin >= 0 &&
-                u.piece_begin <= u.piece_end;
+      g.p = u.group / a.H_kv;
+      g.h = u.group % a.H_kv;
+      unit_ok = g.p < a.P && u.piece_begin >= 0 && u.piece_begin <= u.piece_end;
     }
     if (!unit_ok && tid == 0) record_error(a.err, ERR_PLAN, KID_ATTN_FMA, blockIdx.x, 0);
   }
   const int pb = unit_ok ? u.piece_begin : 0, pe = unit_ok ? u.piece_end : 0;
   const int64_t page_base = (int64_t)layer * a.num_pages;   // first page of this layer's pool
+  // This CTA writes the unit's appended tokens of its KV head itself (fused append).
+  const bool fresh_here = unit_ok && a.k_raw != nullptr && u.fresh_end > u.fresh_begin;
 
   // Producer (thread 0): the first valid piece at or after `from`, its K and V tiles into ring
   // slot `slot` (pool rows ((page_base + page) * H_kv + h) * S + slot0 ..).  Returns the index
-  // of the piece it loaded, or -1 when none is left.
-  auto issue = [&](int from, int slot) -> int {
+  // of the piece it loaded, -1 when none is left, or -2 - index for a piece with tokens of this
+  // step while those may not be loaded yet (fresh_ok false: the fused append has not run).
+  auto issue = [&](int from, int slot, bool fresh_ok) -> int {
     for (int pi = from; pi < pe; ++pi) {
       const Piece pc = a.pieces[pi];
       if (!piece_ok(a, pc)) continue;
+      if (pc.fresh && !fresh_ok) return -2 - pi;
       const uint32_t dst = sbase + (uint32_t)slot * C::kSlotBytes;
       const int32_t y = (int32_t)(((page_base + pc.page) * a.H_kv + g.h) * a.S + pc.slot0);
       mbar_arrive_expect_tx(bars + 8u * slot, C::kSlotBytes);
@@ -184,62 +189,83 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     return -1;
   };
-  // Fused append (decode steps): the unit's appended tokens of its KV head are written here,
-  // before any tile is loaded (the async-proxy fence orders these writes before the CTA's TMA
-  // reads of them).  Each (token, KV head) belongs to exactly one unit.
-  if (unit_ok && a.k_raw != nullptr && u.fresh_end > u.fresh_begin) {
-    append_fresh<D, kThreads>(a, g.h, u.fresh_begin, u.fresh_end, tid, KID_ATTN_FMA);
-    fence_proxy_async_global();
-    __syncthreads();
-  }
   int next_issue = pb;            // (thread 0) first piece not yet looked at
   uint32_t issued = 0;            // (thread 0) tiles issued
-  if (tid == 0 && pb < pe) {
-    tc::tma_prefetch(&maps.k);
-    tc::tma_prefetch(&maps.v);
-    for (int k = 0; k < slots && next_issue < pe; ++k) {
-      const int got = issue(next_issue, k);
+  auto fill_ring = [&](bool fresh_ok) {
+    while (issued < (uint32_t)slots && next_issue < pe) {
+      const int got = issue(next_issue, (int)issued, fresh_ok);
+      if (got <= -2) {            // resumes there once the fused append is written
+        next_issue = -2 - got;
+        return;
+      }
       next_issue = got < 0 ? pe : got + 1;
       if (got >= 0) ++issued;
     }
+  };
+  // The first tiles go out at once, unless they hold tokens this CTA is about to write.
+  if (tid == 0 && pb < pe) {
+    tc::tma_prefetch(&maps.k);
+    tc::tma_prefetch(&maps.v);
+    fill_ring(!fresh_here);
   }
 
-  int cur_seg = -1;
+  // Rotation of every row's query for segment slot `seg` by (i_q - the segment's view offset),
+  // pre-scaled; rows of workers that do not see it are zero and cut = -1.  Threads t0 .. t0 + nt
+  // of the CTA share the work (t = tid - t0).
+  auto rotate = [&](int seg, int t, int nt) {
+    const int* dl = a.delta + (size_t)seg * a.W;
+    constexpr int half = D / 2;
+    for (int idx = t; idx < R * half; idx += nt) {
+      const int r = idx / half, i = idx % half;
+      const int w = r / a.G, hq = g.h * a.G + r % a.G;
+      const int delta = dl[w];
+      float y1 = 0.f, y2 = 0.f;
+      if (delta >= 0 && delta < a.max_position) {
+        const size_t qo = ((size_t)query_row(a, g.p, w) * a.H_q + hq) * D;
+        const float q1 = __bfloat162float(a.q[qo + i]);
+        const float q2 = __bfloat162float(a.q[qo + i + half]);
+        const float c = a.rope_cos[(size_t)delta * half + i];
+        const float sn = a.rope_sin[(size_t)delta * half + i];
+        y1 = (q1 * c - q2 * sn) * a.scale_log2;
+        y2 = (q2 * c + q1 * sn) * a.scale_log2;
+      } else if (delta >= a.max_position && i == 0) {
+        record_error(a.err, ERR_POS_RANGE, KID_ATTN_FMA, blockIdx.x, delta);
+      }
+      Qs[r * D + i] = y1;
+      Qs[r * D + i + half] = y2;
+      if (i == 0) {
+        const bool vis = delta >= 0 && delta < a.max_position;
+        // causal cut (several query tokens per worker): tokens of the segment it may see
+        cut[r] = !vis ? -1 : (a.vlen ? a.vlen[(size_t)seg * a.W + w] : 0x7fffffff);
+      }
+    }
+  };
+  // The unit's first segment (named by its record) is rotated while the fused append runs: two
+  // warps write the appended tokens, the other six rotate.  The async-proxy fence orders the
+  // pool writes before the CTA's TMA reads of them; every (token, KV head) belongs to exactly
+  // one unit.
+  const bool pre_rot = unit_ok && u.seg0 >= 0 && u.seg0 < a.num_seg_slots;
+  if (fresh_here) {
+    if (tid < 64) {
+      append_fresh<D, 64>(a, g.h, u.fresh_begin, u.fresh_end, tid, KID_ATTN_FMA);
+      fence_proxy_async_global();
+    } else if (pre_rot) {
+      rotate(u.seg0, tid - 64, kThreads - 64);
+    }
+  } else if (pre_rot) {
+    rotate(u.seg0, tid, kThreads);
+  }
+  __syncthreads();
+  if (fresh_here && tid == 0) fill_ring(true);
+
+  int cur_seg = pre_rot ? u.seg0 : -1;
   uint32_t tile = 0;              // tiles consumed
   for (int pi = pb; pi < pe; ++pi) {
     const Piece pc = a.pieces[pi];
     if (!piece_ok(a, pc)) continue;                 // every thread skips it the same way
-    if (pc.seg_slot != cur_seg) {
-      // New segment: every row's query rotated by (i_q - the segment's view offset), pre-scaled;
-      // rows of workers that do not see it are zero and cut = -1.
+    if (pc.seg_slot != cur_seg) {                   // a new segment: its query rotation
       cur_seg = pc.seg_slot;
-      const int* dl = a.delta + (size_t)pc.seg_slot * a.W;
-      constexpr int half = D / 2;
-      for (int idx = tid; idx < R * half; idx += kThreads) {
-        const int r = idx / half, i = idx % half;
-        const int w = r / a.G, hq = g.h * a.G + r % a.G;
-        const int delta = dl[w];
-        float y1 = 0.f, y2 = 0.f;
-        if (delta >= 0 && delta < a.max_position) {
-          const size_t qo = ((size_t)query_row(a, g.p, w) * a.H_q + hq) * D;
-          const float q1 = __bfloat162float(a.q[qo + i]);
-          const float q2 = __bfloat162float(a.q[qo + i + half]);
-          const float c = a.rope_cos[(size_t)delta * half + i];
-          const float sn = a.rope_sin[(size_t)delta * half + i];
-          y1 = (q1 * c - q2 * sn) * a.scale_log2;
-          y2 = (q2 * c + q1 * sn) * a.scale_log2;
-        } else if (delta >= a.max_position && i == 0) {
-          record_error(a.err, ERR_POS_RANGE, KID_ATTN_FMA, blockIdx.x, delta);
-        }
-        Qs[r * D + i] = y1;
-        Qs[r * D + i + half] = y2;
-        if (i == 0) {
-          const bool vis = delta >= 0 && delta < a.max_position;
-          // causal cut (several query tokens per worker): tokens of the segment it may see
-          cut[r] = !vis ? -1
-                        : (a.vlen ? a.vlen[(size_t)pc.seg_slot * a.W + w] : 0x7fffffff);
-        }
-      }
+      rotate(cur_seg, tid, kThreads);
     }
     const int slot = (int)(tile % (uint32_t)slots);
     const uint32_t parity = (tile / (uint32_t)slots) & 1u;
@@ -371,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // before the copy's writes)
     if (tid == 0 && next_issue < pe) {
       fence_proxy_async_smem();
-      const int got = issue(next_issue, slot);
+      const int got = issue(next_issue, slot, true);
       next_issue = got < 0 ? pe : got + 1;
       if (got >= 0) ++issued;
     }
@@ -400,48 +426,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-// K3: the log-sum-exp merge of the units' partials (merge_row, hw_merge.cuh), one warp per
-// (group, query row), as a kernel of its own: used after the CUDA-core attention and after the
-// tensor-core attention when that kernel does not merge itself.
-//
-// Register budget: at most 144 registers, with 20 units' loads in flight per row at once (the
-// benchmark workload has 19 units per group).  Measured: 32.85 -> 32.63 us per decode step on
-// the 32K-common, 8-worker workload, 1.359 -> 1.326 ms per 64-layer step on the 16K-common one.
-// (At 144 registers a merge CTA and a CTA of the next call's attention kernel, 8 warps at
-// 184 registers as allocated, fit one SM's 65,536 registers; the shared-memory split still
-// keeps them apart, and forcing the large split made the step slower.)
-constexpr int kMergeWarps = 4;
-constexpr int kMergeChunk = 20;
-
-template <int D>
-__global__ void __maxnreg__(144) merge_kernel(const AttnArgs a) {
-  // May be launched as a programmatic dependent of the attention kernel: wait for its writes.
-  // Whatever follows may start its own prologue now (the library's kernels wait for this grid
-  // before they read anything it writes or overwrite the partials it reads).
-  HW_SPAN_BEGIN(0);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x * kMergeWarps + warp;
-  const bool valid = item < a.num_groups * a.rows;
-  const int gi = valid ? item / a.rows : 0, r = item - gi * a.rows;
-  // The group entry belongs to the call's plan, not to what the attention kernel writes: it is
-  // read before the wait once the plan's sequence word shows that the plan has arrived (an
-  // acquire load; plans without a word were copied before the attention kernel started).
-  Group g{};
-  bool have_g = false;
-  if (valid && plan_seq_now(a.gate) == a.gate.plan_expect) {
-    g = a.groups[gi];
-    have_g = true;
-  }
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  HW_SPAN_BEGIN(1);
-  if (valid) {
-    if (!have_g) g = a.groups[gi];
-    merge_row<D, kMergeChunk>(a, gi, r, g, lane);
-  }
-  HW_SPAN_END(0);
-}
-
 // Ring slots for R query rows: one, so that two CTAs share an SM (each computes while the
 // other's tile lands); the occupancy, not a second slot, hides the load latency.
 template <int D>
@@ -468,8 +452,6 @@ void launch_fma_d(const AttnArgs& a, const TcMaps& maps, int layer, cudaStream_t
 
 }  // namespace
 
-HW_SPAN_EXPORT(merge)
-
 cudaError_t prepare_attention_fma(int D) {
   // Shared-memory limit: the largest layout any row count up to 128 uses.
   int most = 0;
@@ -489,23 +471,6 @@ void launch_attention_fma(const AttnArgs& a, const TcMaps& maps, int layer, cuda
     launch_fma_d<64>(a, maps, layer, s);
   else
     launch_fma_d<128>(a, maps, layer, s);
-}
-
-void launch_merge(const AttnArgs& a, cudaStream_t s, bool pdl) {
-  if (a.num_groups <= 0) return;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.num_groups * a.rows + kMergeWarps - 1) / kMergeWarps);
-  cfg.blockDim = dim3(32 * kMergeWarps);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  if (a.D == 64)
-    cudaLaunchKernelEx(&cfg, merge_kernel<64>, a);
-  else
-    cudaLaunchKernelEx(&cfg, merge_kernel<128>, a);
 }
 
 }  // namespace hw
