@@ -144,6 +144,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   // Wait for the grid this one follows (it may write the queries, this step's tokens, or read
   // the partials this grid overwrites) before anything global is read or written.
   tc::pdl_wait();
+  // The unit record is read while thread 0 checks that the plan has arrived: each of its three
+  // 16-byte vectors carries the low 32 bits of the plan's sequence number, and a vector read
+  // before the plan landed (its copy differs) is read again once the plan is confirmed.
+  const int4* urec = reinterpret_cast<const int4*>(a.units + blockIdx.x);
+  int4 uv[3] = {__ldcg(urec), __ldcg(urec + 1), __ldcg(urec + 2)};
   if (tid == 0) flags[0] = plan_arrived(a.gate, plan_seq_now(a.gate), a.err, KID_ATTN_FMA) ? 1 : 0;
   __syncthreads();
   const bool plan_ok = flags[0] != 0;
@@ -151,7 +156,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   Group g{};
   bool unit_ok = false;
   if (plan_ok) {
-    u = a.units[blockIdx.x];
+    static_assert(sizeof(Unit) == 48, "unit record: three 16-byte vectors");
+    const uint32_t want = (uint32_t)a.gate.plan_expect;
+    if ((uint32_t)uv[0].z != want) uv[0] = __ldcg(urec);
+    if ((uint32_t)uv[1].w != want) uv[1] = __ldcg(urec + 1);
+    if ((uint32_t)uv[2].z != want) uv[2] = __ldcg(urec + 2);
+    int4* ud = reinterpret_cast<int4*>(&u);
+    ud[0] = uv[0];
+    ud[1] = uv[1];
+    ud[2] = uv[2];
     // (problem, KV head) from the group index (groups are numbered p * H_kv + h): no dependent
     // load of the group record
     if (u.group >= 0 && u.group < a.num_groups) {
@@ -202,10 +215,31 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (got >= 0) ++issued;
     }
   };
-  // The first tiles go out at once, unless they hold tokens this CTA is about to write.
+  // The first tiles go out at once, unless they hold tokens this CTA is about to write.  The
+  // unit record names its first tile's pool position when that tile holds none of this step's
+  // tokens (first_tok): it goes out without waiting for the piece record, which is checked
+  // against it afterwards.
   if (tid == 0 && pb < pe) {
     tc::tma_prefetch(&maps.k);
     tc::tma_prefetch(&maps.v);
+    if (u.first_tok >= 0 && u.first_tok < a.num_pages * a.S) {
+      const int32_t pg = u.first_tok / a.S, sl = u.first_tok % a.S;
+      const int32_t y = (int32_t)(((page_base + pg) * a.H_kv + g.h) * a.S + sl);
+      const uint32_t dst = sbase;                     // slot 0
+      mbar_arrive_expect_tx(bars, C::kSlotBytes);
+#pragma unroll
+      for (int hh = 0; hh < C::kHalves; ++hh) {
+        tma_load_2d(dst + hh * C::kHalfBytes, &maps.k, 64 * hh, y, bars,
+                    tc::l2_policy_evict_first());
+        tma_load_2d(dst + C::kTileBytes + hh * C::kHalfBytes, &maps.v, 64 * hh, y, bars,
+                    tc::l2_policy_evict_first());
+      }
+      issued = 1;
+      next_issue = pb + 1;
+      const Piece pc0 = a.pieces[pb];
+      if (!piece_ok(a, pc0) || pc0.fresh || pc0.page != pg || pc0.slot0 != sl)
+        record_error(a.err, ERR_PLAN, KID_ATTN_FMA, blockIdx.x, 7);
+    }
     fill_ring(!fresh_here);
   }
 
@@ -218,12 +252,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int idx = t; idx < R * half; idx += nt) {
       const int r = idx / half, i = idx % half;
       const int w = r / a.G, hq = g.h * a.G + r % a.G;
+      // the query pair and the rotation are loaded together (neither waits for the other)
+      const int qr = query_row(a, g.p, w);
+      float q1 = 0.f, q2 = 0.f;
+      if (qr >= 0) {
+        const size_t qo = ((size_t)qr * a.H_q + hq) * D;
+        q1 = __bfloat162float(a.q[qo + i]);
+        q2 = __bfloat162float(a.q[qo + i + half]);
+      }
       const int delta = dl[w];
       float y1 = 0.f, y2 = 0.f;
       if (delta >= 0 && delta < a.max_position) {
-        const size_t qo = ((size_t)query_row(a, g.p, w) * a.H_q + hq) * D;
-        const float q1 = __bfloat162float(a.q[qo + i]);
-        const float q2 = __bfloat162float(a.q[qo + i + half]);
         const float c = a.rope_cos[(size_t)delta * half + i];
         const float sn = a.rope_sin[(size_t)delta * half + i];
         y1 = (q1 * c - q2 * sn) * a.scale_log2;
@@ -342,7 +381,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
       }
-      __syncthreads();
+      // Warp w computed P and the statistics of chunk rows 2w and 2w + 1 -- the rows it takes in
+      // O = alpha O + P V below: no other warp reads or writes them.
+      __syncwarp();
       {
         // O = alpha O + P V: thread (row pair rp, columns 4 dg .. 4 dg + 3)
         const int rp = tid >> 5, dg = lane;
@@ -390,8 +431,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (has_b) *ob = make_float4(xb01.x, xb01.y, xb23.x, xb23.y);
         }
       }
-      __syncthreads();
+      __syncwarp();                                 // (the next chunk rewrites this warp's P rows)
     }
+    __syncthreads();                                // every warp is done with the slot and Q~
     ++tile;
     // the slot is free: its next piece goes out (the generic reads of the slot are ordered
     // before the copy's writes)

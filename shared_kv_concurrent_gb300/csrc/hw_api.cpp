@@ -140,6 +140,7 @@ struct PlanOffsets {
   size_t pieces, units, groups, delta, vlen, qrow, fresh, bytes;
   int32_t num_pieces, num_units, num_groups, num_seg_slots, num_fresh;
   int32_t width;                       // columns of the rotation table (query rows / G)
+  int32_t max_group_units;             // the most units of any (problem, KV head) group
 };
 
 // An append-only array that keeps its storage across plans: `grow(k)` hands out k slots to be
@@ -1114,6 +1115,8 @@ bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int
   po->num_pieces = np;
   po->num_units = nu_done;
   po->num_groups = P * H;
+  po->max_group_units = 0;
+  for (int32_t p = 0; p < P; ++p) po->max_group_units = std::max(po->max_group_units, ps.prob_units[p]);
   po->num_seg_slots = (int32_t)(ps.delta.size() / (size_t)WT);
   po->width = WT;
   po->num_fresh = nf;
@@ -1254,7 +1257,7 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
   HW_CUDA(cudaGetLastError());
   if (fused) c->pend_k[layer] = c->pend_v[layer] = nullptr;
   const int pm = c->prof_begin(s, 2);      // (a timed merge is not chained to the attention)
-  hw::launch_merge(a, s, pm < 0);
+  hw::launch_merge(a, s, pm < 0, po.max_group_units);
   c->prof_end(pm, s);
   HW_CUDA(cudaGetLastError());
   c->n_launch += 2;
@@ -1354,7 +1357,7 @@ hw_status hw::attention_into_scratch(hw_ctx* c, int32_t layer, const void* q, vo
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
   hw::launch_attention_fma(a, c->maps, layer, s);
   HW_CUDA(cudaGetLastError());
-  hw::launch_merge(a, s);
+  hw::launch_merge(a, s, false, po.max_group_units);
   HW_CUDA(cudaGetLastError());
   HW_CUDA(cudaEventRecord(c->slot_ev[slot], s));
   c->slot_used[slot] = true;

@@ -192,8 +192,10 @@ void launch_attention_fma(const AttnArgs& a, const TcMaps& maps, int layer, cuda
 void launch_attention_tc(const AttnArgs& a, const TcMaps& maps, const LaunchUnits& lu, int layer,
                          cudaStream_t s, cudaEvent_t ev_before = nullptr,
                          cudaEvent_t ev_after = nullptr);
-// pdl: launch as a programmatic dependent of the preceding kernel (it waits for its writes).
-void launch_merge(const AttnArgs& a, cudaStream_t s, bool pdl = false);
+// The merge of the units' partials.  pdl: launch as a programmatic dependent of the preceding
+// kernel (it waits for its writes).  max_group_units (the most units of any group) sets how many
+// warps share a query row.
+void launch_merge(const AttnArgs& a, cudaStream_t s, bool pdl, int max_group_units);
 bool make_tc_maps(const hw_config& cfg, void* k_pool, void* v_pool, TcMaps* out);
 
 // HW_OK for cudaSuccess; otherwise records the error for hw_last_cuda_error and returns

@@ -14,25 +14,25 @@
 
 namespace hw {
 
-// Query row r of group gi (plan entry g), by one warp (lane = float4 column).  The units are
-// taken kChunk at a time with all their loads in flight, merged into a running (M, L, O) that is
-// rescaled when M grows.
+// Running merge state of one query row in one warp: (M, L) and the lane's float4 of O.
+struct MergeAcc {
+  float M, L;
+  float4 O;
+};
+
+// Fold units [k_begin, k_end) of the group (plan entry g) into `acc` for query row r, by one
+// warp (lane = float4 column).  The units are taken kChunk at a time with all their loads in
+// flight; the running (M, L, O) is rescaled when M grows.
 template <int D, int kChunk>
-__device__ __forceinline__ void merge_row(const AttnArgs& a, int gi, int r, const Group& g,
-                                          int lane) {
+__device__ __forceinline__ void merge_units(const AttnArgs& a, int r, const Group& g, int k_begin,
+                                            int k_end, int lane, MergeAcc& acc) {
   constexpr int PS = part_stride(D);
-  if (g.p < 0 || g.p >= a.P || g.h < 0 || g.h >= a.H_kv || g.unit_begin < 0 ||
-      g.unit_begin > g.unit_end || g.unit_end > a.num_units) {
-    if (lane == 0) record_error(a.err, ERR_PLAN, KID_MERGE, gi, r);   // skipped, not trusted
-    return;
-  }
   const bool act = lane < D / 4;
   const size_t stride = (size_t)a.rows * PS;
   const float* base = a.partials + ((size_t)g.unit_begin * a.rows + r) * PS;
-  const int nu = g.unit_end - g.unit_begin;
-  float M = -CUDART_INF_F, L = 0.f;
-  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k0 = 0; k0 < nu; k0 += kChunk) {
+  float M = acc.M, L = acc.L;
+  float4 O = acc.O;
+  for (int k0 = k_begin; k0 < k_end; k0 += kChunk) {
     float2 ml[kChunk];
     float4 o[kChunk];
 #pragma unroll
@@ -40,7 +40,7 @@ __device__ __forceinline__ void merge_row(const AttnArgs& a, int gi, int r, cons
       const int k = k0 + j;
       ml[j] = make_float2(-CUDART_INF_F, 0.f);
       o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (k < nu) {
+      if (k < k_end) {
         ml[j] = *reinterpret_cast<const float2*>(base + k * stride + D);
         if (act) o[j] = *reinterpret_cast<const float4*>(base + k * stride + 4 * lane);
       }
@@ -66,10 +66,44 @@ __device__ __forceinline__ void merge_row(const AttnArgs& a, int gi, int r, cons
     }
     M = cm;
   }
-  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+  acc.M = M;
+  acc.L = L;
+  acc.O = O;
+}
+
+// Combine a second running state into the first (both over disjoint units of the same row).
+__device__ __forceinline__ void merge_combine(MergeAcc& x, const MergeAcc& y) {
+  const float cm = fmaxf(x.M, y.M);
+  if (cm == -CUDART_INF_F) return;
+  const float sx = (x.M == -CUDART_INF_F) ? 0.f : exp2f(x.M - cm);
+  const float sy = (y.M == -CUDART_INF_F) ? 0.f : exp2f(y.M - cm);
+  x.L = x.L * sx + y.L * sy;
+  x.O = make_float4(x.O.x * sx + y.O.x * sy, x.O.y * sx + y.O.y * sy, x.O.z * sx + y.O.z * sy,
+                    x.O.w * sx + y.O.w * sy);
+  x.M = cm;
+}
+
+// Is the group entry usable (else the row is skipped and the error recorded)?
+__device__ __forceinline__ bool merge_group_ok(const AttnArgs& a, int gi, int r, const Group& g,
+                                               int lane) {
+  if (g.p < 0 || g.p >= a.P || g.h < 0 || g.h >= a.H_kv || g.unit_begin < 0 ||
+      g.unit_begin > g.unit_end || g.unit_end > a.num_units) {
+    if (lane == 0) record_error(a.err, ERR_PLAN, KID_MERGE, gi, r);   // skipped, not trusted
+    return false;
+  }
+  return true;
+}
+
+// out (and lse) of query row r of group g from its merged state.
+template <int D>
+__device__ __forceinline__ void merge_store(const AttnArgs& a, int r, const Group& g, int lane,
+                                            const MergeAcc& acc) {
+  const bool act = lane < D / 4;
+  const float inv = (acc.L > 0.f) ? 1.f / acc.L : 0.f;
   const int qr = query_row(a, g.p, r / a.G), hq = g.h * a.G + r % a.G;
   if (qr < 0) return;                           // padding row: no output
   const size_t oi = (size_t)qr * a.H_q + hq;
+  const float4 O = acc.O;
   if (act) {
     if (a.out_f32) {
       reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + oi * D)[lane] =
@@ -84,7 +118,7 @@ __device__ __forceinline__ void merge_row(const AttnArgs& a, int gi, int r, cons
     }
   }
   if (a.lse && lane == 0)
-    a.lse[oi] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+    a.lse[oi] = (acc.L > 0.f) ? (acc.M + log2f(acc.L)) * 0.6931471805599453f : -CUDART_INF_F;
 }
 
 }  // namespace hw

@@ -46,6 +46,27 @@ def test_w2_contiguous_scaled():
     G.run_case(w, steps=3)
 
 
+def test_full_size_w2_contiguous_36_units_per_group():
+    """The 2-worker workload at full size: 288 one-tile units, 36 per (problem, KV head), more
+    than one merge warp keeps in flight (two warps share each query row)."""
+    import gpu_cases as G
+    w = G.small(wl.c2(), steps=3)
+    G.run_case(w, steps=2, bernoulli=0.5)
+
+
+def test_one_kv_head_many_units_cuda_core_and_tensor_cores():
+    """One KV head, so every unit of the step belongs to one group (well over 40: four merge
+    warps per query row, each folding two batches): 10 rows (CUDA-core kernel) and 64 rows
+    (tensor-core kernel)."""
+    import gpu_cases as G
+    w = G.small(wl.c4(), num_workers=2, num_q_heads=5, num_kv_heads=1, common_len=(20000,),
+                worker_len=((300, 77),), steps=3)
+    G.run_case(w, steps=2, bernoulli=0.5)
+    w = G.small(wl.c4(), num_q_heads=8, num_kv_heads=1, common_len=(30000,),
+                worker_len=((0, 1, 127, 128, 129, 255, 257, 600),), steps=3)
+    G.run_case(w, steps=2)
+
+
 def test_w8_paged_permuted_ragged():
     import gpu_cases as G
     w = G.small(wl.c4(), common_len=(3001,), worker_len=((0, 1, 127, 128, 129, 255, 257, 600),),
