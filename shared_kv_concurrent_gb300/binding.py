@@ -141,6 +141,15 @@ def _i32(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
 
+def _host_arg(a, dtype):
+    """A host array argument as (array to keep alive until the call returns, its address); an
+    int is taken as an address already (the caller keeps that array alive), None stays None."""
+    if a is None or isinstance(a, int):
+        return None, a
+    arr = np.ascontiguousarray(np.asarray(a, dtype=dtype))
+    return arr, arr.ctypes.data
+
+
 def _ptr(arr: np.ndarray, ctype):
     return arr.ctypes.data_as(ctypes.POINTER(ctype))
 
@@ -193,9 +202,10 @@ def hw_destroy(ctx: int) -> None:
 def hw_append_kv(ctx: int, layer: int, n_new, k_raw, v_raw, stream=None) -> None:
     """n_new: host int32 [P][W + 1] (array-like), or the address (int) of such an array that
     stays alive for the call (saves the per-call conversion in a decode loop)."""
-    nptr = n_new if isinstance(n_new, int) else _i32(n_new).ctypes.data
+    keep, nptr = _host_arg(n_new, np.int32)
     st = (_lib or load()).hw_append_kv(ctx, layer, nptr, _dptr(k_raw), _dptr(v_raw),
                                        _stream(stream))
+    del keep
     if st:
         _check(st, "hw_append_kv")
 
@@ -253,22 +263,19 @@ def hw_compact_segments(ctx: int, problem: int, first: int, count: int, stream=N
 
 def hw_step_end(ctx: int, finished=None, stream=None) -> None:
     """finished: host uint8 [P][W] (array-like), None, or the address (int) of such an array."""
-    if finished is None or isinstance(finished, int):
-        fptr = finished
-    elif isinstance(finished, np.ndarray) and finished.dtype == np.uint8 and finished.flags.c_contiguous:
-        fptr = finished.ctypes.data
-    else:
-        fptr = np.ascontiguousarray(np.asarray(finished, dtype=np.uint8)).ctypes.data
+    keep, fptr = _host_arg(finished, np.uint8)
     st = (_lib or load()).hw_step_end(ctx, fptr, _stream(stream))
+    del keep
     if st:
         _check(st, "hw_step_end")
 
 
 def hw_step_scratch_size(ctx: int, n_new, out_dtype: int) -> int:
     n = ctypes.c_size_t()
-    nptr = n_new if isinstance(n_new, int) else _i32(n_new).ctypes.data
+    keep, nptr = _host_arg(n_new, np.int32)
     _check(load().hw_step_scratch_size(ctx, nptr, out_dtype, ctypes.byref(n)),
            "hw_step_scratch_size")
+    del keep
     return n.value
 
 
@@ -279,14 +286,12 @@ def hw_decode_step_host(ctx: int, n_new, in_host: int, in_bytes: int, out_host: 
     packed [K][V][Q] input and the [L][P][W][H_q][D] output (page-locked for asynchronous
     copies); scratch: device address; n_new and finished as hw_append_kv and hw_step_end
     (array-likes, or addresses of arrays that stay alive for the call)."""
-    nptr = n_new if isinstance(n_new, int) else _i32(n_new).ctypes.data
-    if finished is None or isinstance(finished, int):
-        fptr = finished
-    else:
-        fptr = np.ascontiguousarray(np.asarray(finished, dtype=np.uint8)).ctypes.data
+    keep_n, nptr = _host_arg(n_new, np.int32)
+    keep_f, fptr = _host_arg(finished, np.uint8)
     st = (_lib or load()).hw_decode_step_host(ctx, nptr, in_host, in_bytes, out_host, out_dtype,
                                               fptr, scratch, scratch_bytes, int(bool(sync)),
                                               _stream(stream))
+    del keep_n, keep_f
     if st:
         _check(st, "hw_decode_step_host")
 
