@@ -318,73 +318,155 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int r0 = 0; r0 < R; r0 += kChunkRows) {
       const int CR = min(kChunkRows, R - r0);
       {
-        // S = Q~ K^T and the online softmax of the tile, fused: thread (row r of the chunk, token
-        // group tg) takes tokens tg + 16 k, k < 8, and the 16 threads of a row (one half-warp)
-        // reduce its maximum and sum with shuffles.  A row's 8-element query chunk is loaded
-        // once into registers and used for all eight tokens (shared-memory broadcasts deliver
-        // 4 bytes per wavefront, so re-reading the queries per token would cost more than the
-        // K tile itself); the 16 threads of a row read 16 consecutive tokens' chunks (swizzled
-        // rows: no bank conflict).
-        const int r = tid >> 4, tg = tid & 15;
-        if (r < CR) {
-          const unsigned hmask = (lane < 16) ? 0x0000ffffu : 0xffff0000u;   // this row's lanes
-          float2 acc[kTile / 16];           // per token: (even, odd) element accumulators
+        // S = Q~ K^T and the online softmax of the tile, fused.  Warp w takes chunk rows
+        // ra = 2w and rb = 2w + 1; lane = (half dh, token group tg): tokens tg + 16 k (k < 8) of
+        // both rows over the dims of half dh, so every K chunk loaded feeds two rows (the bytes
+        // shared memory delivers to registers, not the FMAs, set the pace of this loop).  The
+        // 8-element query chunks stay in registers across the eight tokens; the 16 lanes of a
+        // half read 16 consecutive tokens' chunks (swizzled rows: no bank conflict).  The halves
+        // then swap partial sums -- half 0 keeps row ra, half 1 row rb -- and the 16 lanes of a
+        // half reduce their row's maximum and sum with shuffles.
+        const int ra = 2 * warp, rb = ra + 1;
+        if (ra < CR) {                                  // (uniform in the warp)
+          const bool has_b = rb < CR;
+          const int dh = lane >> 4, tg = lane & 15;
+          constexpr int NCH = D / 16;                   // 8-element chunks per half of the dims
+          float acc_a[kTile / 16], acc_b[kTile / 16];    // per token: this half's dot product
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k) acc[k] = make_float2(0.f, 0.f);
-          const float* qrow = Qs + (size_t)(r0 + r) * D;
+          for (int k = 0; k < kTile / 16; ++k) acc_a[k] = acc_b[k] = 0.f;
+          const float* qa_row = Qs + (size_t)(r0 + ra) * D;
+          const float* qb_row = Qs + (size_t)(r0 + (has_b ? rb : ra)) * D;
 #pragma unroll 1
-          for (int c = 0; c < D / 8; ++c) {
-            const float4 qa = *reinterpret_cast<const float4*>(qrow + 8 * c);
-            const float4 qb = *reinterpret_cast<const float4*>(qrow + 8 * c + 4);
-            const float2 q01 = make_float2(qa.x, qa.y), q23 = make_float2(qa.z, qa.w);
-            const float2 q45 = make_float2(qb.x, qb.y), q67 = make_float2(qb.z, qb.w);
+          for (int cc = 0; cc < NCH; ++cc) {
+            const int c = dh * NCH + cc;
+            const float4 a0 = *reinterpret_cast<const float4*>(qa_row + 8 * c);
+            const float4 a1 = *reinterpret_cast<const float4*>(qa_row + 8 * c + 4);
+            const float4 b0 = *reinterpret_cast<const float4*>(qb_row + 8 * c);
+            const float4 b1 = *reinterpret_cast<const float4*>(qb_row + 8 * c + 4);
 #pragma unroll
             for (int k = 0; k < kTile / 16; ++k) {
               const uint4 kw = *reinterpret_cast<const uint4*>(kt + swz<D>(tg + 16 * k, c));
-              acc[k] = fma2(q01, make_float2(bf_lo(kw.x), bf_hi(kw.x)), acc[k]);
-              acc[k] = fma2(q23, make_float2(bf_lo(kw.y), bf_hi(kw.y)), acc[k]);
-              acc[k] = fma2(q45, make_float2(bf_lo(kw.z), bf_hi(kw.z)), acc[k]);
-              acc[k] = fma2(q67, make_float2(bf_lo(kw.w), bf_hi(kw.w)), acc[k]);
+              const float k0 = bf_lo(kw.x), k1 = bf_hi(kw.x), k2 = bf_lo(kw.y), k3 = bf_hi(kw.y);
+              const float k4 = bf_lo(kw.z), k5 = bf_hi(kw.z), k6 = bf_lo(kw.w), k7 = bf_hi(kw.w);
+              float x = acc_a[k], y = acc_b[k];
+              x = fmaf(a0.x, k0, x); y = fmaf(b0.x, k0, y);
+              x = fmaf(a0.y, k1, x); y = fmaf(b0.y, k1, y);
+              x = fmaf(a0.z, k2, x); y = fmaf(b0.z, k2, y);
+              x = fmaf(a0.w, k3, x); y = fmaf(b0.w, k3, y);
+              x = fmaf(a1.x, k4, x); y = fmaf(b1.x, k4, y);
+              x = fmaf(a1.y, k5, x); y = fmaf(b1.y, k5, y);
+              x = fmaf(a1.z, k6, x); y = fmaf(b1.z, k6, y);
+              x = fmaf(a1.w, k7, x); y = fmaf(b1.w, k7, y);
+              acc_a[k] = x;
+              acc_b[k] = y;
             }
           }
-          // Online softmax of the row over this tile: tokens past the piece or past the row's
-          // causal cut (cut -1: the row does not see the segment) score -inf.
-          const int rr = r0 + r;
-          const int cap = cut[rr];
-          const int lim = cap < 0 ? 0 : min(nv, cap - pc.pos0);
-          const float m_old = Ms[rr];
+          // swap the halves' partial sums: this lane keeps its own row's score
           float sv[kTile / 16];
-          float mx = -CUDART_INF_F;
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k) {
-            sv[k] = (tg + 16 * k < lim) ? acc[k].x + acc[k].y : -CUDART_INF_F;
-            mx = fmaxf(mx, sv[k]);
+            const float mine = dh ? acc_b[k] : acc_a[k], other = dh ? acc_a[k] : acc_b[k];
+            sv[k] = mine + __shfl_xor_sync(0xffffffffu, other, 16);
           }
+          const int r = dh ? rb : ra;                   // this half's row (in the chunk)
+          if (r < CR) {                                 // (uniform in the half)
+            const unsigned hmask = dh ? 0xffff0000u : 0x0000ffffu;
+            // Online softmax of the row over this tile: tokens past the piece or past the row's
+            // causal cut (cut -1: the row does not see the segment) score -inf.
+            const int rr = r0 + r;
+            const int cap = cut[rr];
+            const int lim = cap < 0 ? 0 : min(nv, cap - pc.pos0);
+            const float m_old = Ms[rr];
+            float mx = -CUDART_INF_F;
 #pragma unroll
-          for (int off = 8; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(hmask, mx, off));
-          const float m_new = fmaxf(m_old, mx);
-          float alpha = 1.f, ps = 0.f;
-          float* prow = Ss + r * kSStride;
+            for (int k = 0; k < kTile / 16; ++k) {
+              if (tg + 16 * k >= lim) sv[k] = -CUDART_INF_F;
+              mx = fmaxf(mx, sv[k]);
+            }
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k) {
-            const float pk = (sv[k] == -CUDART_INF_F) ? 0.f : exp2f(sv[k] - m_new);
-            ps += pk;
-            prow[tg + 16 * k] = pk;
-          }
-          if (m_new != -CUDART_INF_F) alpha = (m_old == -CUDART_INF_F) ? 0.f : exp2f(m_old - m_new);
+            for (int off = 8; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(hmask, mx, off));
+            const float m_new = fmaxf(m_old, mx);
+            float alpha = 1.f, ps = 0.f;
+            float* prow = Ss + r * kSStride;
 #pragma unroll
-          for (int off = 8; off; off >>= 1) ps += __shfl_xor_sync(hmask, ps, off);
-          if (tg == 0) {               // (every lane of the row has read Ms above)
-            Ms[rr] = m_new;
-            Ls[rr] = Ls[rr] * alpha + ps;
-            As[rr] = alpha;
+            for (int k = 0; k < kTile / 16; ++k) {
+              const float pk = (sv[k] == -CUDART_INF_F) ? 0.f : exp2f(sv[k] - m_new);
+              ps += pk;
+              prow[tg + 16 * k] = pk;
+            }
+            if (m_new != -CUDART_INF_F) alpha = (m_old == -CUDART_INF_F) ? 0.f : exp2f(m_old - m_new);
+#pragma unroll
+            for (int off = 8; off; off >>= 1) ps += __shfl_xor_sync(hmask, ps, off);
+            if (tg == 0) {             // (every lane of the row has read Ms above)
+              Ms[rr] = m_new;
+              Ls[rr] = Ls[rr] * alpha + ps;
+              As[rr] = alpha;
+            }
           }
         }
       }
       // Warp w computed P and the statistics of chunk rows 2w and 2w + 1 -- the rows it takes in
       // O = alpha O + P V below: no other warp reads or writes them.
       __syncwarp();
-      {
+      if constexpr (D == 128) {
+        // O = alpha O + P V.  Warp w, rows ra = 2w and rb = 2w + 1; lane = (token half th, column
+        // group cg): tokens [64 th, 64 th + 64) and columns 8 cg .. 8 cg + 7 of both rows, so
+        // every V chunk loaded feeds two rows.  The halves then swap partial sums (half 0 keeps
+        // row ra, half 1 row rb) and each writes its row's columns.  P is zero past the piece's
+        // tokens, so a group of four that runs past them adds nothing.
+        const int ra = 2 * warp, rb = ra + 1;
+        if (ra < CR) {                                  // (uniform in the warp)
+          const bool has_b = rb < CR;
+          const int th = lane >> 4, cg = lane & 15;
+          const float* pa = Ss + ra * kSStride;
+          const float* pbr = Ss + (has_b ? rb : ra) * kSStride;
+          float2 ya[4], yb[4];                          // 8 columns per row, as (even, odd)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            ya[i] = make_float2(0.f, 0.f);
+            yb[i] = make_float2(0.f, 0.f);
+          }
+          const int nv4 = (nv + 3) & ~3;
+          const int k_end = min(nv4, 64 * th + 64);
+#pragma unroll 1
+          for (int k = 64 * th; k < k_end; k += 4) {
+            const float4 p4 = *reinterpret_cast<const float4*>(pa + k);
+            const float4 q4 = *reinterpret_cast<const float4*>(pbr + k);
+            uint4 vw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vw[e] = *reinterpret_cast<const uint4*>(vt + swz<D>(k + e, cg));
+            const float pp[4] = {p4.x, p4.y, p4.z, p4.w}, qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 pe = make_float2(pp[e], pp[e]), qe = make_float2(qq[e], qq[e]);
+              const uint32_t wv[4] = {vw[e].x, vw[e].y, vw[e].z, vw[e].w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 v = make_float2(bf_lo(wv[i]), bf_hi(wv[i]));
+                ya[i] = fma2(pe, v, ya[i]);
+                yb[i] = fma2(qe, v, yb[i]);
+              }
+            }
+          }
+          float fin[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 mine = th ? yb[i] : ya[i], other = th ? ya[i] : yb[i];
+            fin[2 * i] = mine.x + __shfl_xor_sync(0xffffffffu, other.x, 16);
+            fin[2 * i + 1] = mine.y + __shfl_xor_sync(0xffffffffu, other.y, 16);
+          }
+          const int r = th ? rb : ra;
+          if (r < CR) {
+            float4* o = reinterpret_cast<float4*>(Os + (size_t)(r0 + r) * D + 8 * cg);
+            const float al = As[r0 + r];
+            const float4 o0 = o[0], o1 = o[1];
+            o[0] = make_float4(fmaf(al, o0.x, fin[0]), fmaf(al, o0.y, fin[1]), fmaf(al, o0.z, fin[2]),
+                               fmaf(al, o0.w, fin[3]));
+            o[1] = make_float4(fmaf(al, o1.x, fin[4]), fmaf(al, o1.y, fin[5]), fmaf(al, o1.z, fin[6]),
+                               fmaf(al, o1.w, fin[7]));
+          }
+        }
+      } else {
         // O = alpha O + P V: thread (row pair rp, columns 4 dg .. 4 dg + 3)
         const int rp = tid >> 5, dg = lane;
         const int ra = 2 * rp, rb = 2 * rp + 1;
