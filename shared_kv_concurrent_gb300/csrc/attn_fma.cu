@@ -141,9 +141,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     Ms[r] = -CUDART_INF_F;
     Ls[r] = 0.f;
   }
-  // Wait for the grid this one follows (it may write the queries, this step's tokens, or read
-  // the partials this grid overwrites) before anything global is read or written.
-  tc::pdl_wait();
+  // Before the programmatic wait this kernel reads only what belongs to its plan (delivered on
+  // the library's copy stream and checked through its sequence word, or copied before the
+  // launch), the constant rotation table, and K/V tiles that the plan marks as written before
+  // the grids this one may overlap; it writes nothing global but the error word.
   // The unit record is read while thread 0 checks that the plan has arrived: each of its three
   // 16-byte vectors carries the low 32 bits of the plan's sequence number, and a vector read
   // before the plan landed (its copy differs) is read again once the plan is confirmed.
@@ -215,10 +216,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (got >= 0) ++issued;
     }
   };
-  // The first tiles go out at once, unless they hold tokens this CTA is about to write.  The
-  // unit record names its first tile's pool position when that tile holds none of this step's
-  // tokens (first_tok): it goes out without waiting for the piece record, which is checked
-  // against it afterwards.
+  // The unit record names its first tile's pool position when that tile holds no token of
+  // this step or of the step before (first_tok): it goes out now, before the programmatic wait,
+  // without waiting for the piece record, which is checked against it afterwards.  The other
+  // tiles go out after the wait (those with tokens this CTA appends, after the append).
   if (tid == 0 && pb < pe) {
     tc::tma_prefetch(&maps.k);
     tc::tma_prefetch(&maps.v);
@@ -240,59 +241,69 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!piece_ok(a, pc0) || pc0.fresh || pc0.page != pg || pc0.slot0 != sl)
         record_error(a.err, ERR_PLAN, KID_ATTN_FMA, blockIdx.x, 7);
     }
-    fill_ring(!fresh_here);
   }
 
   // Rotation of every row's query for segment slot `seg` by (i_q - the segment's view offset),
   // pre-scaled; rows of workers that do not see it are zero and cut = -1.  Threads t0 .. t0 + nt
-  // of the CTA share the work (t = tid - t0).
-  auto rotate = [&](int seg, int t, int nt) {
+  // of the CTA share the work (t = tid - t0), in two passes with the same items per thread:
+  // rot_factors puts each item's (cos, sin) where its rotated pair goes (plan and table data
+  // only: it may run before the programmatic wait), rot_apply reads the query pair and
+  // replaces them (zero factors: a row that does not see the segment).
+  constexpr int half = D / 2;
+  auto rot_factors = [&](int seg, int t, int nt) {
     const int* dl = a.delta + (size_t)seg * a.W;
-    constexpr int half = D / 2;
     for (int idx = t; idx < R * half; idx += nt) {
       const int r = idx / half, i = idx % half;
-      const int w = r / a.G, hq = g.h * a.G + r % a.G;
-      // the query pair and the rotation are loaded together (neither waits for the other)
-      const int qr = query_row(a, g.p, w);
-      float q1 = 0.f, q2 = 0.f;
-      if (qr >= 0) {
-        const size_t qo = ((size_t)qr * a.H_q + hq) * D;
-        q1 = __bfloat162float(a.q[qo + i]);
-        q2 = __bfloat162float(a.q[qo + i + half]);
-      }
+      const int w = r / a.G;
       const int delta = dl[w];
-      float y1 = 0.f, y2 = 0.f;
-      if (delta >= 0 && delta < a.max_position) {
-        const float c = a.rope_cos[(size_t)delta * half + i];
-        const float sn = a.rope_sin[(size_t)delta * half + i];
-        y1 = (q1 * c - q2 * sn) * a.scale_log2;
-        y2 = (q2 * c + q1 * sn) * a.scale_log2;
+      const bool vis = delta >= 0 && delta < a.max_position;
+      float c = 0.f, sn = 0.f;
+      if (vis) {
+        c = a.rope_cos[(size_t)delta * half + i];
+        sn = a.rope_sin[(size_t)delta * half + i];
       } else if (delta >= a.max_position && i == 0) {
         record_error(a.err, ERR_POS_RANGE, KID_ATTN_FMA, blockIdx.x, delta);
       }
-      Qs[r * D + i] = y1;
-      Qs[r * D + i + half] = y2;
-      if (i == 0) {
-        const bool vis = delta >= 0 && delta < a.max_position;
-        // causal cut (several query tokens per worker): tokens of the segment it may see
-        cut[r] = !vis ? -1 : (a.vlen ? a.vlen[(size_t)seg * a.W + w] : 0x7fffffff);
-      }
+      Qs[r * D + i] = c;
+      Qs[r * D + i + half] = sn;
+      // causal cut (several query tokens per worker): tokens of the segment it may see
+      if (i == 0) cut[r] = !vis ? -1 : (a.vlen ? a.vlen[(size_t)seg * a.W + w] : 0x7fffffff);
     }
   };
-  // The unit's first segment (named by its record) is rotated while the fused append runs: two
-  // warps write the appended tokens, the other six rotate.  The async-proxy fence orders the
-  // pool writes before the CTA's TMA reads of them; every (token, KV head) belongs to exactly
-  // one unit.
-  const bool pre_rot = unit_ok && u.seg0 >= 0 && u.seg0 < a.num_seg_slots;
-  if (fresh_here) {
-    if (tid < 64) {
-      append_fresh<D, 64>(a, g.h, u.fresh_begin, u.fresh_end, tid, KID_ATTN_FMA);
-      fence_proxy_async_global();
-    } else if (pre_rot) {
-      rotate(u.seg0, tid - 64, kThreads - 64);
+  auto rot_apply = [&](int t, int nt) {
+    for (int idx = t; idx < R * half; idx += nt) {
+      const int r = idx / half, i = idx % half;
+      const int w = r / a.G, hq = g.h * a.G + r % a.G;
+      const float c = Qs[r * D + i], sn = Qs[r * D + i + half];
+      float y1 = 0.f, y2 = 0.f;
+      const int qr = query_row(a, g.p, w);
+      if ((c != 0.f || sn != 0.f) && qr >= 0) {      // (cos and sin of an angle are never both 0)
+        const size_t qo = ((size_t)qr * a.H_q + hq) * D;
+        const float q1 = __bfloat162float(a.q[qo + i]);
+        const float q2 = __bfloat162float(a.q[qo + i + half]);
+        y1 = (q1 * c - q2 * sn) * a.scale_log2;
+        y2 = (q2 * c + q1 * sn) * a.scale_log2;
+      }
+      Qs[r * D + i] = y1;
+      Qs[r * D + i + half] = y2;
     }
+  };
+  // The unit's first segment (named by its record): its rotation factors before the wait.  The
+  // fused append, if the unit has appended tokens, runs after it on two warps while the other
+  // six finish the rotation; the async-proxy fence orders the pool writes before the CTA's TMA
+  // reads of them; every (token, KV head) belongs to exactly one unit.
+  const bool pre_rot = unit_ok && u.seg0 >= 0 && u.seg0 < a.num_seg_slots;
+  const int rot_t = fresh_here ? tid - 64 : tid, rot_nt = fresh_here ? kThreads - 64 : kThreads;
+  if (pre_rot && rot_t >= 0) rot_factors(u.seg0, rot_t, rot_nt);
+  // Wait for the grid this one follows (it may write the queries, this step's tokens, or read
+  // the partials this grid overwrites).
+  tc::pdl_wait();
+  if (tid == 0 && pb < pe) fill_ring(!fresh_here);
+  if (fresh_here && tid < 64) {
+    append_fresh<D, 64>(a, g.h, u.fresh_begin, u.fresh_end, tid, KID_ATTN_FMA);
+    fence_proxy_async_global();
   } else if (pre_rot) {
-    rotate(u.seg0, tid, kThreads);
+    rot_apply(rot_t, rot_nt);
   }
   __syncthreads();
   if (fresh_here && tid == 0) fill_ring(true);
@@ -304,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!piece_ok(a, pc)) continue;                 // every thread skips it the same way
     if (pc.seg_slot != cur_seg) {                   // a new segment: its query rotation
       cur_seg = pc.seg_slot;
-      rotate(cur_seg, tid, kThreads);
+      rot_factors(cur_seg, tid, kThreads);
+      rot_apply(tid, kThreads);
     }
     const int slot = (int)(tile % (uint32_t)slots);
     const uint32_t parity = (tile / (uint32_t)slots) & 1u;
