@@ -570,7 +570,8 @@ hw_status hw_create(const hw_config* cfg, void* k_pool, void* v_pool, void* work
 namespace {
 bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int64_t unit_cap,
                           int64_t target_override, bool fuse, uint64_t seq,
-                          const int32_t* n_q = nullptr, const int64_t* ranges = nullptr);
+                          const int32_t* n_q = nullptr, const int64_t* ranges = nullptr,
+                          const int32_t* q_row0 = nullptr);
 }  // namespace
 
 extern "C" {
@@ -729,10 +730,12 @@ namespace {
 // unit_cap > 0 bounds the number of units (one partial result each); 0 = the default split.
 // n_q (host [P][W], or null for one query per worker): several causal query tokens per worker;
 // the rotation table then has one column per query row of a problem (its width WT is the
-// largest count of any problem), with the causal length table and the query-row map.
+// largest count of any problem), with the causal length table and the query-row map.  q_row0
+// (host [P][W], or null): the q / out / lse row of each worker's first query token, for a call
+// that covers only some workers' tokens (null: the tokens present, numbered in order).
 bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int64_t unit_cap = 0,
                           int64_t target_override = 0, bool fuse = false, uint64_t seq = 0,
-                          const int32_t* n_q, const int64_t* ranges) {
+                          const int32_t* n_q, const int64_t* ranges, const int32_t* q_row0) {
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
   int32_t WT = W;                       // rotation-table width: query rows per problem / G
   if (n_q) {
@@ -821,7 +824,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int
             vlen[(size_t)r * WT + v] = k + 1 == ps.view_ref.size() ? n - back : n;
           }
         }
-        if (n_q) ps.qrow[(size_t)p * WT + v] = ps.qrow_next++;
+        if (n_q) ps.qrow[(size_t)p * WT + v] = q_row0 ? q_row0[(size_t)p * W + w] + t : ps.qrow_next++;
       }
       v0 += nq;
     }
@@ -1127,7 +1130,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int
 // worker (the last tokens of its own block).
 static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* n_q, void* out,
                         int32_t out_dtype, float* lse, void* stream,
-                        const int64_t* ranges = nullptr) {
+                        const int64_t* ranges = nullptr, const int32_t* q_row0 = nullptr) {
   if (!c || layer < 0 || layer >= c->cfg.num_layers) return HW_ERR_INVALID_ARG;
   if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
   if (c->step_active && !c->appended[layer]) return HW_ERR_INVALID_ARG;
@@ -1184,7 +1187,7 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
     // partials fit the workspace: units * rows stays within its max_units * (W * G) rows
     const int64_t cap = n_q ? (int64_t)c->lay.max_units * c->rows / (width * c->G) : 0;
     if (!build_attention_plan(c, c->h_slot(slot), c->lay.slot_seq_off, &po, cap, c->wave_ctas(),
-                              false, seq, n_q, ranges))
+                              false, seq, n_q, ranges, q_row0))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
     hbase = c->h_slot(slot);
@@ -1278,8 +1281,50 @@ hw_status hw_concurrent_attention(hw_ctx* c, int32_t layer, const void* q, void*
 
 hw_status hw_concurrent_attention_mq(hw_ctx* c, int32_t layer, const void* q, const int32_t* n_q,
                                      void* out, int32_t out_dtype, float* lse, void* stream) {
-  if (!n_q) return HW_ERR_INVALID_ARG;
-  return attend(c, layer, q, n_q, out, out_dtype, lse, stream);
+  if (!c || !n_q) return HW_ERR_INVALID_ARG;
+  const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers;
+  const int64_t cap = kMaxRows / c->G;          // query tokens of a problem per attention call
+  int64_t width = 0;
+  for (int32_t p = 0; p < P; ++p) {
+    int64_t rows = 0;
+    for (int32_t w = 0; w < W; ++w) {
+      const int32_t n = n_q[(size_t)p * W + w];
+      if (n < 0 || n > c->segs[c->live[p][w]].visible()) return HW_ERR_INVALID_ARG;
+      if (n > cap) return HW_ERR_CAPACITY;       // one worker's tokens exceed a tile
+      rows += n;
+    }
+    width = std::max(width, rows);
+  }
+  if (width <= cap) return attend(c, layer, q, n_q, out, out_dtype, lse, stream);
+  // Row split: each problem's workers, in order, go into parts of at most `cap` query tokens;
+  // part k of every problem is attended in call k (the others' counts zero), each token keeping
+  // its row of q / out / lse.  The K/V stream once per call.
+  std::vector<int32_t> row0((size_t)P * W), part((size_t)P * W);
+  int32_t next_row = 0, parts = 0;
+  for (int32_t p = 0; p < P; ++p) {
+    int32_t k = 0;
+    int64_t used = 0;
+    for (int32_t w = 0; w < W; ++w) {
+      const int32_t n = n_q[(size_t)p * W + w];
+      row0[(size_t)p * W + w] = next_row;
+      next_row += n;
+      if (used + n > cap) {
+        ++k;
+        used = 0;
+      }
+      used += n;
+      part[(size_t)p * W + w] = k;
+    }
+    parts = std::max(parts, k + 1);
+  }
+  std::vector<int32_t> nq_k((size_t)P * W);
+  for (int32_t k = 0; k < parts; ++k) {
+    for (size_t i = 0; i < nq_k.size(); ++i) nq_k[i] = part[i] == k ? n_q[i] : 0;
+    const hw_status st = attend(c, layer, q, nq_k.data(), out, out_dtype, lse, stream, nullptr,
+                                row0.data());
+    if (st != HW_OK) return st;
+  }
+  return HW_OK;
 }
 
 hw_status hw_concurrent_attention_range(hw_ctx* c, int32_t layer, const void* q,

@@ -174,17 +174,17 @@ def test_multi_query_head_dim_64_tensor_cores():
     G.run_mq_case(w, [[0, 3, 1, 2, 1]], [[3, 1, 2, 4]], seed=4)
 
 
-def test_multi_query_over_one_tile_is_refused():
+def test_multi_query_one_worker_over_one_tile_is_refused():
     import torch
     from shared_kv_concurrent_gb300 import binding
     from shared_kv_concurrent_gb300.runner import WorkloadRunner
     import gpu_cases as G
     w = G.small(wl.c4(), common_len=(500,), worker_len=((20,) * 8,), steps=2)
     r = WorkloadRunner(w)
-    n_q = np.full((1, 8), 2, np.int32)
-    n_q[0, 0] = 3                                   # 17 query rows x G 8 > 128
-    q = torch.zeros(17, 64, 128, dtype=torch.bfloat16, device="cuda")
-    out = torch.zeros(17, 64, 128, dtype=torch.bfloat16, device="cuda")
+    n_q = np.full((1, 8), 1, np.int32)
+    n_q[0, 0] = 17                                  # one worker's 17 tokens x G 8 > 128 rows
+    q = torch.zeros(24, 64, 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(24, 64, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(binding.HogwildError) as e:
         r.cache.concurrent_attention_mq(0, q, n_q, out)
     assert e.value.status == binding.HW_ERR_CAPACITY
@@ -193,6 +193,25 @@ def test_multi_query_over_one_tile_is_refused():
         r.cache.concurrent_attention_mq(0, q, n_q, out)
     assert e.value.status == binding.HW_ERR_INVALID_ARG
     r.cache.close()
+
+
+def test_multi_query_rows_split_over_several_launches():
+    """More query rows than one 128-row tile: 8 workers x G 8 with 3 + 2 + ... tokens each
+    (200 rows in one problem), then two problems whose parts differ in number; every token's
+    output, at its own row, against the oracle (tensor-core path), and a CUDA-core case."""
+    import gpu_cases as G
+    w = G.small(wl.c4(), common_len=(1500,), worker_len=((0, 300, 17, 256, 129, 1, 600, 40),),
+                steps=3)
+    n_new = [[0, 3, 3, 3, 3, 3, 3, 3, 3]]
+    n_q = [[3, 3, 3, 3, 4, 3, 3, 3]]                # 25 tokens x 8 = 200 rows: two launches
+    G.run_mq_case(w, n_new, n_q)
+    w = G.small(wl.c5(), num_problems=2, num_q_heads=64, common_len=(700, 1300),
+                worker_len=((9, 0, 130, 20), (3, 5, 0, 1)), steps=3)
+    # G 8: 16 tokens per launch; problem 0: 20 tokens (two parts), problem 1: 9 (one part)
+    G.run_mq_case(w, [[0, 5, 5, 5, 5], [0, 3, 3, 0, 3]], [[5, 5, 5, 5], [3, 3, 0, 3]])
+    w = G.small(wl.c2(), common_len=(1000,), worker_len=((130, 70),), page_size=1280, steps=3)
+    # G 5: 25 tokens per launch; 20 + 15 tokens: two launches, the CUDA-core kernel
+    G.run_mq_case(w, [[0, 3, 3]], [[20, 15]])
 
 
 def test_compaction_between_steps():
