@@ -344,6 +344,19 @@ hw_status hw_compact_segments(hw_ctx* ctx, int32_t problem, int32_t first, int32
                               void* stream);
 
 /*
+ * A compaction policy over hw_compact_segments, between steps: every problem with more than
+ * max_paragraphs committed paragraphs (common segments after the prompt) has them merged --
+ * in the combined and step-wise layouts all of them into one segment after the prompt; in the
+ * contiguous and no-sync layouts, whose views depend on the writer, each run of consecutive
+ * paragraphs of one writer.  The prompt is never re-rotated.  Each merge re-rotates and copies
+ * the merged tokens of every layer (one kernel), so a larger max_paragraphs compacts less
+ * often.  merged (host, or NULL) receives the number of merges enqueued.
+ * Errors: HW_ERR_INVALID_ARG (during a step, max_paragraphs < 1), else those of
+ * hw_compact_segments; the merges before a failing one stand.
+ */
+hw_status hw_compact_auto(hw_ctx* ctx, int32_t max_paragraphs, void* stream, int32_t* merged);
+
+/*
  * Synchronise ``stream`` and read the device error word.  Returns HW_OK, or
  * HW_ERR_DEVICE_CHECK / HW_ERR_DEVICE_TIMEOUT if a kernel recorded one (the word is then
  * cleared).  info: host uint32[4] or NULL: {code, kernel id, detail a, detail b}.

@@ -62,6 +62,11 @@ class HogwildCache:
         """Merge common segments first .. first+count-1 into one RoPE frame (between steps)."""
         binding.hw_compact_segments(self.ctx, problem, first, count, stream)
 
+    def compact_auto(self, max_paragraphs: int, stream=None) -> int:
+        """Merge the committed paragraphs of problems that have more than max_paragraphs
+        (hw_compact_auto); returns the number of merges."""
+        return binding.hw_compact_auto(self.ctx, max_paragraphs, stream)
+
     def concurrent_attention_mq(self, layer: int, q, n_q, out=None, out_dtype: str = "bf16",
                                 lse=None, stream=None):
         """Several causal query tokens per worker (the last n_q[p][w] tokens of its block)."""

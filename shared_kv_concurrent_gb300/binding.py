@@ -31,7 +31,7 @@ EXPORTED = (
     "hw_status_string", "hw_last_cuda_error", "hw_pool_size", "hw_workspace_size", "hw_create",
     "hw_destroy", "hw_append_kv", "hw_concurrent_attention", "hw_concurrent_attention_noalloc",
     "hw_concurrent_attention_mq", "hw_concurrent_attention_range", "hw_merge_attention",
-    "hw_compact_segments",
+    "hw_compact_segments", "hw_compact_auto",
     "hw_step_end", "hw_decode_step_host", "hw_step_scratch_size",
     "hw_check_device_errors", "hw_debug_expire_plans", "hw_profile_enable", "hw_profile_read",
     "hw_get_counts", "hw_get_segment", "hw_get_blocks", "hw_get_view",
@@ -97,6 +97,7 @@ def load() -> ctypes.CDLL:
         "hw_merge_attention": (ctypes.c_int, [_I32, ctypes.c_int64, _I32, _P, _P, _P, _I32, _P,
                                               _P]),
         "hw_compact_segments": (ctypes.c_int, [_P, _I32, _I32, _I32, _P]),
+        "hw_compact_auto": (ctypes.c_int, [_P, _I32, _P, _PI32]),
         "hw_step_end": (ctypes.c_int, [_P, _P, _P]),
         "hw_decode_step_host": (ctypes.c_int, [_P, _P, _P, ctypes.c_size_t, _P, _I32, _P, _P,
                                                ctypes.c_size_t, _I32, _P]),
@@ -259,6 +260,14 @@ def hw_concurrent_attention_noalloc(ctx: int, layer: int, q, out, out_dtype: int
 def hw_compact_segments(ctx: int, problem: int, first: int, count: int, stream=None) -> None:
     _check(load().hw_compact_segments(ctx, problem, first, count, _stream(stream)),
            "hw_compact_segments")
+
+
+def hw_compact_auto(ctx: int, max_paragraphs: int, stream=None) -> int:
+    """The compaction policy; returns the number of merges enqueued."""
+    n = ctypes.c_int32()
+    _check(load().hw_compact_auto(ctx, int(max_paragraphs), _stream(stream), ctypes.byref(n)),
+           "hw_compact_auto")
+    return n.value
 
 
 def hw_step_end(ctx: int, finished=None, stream=None) -> None:

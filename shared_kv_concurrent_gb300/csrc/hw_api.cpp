@@ -1542,6 +1542,38 @@ hw_status hw_compact_segments(hw_ctx* c, int32_t problem, int32_t first, int32_t
   return HW_OK;
 }
 
+hw_status hw_compact_auto(hw_ctx* c, int32_t max_paragraphs, void* stream, int32_t* merged) {
+  if (!c || max_paragraphs < 1) return HW_ERR_INVALID_ARG;
+  if (merged) *merged = 0;
+  if (c->step_active) return HW_ERR_INVALID_ARG;          // between steps only
+  const bool by_writer =
+      c->cfg.layout == HW_LAYOUT_CONTIGUOUS || c->cfg.layout == HW_LAYOUT_NO_SYNC;
+  for (int32_t p = 0; p < c->cfg.num_problems; ++p) {
+    const std::vector<int32_t>& com = c->common[p];
+    if ((int64_t)com.size() - 1 <= max_paragraphs) continue;
+    if (!by_writer) {
+      // every committed paragraph (all but the prompt) into one RoPE frame
+      const hw_status st = hw_compact_segments(c, p, 1, (int32_t)com.size() - 1, stream);
+      if (st != HW_OK) return st;
+      if (merged) ++*merged;
+      continue;
+    }
+    // views that depend on the writer: each run of consecutive paragraphs of one writer
+    for (int32_t i = 1; i < (int32_t)c->common[p].size(); ++i) {   // (a merged run: one entry)
+      const std::vector<int32_t>& cm = c->common[p];
+      const int32_t origin = c->segs[cm[i]].origin;
+      int32_t j = i + 1;
+      while (j < (int32_t)cm.size() && c->segs[cm[j]].origin == origin) ++j;
+      if (j - i >= 2) {
+        const hw_status st = hw_compact_segments(c, p, i, j - i, stream);
+        if (st != HW_OK) return st;
+        if (merged) ++*merged;
+      }
+    }
+  }
+  return HW_OK;
+}
+
 hw_status hw_check_device_errors(hw_ctx* c, void* stream, uint32_t* info) {
   if (!c) return HW_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;

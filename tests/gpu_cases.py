@@ -79,13 +79,15 @@ def check_pools(runner, cache, layer, max_tokens_per_seg=None, dev_layer=None, r
 
 def run_case(w: wl.Workload, steps: int, out_dtype="f32", bernoulli=None, pools=True,
              pool_sample=None, tol=TOL, layer_ids=None, check_steps=None, compact_after=None,
-             max_segments=0):
+             max_segments=0, compact_auto=None):
     """Run ``steps`` decode steps on both sides; compare tables after every step end.
 
     ``layer_ids``: the workload layers the oracle computes (default all); the library always
     runs every layer.  ``compact_after``: {step: [(problem, first, count), ...]} compactions
     done on both sides after that step's end (a range that reaches past the common list is
-    cut to it).  ``check_steps``: the steps whose outputs (and pools) are compared
+    cut to it).  ``compact_auto``: after every step end the library's compaction policy
+    (hw_compact_auto with that max_paragraphs) on the device, and the same merges, as the policy
+    states them, on the oracle (at least one merge must happen in the run).  ``check_steps``: the steps whose outputs (and pools) are compared
     (default all) -- the oracle still appends every step, so later steps see the same cache.
     """
     import torch
@@ -99,6 +101,7 @@ def run_case(w: wl.Workload, steps: int, out_dtype="f32", bernoulli=None, pools=
     P, W, Hq, D = w.num_problems, w.num_workers, w.num_q_heads, w.head_dim
     dt = torch.float32 if out_dtype == "f32" else torch.bfloat16
     rerotated = {}                        # compacted segment -> compactions its keys went through
+    auto_merges = 0
     for step in range(steps):
         inputs = r.step_inputs(step)
         r.append(inputs)
@@ -134,8 +137,38 @@ def run_case(w: wl.Workload, steps: int, out_dtype="f32", bernoulli=None, pools=
             r.cache.compact_segments(p, first, count)
             rerotated[c.compact(p, first, count)] = depth
             dev_tables_equal(r, c)
+        if compact_auto is not None:
+            ranges = []
+            for p in range(w.num_problems):
+                com = c.common[p]
+                if len(com) - 1 <= compact_auto:
+                    continue
+                if w.layout in ("contiguous", "no_sync"):
+                    # runs of consecutive paragraphs of one writer
+                    i = 1
+                    while i < len(com):
+                        j = i + 1
+                        while j < len(com) and c.segments[com[j]].origin == c.segments[com[i]].origin:
+                            j += 1
+                        if j - i >= 2:
+                            ranges.append((p, i, j - i))
+                        i = j
+                else:
+                    ranges.append((p, 1, len(com) - 1))
+            merges = r.cache.compact_auto(compact_auto)
+            assert merges == len(ranges), (step, merges, ranges)
+            auto_merges += merges
+            # the oracle applies them left to right; a merged run leaves one entry behind
+            shift = {}
+            for p, first, count in ranges:
+                first -= shift.get(p, 0)
+                depth = 1 + max(rerotated.get(sid, 0) for sid in c.common[p][first:first + count])
+                rerotated[c.compact(p, first, count)] = depth
+                shift[p] = shift.get(p, 0) + count - 1
+            dev_tables_equal(r, c)
     st, info = r.cache.check_device_errors()
     assert st == binding.HW_OK, info
+    assert compact_auto is None or auto_merges > 0
     r.cache.close()
     return worst
 

@@ -214,6 +214,18 @@ def test_multi_query_rows_split_over_several_launches():
     G.run_mq_case(w, [[0, 3, 3]], [[20, 15]])
 
 
+def test_compaction_policy_between_steps():
+    """The library's compaction policy after every step end (more than two paragraphs: merge
+    them), with random commits, in the combined layout (all paragraphs into one segment) and
+    the contiguous one (runs of one writer): outputs, tables and re-rotated pools against the
+    oracle, which applies the merges the policy states."""
+    import gpu_cases as G
+    for layout in ("combined", "contiguous"):
+        w = G.small(wl.c5(), num_problems=2, common_len=(700, 300),
+                    worker_len=((9, 0, 130, 20), (3, 5, 0, 1)), steps=8, layout=layout)
+        G.run_case(w, steps=7, bernoulli=0.5, compact_auto=2, max_segments=256)
+
+
 def test_compaction_between_steps():
     """Commits build up committed segments; compactions merge ranges of them (the prompt with
     the first paragraphs, then later paragraphs) and the following steps attend to the merged
