@@ -186,12 +186,12 @@ hw_status hw_concurrent_attention(hw_ctx* ctx, int32_t layer, const void* q, voi
  *          appended tokens included).
  *   out:   device [N][H_q][D], bf16 or fp32 (out_dtype); lse: device fp32 [N][H_q] or NULL.
  * A problem's query rows, (sum_w n_q[p][w]) * H_q / H_kv, are attended 128 at a time: when
- * they exceed one 128-row tile, each problem's workers (in order) are cut into parts that fit,
- * and part k of every problem goes into the k-th of several attention launches (the K/V are
- * streamed once per launch; every token keeps its row of q / out / lse).  Limit: one worker's
- * rows, n_q[p][w] * H_q / H_kv, fit a tile, else HW_ERR_CAPACITY and nothing is enqueued.
- * N = 0 enqueues nothing.  The layer's recorded append (hw_append_kv) is written first, by the
- * append kernel.
+ * they exceed one 128-row tile, each problem's query tokens (workers in order, each worker's
+ * tokens in order) are cut into parts of at most 128 rows -- a worker's tokens may straddle
+ * parts, each keeping its causal offset -- and part k of every problem goes into the k-th of
+ * several attention launches (the K/V are streamed once per launch; every token keeps its row
+ * of q / out / lse).  N = 0 enqueues nothing.  The layer's recorded append (hw_append_kv) is
+ * written first, by the append kernel.
  * Errors: as hw_concurrent_attention; HW_ERR_INVALID_ARG for a NULL n_q or a count out of
  * range.  An error from a later launch of a split call leaves the earlier launches' rows
  * written.

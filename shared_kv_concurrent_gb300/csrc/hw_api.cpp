@@ -571,7 +571,7 @@ namespace {
 bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int64_t unit_cap,
                           int64_t target_override, bool fuse, uint64_t seq,
                           const int32_t* n_q = nullptr, const int64_t* ranges = nullptr,
-                          const int32_t* q_row0 = nullptr);
+                          const int32_t* q_row0 = nullptr, const int32_t* q_tail = nullptr);
 }  // namespace
 
 extern "C" {
@@ -732,10 +732,13 @@ namespace {
 // the rotation table then has one column per query row of a problem (its width WT is the
 // largest count of any problem), with the causal length table and the query-row map.  q_row0
 // (host [P][W], or null): the q / out / lse row of each worker's first query token, for a call
-// that covers only some workers' tokens (null: the tokens present, numbered in order).
+// that covers only some workers' tokens (null: the tokens present, numbered in order); q_tail
+// (host [P][W], or null for none): the worker's query tokens after this call's, for a call that
+// takes a worker's first tokens only (the causal offsets count from its last token).
 bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int64_t unit_cap = 0,
                           int64_t target_override = 0, bool fuse = false, uint64_t seq = 0,
-                          const int32_t* n_q, const int64_t* ranges, const int32_t* q_row0) {
+                          const int32_t* n_q, const int64_t* ranges, const int32_t* q_row0,
+                          const int32_t* q_tail) {
   const int32_t P = c->cfg.num_problems, W = c->cfg.num_workers, H = c->cfg.num_kv_heads;
   int32_t WT = W;                       // rotation-table width: query rows per problem / G
   if (n_q) {
@@ -815,7 +818,7 @@ bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int
       });
       const int32_t vb = n_q ? v0 : w;
       for (int32_t t = 0; t < nq; ++t) {
-        const int32_t back = nq - 1 - t, v = vb + t;
+        const int32_t back = nq - 1 - t + (q_tail ? q_tail[(size_t)p * W + w] : 0), v = vb + t;
         for (size_t k = 0; k < ps.view_ref.size(); ++k) {
           const int32_t r = ps.view_ref[k];
           delta[(size_t)r * WT + v] = (int32_t)(total - 1 - back - ps.view_off[k]);
@@ -1130,7 +1133,8 @@ bool build_attention_plan(hw_ctx* c, char* buf, size_t cap, PlanOffsets* po, int
 // worker (the last tokens of its own block).
 static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* n_q, void* out,
                         int32_t out_dtype, float* lse, void* stream,
-                        const int64_t* ranges = nullptr, const int32_t* q_row0 = nullptr) {
+                        const int64_t* ranges = nullptr, const int32_t* q_row0 = nullptr,
+                        const int32_t* q_tail = nullptr) {
   if (!c || layer < 0 || layer >= c->cfg.num_layers) return HW_ERR_INVALID_ARG;
   if (out_dtype != HW_OUT_BF16 && out_dtype != HW_OUT_F32) return HW_ERR_INVALID_ARG;
   if (c->step_active && !c->appended[layer]) return HW_ERR_INVALID_ARG;
@@ -1143,7 +1147,9 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
       int64_t rows = 0;
       for (int32_t w = 0; w < W; ++w) {
         const int32_t n = n_q[(size_t)p * W + w];
-        if (n < 0 || n > c->segs[c->live[p][w]].visible()) return HW_ERR_INVALID_ARG;
+        const int32_t tail = q_tail ? q_tail[(size_t)p * W + w] : 0;
+        if (n < 0 || tail < 0 || (int64_t)n + tail > c->segs[c->live[p][w]].visible())
+          return HW_ERR_INVALID_ARG;
         rows += n;
       }
       total += rows;
@@ -1187,7 +1193,7 @@ static hw_status attend(hw_ctx* c, int32_t layer, const void* q, const int32_t* 
     // partials fit the workspace: units * rows stays within its max_units * (W * G) rows
     const int64_t cap = n_q ? (int64_t)c->lay.max_units * c->rows / (width * c->G) : 0;
     if (!build_attention_plan(c, c->h_slot(slot), c->lay.slot_seq_off, &po, cap, c->wave_ctas(),
-                              false, seq, n_q, ranges, q_row0))
+                              false, seq, n_q, ranges, q_row0, q_tail))
       return HW_ERR_CAPACITY;
     dbase = c->d_slot(slot);
     hbase = c->h_slot(slot);
@@ -1290,38 +1296,45 @@ hw_status hw_concurrent_attention_mq(hw_ctx* c, int32_t layer, const void* q, co
     for (int32_t w = 0; w < W; ++w) {
       const int32_t n = n_q[(size_t)p * W + w];
       if (n < 0 || n > c->segs[c->live[p][w]].visible()) return HW_ERR_INVALID_ARG;
-      if (n > cap) return HW_ERR_CAPACITY;       // one worker's tokens exceed a tile
       rows += n;
     }
     width = std::max(width, rows);
   }
   if (width <= cap) return attend(c, layer, q, n_q, out, out_dtype, lse, stream);
-  // Row split: each problem's workers, in order, go into parts of at most `cap` query tokens;
-  // part k of every problem is attended in call k (the others' counts zero), each token keeping
-  // its row of q / out / lse.  The K/V stream once per call.
-  std::vector<int32_t> row0((size_t)P * W), part((size_t)P * W);
+  // Row split: each problem's query tokens, worker by worker in order, are cut into parts of
+  // at most `cap` tokens (a worker's tokens may straddle parts); part k of every problem is
+  // attended in launch k.  A worker's piece of a part is a run of its tokens: their q / out /
+  // lse rows (row0) and the worker's tokens after them (tail, which keeps the causal offsets)
+  // go with it.  The K/V are streamed once per launch.
+  std::vector<int32_t> first_row((size_t)P * W);
   int32_t next_row = 0, parts = 0;
-  for (int32_t p = 0; p < P; ++p) {
-    int32_t k = 0;
-    int64_t used = 0;
-    for (int32_t w = 0; w < W; ++w) {
-      const int32_t n = n_q[(size_t)p * W + w];
-      row0[(size_t)p * W + w] = next_row;
-      next_row += n;
-      if (used + n > cap) {
-        ++k;
-        used = 0;
-      }
-      used += n;
-      part[(size_t)p * W + w] = k;
-    }
-    parts = std::max(parts, k + 1);
+  for (size_t i = 0; i < first_row.size(); ++i) {
+    first_row[i] = next_row;
+    next_row += n_q[i];
   }
-  std::vector<int32_t> nq_k((size_t)P * W);
+  for (int32_t p = 0; p < P; ++p) {
+    int64_t rows = 0;
+    for (int32_t w = 0; w < W; ++w) rows += n_q[(size_t)p * W + w];
+    parts = std::max<int32_t>(parts, (int32_t)((rows + cap - 1) / cap));
+  }
+  std::vector<int32_t> nq_k((size_t)P * W), row0_k((size_t)P * W), tail_k((size_t)P * W);
   for (int32_t k = 0; k < parts; ++k) {
-    for (size_t i = 0; i < nq_k.size(); ++i) nq_k[i] = part[i] == k ? n_q[i] : 0;
+    for (int32_t p = 0; p < P; ++p) {
+      // tokens [k cap, (k + 1) cap) of the problem's token sequence
+      const int64_t lo = (int64_t)k * cap, hi = lo + cap;
+      int64_t start = 0;                        // the worker's first token in that sequence
+      for (int32_t w = 0; w < W; ++w) {
+        const size_t i = (size_t)p * W + w;
+        const int64_t n = n_q[i];
+        const int64_t a = std::max(lo, start), b = std::min(hi, start + n);
+        nq_k[i] = b > a ? (int32_t)(b - a) : 0;
+        row0_k[i] = first_row[i] + (int32_t)(b > a ? a - start : 0);
+        tail_k[i] = b > a ? (int32_t)(start + n - b) : 0;
+        start += n;
+      }
+    }
     const hw_status st = attend(c, layer, q, nq_k.data(), out, out_dtype, lse, stream, nullptr,
-                                row0.data());
+                                row0_k.data(), tail_k.data());
     if (st != HW_OK) return st;
   }
   return HW_OK;

@@ -174,7 +174,7 @@ def test_multi_query_head_dim_64_tensor_cores():
     G.run_mq_case(w, [[0, 3, 1, 2, 1]], [[3, 1, 2, 4]], seed=4)
 
 
-def test_multi_query_one_worker_over_one_tile_is_refused():
+def test_multi_query_count_past_the_block_is_refused():
     import torch
     from shared_kv_concurrent_gb300 import binding
     from shared_kv_concurrent_gb300.runner import WorkloadRunner
@@ -182,13 +182,13 @@ def test_multi_query_one_worker_over_one_tile_is_refused():
     w = G.small(wl.c4(), common_len=(500,), worker_len=((20,) * 8,), steps=2)
     r = WorkloadRunner(w)
     n_q = np.full((1, 8), 1, np.int32)
-    n_q[0, 0] = 17                                  # one worker's 17 tokens x G 8 > 128 rows
-    q = torch.zeros(24, 64, 128, dtype=torch.bfloat16, device="cuda")
-    out = torch.zeros(24, 64, 128, dtype=torch.bfloat16, device="cuda")
+    n_q[0, 0] = 21                                  # more than the block holds
+    q = torch.zeros(28, 64, 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(28, 64, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(binding.HogwildError) as e:
         r.cache.concurrent_attention_mq(0, q, n_q, out)
-    assert e.value.status == binding.HW_ERR_CAPACITY
-    n_q[0, 0] = 21                                  # more than the block holds
+    assert e.value.status == binding.HW_ERR_INVALID_ARG
+    n_q[0, 0] = -1
     with pytest.raises(binding.HogwildError) as e:
         r.cache.concurrent_attention_mq(0, q, n_q, out)
     assert e.value.status == binding.HW_ERR_INVALID_ARG
@@ -196,9 +196,10 @@ def test_multi_query_one_worker_over_one_tile_is_refused():
 
 
 def test_multi_query_rows_split_over_several_launches():
-    """More query rows than one 128-row tile: 8 workers x G 8 with 3 + 2 + ... tokens each
-    (200 rows in one problem), then two problems whose parts differ in number; every token's
-    output, at its own row, against the oracle (tensor-core path), and a CUDA-core case."""
+    """More query rows than one 128-row tile: 8 workers x G 8 with 3 or 4 tokens each (200
+    rows in one problem), two problems whose parts differ in number, one worker's 40 tokens
+    over three launches (its tokens cut inside the worker: the causal offsets of the later
+    ones), and a CUDA-core case; every token's output, at its own row, against the oracle."""
     import gpu_cases as G
     w = G.small(wl.c4(), common_len=(1500,), worker_len=((0, 300, 17, 256, 129, 1, 600, 40),),
                 steps=3)
@@ -212,6 +213,14 @@ def test_multi_query_rows_split_over_several_launches():
     w = G.small(wl.c2(), common_len=(1000,), worker_len=((130, 70),), page_size=1280, steps=3)
     # G 5: 25 tokens per launch; 20 + 15 tokens: two launches, the CUDA-core kernel
     G.run_mq_case(w, [[0, 3, 3]], [[20, 15]])
+    # one worker's 40 tokens (320 rows at G 8) and a neighbour's 3: three launches (steps=8
+    # leaves room in the position table for the 47 appended tokens)
+    w = G.small(wl.c4(), common_len=(900,), worker_len=((0, 300, 17, 256, 129, 1, 600, 40),),
+                steps=8)
+    G.run_mq_case(w, [[0, 1, 40, 1, 1, 1, 1, 1, 1]], [[1, 40, 3, 0, 0, 1, 0, 2]])
+    # the CUDA-core kernel: 60 tokens of one worker at G 5 (three launches of at most 25)
+    w = G.small(wl.c2(), common_len=(1000,), worker_len=((130, 70),), page_size=1280, steps=3)
+    G.run_mq_case(w, [[0, 3, 3]], [[60, 2]])
 
 
 def test_compaction_policy_between_steps():
