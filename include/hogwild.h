@@ -308,9 +308,9 @@ hw_status hw_step_end(hw_ctx* ctx, const uint8_t* finished, void* stream);
  * asynchronous.  Between steps only (HW_ERR_INVALID_ARG if a step is open).
  * Errors: HW_ERR_INVALID_ARG (NULL pointer, bad out_dtype, a negative count, in_bytes not as
  * above, unaligned scratch, a step open) and HW_ERR_CAPACITY (scratch too small) with nothing
- * enqueued; otherwise those of hw_append_kv (the first append's errors leave no open step),
- * hw_concurrent_attention (every layer is appended by then: hw_step_end can close the step)
- * and hw_step_end.
+ * enqueued; otherwise those of hw_append_kv (the first append's errors leave no open step; the
+ * input copy into scratch is already enqueued then, nothing else), hw_concurrent_attention
+ * (every layer is appended by then: hw_step_end can close the step) and hw_step_end.
  */
 hw_status hw_decode_step_host(hw_ctx* ctx, const int32_t* n_new, const void* in_host,
                               size_t in_bytes, void* out_host, int32_t out_dtype,
