@@ -96,6 +96,26 @@ def test_null_arguments_rejected_before_cuda(lib):
     a, b = ctypes.c_int32(), ctypes.c_int32()
     assert lib.hw_get_counts(None, ctypes.byref(a), ctypes.byref(b)) == binding.HW_ERR_INVALID_ARG
     assert lib.hw_debug_expire_plans(None, 1) == binding.HW_ERR_INVALID_ARG
+    nq = (ctypes.c_int32 * 2)(1, 1)
+    assert lib.hw_concurrent_attention_mq(None, 0, None, nq, None, 0, None, None) == \
+        binding.HW_ERR_INVALID_ARG
+    rg = (ctypes.c_int64 * 2)(0, 1)
+    assert lib.hw_concurrent_attention_range(None, 0, None, rg, None, None, None) == \
+        binding.HW_ERR_INVALID_ARG
+    assert lib.hw_concurrent_attention_noalloc(None, 0, None, None, 0, None, None) == \
+        binding.HW_ERR_INVALID_ARG
+    assert lib.hw_compact_segments(None, 0, 0, 2, None) == binding.HW_ERR_INVALID_ARG
+    merged = ctypes.c_int32()
+    assert lib.hw_compact_auto(None, 2, None, ctypes.byref(merged)) == binding.HW_ERR_INVALID_ARG
+    size = ctypes.c_size_t()
+    assert lib.hw_step_scratch_size(None, n, 0, ctypes.byref(size)) == binding.HW_ERR_INVALID_ARG
+    assert lib.hw_decode_step_host(None, n, None, 0, None, 0, None, None, 0, 1, None) == \
+        binding.HW_ERR_INVALID_ARG
+    # the merge needs no context: bad shapes are refused before any CUDA call
+    assert lib.hw_merge_attention(0, 4, 128, None, None, None, 0, None, None) == \
+        binding.HW_ERR_INVALID_ARG
+    assert lib.hw_merge_attention(2, 4, 6, None, None, None, 0, None, None) == \
+        binding.HW_ERR_INVALID_ARG
     lib.hw_destroy(None)
 
 
