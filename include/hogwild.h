@@ -290,7 +290,8 @@ hw_status hw_step_end(hw_ctx* ctx, const uint8_t* finished, void* stream);
  * inputs and outputs are in host memory.  Every layer's K, V and queries go to the device in
  * one host-to-device copy and every layer's output comes back in one device-to-host copy;
  * in between, hw_append_kv for every layer, hw_concurrent_attention for every layer and
- * hw_step_end, all on `stream`.
+ * hw_step_end, all on `stream` -- the step's attention plan too, copied in stream order
+ * (the separate calls send it on the library's copy stream, where the kernels check for it).
  *   n_new:    host int32[P][W + 1], as hw_append_kv (the same counts for every layer).
  *   in_host:  host, packed [K][V][Q]: K and V bf16 [L][sum n_new][H_kv][D] each (layer-major;
  *             within a layer as hw_append_kv's k_raw / v_raw), then Q bf16 [L][P][W][H_q][D]

@@ -124,11 +124,23 @@ class HogwildCache:
         tensor of L*P*W*H_q*D elements of out_dtype.  The device scratch is kept between calls
         (grown when a step needs more)."""
         dt = HW_OUT_F32 if out_dtype == "f32" else HW_OUT_BF16
-        scratch = self.reserve_step_scratch(n_new, out_dtype)
-        binding.hw_decode_step_host(self.ctx, n_new, in_host.data_ptr(),
-                                    in_host.numel() * in_host.element_size(), out_host.data_ptr(),
-                                    dt, finished, scratch.data_ptr(), scratch.numel(), sync,
-                                    stream)
+        scratch = getattr(self, "_step_scratch", None)
+        if scratch is None:
+            scratch = self.reserve_step_scratch(n_new, out_dtype)
+        args = (in_host.data_ptr(), in_host.numel() * in_host.element_size(), out_host.data_ptr(),
+                dt, finished)
+        try:
+            binding.hw_decode_step_host(self.ctx, n_new, *args, scratch.data_ptr(),
+                                        scratch.numel(), sync, stream)
+        except HogwildError as e:
+            # A scratch too small is refused before anything is enqueued: grow it and retry.
+            # (The size is asked for only then, not on every step.)
+            if (e.status != binding.HW_ERR_CAPACITY or
+                    binding.hw_step_scratch_size(self.ctx, n_new, dt) <= scratch.numel()):
+                raise
+            scratch = self.reserve_step_scratch(n_new, out_dtype)
+            binding.hw_decode_step_host(self.ctx, n_new, *args, scratch.data_ptr(),
+                                        scratch.numel(), sync, stream)
 
     def reserve_step_scratch(self, n_new, out_dtype: str = "bf16"):
         """The device scratch of decode_step_host for the counts n_new, allocated (or grown)

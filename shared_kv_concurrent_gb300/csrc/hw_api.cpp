@@ -249,6 +249,9 @@ struct hw_ctx {
   bool step_plan_ok = false;
   PlanOffsets step_po{};
   hw::PlanGate step_gate{};
+  // Set by hw_decode_step_host while it records the step's appends: the step's plan is then
+  // copied on the call's stream, in order with the step's kernels, and needs no sequence word.
+  bool plan_in_order = false;
   PlanScratch ps;
   // Fused append: when the step's plan lists its appended tokens (step_fused), hw_append_kv
   // only records the layer's k_raw / v_raw here and the layer's attention kernel writes them;
@@ -396,6 +399,13 @@ struct hw_ctx {
       gate->plan_expect = ~seq;
       --expire_plans;
     }
+    return HW_OK;
+  }
+  // The same, copied on `s` in stream order, in one copy: whatever `s` runs afterwards reads
+  // the plan without checking for it (a null gate; the plan carries sequence number 0).
+  hw_status upload_slot_in_order(int slot, size_t bytes, cudaStream_t s, hw::PlanGate* gate) {
+    HW_CUDA(cudaMemcpyAsync(d_slot(slot), h_slot(slot), bytes, cudaMemcpyHostToDevice, s));
+    *gate = hw::PlanGate{nullptr, 0};
     return HW_OK;
   }
   static uint64_t next_seq() { return ++g_upload_seq; }
@@ -680,7 +690,7 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
     // Small appends (decode) are written by the attention kernel itself.
     bool fuse = true;
     for (int32_t i = 0; i < P * B && fuse; ++i) fuse = n_new[i] <= kFuseTok;
-    const uint64_t seq = c->next_seq();
+    const uint64_t seq = c->plan_in_order ? 0 : c->next_seq();
     bool plan_ok = plan_off < c->lay.slot_seq_off &&
                    build_attention_plan(c, c->h_slot(slot) + plan_off, c->lay.slot_seq_off - plan_off,
                                         &po, 0, c->wave_ctas(), fuse, seq);
@@ -690,7 +700,9 @@ hw_status hw_append_kv(hw_ctx* c, int32_t layer, const int32_t* n_new, const voi
                 build_attention_plan(c, c->h_slot(slot) + plan_off, c->lay.slot_seq_off - plan_off,
                                      &po, 0, c->wave_ctas(), false, seq);
     }
-    st = c->upload_slot(slot, plan_off + (plan_ok ? po.bytes : 0), seq, &c->step_gate);
+    const size_t up = plan_off + (plan_ok ? po.bytes : 0);
+    st = c->plan_in_order ? c->upload_slot_in_order(slot, up, s, &c->step_gate)
+                          : c->upload_slot(slot, up, seq, &c->step_gate);
     if (st != HW_OK) return st;
     c->step_slot = slot;
     c->step_runs = nr;
@@ -1773,12 +1785,19 @@ hw_status hw_decode_step_host(hw_ctx* c, const int32_t* n_new, const void* in_ho
   }
   // Every layer's append, then every layer's attention: an error from an attention call leaves
   // a step that hw_step_end can close.  (An append after the first one fails only on the
-  // arguments checked above.)
+  // arguments checked above.)  The step's plan goes up with the first append on this stream,
+  // in order with the kernels that read it (one copy, no sequence word).
+  struct InOrder {
+    hw_ctx* c;
+    ~InOrder() { c->plan_in_order = false; }
+  } in_order{c};
+  c->plan_in_order = true;
   for (int32_t l = 0; l < cfg.num_layers; ++l) {
     const hw_status st = hw_append_kv(c, l, n_new, total ? dev + sl.k + l * kv_layer : nullptr,
                                       total ? dev + sl.v + l * kv_layer : nullptr, stream);
     if (st != HW_OK) return st;
   }
+  c->plan_in_order = false;
   for (int32_t l = 0; l < cfg.num_layers; ++l) {
     const hw_status st = attend(c, l, dev + sl.q + l * q_layer, nullptr,
                                 dev + sl.out + l * out_layer, out_dtype, nullptr, stream);

@@ -26,9 +26,12 @@ def built():
     build()
 
 
-def run_host_steps(w, steps, out_dtype="bf16", bernoulli=None, sync_every=1):
+def run_host_steps(w, steps, out_dtype="bf16", bernoulli=None, sync_every=1,
+                   small_scratch=False):
     """``steps`` decode steps through hw_decode_step_host; with sync_every > 1 only every
-    sync_every-th call synchronises (the others only enqueue, each with its own buffers)."""
+    sync_every-th call synchronises (the others only enqueue, each with its own buffers).
+    small_scratch: the cache starts with a device scratch too small for a step, which the
+    first call must refuse before enqueuing anything and the wrapper then grows."""
     import torch
 
     import gpu_cases as G
@@ -37,6 +40,8 @@ def run_host_steps(w, steps, out_dtype="bf16", bernoulli=None, sync_every=1):
     from shared_kv_concurrent_gb300 import binding
     from shared_kv_concurrent_gb300.runner import WorkloadRunner
     r = WorkloadRunner(w)
+    if small_scratch:
+        r.cache._step_scratch = torch.empty(256, dtype=torch.uint8, device="cuda")
     P, W, Hq, D, L = w.num_problems, w.num_workers, w.num_q_heads, w.head_dim, w.num_layers
     dt = torch.float32 if out_dtype == "f32" else torch.bfloat16
     ins = [r.packed_inputs(s) for s in range(steps)]
@@ -77,6 +82,11 @@ def test_host_step_tensor_cores_with_commits():
 def test_host_step_cuda_core_kernel():
     w = dataclasses.replace(wl.tiny(), steps=5)
     run_host_steps(w, 4, bernoulli=0.5)
+
+
+def test_host_step_scratch_grown_after_the_refusal():
+    w = dataclasses.replace(wl.tiny(), steps=4)
+    run_host_steps(w, 3, small_scratch=True)
 
 
 def test_host_step_layers_fp32_enqueue_only():
