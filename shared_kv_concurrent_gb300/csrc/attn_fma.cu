@@ -12,9 +12,13 @@
 // kernel loads) are staged once into a ring of one or two slots in shared memory, completion
 // on an mbarrier, and kept in bf16; the rotated, pre-scaled queries (log2(e)/sqrt(D)) and the
 // running output O of every row stay in shared memory in fp32.  Per tile and per chunk of 16
-// query rows: S = Q~ K^T and the online softmax (running max and sum, rescale factor) with a
-// thread per (row, 8 tokens), a row's 16 threads reducing by shuffles; O = alpha O + P V with a
-// thread per (row pair, 4 columns).  In a decode step the CTA first writes its unit's appended
+// query rows, warp w takes rows 2w and 2w + 1 in both passes: S = Q~ K^T and the online softmax
+// (running max and sum, rescale factor) with a lane per (half of the dims, 8 tokens) of both
+// rows, the halves swapping partial sums and a row's 16 lanes reducing by shuffles; then
+// O = alpha O + P V with a lane per (half of the tokens, 8 columns) of both rows, the halves
+// again swapping partial sums (D = 64: a lane per 4 columns of both rows over all the tokens).
+// So every K or V chunk read from shared memory feeds two rows.
+// In a decode step the CTA first writes its unit's appended
 // tokens itself (fused append).  Every wait is bounded (about a second): one that runs out records
 // ERR_TIMEOUT, and the CTA waits (bounded by the clock) for its copies in flight, then writes
 // empty partials.  The kernel is launched as a programmatic dependent: it waits for the grid
