@@ -8,7 +8,8 @@ kernel sets up and loads its first K/V tile while the previous step still runs, 
 go up on the library's copy stream without a stream wait.  None of that happens when a test
 synchronises after every call, so these tests drive the same pattern -- every step with its
 own output buffers, inputs kept alive -- and compare every step against the fp64 oracle only
-after one final synchronisation: outputs (1e-2 max-abs), lse, tables and stored pools.
+after one final synchronisation: outputs (1e-2 max-abs), lse, tables and stored pools -- on
+both attention kernels (tensor cores from 16 query rows per KV head, CUDA cores below).
 """
 import numpy as np
 import pytest
@@ -120,3 +121,20 @@ def test_chained_multi_layer_fp32_output():
     import dataclasses
     w = dataclasses.replace(wl.c3(), num_layers=3, common_len=(3000,), steps=6)
     run_chained(w, caches=2, steps_per_cache=5, out_dtype="f32")
+
+
+def test_chained_cuda_core_w2_contiguous():
+    """The 2-worker contiguous workload: 10 query rows per KV head, the CUDA-core kernel, whose
+    set-up (plan check, unit record, first tile, first rotation factors) runs before its grid
+    wait and writes the step's tokens itself; three caches, six steps each."""
+    import dataclasses
+    w = dataclasses.replace(wl.c2(), steps=7)
+    run_chained(w, caches=3, steps_per_cache=6)
+
+
+def test_chained_cuda_core_head_dim_64_with_commits():
+    """8 rows at head dim 64 (CUDA-core kernel) with both workers committing after steps 1 and
+    3; two caches, six steps each."""
+    import dataclasses
+    w = dataclasses.replace(wl.tiny(), steps=7, commit_steps=(1, 3))
+    run_chained(w, caches=2, steps_per_cache=6)
