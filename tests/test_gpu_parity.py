@@ -103,6 +103,17 @@ def test_head_dim_64_tensor_cores():
     G.run_case(w, steps=3, bernoulli=0.5)
 
 
+def test_single_worker_is_ordinary_decode_on_both_kernels():
+    """W = 1, the degenerate case: the view is the common history then the worker's own block,
+    i.e. ordinary RoPE decode attention; the worker commits every other step, so its blocks
+    keep moving into the history.  8 rows per KV head (CUDA-core kernel) and 16 (tensor cores)."""
+    import gpu_cases as G
+    for H_q in (16, 32):
+        w = G.small(wl.tiny(), num_workers=1, num_q_heads=H_q, num_kv_heads=2,
+                    common_len=(900,), worker_len=((130,),), steps=5, commit_steps=(0, 2))
+        G.run_case(w, steps=5)
+
+
 def test_max_rows_128():
     import gpu_cases as G
     w = G.small(wl.c4(), num_workers=16, common_len=(600,),
