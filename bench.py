@@ -364,15 +364,9 @@ def run_ours(args):
     sm_hz = 2.07e9                             # GB300 maximum SM clock (cycles of the delay)
 
     def device_delay():
-        # One SM spins for most of the delay; its last ~0.5 ms streams the flush buffer (reads
-        # only, none of the workload's data) on every SM, so that the timed steps start on a
-        # GPU in the state a continuous decode loop keeps it in.  After a spin alone the first
-        # steps of a chain run slower: 20 timed steps 33.1-33.3 us each against 32.8-33.0 with
-        # the reads, and a 240-step chain's first 20 steps 33.1 us against 32.7 for the next.
+        # One SM spins while the host queues the steps (a kernel of torch's own: nothing here
+        # may make the host wait for the device, or the steps would go out at host speed).
         torch.cuda._sleep(int(min(0.2, 3 * args.steps * host_step + 2e-3) * sm_hz))
-        words = flush.view(torch.int32)
-        for _ in range(max(1, int(0.5e-3 * 6.5e12 / flush.numel()))):
-            torch.amax(words)          # a reduction in the buffer's own type: no cast copy
 
     device_delay()
     e_start.record()
@@ -482,9 +476,8 @@ def run_ours(args):
                           f"the timed region; the e2e leg flushes L2 (2x L2 memset) before "
                           f"every step"),
                    "timing": "one CUDA event pair around all timed steps",
-                   "delay": ("before the start event: one SM spins while the host queues the "
-                             "timed steps, then ~0.5 ms of reads of the L2-flush buffer on "
-                             "every SM (no workload data)"),
+                   "delay": ("before the start event one SM spins while the host queues the "
+                             "timed steps"),
                    "step": "append 1 token/worker + concurrent attention + step end"},
         "pct_of_peak": 100.0 * value / world / peak,
         "worker_tokens_per_s": world * P * W * args.steps / t_total,
